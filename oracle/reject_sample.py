@@ -1,0 +1,212 @@
+"""Accept / reject / resample of speculative decoding, fp64 on the CPU.
+
+What the pages fix, and the readings taken where they are silent:
+
+* Temperature softmax of the target logits z and the draft logits d with one
+  shared temperature T: p = softmax(z / T), q = softmax(d / T) (page 1 §3.3
+  asks for matching draft and target temperatures).
+* Accept draft token x with probability min(1, p(x) / q(x)): accept at once if
+  p(x) >= q(x), otherwise with probability p(x) / q(x) (page 1 §2.3 and §4.1;
+  page 2 §2.1).  With a uniform u in [0, 1) the test is u * q(x) < p(x).
+* Stop at the first rejection and drop the later drafts (page 1 §4.3, third
+  point).
+* After a rejection, draw the replacement from normalize(max(0, p - q)); when
+  every draft was accepted draw the extra (bonus) token from p of the last
+  accepted position (page 3, formal definition: g drafts + 1 bonus and the
+  residual max(0, pi_t - pi_d); the sentence there attaches the residual to
+  the all-accepted case, which contradicts the exactness it claims, so the
+  residual is used after a rejection and p for the bonus).
+* Tree verify (page 1 §5.3; page 2 §5.4; page 3 tree-attention section): the
+  pages give no acceptance rule for several children of one node.  Reading
+  taken: children were drafted i.i.d. from q of their parent; they are tested
+  in ascending node order; after each rejected child the working target
+  becomes P <- normalize(max(0, P - q)); the first accepted child becomes the
+  new node (with P = p and q of that node); if every child is rejected, or
+  the node is a leaf, one token is drawn from the working P.  A chain is the
+  tree in which node i has the single child i + 1.
+* Sampling is by inverse CDF in vocabulary order: the token is the smallest k
+  with C_k > u * Z, where C is the running sum of the weights and Z their
+  total.
+* A residual of total mass 0 cannot follow a genuine rejection (a rejection
+  implies p(x) < q(x)); it only arises for a drafted token of zero draft
+  probability.  Reading taken: the working distribution then falls back to
+  the target p of the node.
+* Rows containing NaN or +inf, or only -inf, have no distribution: the whole
+  request is reported as failed (accepted length -1).  -inf entries are
+  allowed and have probability 0.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .uniforms import uniforms_for
+
+NONFINITE = 5     # request failed: a row it needs has no distribution
+NEAR = 1e-6       # decisions closer than this to their threshold are flagged
+
+
+def softmax_rows(logits: np.ndarray, T: float) -> np.ndarray:
+    """softmax(z / T) of each row, in fp64, from the given (bf16/fp32) values."""
+    z = np.asarray(logits, dtype=np.float64)
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp((z - m) / float(T))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def row_has_distribution(row: np.ndarray) -> bool:
+    row = np.asarray(row, dtype=np.float64)
+    if np.isnan(row).any() or np.isposinf(row).any():
+        return False
+    return bool(np.isfinite(row).any())
+
+
+def inverse_cdf(weights: np.ndarray, u: float):
+    """Smallest k with C_k > u * Z (C = running sum of weights, Z = total).
+
+    Returns (k, distance) where distance = min |u - t| over the two CDF
+    thresholds t = C_{k-1}/Z, C_k/Z that bracket u.
+    """
+    C = np.cumsum(np.asarray(weights, dtype=np.float64))
+    Z = C[-1]
+    k = int(np.searchsorted(C, u * Z, side="right"))
+    k = min(k, C.shape[0] - 1)
+    lo = C[k - 1] / Z if k > 0 else 0.0
+    hi = C[k] / Z
+    return k, min(abs(u - lo), abs(hi - u))
+
+
+class UniformChooser:
+    """Decisions driven by one request's counter-based uniforms."""
+
+    def __init__(self, u_acc: np.ndarray, u_smp: np.ndarray):
+        self.u_acc = u_acc
+        self.u_smp = u_smp
+        self.min_margin = np.inf     # smallest |u - threshold| seen
+
+    def accept(self, node: int, P_x: float, Q_x: float) -> bool:
+        u = self.u_acc[node]
+        if Q_x > 0.0:
+            self.min_margin = min(self.min_margin, abs(u - P_x / Q_x))
+        return u * Q_x < P_x
+
+    def sample(self, node: int, weights: np.ndarray) -> int:
+        k, dist = inverse_cdf(weights, self.u_smp[node])
+        self.min_margin = min(self.min_margin, dist)
+        return k
+
+
+def children_lists(parent: np.ndarray | None, M: int):
+    kids = [[] for _ in range(M)]
+    for c in range(1, M):
+        par = c - 1 if parent is None else int(parent[c])
+        kids[par].append(c)
+    return kids
+
+
+def verify_request(p_row, q_row, tokens, children, chooser):
+    """The verify walk of one request.
+
+    p_row(n), q_row(n): normalized fp64 target / draft distributions of node n
+    (the distributions over n's children).  tokens[c]: drafted token of node c.
+    children[n]: child node indices of n in ascending order.
+    chooser: object with accept(node, P_x, Q_x) -> bool and
+             sample(node, weights) -> token.
+
+    Returns dict(path, emitted, final, tested, Z, p_sampled):
+      path      nodes on the accepted path, starting with the root 0
+      emitted   accepted tokens followed by the one sampled token
+      final     node at which the sample was drawn
+      tested    {child: (P(x_c), Q(x_c))} as used in each accept test
+      Z         residual mass normalizing the sampling distribution (1 for a
+                bonus draw from p)
+      p_sampled probability of the sampled token under that distribution
+    """
+    node = 0
+    path = [0]
+    emitted = []
+    tested = {}
+    while True:
+        p_node = p_row(node)
+        P = p_node
+        Z = 1.0
+        accepted = None
+        if children[node]:
+            Q = q_row(node)
+            for c in children[node]:
+                x = int(tokens[c])
+                tested[c] = (float(P[x]), float(Q[x]))
+                if chooser.accept(c, float(P[x]), float(Q[x])):
+                    accepted = c
+                    break
+                r = np.maximum(P - Q, 0.0)
+                Z = float(r.sum())
+                P = r / Z if Z > 0.0 else p_node
+                if Z <= 0.0:
+                    Z = 1.0
+        if accepted is None:
+            tok = chooser.sample(node, P)
+            emitted.append(tok)
+            return dict(path=path, emitted=emitted, final=node, tested=tested,
+                        Z=Z, p_sampled=float(P[tok] / P.sum()))
+        path.append(accepted)
+        emitted.append(int(tokens[accepted]))
+        node = accepted
+
+
+def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
+                         offset, b_base=0):
+    """Verify decisions for a batch.
+
+    target, draft : [B, M, V] logits (row n = distribution over n's children)
+    tokens        : [B, M] drafted tokens (tokens[b, 0] ignored)
+    parent        : [B, M] parent indices (parent[b, 0] = -1) or None (chain)
+    temperature   : [B] > 0
+    seed, offset  : Philox key word and counter word 2; b_base + b is word 1
+
+    Returns dict of numpy arrays:
+      out_tokens [B, M] int32 (emitted tokens, then -1)
+      path       [B, M] int32 (accepted path node indices, then -1)
+      accepted_len [B] int32 (-1 for a failed request)
+      probe      [B, M, 4] float64: per tested node (P(x), Q(x)); at the final
+                 node (Z, probability of the sampled token); -1 elsewhere
+      margin     [B] float64: smallest |u - threshold| over the request's
+                 decisions (draws closer than 1e-6 are 'near threshold')
+      status     [B] int32: 0 or NONFINITE
+    """
+    target = np.asarray(target)
+    draft = np.asarray(draft)
+    B, M, V = target.shape
+    out_tokens = np.full((B, M), -1, dtype=np.int32)
+    path_out = np.full((B, M), -1, dtype=np.int32)
+    acc = np.full(B, -1, dtype=np.int32)
+    probe = np.full((B, M, 4), -1.0, dtype=np.float64)
+    margin = np.full(B, np.inf, dtype=np.float64)
+    status = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        par = None if parent is None else np.asarray(parent[b])
+        kids = children_lists(par, M)
+        T = float(np.float32(temperature[b]))
+        needed = [target[b, n] for n in range(M)]
+        needed += [draft[b, n] for n in range(M) if kids[n]]
+        if not (T > 0.0 and np.isfinite(T)) or \
+                not all(row_has_distribution(r) for r in needed):
+            status[b] = NONFINITE
+            continue
+        u_acc, u_smp = uniforms_for(seed, offset, b_base + b, M)
+        chooser = UniformChooser(u_acc, u_smp)
+        res = verify_request(
+            lambda n: softmax_rows(target[b, n], T),
+            lambda n: softmax_rows(draft[b, n], T),
+            tokens[b], kids, chooser)
+        a = len(res["path"]) - 1
+        acc[b] = a
+        path_out[b, :a + 1] = res["path"]
+        out_tokens[b, :a + 1] = res["emitted"]
+        for c, (px, qx) in res["tested"].items():
+            probe[b, c, 0] = px
+            probe[b, c, 1] = qx
+        probe[b, res["final"], 2] = res["Z"]
+        probe[b, res["final"], 3] = res["p_sampled"]
+        margin[b] = chooser.min_margin
+    return dict(out_tokens=out_tokens, path=path_out, accepted_len=acc,
+                probe=probe, margin=margin, status=status)

@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verify step on one GB300 (or N).
+
+A step is one pass of the whole verify path over one batch of the workload:
+spec_verify_attn (KV append + masked verify attention, one layer),
+spec_reject_sample (temperature softmax, accept/reject, residual/bonus draw)
+and kv_commit (rollback / path compaction).  Inputs are seeded synthetic
+data resident in HBM before the timed region; the KV cache (GBs) exceeds the
+129 MB L2, so no flush is needed between steps.  Each step uses a new
+uniform offset so the decisions vary; kv_commit writes the new context
+lengths to a separate buffer so every step starts from the same state.
+
+One JSON line on rank 0.  Under torchrun each rank runs its own replica of
+the workload (the path shards by request, no collective), timing is the max
+over ranks and `value` counts the steps of all ranks ("weak" scaling).
+
+--impl reference times the CPU oracle on the host cores instead, each step a
+bounded sample (a few requests) of the same workload scaled to whole steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/s and accepted tokens/s at 1 GB300; achieved HBM TB/s vs peak"
+UNIT = "verify steps/s"
+DEFAULT_WORKLOAD = "stress_gqa_152k"
+
+# DRAM traffic of one spec_verify_attn call measured by ncu on the workload
+# below (profiles/verify_attn_stress_gqa_152k.md), valid only for the kernel
+# sources whose digest is recorded with it.
+TRAFFIC = {"digest": None, "bytes_per_call": None}
+
+
+def attn_sources_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_19_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("attn") or f in ("api.cu", "common.cuh"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 7:
+                    continue
+                try:
+                    sm.append(float(p[0]))
+                    smax.append(float(p[1]))
+                except ValueError:
+                    continue
+                for name, v in zip(self.NAMES, p[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+
+def build_inputs(wl, seed, device):
+    from synth import kv_inputs_device, logits_inputs
+    lg = logits_inputs(wl, seed)
+    kv = kv_inputs_device(wl, seed, device)
+    return lg, kv
+
+
+def algorithmic_bytes(wl, ctx_lens, parent):
+    """Bytes each row of the path must move once (per step)."""
+    e = 2 if wl.dtype == "bf16" else 4
+    B, M = wl.B, wl.M
+    L = ctx_lens.astype(np.int64) + M
+    attn = int(L.sum()) * wl.Hkv * wl.D * 2 * e            # K and V read
+    attn += B * M * wl.Hkv * wl.D * 2 * e                   # append write
+    attn += 2 * B * M * wl.Hq * wl.D * e                    # q read, out write
+    if parent is None:
+        draft_rows = B * (M - 1)
+    else:
+        draft_rows = int(sum(len(set(p[1:].tolist())) for p in parent))
+    reject = (B * M + draft_rows) * wl.V * e
+    return attn, reject
+
+
+class NativeStep:
+    def __init__(self, wl, lg, kv, device, steps_total):
+        import speculative_decoding_verification_19_gb300 as sv
+        self.sv = sv
+        self.wl = wl
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.dt = dt
+        B, M = wl.B, wl.M
+        self.dims = sv.make_dims(B=B, M=M, Hq=wl.Hq, Hkv=wl.Hkv, D=wl.D,
+                                 max_blocks=kv["max_blocks"], num_blocks=kv["num_blocks"],
+                                 V=wl.V, kv_dtype=dt, logits_dtype=dt)
+        self.ws = sv.workspace(self.dims, device=device)
+        T = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to(device, t)  # noqa: E731
+        self.target = T(lg["target"], dt)
+        self.draft = T(lg["draft"], dt)
+        self.tokens = T(lg["tokens"], torch.int32)
+        self.parent = None if lg["parent"] is None else T(lg["parent"], torch.int32)
+        self.temperature = T(lg["temperature"], torch.float32)
+        self.q, self.k_new, self.v_new = kv["q"], kv["k_new"], kv["v_new"]
+        self.k_cache, self.v_cache = kv["k_cache"], kv["v_cache"]
+        self.block_table = T(kv["block_table"], torch.int32)
+        self.ctx_lens = T(kv["ctx_lens"], torch.int32)
+        self.new_ctx = torch.empty_like(self.ctx_lens)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=device)
+        self.out_tokens = torch.empty(B, M, dtype=torch.int32, device=device)
+        self.path = torch.empty(B, M, dtype=torch.int32, device=device)
+        self.acc = torch.empty(steps_total, B, dtype=torch.int32, device=device)
+
+    def step(self, i, events=None):
+        sv = self.sv
+        n = 0
+        if events:
+            events[0].record()
+        n += sv.spec_verify_attn(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                 self.block_table, self.ctx_lens, self.parent, self.out,
+                                 self.lse, self.dims, self.ws)
+        if events:
+            events[1].record()
+        n += sv.spec_reject_sample(self.target, self.draft, self.tokens, self.parent,
+                                   self.temperature, 20261202, i, self.out_tokens, self.path,
+                                   self.acc[i], None, self.dims, self.ws)
+        if events:
+            events[2].record()
+        n += sv.kv_commit(self.k_cache, self.v_cache, self.block_table, self.ctx_lens,
+                          self.new_ctx, self.path, self.acc[i], self.dims, self.ws)
+        if events:
+            events[3].record()
+        return n
+
+    def host_inputs(self):
+        """Pinned host copies of one step's inputs, and pinned result buffers."""
+        ins = {k: getattr(self, k).cpu().pin_memory() for k in
+               ("q", "k_new", "v_new", "target", "draft", "tokens", "temperature",
+                "block_table", "ctx_lens")}
+        if self.parent is not None:
+            ins["parent"] = self.parent.cpu().pin_memory()
+        outs = {"out_tokens": torch.empty_like(self.out_tokens, device="cpu").pin_memory(),
+                "path": torch.empty_like(self.path, device="cpu").pin_memory(),
+                "acc": torch.empty(self.wl.B, dtype=torch.int32).pin_memory(),
+                "new_ctx": torch.empty_like(self.new_ctx, device="cpu").pin_memory()}
+        return ins, outs
+
+    def e2e_step(self, i, ins, outs):
+        for k, v in ins.items():
+            getattr(self, k).copy_(v, non_blocking=True)
+        n = self.step(i)
+        outs["out_tokens"].copy_(self.out_tokens, non_blocking=True)
+        outs["path"].copy_(self.path, non_blocking=True)
+        outs["acc"].copy_(self.acc[i], non_blocking=True)
+        outs["new_ctx"].copy_(self.new_ctx, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return n
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle over single requests of the workload (host copies)."""
+
+    def __init__(self, wl, lg, kv, reqs):
+        self.wl = wl
+        self.lg = lg
+        self.reqs = list(reqs)
+        self.data = {}
+        bt = kv["block_table"]
+        for b in self.reqs:
+            pages = bt[b][bt[b] >= 0]
+            idx = torch.from_numpy(pages.astype(np.int64)).to(kv["k_cache"].device)
+            kc = kv["k_cache"].index_select(0, idx).float().cpu().numpy()
+            vc = kv["v_cache"].index_select(0, idx).float().cpu().numpy()
+            table = np.arange(len(pages), dtype=np.int32)[None]
+            self.data[b] = dict(
+                kc=kc, vc=vc, table=table, ctx=kv["ctx_lens"][b:b + 1],
+                q=kv["q"][b:b + 1].float().cpu().numpy(),
+                kn=kv["k_new"][b:b + 1].float().cpu().numpy(),
+                vn=kv["v_new"][b:b + 1].float().cpu().numpy())
+
+    def run(self, b, offset):
+        from oracle import oracle_kv_commit, oracle_reject_sample, oracle_verify_attn
+        d = self.data[b]
+        par = None if self.lg["parent"] is None else self.lg["parent"][b:b + 1]
+        _, _, kc, vc = oracle_verify_attn(d["q"], d["kc"], d["vc"], d["table"], d["ctx"],
+                                          d["kn"], d["vn"], parent=par)
+        r = oracle_reject_sample(self.lg["target"][b:b + 1], self.lg["draft"][b:b + 1],
+                                 self.lg["tokens"][b:b + 1], par,
+                                 self.lg["temperature"][b:b + 1], 20261202, offset,
+                                 b_base=b)
+        oracle_kv_commit(kc, vc, d["table"], d["ctx"], r["path"], r["accepted_len"])
+        return r
+
+
+def cpu_baseline(wl, lg, kv, budget_s=12.0, max_reqs=8):
+    reqs = list(range(min(max_reqs, wl.B)))
+    sample = OracleSample(wl, lg, kv, reqs)
+    t0 = time.perf_counter()
+    done = 0
+    for b in reqs:
+        sample.run(b, 0)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": (done / wl.B) / el, "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{done} of {wl.B} requests of one step (append+attention over all "
+                      f"{wl.Hkv} KV heads, reject-sample, commit), fp64 numpy, "
+                      f"{el:.1f} s; value scaled to whole steps"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_native(args, wl, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    seed = args.seed + rank
+    lg, kv = build_inputs(wl, seed, device)
+    K, W = args.steps, args.warmup
+    st = NativeStep(wl, lg, kv, device, max(K, W, 1) + W + K)
+    attn_b, rej_b = algorithmic_bytes(wl, kv["ctx_lens"], lg["parent"])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, lg, kv)
+
+    for i in range(W):
+        st.step(i)
+    torch.cuda.synchronize()
+    launches_per_step = st.step(W)  # one more untimed step to count launches
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record()
+    for i in range(K):
+        st.step(W + 1 + i, ev[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_max = max_over_ranks(ms_total, world, device)
+    attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    rej_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    com_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+    acc = st.acc[W + 1:W + 1 + K].cpu().numpy()
+    assert np.all(acc >= 0), "a request failed inside the timed region"
+    emitted_per_step = float((acc + 1).sum(axis=1).mean())
+
+    # end to end through the public API with pinned host buffers
+    ins, outs = st.host_inputs()
+    h2d = sum(v.numel() * v.element_size() for v in ins.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    for i in range(2):
+        st.e2e_step(i, ins, outs)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(K):
+        st.e2e_step(i, ins, outs)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+
+    steps_per_s = world * K / (ms_max / 1e3)
+    peaks = measured_peaks()
+    achieved = attn_b / (attn_ms / 1e3) / 1e9
+    traffic = TRAFFIC["bytes_per_call"] if TRAFFIC["digest"] == attn_sources_digest() else None
+    line = {
+        "metric": METRIC, "value": round(steps_per_s, 3), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_max / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "M": wl.M,
+                   "V": wl.V, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "ctx": list(wl.ctx), "layers": 1,
+                   "parallelism": f"replicas x{world} (request shards, no collective)",
+                   "l2": "inputs larger than L2 (KV cache %.1f GB), no flush"
+                         % (2 * kv["k_cache"].numel() * kv["k_cache"].element_size() / 1e9)},
+        "accepted_tokens_per_s": round(steps_per_s * emitted_per_step, 1),
+        "emitted_tokens_per_step": round(emitted_per_step, 2),
+        "hbm_tb_s": round((attn_b + rej_b) / (ms_max / K / 1e3) / 1e12, 3),
+        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (append+split+combine)",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "bytes_per_call": attn_b, "traffic": traffic},
+        "kernels": {"attn_ms": round(attn_ms, 4), "reject_ms": round(rej_ms, 4),
+                    "commit_ms": round(com_ms, 4),
+                    "reject_gbs": round(rej_b / (rej_ms / 1e3) / 1e9, 1),
+                    "reject_frac": round(rej_b / (rej_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "reject_bytes": rej_b},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * K / e2e_s, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    from synth import context_lengths, kv_inputs_host, logits_inputs
+    reqs_per_step = 1
+    lg = logits_inputs(wl, args.seed)
+    K, W = args.steps, args.warmup
+    n = min(wl.B, 4)   # distinct requests cycled through by the oracle
+    # host-side inputs of the requests the oracle will see
+    kv = kv_inputs_host(wl.scaled(B=n), args.seed,
+                        ctx=context_lengths(wl, args.seed)[:n])
+    kvt = dict(kv)
+    for k in ("q", "k_new", "v_new", "k_cache", "v_cache"):
+        kvt[k] = torch.from_numpy(kv[k])
+    sample = OracleSample(wl, lg, kvt, range(n))
+    for i in range(W):
+        sample.run(i % n, i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        sample.run((W + i) % n, W + i)
+    el = time.perf_counter() - t0
+    value = (K * reqs_per_step / wl.B) / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(1e3 / value, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V,
+                   "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "ctx": list(wl.ctx)},
+        "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"each step = {reqs_per_step} of {wl.B} requests through "
+                                   "the fp64 numpy oracle (append+attention, "
+                                   "reject-sample, commit), scaled to whole steps"},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least three untimed steps
+    from synth import workload
+    wl = workload(args.workload)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        run_native(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * spec_verify.h -- C ABI of the speculative-decoding verify step on GB300.
+ *
+ * The verify step of speculative decoding (draft model proposes gamma tokens
+ * or a tree of them; the target model checks them all in one forward) has
+ * three data-parallel parts, and this library does exactly those:
+ *
+ *   spec_verify_attn    append the new rows' K/V to a paged cache and run the
+ *                       masked attention of the gamma+1 (or tree) queries;
+ *   spec_reject_sample  temperature softmax of target and draft logits,
+ *                       accept/reject of each draft token, and the
+ *                       replacement or bonus draw;
+ *   kv_commit           roll the cache back to the accepted prefix, or
+ *                       compact the accepted tree path.
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is caller-owned DEVICE memory, dense and
+ *     row-major in the stated shape.  The library never allocates, never
+ *     frees and never synchronises (except spec_get_device_status).  All work
+ *     is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).  Calls are re-entrant; the only state kept
+ *     between calls is a per-thread count of launches (spec_last_launch_count).
+ *   - B requests, M query rows per request (row 0 = the pending root token
+ *     whose K/V is not cached yet, rows 1.. = drafts or tree nodes), Hq query
+ *     heads, Hkv KV heads (Hq % Hkv == 0), head size D, vocabulary V.
+ *   - Tree topology: parent[B][M] int32 with parent[b][0] = -1 and
+ *     0 <= parent[b][n] < n for n >= 1 (BFS or any topological numbering).
+ *     parent == NULL means the chain parent[n] = n - 1.
+ *   - Errors the host can see (bad sizes, NULL pointers, short workspace)
+ *     return at once and launch nothing.  Errors only the device can see
+ *     (a block id out of range, a context that does not fit the block table,
+ *     a bad temperature, a row with no distribution) set a bit in the status
+ *     word kept in the workspace and make the affected request a no-op with
+ *     defined outputs; read them with spec_get_device_status.
+ *
+ * Sources: three practitioner pages on speculative decoding -- page 1
+ * "投机推理..." (kwkr.cn) §2.1, §2.3, §4.1, §4.3, §5.1, §5.3; page 2
+ * "推测解码..." (cf-1.com) §2.1-§2.3, §3.3, §4.3, §5.4; page 3
+ * "推测解码的工程真相 2026" (blog.lonae.com), formal-definition and
+ * tree-attention sections.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spec_status {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,   /* bad size, NULL pointer, bad temperature/topology */
+  SPEC_ERR_CAPACITY = 2,      /* ctx + M exceeds the request's block-table capacity */
+  SPEC_ERR_UNSUPPORTED = 3,   /* shape or dtype this build has no kernel for */
+  SPEC_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  SPEC_ERR_NONFINITE = 5,     /* a logits row holds NaN/+inf or only -inf */
+  SPEC_ERR_DEVICE_BOUNDS = 6  /* a block id or token id out of range */
+} spec_status;
+
+typedef enum spec_dtype { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+
+typedef struct spec_dims {
+  int32_t B;            /* requests in the batch */
+  int32_t M;            /* query rows per request: gamma+1, or tree nodes incl. root */
+  int32_t Hq;           /* query heads */
+  int32_t Hkv;          /* KV heads; query head h reads KV head h / (Hq/Hkv) */
+  int32_t D;            /* head size (64 or 128) */
+  int32_t block;        /* tokens per KV block; must be 16 */
+  int32_t max_blocks;   /* entries per block-table row */
+  int32_t num_blocks;   /* physical blocks in each cache */
+  int32_t V;            /* vocabulary size */
+  int32_t kv_dtype;     /* spec_dtype of q, k_new, v_new, caches and out */
+  int32_t logits_dtype; /* spec_dtype of target and draft logits */
+  float softmax_scale;  /* attention score scale; 0 selects 1/sqrt(D) */
+} spec_dims;
+
+/* Bytes of caller-owned device workspace every call with these dims needs
+ * (status word, split-KV partials, row statistics, per-request state).
+ * Returns 0 if the dims are invalid. */
+size_t spec_workspace_size(const spec_dims* dims);
+
+/* Zero the workspace (status word included).  Call once after allocating it;
+ * afterwards every call leaves it ready for the next.  An async memset on
+ * `stream`. */
+spec_status spec_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream` and read the device status word: bit (1 << code) is
+ * set for every spec_status code a device-side check raised since the last
+ * clear.  clear != 0 resets the word afterwards. */
+spec_status spec_get_device_status(void* ws, void* stream, int32_t* flags,
+                                   int32_t clear);
+
+/*
+ * spec_verify_attn -- KV append and verify attention (one layer).
+ *
+ * Page 1 §2.1: feed all candidate positions at once; under the causal mask
+ * each position sees only what precedes it, so the parallel pass equals
+ * token-by-token decoding, provided the KV cache is extended in the right
+ * order.  Page 2 §3.3: reuse the cached prefix and compute K/V only for the
+ * new positions.  Page 3 (tree-attention section) and page 2 §5.4: a draft
+ * tree is verified in one pass under a mask that follows the tree.
+ *
+ *   q        [B, M, Hq, D]   kv_dtype   queries (position encoding applied)
+ *   k_new    [B, M, Hkv, D]  kv_dtype   K of the M new rows
+ *   v_new    [B, M, Hkv, D]  kv_dtype   V of the M new rows
+ *   k_cache  [num_blocks, Hkv, 16, D]   paged K cache (in/out)
+ *   v_cache  [num_blocks, Hkv, 16, D]   paged V cache (in/out)
+ *   block_table [B, max_blocks] int32   position t of request b lives in
+ *                                       block block_table[b][t/16], slot t%16
+ *   ctx_lens [B] int32      cached tokens of request b before this step
+ *   parent   [B, M] int32 or NULL (chain)
+ *   out      [B, M, Hq, D]   kv_dtype   attention output
+ *   lse      [B, M, Hq] float or NULL   natural-log log-sum-exp of the
+ *                                       scaled scores of each row
+ *
+ * Effect: rows i = 0..M-1 of k_new/v_new are written to positions
+ * ctx+i; the remaining slots of the last block touched are set to zero.
+ * Then row i attends to positions 0..ctx-1 and to the new positions
+ * ctx+k for every k that is i or an ancestor of i (k <= i for a chain),
+ * with scores scaled by softmax_scale.
+ * A request whose ctx + M exceeds max_blocks*16 (SPEC_ERR_CAPACITY, the
+ * pages' cue to fall back to plain decoding) or whose needed block ids are
+ * out of range (SPEC_ERR_DEVICE_BOUNDS) leaves the caches untouched and
+ * gets out = 0, lse = -inf.
+ */
+spec_status spec_verify_attn(const void* q, const void* k_new,
+                             const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_table,
+                             const int32_t* ctx_lens, const int32_t* parent,
+                             void* out, float* lse, const spec_dims* dims,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * spec_reject_sample -- accept / reject / resample of the drafts.
+ *
+ * p = softmax(target/T), q = softmax(draft/T) with the request's temperature
+ * (page 1 §3.3).  Draft token x of node c is accepted iff
+ * u_acc(c) * q(x) < p(x), i.e. with probability min(1, p/q) (page 1 §2.3,
+ * §4.1; page 2 §2.1); the walk stops at the first rejection (page 1 §4.3).
+ * After a rejection the token is drawn from normalize(max(0, p - q)); if the
+ * walk reaches a node without children the bonus token is drawn from p
+ * (page 3, formal definition).  In a tree the children of a node are tried
+ * in ascending order and each rejection replaces the working target P by
+ * normalize(max(0, P - q)); the first accepted child is entered.  Draws use
+ * the inverse CDF in vocabulary order: the smallest k with C_k > u*Z.
+ *
+ * Uniforms: Philox4x64-10 (Salmon et al., SC'11), key (seed, 0), counter
+ * (n+1, b_base+b, offset, 0) for node n of request b; u_acc = (w0>>40)*2^-24,
+ * u_smp = (w1>>40)*2^-24.
+ *
+ *   target_logits [B, M, V] logits_dtype   row n: law of n's children
+ *   draft_logits  [B, M, V] logits_dtype   row n: q that drafted n's children
+ *                                          (rows of leaves are not read)
+ *   tokens        [B, M] int32   drafted token of node n (tokens[b][0] unused)
+ *   parent        [B, M] int32 or NULL (chain)
+ *   temperature   [B] float      > 0 and finite
+ *   out_tokens    [B, M] int32   emitted tokens: the a accepted drafts, then
+ *                                the drawn token; -1 after that
+ *   path          [B, M] int32   accepted node indices, starting with 0; -1 after
+ *   accepted_len  [B] int32      a (number of accepted drafts), -1 if failed
+ *   probe         [B, M, 4] float or NULL: for every tested node n, p(x_n)
+ *                 and q(x_n) as used in its test (cols 0, 1); at the node
+ *                 where the draw happened, the mass Z of the residual that
+ *                 was drawn from (1 for a bonus draw) and the probability of
+ *                 the drawn token (cols 2, 3); -1 elsewhere.
+ * A failed request (bad temperature, token, topology, or a needed row with
+ * no distribution) gets accepted_len = -1 and -1 rows.
+ */
+spec_status spec_reject_sample(const void* target_logits,
+                               const void* draft_logits,
+                               const int32_t* tokens, const int32_t* parent,
+                               const float* temperature, uint64_t seed,
+                               uint64_t offset, uint64_t b_base,
+                               int32_t* out_tokens, int32_t* path,
+                               int32_t* accepted_len, float* probe,
+                               const spec_dims* dims, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/*
+ * kv_commit -- roll back / compact the cache to the accepted path.
+ *
+ * Page 2 §3.3: after a partial acceptance the cache past the accepted
+ * position is dropped; page 2 §5.4 and page 3 (tree section): a tree verify
+ * rolls back along the accepted path.  The K/V of the root and of the a
+ * accepted nodes are kept; for j = 1..a (increasing), the slot ctx+path[j]
+ * is moved to slot ctx+j.  new_ctx_lens[b] = ctx_lens[b] + a + 1 (the drawn
+ * token's K/V comes with the next step).  For a chain nothing moves.
+ *
+ *   k_cache, v_cache, block_table, ctx_lens  as in spec_verify_attn
+ *   new_ctx_lens [B] int32   output; may alias ctx_lens
+ *   path [B, M], accepted_len [B]  as produced by spec_reject_sample
+ * Requests with accepted_len < 0, a bad path, or out-of-range block ids are
+ * left unchanged (new length = old length) and flagged in the status word.
+ */
+spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,
+                      const int32_t* ctx_lens, int32_t* new_ctx_lens,
+                      const int32_t* path, const int32_t* accepted_len,
+                      const spec_dims* dims, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Host-side Philox4x64-10 block (the generator the kernels use), for
+ * known-answer tests: out = Philox4x64-10(counter, key). */
+void spec_philox_block(const uint64_t key[2], const uint64_t counter[4],
+                       uint64_t out[4]);
+
+/* Human-readable name of a status code. */
+const char* spec_status_string(int32_t status);
+
+/* Number of kernel launches the last call on this thread enqueued. */
+int32_t spec_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

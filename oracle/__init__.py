@@ -37,6 +37,8 @@ from .reject_sample import (  # noqa: F401
     inverse_cdf,
     softmax_rows,
     NONFINITE,
+    INVALID_ARG,
+    BAD_TOKEN,
 )
 from .attention import (  # noqa: F401
     oracle_kv_append,

@@ -41,7 +41,9 @@ import numpy as np
 
 from .uniforms import uniforms_for
 
+INVALID_ARG = 1   # request failed: bad temperature or topology
 NONFINITE = 5     # request failed: a row it needs has no distribution
+BAD_TOKEN = 6     # request failed: a drafted token outside [0, V)
 NEAR = 1e-6       # decisions closer than this to their threshold are flagged
 
 
@@ -93,6 +95,14 @@ class UniformChooser:
         k, dist = inverse_cdf(weights, self.u_smp[node])
         self.min_margin = min(self.min_margin, dist)
         return k
+
+
+def valid_topology(parent: np.ndarray) -> bool:
+    """parent[0] = -1 and 0 <= parent[n] < n for n >= 1."""
+    if parent[0] != -1:
+        return False
+    n = np.arange(1, len(parent))
+    return bool(np.all((parent[1:] >= 0) & (parent[1:] < n)))
 
 
 def children_lists(parent: np.ndarray | None, M: int):
@@ -160,7 +170,7 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
     target, draft : [B, M, V] logits (row n = distribution over n's children)
     tokens        : [B, M] drafted tokens (tokens[b, 0] ignored)
     parent        : [B, M] parent indices (parent[b, 0] = -1) or None (chain)
-    temperature   : [B] > 0
+    temperature   : [B] positive normal finite fp32 values
     seed, offset  : Philox key word and counter word 2; b_base + b is word 1
 
     Returns dict of numpy arrays:
@@ -171,7 +181,8 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
                  node (Z, probability of the sampled token); -1 elsewhere
       margin     [B] float64: smallest |u - threshold| over the request's
                  decisions (draws closer than 1e-6 are 'near threshold')
-      status     [B] int32: 0 or NONFINITE
+      status     [B] int32: 0, INVALID_ARG, NONFINITE or BAD_TOKEN
+    Failed requests (status != 0) keep accepted_len -1 and -1 rows.
     """
     target = np.asarray(target)
     draft = np.asarray(draft)
@@ -186,10 +197,17 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
         par = None if parent is None else np.asarray(parent[b])
         kids = children_lists(par, M)
         T = float(np.float32(temperature[b]))
+        # temperature must be a positive, normal, finite fp32 value
+        if not (T >= float(np.finfo(np.float32).tiny) and np.isfinite(T)) or (
+                par is not None and not valid_topology(par)):
+            status[b] = INVALID_ARG
+            continue
+        if np.any((tokens[b, 1:] < 0) | (tokens[b, 1:] >= V)):
+            status[b] = BAD_TOKEN
+            continue
         needed = [target[b, n] for n in range(M)]
         needed += [draft[b, n] for n in range(M) if kids[n]]
-        if not (T > 0.0 and np.isfinite(T)) or \
-                not all(row_has_distribution(r) for r in needed):
+        if not all(row_has_distribution(r) for r in needed):
             status[b] = NONFINITE
             continue
         u_acc, u_smp = uniforms_for(seed, offset, b_base + b, M)

@@ -1,0 +1,30 @@
+"""GB300-native verify step of speculative decoding.
+
+The compute lives in libspecverify.so (hand-written CUDA for sm_103a, C ABI
+in include/spec_verify.h).  This package is its thin Python binding:
+
+  spec_verify_attn    KV append + masked verify attention over a paged cache
+  spec_reject_sample  temperature softmax, accept/reject, residual/bonus draw
+  kv_commit           rollback / tree-path compaction of the KV cache
+
+plus helpers to size and initialise the caller-owned workspace and to read
+the device status word.
+"""
+from ._native import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    SPEC_BF16,
+    SPEC_F32,
+    SpecDims,
+    SpecError,
+    device_status,
+    dtype_code,
+    kv_commit,
+    lib,
+    make_dims,
+    philox_block,
+    spec_reject_sample,
+    spec_verify_attn,
+    workspace,
+    workspace_size,
+)

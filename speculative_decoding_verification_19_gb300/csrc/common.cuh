@@ -1,0 +1,98 @@
+// Shared device helpers of the verify-step kernels: element loads, status
+// flags, warp reductions and the workspace layout.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spec_verify.h"
+
+namespace specv {
+
+constexpr int kBlock = 16;          // tokens per KV block
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Unpack the 8 bf16 (or 4 fp32) values of one 16-byte vector to fp32.
+__device__ __forceinline__ void unpack16(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void unpack16(const uint4& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+template <typename T> struct Vec16 { static constexpr int n = 16 / sizeof(T); };
+
+// ---------------------------------------------------------------------------
+// status word (bit (1 << code) per raised spec_status code)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_status(uint32_t* status, int code) {
+  atomicOr(status, 1u << code);
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_or(int v) {
+  return __reduce_or_sync(0xffffffffu, (unsigned)v);
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// workspace layout (computed identically by every entry point)
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  size_t status_off;      // uint32 status word
+  size_t attn_ok_off;     // [B] int32 per-request verdict of the append
+  size_t attn_off;        // split-KV partials: [B, Hkv, max_splits, R, D+1] f32
+  size_t attn_bytes;
+  int split_keys;         // keys per split (multiple of 16)
+  int max_splits;
+  int rows;               // R = group * M
+  size_t rs_off;          // reject-sample chunk stats: [B, 2, M, n_chunks] float2
+  size_t rs_bytes;
+  int rs_chunk;           // logits per chunk
+  int rs_chunks;          // chunks per row
+  size_t total;
+};
+
+WsLayout workspace_layout(const spec_dims& d);
+
+}  // namespace specv

@@ -16,5 +16,6 @@ from .workloads import (  # noqa: F401
     logits_inputs,
     kv_layout,
     kv_inputs_host,
+    kv_inputs_device,
     random_tree,
 )

@@ -275,3 +275,37 @@ def expected_ctx_mean(wl: Workload) -> float:
 def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
+
+
+def kv_inputs_device(wl: Workload, seed: int, device, B: int | None = None,
+                     ctx: np.ndarray | None = None) -> dict:
+    """Like kv_inputs_host, but the large caches are drawn on the device.
+
+    Block tables, context lengths, queries and the new K/V rows come from the
+    host generator (same values as kv_inputs_host); the two caches are drawn
+    with torch's seeded device generator, so full-size workloads (several GB
+    of cache) need no host round trip.  Returns torch tensors on `device`
+    (bf16 or fp32) plus the layout arrays as numpy.
+    """
+    import torch
+
+    lay = kv_layout(wl, seed, B=B, ctx=ctx)
+    Bn = lay["block_table"].shape[0]
+    rng = np.random.default_rng([seed, 4])
+    M, Hq, Hkv, D = wl.M, wl.Hq, wl.Hkv, wl.D
+
+    def normal(*shape):
+        return _cast(rng.standard_normal(shape, dtype=np.float32), wl.dtype)
+
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    q = torch.from_numpy(normal(Bn, M, Hq, D)).to(device=device, dtype=tdt)
+    k_new = torch.from_numpy(normal(Bn, M, Hkv, D)).to(device=device, dtype=tdt)
+    v_new = torch.from_numpy(normal(Bn, M, Hkv, D)).to(device=device, dtype=tdt)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 17)
+    shape = (lay["num_blocks"], Hkv, wl.block, D)
+    k_cache = torch.randn(shape, generator=g, device=device, dtype=tdt)
+    v_cache = torch.randn(shape, generator=g, device=device, dtype=tdt)
+    out = dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache)
+    out.update(lay)
+    return out

@@ -1,0 +1,124 @@
+"""GPU parity of spec_reject_sample against the CPU oracle.
+
+Bit-exact accepted lengths, paths and emitted tokens for every request whose
+draws are clear of their thresholds by 1e-6 (the oracle reports the margin);
+probe probabilities within 1e-5.  Covers the five workloads at their full
+batch and vocabulary, ragged and unaligned vocabularies, trees, the
+all-accept / all-reject edge cases, failed requests, and a 10^6-trial
+chi-square of the GPU's own output law.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+from harness import compare_reject, gpu_reject  # noqa: E402
+from oracle import oracle_reject_sample, softmax_rows  # noqa: E402
+from synth import logits_inputs, workload  # noqa: E402
+
+
+def _run(wl, lg, seed, offset, b_base=0):
+    g = gpu_reject(wl, lg, seed, offset, b_base=b_base)
+    o = oracle_reject_sample(lg["target"], lg["draft"], lg["tokens"],
+                             lg["parent"], lg["temperature"], seed, offset,
+                             b_base=b_base)
+    near = compare_reject(g, o)
+    return g, o, near
+
+
+@pytest.mark.parametrize("name", ["tiny_chain", "chain_7b", "chain_gqa_128k",
+                                  "tree_64", "stress_gqa_152k"])
+def test_workload_full_size(name):
+    wl = workload(name)
+    lg = logits_inputs(wl, seed=0)
+    total_near = 0
+    for offset in (0, 1, 2):
+        g, o, near = _run(wl, lg, seed=1234, offset=offset)
+        total_near += near
+        assert g["status"] == 0
+    # near-threshold exclusions must stay rare
+    assert total_near <= max(1, wl.B // 20)
+
+
+@pytest.mark.parametrize("B,gamma,V", [(1, 1, 8), (3, 2, 32), (3, 8, 1000),
+                                       (2, 5, 32007), (4, 3, 4097), (2, 8, 50)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ragged_shapes(B, gamma, V, dtype):
+    wl = workload("chain_7b").scaled(B=B, gamma=gamma, V=V, dtype=dtype, T=0.9)
+    lg = logits_inputs(wl, seed=B * 100 + gamma)
+    for offset in range(3):
+        _run(wl, lg, seed=99, offset=offset, b_base=5)
+
+
+@pytest.mark.parametrize("V", [64, 32000])
+def test_trees(V):
+    wl = workload("tree_64").scaled(B=6, V=V)
+    lg = logits_inputs(wl, seed=3)
+    for offset in range(4):
+        _run(wl, lg, seed=7, offset=offset)
+
+
+def test_small_trees_many_rejections():
+    # wide fan-out, noisy draft: several rejections per node
+    wl = workload("tree_64").scaled(B=8, V=48, gamma=2, tree_width=8,
+                                    tree_nodes=40, noise=3.0)
+    lg = logits_inputs(wl, seed=4)
+    for offset in range(6):
+        _run(wl, lg, seed=11, offset=offset)
+
+
+def test_all_accept_and_all_reject():
+    wl = workload("chain_7b").scaled(B=16, V=4000)
+    lg = logits_inputs(wl, seed=5)
+    same = dict(lg, draft=lg["target"].copy())
+    g, o, _ = _run(wl, same, seed=1, offset=0)
+    assert np.all(g["accepted_len"] == wl.gamma)
+    assert np.allclose(g["probe"][:, wl.gamma, 2], 1.0)
+    rej = dict(lg, target=lg["target"].copy())
+    x1 = lg["tokens"][:, 1]
+    rej["target"][np.arange(wl.B), 0, x1] = -np.inf
+    g, o, _ = _run(wl, rej, seed=1, offset=0)
+    assert np.all(g["accepted_len"] == 0)
+    assert np.all(g["out_tokens"][:, 0] != x1)
+
+
+def test_failed_requests():
+    wl = workload("chain_7b").scaled(B=5, V=300)
+    lg = logits_inputs(wl, seed=6)
+    lg["target"][1, 2, 7] = np.nan
+    lg["draft"][2, 0, 3] = np.inf
+    lg["temperature"][3] = 0.0
+    lg["tokens"][4, 2] = 300
+    g, o, _ = _run(wl, lg, seed=2, offset=0)
+    assert list(g["accepted_len"][1:]) == [-1, -1, -1, -1]
+    assert g["accepted_len"][0] >= 0
+    assert g["status"] == (1 << 1) | (1 << 5) | (1 << 6)
+    assert np.all(g["out_tokens"][1:] == -1) and np.all(g["path"][1:] == -1)
+
+
+def test_gpu_output_law_chi_square():
+    """10^6 independent requests: the first emitted token follows p."""
+    B, gamma, V = 1_000_000, 3, 8
+    rng = np.random.default_rng(12)
+    z = rng.normal(0, 1.5, V)
+    d = z + rng.normal(0, 1.0, V)
+    q = softmax_rows(d[None], 1.0)[0]
+    p = softmax_rows(z[None], 1.0)[0]
+    M = gamma + 1
+    lg = dict(target=np.broadcast_to(z.astype(np.float32), (B, M, V)),
+              draft=np.broadcast_to(d.astype(np.float32), (B, M, V)),
+              tokens=rng.choice(V, size=(B, M), p=q).astype(np.int32),
+              parent=None, temperature=np.ones(B, dtype=np.float32))
+    wl = workload("tiny_chain").scaled(B=B, gamma=gamma, V=V, dtype="f32")
+    g = gpu_reject(wl, lg, seed=31337, offset=0, probe=False)
+    counts = np.bincount(g["out_tokens"][:, 0], minlength=V)
+    assert stats.chisquare(counts, p * B).pvalue > 1e-3
+    alpha = np.minimum(p, q).sum()
+    first = (g["accepted_len"] >= 1).mean()
+    assert abs(first - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / B)
+    emitted = g["accepted_len"] + 1
+    expect = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(emitted.mean() - expect) < 4 * emitted.std() / np.sqrt(B)

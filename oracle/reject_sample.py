@@ -62,19 +62,26 @@ def row_has_distribution(row: np.ndarray) -> bool:
     return bool(np.isfinite(row).any())
 
 
-def inverse_cdf(weights: np.ndarray, u: float):
+def inverse_cdf(weights: np.ndarray, u: float, tol: float = NEAR):
     """Smallest k with C_k > u * Z (C = running sum of weights, Z = total).
 
-    Returns (k, distance) where distance = min |u - t| over the two CDF
-    thresholds t = C_{k-1}/Z, C_k/Z that bracket u.
+    Returns (k, distance, band): distance = min |u - t| over the two CDF
+    thresholds t = C_{k-1}/Z, C_k/Z that bracket u; band = (k_lo, k_hi), the
+    index range of tokens whose CDF interval meets [u - tol, u + tol] (the
+    tokens any draw within tol of u could select).
     """
-    C = np.cumsum(np.asarray(weights, dtype=np.float64))
+    w = np.asarray(weights, dtype=np.float64)
+    C = np.cumsum(w)
     Z = C[-1]
     k = int(np.searchsorted(C, u * Z, side="right"))
     k = min(k, C.shape[0] - 1)
     lo = C[k - 1] / Z if k > 0 else 0.0
     hi = C[k] / Z
-    return k, min(abs(u - lo), abs(hi - u))
+    k_lo = int(np.searchsorted(C, (u - tol) * Z, side="right"))
+    k_hi = int(np.searchsorted(C, (u + tol) * Z, side="right"))
+    k_lo = min(max(k_lo, 0), C.shape[0] - 1)
+    k_hi = min(max(k_hi, 0), C.shape[0] - 1)
+    return k, min(abs(u - lo), abs(hi - u)), (k_lo, k_hi)
 
 
 class UniformChooser:
@@ -83,17 +90,24 @@ class UniformChooser:
     def __init__(self, u_acc: np.ndarray, u_smp: np.ndarray):
         self.u_acc = u_acc
         self.u_smp = u_smp
-        self.min_margin = np.inf     # smallest |u - threshold| seen
+        self.acc_margin = np.inf     # smallest |u - p/q| over the accept tests
+        self.smp_margin = np.inf     # |u - nearest CDF step| of the draw
+        self.band = None             # tokens a draw within NEAR could select
+
+    @property
+    def min_margin(self):
+        return min(self.acc_margin, self.smp_margin)
 
     def accept(self, node: int, P_x: float, Q_x: float) -> bool:
         u = self.u_acc[node]
         if Q_x > 0.0:
-            self.min_margin = min(self.min_margin, abs(u - P_x / Q_x))
+            self.acc_margin = min(self.acc_margin, abs(u - P_x / Q_x))
         return u * Q_x < P_x
 
     def sample(self, node: int, weights: np.ndarray) -> int:
-        k, dist = inverse_cdf(weights, self.u_smp[node])
-        self.min_margin = min(self.min_margin, dist)
+        k, dist, band = inverse_cdf(weights, self.u_smp[node])
+        self.smp_margin = min(self.smp_margin, dist)
+        self.band = band
         return k
 
 
@@ -181,6 +195,10 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
                  node (Z, probability of the sampled token); -1 elsewhere
       margin     [B] float64: smallest |u - threshold| over the request's
                  decisions (draws closer than 1e-6 are 'near threshold')
+      acc_margin [B] float64: the same over the accept tests only
+      smp_margin [B] float64: the same for the final draw only
+      band       [B, 2] int32: token index range a draw within 1e-6 of u
+                 could have selected (the final draw)
       status     [B] int32: 0, INVALID_ARG, NONFINITE or BAD_TOKEN
     Failed requests (status != 0) keep accepted_len -1 and -1 rows.
     """
@@ -192,6 +210,9 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
     acc = np.full(B, -1, dtype=np.int32)
     probe = np.full((B, M, 4), -1.0, dtype=np.float64)
     margin = np.full(B, np.inf, dtype=np.float64)
+    acc_margin = np.full(B, np.inf, dtype=np.float64)
+    smp_margin = np.full(B, np.inf, dtype=np.float64)
+    band = np.full((B, 2), -1, dtype=np.int32)
     status = np.zeros(B, dtype=np.int32)
     for b in range(B):
         par = None if parent is None else np.asarray(parent[b])
@@ -226,5 +247,9 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
         probe[b, res["final"], 2] = res["Z"]
         probe[b, res["final"], 3] = res["p_sampled"]
         margin[b] = chooser.min_margin
+        acc_margin[b] = chooser.acc_margin
+        smp_margin[b] = chooser.smp_margin
+        band[b] = chooser.band
     return dict(out_tokens=out_tokens, path=path_out, accepted_len=acc,
-                probe=probe, margin=margin, status=status)
+                probe=probe, margin=margin, acc_margin=acc_margin,
+                smp_margin=smp_margin, band=band, status=status)

@@ -42,7 +42,7 @@ def test_inverse_cdf_counts_match_weights():
         G = 1 << 14
         counts = np.zeros(7)
         for i in range(G):
-            k, _ = inverse_cdf(w, (i + 0.5) / G)
+            k, _, _ = inverse_cdf(w, (i + 0.5) / G)
             counts[k] += 1
         assert np.max(np.abs(counts / G - w / w.sum())) <= 2.0 / G
         assert counts[w == 0].sum() == 0
@@ -56,6 +56,11 @@ def test_inverse_cdf_boundary_is_strict():
     assert inverse_cdf(w, 0.999999)[0] == 3
     # zero-mass prefix is skipped even at u = 0
     assert inverse_cdf(np.array([0.0, 0.0, 2.0]), 0.0)[0] == 2
+    # the band holds every token a draw within the tolerance could select
+    k, dist, band = inverse_cdf(w, 0.25, tol=1e-3)
+    assert (k, band) == (1, (0, 1)) and dist == 0.0
+    k, dist, band = inverse_cdf(w, 0.6, tol=1e-3)
+    assert (k, band) == (2, (2, 2)) and abs(dist - 0.1) < 1e-12
 
 
 def test_accept_primitive_rate():

@@ -50,7 +50,7 @@ def attn_sources_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_19_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("attn") or f in ("api.cu", "common.cuh"):
+        if f.startswith("attn") or f in ("api.cu", "common.cuh", "tc_ptx.cuh"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]

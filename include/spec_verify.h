@@ -56,10 +56,18 @@ typedef enum spec_status {
   SPEC_ERR_UNSUPPORTED = 3,   /* shape or dtype this build has no kernel for */
   SPEC_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   SPEC_ERR_NONFINITE = 5,     /* a logits row holds NaN/+inf or only -inf */
-  SPEC_ERR_DEVICE_BOUNDS = 6  /* a block id or token id out of range */
+  SPEC_ERR_DEVICE_BOUNDS = 6, /* a block id or token id out of range */
+  SPEC_ERR_TIMEOUT = 7        /* a device-side wait gave up (bounded, never hangs) */
 } spec_status;
 
 typedef enum spec_dtype { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+
+/* Attention kernel selection (spec_dims.attn_impl). */
+typedef enum spec_attn_impl {
+  SPEC_ATTN_AUTO = 0,          /* tensor cores when group*M >= 16, else CUDA cores */
+  SPEC_ATTN_CUDA_CORES = 1,    /* split-KV on CUDA cores: group*M <= 64, D 64/128, bf16/f32 */
+  SPEC_ATTN_TENSOR_CORES = 2   /* tcgen05 + TMA: bf16, D = 128, group*M <= 128 */
+} spec_attn_impl;
 
 typedef struct spec_dims {
   int32_t B;            /* requests in the batch */
@@ -74,6 +82,7 @@ typedef struct spec_dims {
   int32_t kv_dtype;     /* spec_dtype of q, k_new, v_new, caches and out */
   int32_t logits_dtype; /* spec_dtype of target and draft logits */
   float softmax_scale;  /* attention score scale; 0 selects 1/sqrt(D) */
+  int32_t attn_impl;    /* spec_attn_impl; 0 = automatic choice */
 } spec_dims;
 
 /* Bytes of caller-owned device workspace every call with these dims needs

@@ -11,6 +11,9 @@ plus helpers to size and initialise the caller-owned workspace and to read
 the device status word.
 """
 from ._native import (  # noqa: F401
+    ATTN_AUTO,
+    ATTN_CUDA_CORES,
+    ATTN_TENSOR_CORES,
     EXPORTS,
     LIB_PATH,
     SPEC_BF16,

@@ -38,11 +38,15 @@ WsLayout workspace_layout(const spec_dims& d) {
   };
   L.status_off = take(16);
   L.attn_ok_off = take(sizeof(int32_t) * (size_t)d.B);
+  L.tc_ntiles_off = take(sizeof(int32_t) * (size_t)d.B);
+  L.tc_prefix_off = take(sizeof(int32_t) * ((size_t)d.B + 1));
   const int group = d.Hkv > 0 ? d.Hq / d.Hkv : 0;
   L.rows = group * d.M;
   L.split_keys = attn_split_keys(d);
   L.max_splits = (int)ceil_div64((int64_t)d.max_blocks * kBlock, L.split_keys);
   L.attn_bytes = sizeof(float) * (size_t)d.B * d.Hkv * L.max_splits * L.rows * (d.D + 1);
+  const size_t tc_bytes = d.Hkv > 0 ? sizeof(float) * attn_tc_part_floats(d) : 0;
+  if (tc_bytes > L.attn_bytes) L.attn_bytes = tc_bytes;
   L.attn_off = take(L.attn_bytes);
   L.rs_chunk = rs_chunk_elems(d.logits_dtype);
   L.rs_chunks = (int)ceil_div64(d.V, L.rs_chunk);
@@ -128,7 +132,26 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
       !aligned16(v_cache) || !aligned16(out))
     return SPEC_ERR_INVALID_ARG;
   const int R = (dims->Hq / dims->Hkv) * dims->M;
-  if (R > 64) return SPEC_ERR_UNSUPPORTED;
+  // kernel choice: tensor cores when the rows that share a KV head fill
+  // enough of an M=128 MMA tile, CUDA cores otherwise
+  const bool tc_ok = dims->kv_dtype == SPEC_BF16 && dims->D == 128 && R <= 128 &&
+                     (int64_t)dims->B * dims->Hkv *
+                             ceil_div64((int64_t)dims->max_blocks * kBlock, 64) <
+                         ((int64_t)1 << 31);
+  const bool simt_ok = R <= 64;
+  bool use_tc;
+  if (dims->attn_impl == SPEC_ATTN_TENSOR_CORES) {
+    if (!tc_ok) return SPEC_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else if (dims->attn_impl == SPEC_ATTN_CUDA_CORES) {
+    if (!simt_ok) return SPEC_ERR_UNSUPPORTED;
+    use_tc = false;
+  } else if (dims->attn_impl == SPEC_ATTN_AUTO) {
+    use_tc = tc_ok && (R >= 16 || !simt_ok);
+    if (!use_tc && !simt_ok) return SPEC_ERR_UNSUPPORTED;
+  } else {
+    return SPEC_ERR_INVALID_ARG;
+  }
   const WsLayout lay = workspace_layout(*dims);
   AttnArgs a;
   a.q = q;
@@ -145,7 +168,8 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
   a.scale = dims->softmax_scale != 0.f ? dims->softmax_scale : 1.0f / sqrtf((float)dims->D);
   a.ws = ws;
   int launches = 0;
-  const cudaError_t e = attn_launch_simt(a, lay, static_cast<cudaStream_t>(stream), &launches);
+  const cudaError_t e = use_tc ? attn_launch_tc(a, lay, static_cast<cudaStream_t>(stream), &launches)
+                               : attn_launch_simt(a, lay, static_cast<cudaStream_t>(stream), &launches);
   g_launches = launches;
   return from_cuda(e);
 }
@@ -234,6 +258,7 @@ const char* spec_status_string(int32_t status) {
     case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
     case SPEC_ERR_NONFINITE: return "SPEC_ERR_NONFINITE";
     case SPEC_ERR_DEVICE_BOUNDS: return "SPEC_ERR_DEVICE_BOUNDS";
+    case SPEC_ERR_TIMEOUT: return "SPEC_ERR_TIMEOUT";
     default: return "SPEC_ERR_UNKNOWN";
   }
 }

@@ -328,18 +328,33 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
+cudaError_t kv_append_launch(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
+  const spec_dims& d = a.d;
+  int32_t* req_ok = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + lay.attn_ok_off);
+  uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(a.ws) + lay.status_off);
+  if (d.kv_dtype == SPEC_BF16) {
+    using T = __nv_bfloat16;
+    kv_append_kernel<T><<<d.B, 256, 0, st>>>(
+        static_cast<const T*>(a.k_new), static_cast<const T*>(a.v_new), static_cast<T*>(a.k_cache),
+        static_cast<T*>(a.v_cache), a.block_table, a.ctx_lens, a.parent, d, req_ok, status);
+  } else {
+    kv_append_kernel<float><<<d.B, 256, 0, st>>>(
+        static_cast<const float*>(a.k_new), static_cast<const float*>(a.v_new),
+        static_cast<float*>(a.k_cache), static_cast<float*>(a.v_cache), a.block_table, a.ctx_lens,
+        a.parent, d, req_ok, status);
+  }
+  ++*launches;
+  return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t launch_simt(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
   const spec_dims& d = a.d;
   const int R = (d.Hq / d.Hkv) * d.M;
   int32_t* req_ok = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + lay.attn_ok_off);
   float* part = reinterpret_cast<float*>(static_cast<char*>(a.ws) + lay.attn_off);
-  uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(a.ws) + lay.status_off);
 
-  kv_append_kernel<T><<<d.B, 256, 0, st>>>(
-      static_cast<const T*>(a.k_new), static_cast<const T*>(a.v_new), static_cast<T*>(a.k_cache),
-      static_cast<T*>(a.v_cache), a.block_table, a.ctx_lens, a.parent, d, req_ok, status);
-  ++*launches;
+  kv_append_launch(a, lay, st, launches);
 
   const size_t smem = attn_simt_smem_bytes(R, d.D);
   const dim3 grid(lay.max_splits, d.Hkv, d.B);

@@ -21,7 +21,18 @@ struct AttnArgs {
   void* ws;
 };
 
+// CTAs of the persistent tensor-core kernel never exceed this (partials are
+// sized for it).
+constexpr int kMaxAttnCtas = 512;
+
+// Floats per partial row of the tensor-core path: D outputs, the log2-sum-exp
+// at index D, padded so every row starts on a 16-byte boundary.
+__host__ __device__ constexpr int tc_part_stride(int D) { return D + 4; }
+
 size_t attn_simt_smem_bytes(int R, int D);
+size_t attn_tc_part_floats(const spec_dims& d);
+cudaError_t kv_append_launch(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
 cudaError_t attn_launch_simt(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
+cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
 
 }  // namespace specv

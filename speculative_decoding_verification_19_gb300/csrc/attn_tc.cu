@@ -1,0 +1,590 @@
+// Verify attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// with TMA-staged paged K/V tiles.
+//
+// What is computed is the same as the CUDA-core kernels in attn.cu (page 1
+// §2.1, page 2 §3.3, page 3 tree-attention section): every new row attends
+// to the cached prefix and to its ancestors-or-self among the new rows.
+//
+// Shape of the work.  For one request b and KV head h, the R = group*M query
+// rows that read h are stacked into one M=128 MMA tile (rows past R are zero
+// padding), so every K/V byte is read from HBM once and used by all R rows:
+// arithmetic intensity is R flop/byte, above what CUDA cores can serve at
+// HBM speed for R >= ~16 and far below the tensor-core ridge.  The key axis
+// of all (b, h) pairs is cut into 64-key tiles (4 blocks of 16), and the
+// tiles of the whole batch are split evenly over one persistent CTA per SM;
+// a pair that straddles two CTAs yields two partial results that a small
+// kernel merges by log-sum-exp.
+//
+// Per CTA, warp-specialised:
+//   warp 0      TMA producer: Q of each pair (two 64-column halves) and the
+//               K and V pages of each tile into a 4-stage ring (32 KB/stage)
+//   warp 1      MMA issuer: S = Q K^T into TMEM (double-buffered), then
+//               O += P V with P read back from TMEM (aliasing S)
+//   warps 2..5  softmax: one thread per query row (TMEM lane), mask, exp2,
+//               P written as bf16 into TMEM; O is rescaled in TMEM only when
+//               the running maximum grows by more than 2^8.
+// TMEM: S0 cols [0,64), S1 [64,128), O [128,256).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace specv {
+namespace tc {
+
+constexpr int kTileKeys = 64;
+constexpr int kPages = kTileKeys / kBlock;  // 4
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
+constexpr int kHalfBytes = kPages * kBoxBytes;  // 8 KB
+constexpr int kStageBytes = 4 * kHalfBytes;     // K lo, K hi, V lo, V hi
+constexpr int kQHalfBytes = 128 * 128;          // 128 rows x 128 B
+constexpr int kQBytes = 2 * kQHalfBytes;
+constexpr int kTmemCols = 256;
+constexpr int kOCol = 128;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 2 * kQBytes + sizeof(Bars) + 1024;
+
+size_t smem_bytes() { return kSmemBytes; }
+
+// Position in the flat tile sequence: request b, KV head h, tile of the pair.
+struct Cursor {
+  int b, h, tile, nt;
+  __device__ void seek(int64_t g, const int32_t* ntiles, const int32_t* prefix, int B) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)prefix[mid] <= g) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+    nt = ntiles[b];
+    const int64_t off = g - prefix[b];
+    h = (int)(off / nt);
+    tile = (int)(off % nt);
+  }
+  __device__ void next(const int32_t* ntiles, int B, int Hkv) {
+    if (++tile < nt) return;
+    tile = 0;
+    if (++h < Hkv) return;
+    h = 0;
+    do {
+      ++b;
+    } while (b < B && ntiles[b] == 0);
+    nt = b < B ? ntiles[b] : 0;
+  }
+};
+
+__device__ __forceinline__ int tile_pages(int L, int tile) {
+  const int keys = L - tile * kTileKeys;
+  return keys >= kTileKeys ? kPages : ceil_div(keys, kBlock);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ block_table,
+    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ parent,
+    const int32_t* __restrict__ ntiles, const int32_t* __restrict__ prefix, spec_dims d,
+    float qscale2, float* __restrict__ part, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint8_t* qbufs = smem + kStages * kStageBytes;
+  Bars* bars = reinterpret_cast<Bars*>(qbufs + 2 * kQBytes);
+
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  const int B = d.B, Hkv = d.Hkv, M = d.M;
+  const int group = d.Hq / d.Hkv;
+  const int R = group * M;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int64_t T = prefix[B];
+  const int64_t g0 = (int64_t)c * T / G, g1 = (int64_t)(c + 1) * T / G;
+  if (g0 >= g1) return;  // uniform: nothing allocated yet
+  const int n_sm_warps = ceil_div(R, 32);
+
+  // zero both Q buffers once: rows R..127 stay zero padding
+  for (int i = tid; i < 2 * kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qbufs)[i] = make_uint4(0, 0, 0, 0);
+  ptx::fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->q_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), n_sm_warps);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_q);
+      ptx::prefetch_tmap(&tm_k);
+      ptx::prefetch_tmap(&tm_v);
+      Cursor cu;
+      cu.seek(g0, ntiles, prefix, B);
+      int seg = -1;
+      int64_t t = 0;
+      for (int64_t g = g0; g < g1; ++g, ++t) {
+        const bool first = (g == g0) || cu.tile == 0;
+        if (first) {
+          ++seg;
+          const int qb = seg & 1;
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg >> 1) & 1) ^ 1, abort,
+                              kTimeoutNs))
+            break;
+          const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
+          ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
+          for (int half = 0; half < 2; ++half)
+            ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q, qf,
+                             half * 64, cu.h * group, 0, cu.b);
+        }
+        const int stage = (int)(t % kStages);
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
+                            abort, kTimeoutNs))
+          break;
+        const int L = ctx_lens[cu.b] + M;
+        const int np = tile_pages(L, cu.tile);
+        const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
+        ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * 4u * kBoxBytes);
+        uint8_t* sb = stages + stage * kStageBytes;
+        const int32_t* bt = block_table + (int64_t)cu.b * d.max_blocks + cu.tile * kPages;
+        for (int p = 0; p < np; ++p) {
+          const int blk = bt[p];
+          for (int half = 0; half < 2; ++half) {
+            ptx::tma_load_4d(ptx::smem_u32(sb + half * kHalfBytes + p * kBoxBytes), &tm_k, fb,
+                             half * 64, 0, cu.h, blk);
+            ptx::tma_load_4d(ptx::smem_u32(sb + (2 + half) * kHalfBytes + p * kBoxBytes), &tm_v,
+                             fb, half * 64, 0, cu.h, blk);
+          }
+        }
+        cu.next(ntiles, B, Hkv);
+      }
+      // every load issued must have landed before the CTA may exit
+      const int64_t issued = t;
+      for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
+        ptx::mbar_wait(ptx::smem_u32(&bars->full[u % kStages]), (uint32_t)((u / kStages) & 1),
+                       abort, kTimeoutNs);
+      for (int sg = seg > 0 ? seg - 1 : 0; sg <= seg; ++sg)
+        ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg & 1]), (uint32_t)((sg >> 1) & 1), abort,
+                       kTimeoutNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t id_qk_full = ptx::idesc_bf16_f32(128, kTileKeys, false, false);
+      const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+      Cursor cu;
+      cu.seek(g0, ntiles, prefix, B);
+      int seg = -1;
+      int64_t t = 0;
+      bool have_prev = false;
+      int prev_stage = 0, prev_np = 0, prev_first = 0;
+      bool ok = true;
+      auto issue_pv = [&](int64_t u) -> bool {
+        const int sbuf = (int)(u & 1);
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u >> 1) & 1), abort,
+                            kTimeoutNs))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t vbase = ptx::smem_u32(stages + prev_stage * kStageBytes + 2 * kHalfBytes);
+        for (int j = 0; j < prev_np; ++j) {
+          const uint64_t bdesc = ptx::sdesc_sw128(vbase + j * 2 * 1024, kHalfBytes, 1024);
+          ptx::mma_ts(tmem + kOCol, tmem + sbuf * kTileKeys + j * 8, bdesc, id_pv,
+                      (prev_first && j == 0) ? 0u : 1u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->o_done));
+        ptx::mma_commit(ptx::smem_u32(&bars->empty[prev_stage]));
+        return true;
+      };
+      for (int64_t g = g0; g < g1 && ok; ++g, ++t) {
+        const bool first = (g == g0) || cu.tile == 0;
+        const bool last = (g == g1 - 1) || cu.tile == cu.nt - 1;
+        if (first) ++seg;
+        const int qb = seg & 1;
+        if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), (uint32_t)((seg >> 1) & 1),
+                                     abort, kTimeoutNs))
+          break;
+        const int stage = (int)(t % kStages);
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
+                            abort, kTimeoutNs))
+          break;
+        if (t >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)((t - 2) & 1), abort,
+                                      kTimeoutNs))
+          break;
+        ptx::tc_fence_after();
+        const int L = ctx_lens[cu.b] + M;
+        const int np = tile_pages(L, cu.tile);
+        const uint32_t idqk = np == kPages ? id_qk_full : ptx::idesc_bf16_f32(128, np * 16, false, false);
+        const uint32_t qbase = ptx::smem_u32(qbufs + qb * kQBytes);
+        const uint32_t kbase = ptx::smem_u32(stages + stage * kStageBytes);
+        const int sbuf = (int)(t & 1);
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ad = ptx::sdesc_sw128(qbase + (k >> 2) * kQHalfBytes + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(kbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+          ptx::mma_ss(tmem + sbuf * kTileKeys, ad, bd, idqk, k > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[sbuf]));
+        if (last) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qb]));
+        if (have_prev) ok = issue_pv(t - 1);
+        have_prev = true;
+        prev_stage = stage;
+        prev_np = np;
+        prev_first = first ? 1 : 0;
+        cu.next(ntiles, B, Hkv);
+      }
+      if (ok && have_prev && !*abort) issue_pv(t - 1);
+      // all MMAs issued by this thread complete before TMEM is released
+      ptx::mma_commit(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, abort, kTimeoutNs);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int sp = warp & 3;  // TMEM sub-partition this warp may access
+    const int row = sp * 32 + lane;
+    if (sp < n_sm_warps) {
+      const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+      Cursor cu;
+      cu.seek(g0, ntiles, prefix, B);
+      int64_t t = 0;
+      float m_used = -INFINITY, l = 0.f;
+      unsigned long long anc = 0;
+      int ctx = 0, L = 0;
+      const bool real = row < R;
+      for (int64_t g = g0; g < g1; ++g, ++t) {
+        const bool first = (g == g0) || cu.tile == 0;
+        const bool last = (g == g1 - 1) || cu.tile == cu.nt - 1;
+        if (first) {
+          ctx = ctx_lens[cu.b];
+          L = ctx + M;
+          m_used = -INFINITY;
+          l = 0.f;
+          anc = 0;
+          if (real) {
+            const int i = row / group;
+            if (parent == nullptr) {
+              anc = (i >= 63) ? ~0ull : ((1ull << (i + 1)) - 1);
+            } else {
+              const int32_t* par = parent + (int64_t)cu.b * M;
+              int n = i;
+              for (int step = 0; step <= 64 && n >= 0; ++step) {
+                anc |= 1ull << n;
+                n = par[n];
+              }
+            }
+          }
+        }
+        const int sbuf = (int)(t & 1);
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]), (uint32_t)((t >> 1) & 1), abort,
+                            kTimeoutNs))
+          break;
+        ptx::tc_fence_after();
+        uint32_t s0[32], s1[32];
+        ptx::tmem_ld32(lane_base + sbuf * kTileKeys, s0);
+        ptx::tmem_ld32(lane_base + sbuf * kTileKeys + 32, s1);
+        ptx::tmem_wait_ld();
+        const int kpos0 = cu.tile * kTileKeys;
+        const int nkeys = tile_pages(L, cu.tile) * kBlock;
+        float x[64];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int pos = kpos0 + j;
+          bool vis = real && j < nkeys && pos < L;
+          if (vis && pos >= ctx) vis = (anc >> (pos - ctx)) & 1ull;
+          const float sraw = __uint_as_float(j < 32 ? s0[j] : s1[j - 32]);
+          x[j] = vis ? sraw * qscale2 : -INFINITY;
+          mt = fmaxf(mt, x[j]);
+        }
+        bool need = false;
+        if (first) {
+          m_used = mt;
+        } else if (mt > m_used + 8.0f) {
+          need = true;
+        }
+        // PV(t-1) must be complete before O is touched (and keeps the
+        // o_done phase this warp tracks within one of the barrier's)
+        if (t >= 1 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)((t - 1) & 1), abort,
+                                      kTimeoutNs))
+          break;
+        if (__any_sync(0xffffffffu, need)) {
+          ptx::tc_fence_after();
+          const float f = need ? exp2f(m_used - mt) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            ptx::tmem_ld32(lane_base + kOCol + cc * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+            ptx::tmem_st32(lane_base + kOCol + cc * 32, o);
+          }
+          ptx::tmem_wait_st();
+          if (need) {
+            l *= f;
+            m_used = mt;
+          }
+        }
+        uint32_t pk[32];
+        float lsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float a = (x[2 * j] == -INFINITY) ? 0.f : exp2f(x[2 * j] - m_used);
+          const float b2 = (x[2 * j + 1] == -INFINITY) ? 0.f : exp2f(x[2 * j + 1] - m_used);
+          lsum += a + b2;
+          pk[j] = ptx::pack_bf16x2(a, b2);
+        }
+        l += lsum;
+        ptx::tmem_st32(lane_base + sbuf * kTileKeys, pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sbuf]));
+        if (last) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)(t & 1), abort, kTimeoutNs))
+            break;
+          ptx::tc_fence_after();
+          const int64_t slot = (int64_t)cu.b * Hkv + cu.h + c;
+          float* prow = part + (slot * R + (real ? row : 0)) * (int64_t)tc_part_stride(d.D);
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            ptx::tmem_ld32(lane_base + kOCol + cc * 32, o);
+            ptx::tmem_wait_ld();
+            if (real) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                float4 v = make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                       __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                *reinterpret_cast<float4*>(prow + cc * 32 + j) = v;
+              }
+            }
+          }
+          if (real) prow[d.D] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+          ptx::tc_fence_before();
+        }
+        cu.next(ntiles, B, Hkv);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0 && *abort) raise_status(status, SPEC_ERR_TIMEOUT);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// plan: tiles per request and their exclusive prefix over (request, head)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) attn_plan_kernel(const int32_t* __restrict__ ctx_lens,
+                                                         const int32_t* __restrict__ req_ok,
+                                                         spec_dims d, int32_t* __restrict__ ntiles,
+                                                         int32_t* __restrict__ prefix) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < d.B; base += 1024) {
+    const int b = base + tid;
+    int nt = 0;
+    if (b < d.B && req_ok[b]) nt = ceil_div(ctx_lens[b] + d.M, kTileKeys);
+    if (b < d.B) ntiles[b] = nt;
+    int v = nt * d.Hkv;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int wpre = 0;
+    for (int i = 0; i < warp; ++i) wpre += warp_tot[i];
+    const int c0 = carry;
+    if (b < d.B) prefix[b] = c0 + wpre + incl - v;
+    __syncthreads();
+    if (tid == 1023) carry = c0 + wpre + incl;
+    __syncthreads();
+  }
+  if (tid == 0) prefix[d.B] = carry;
+}
+
+// ---------------------------------------------------------------------------
+// merge of the partials of each (request, KV head)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(128) attn_tc_combine_kernel(
+    const float* __restrict__ part, const int32_t* __restrict__ ntiles,
+    const int32_t* __restrict__ prefix, spec_dims d, int G, T* __restrict__ out,
+    float* __restrict__ lse) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int group = d.Hq / d.Hkv;
+  const int R = group * d.M;
+  const int D = d.D;
+  const int64_t Ttot = prefix[d.B];
+  const int nt = ntiles[b];
+  int c_first = 1, c_last = 0;
+  if (nt > 0) {
+    const int64_t ps = (int64_t)prefix[b] + (int64_t)h * nt, pe = ps + nt;
+    c_first = (int)(((ps + 1) * G - 1) / Ttot);
+    c_last = (int)((pe * G - 1) / Ttot);
+  }
+  const int64_t pair = (int64_t)b * d.Hkv + h;
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  for (int r = warp; r < R; r += blockDim.x / kWarp) {
+    const int i = r / group, hq = h * group + r % group;
+    // CTAs with an empty tile range wrote nothing (their slot may belong to
+    // a neighbouring pair), so they are skipped
+    float m = -INFINITY;
+    for (int cc = c_first; cc <= c_last; ++cc) {
+      if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
+      m = fmaxf(m, part[((pair + cc) * R + r) * (int64_t)tc_part_stride(D) + D]);
+    }
+    float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (m != -INFINITY) {
+      for (int cc = c_first; cc <= c_last; ++cc) {
+        if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
+        const float* prow = part + ((pair + cc) * R + r) * (int64_t)tc_part_stride(D);
+        const float ls = prow[D];
+        if (ls == -INFINITY) continue;
+        const float w = exp2f(ls - m);
+        wsum += w;
+        for (int k = 0; k < D / kWarp; ++k) acc[k] += w * prow[lane + k * kWarp];
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    T* orow = out + (((int64_t)b * d.M + i) * d.Hq + hq) * D;
+    for (int k = 0; k < D / kWarp; ++k) orow[lane + k * kWarp] = from_f32<T>(acc[k] * inv);
+    if (lse != nullptr && lane == 0)
+      lse[((int64_t)b * d.M + i) * d.Hq + hq] =
+          wsum > 0.f ? (m + log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4],
+                     const cuuint64_t strides[3], const cuuint32_t box[4]) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+size_t attn_tc_part_floats(const spec_dims& d) {
+  const int R = (d.Hq / d.Hkv) * d.M;
+  return ((size_t)d.B * d.Hkv + kMaxAttnCtas) * R * tc_part_stride(d.D);
+}
+
+cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
+  using namespace tc;
+  const spec_dims& d = a.d;
+  const int group = d.Hq / d.Hkv;
+  char* ws = static_cast<char*>(a.ws);
+  int32_t* req_ok = reinterpret_cast<int32_t*>(ws + lay.attn_ok_off);
+  int32_t* ntiles = reinterpret_cast<int32_t*>(ws + lay.tc_ntiles_off);
+  int32_t* prefix = reinterpret_cast<int32_t*>(ws + lay.tc_prefix_off);
+  float* part = reinterpret_cast<float*>(ws + lay.attn_off);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)d.D, (cuuint64_t)d.Hq, (cuuint64_t)d.M, (cuuint64_t)d.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d.D * 2, (cuuint64_t)d.Hq * d.D * 2,
+                                   (cuuint64_t)d.M * d.Hq * d.D * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)d.M, 1};
+    if (!make_map(&tm_q, a.q, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)d.D, (cuuint64_t)kBlock, (cuuint64_t)d.Hkv,
+                                (cuuint64_t)d.num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)d.D * 2, (cuuint64_t)kBlock * d.D * 2,
+                                   (cuuint64_t)d.Hkv * kBlock * d.D * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kBlock, 1, 1};
+    if (!make_map(&tm_k, a.k_cache, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map(&tm_v, a.v_cache, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int G = sms < kMaxAttnCtas ? sms : kMaxAttnCtas;
+
+  kv_append_launch(a, lay, st, launches);
+  attn_plan_kernel<<<1, 1024, 0, st>>>(a.ctx_lens, req_ok, d, ntiles, prefix);
+  ++*launches;
+  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const float qscale2 = a.scale * 1.4426950408889634f;
+  attn_tc_kernel<<<G, kThreads, kSmemBytes, st>>>(tm_q, tm_k, tm_v, a.block_table, a.ctx_lens,
+                                                   a.parent, ntiles, prefix, d, qscale2, part,
+                                                   status);
+  ++*launches;
+  attn_tc_combine_kernel<__nv_bfloat16><<<dim3(d.Hkv, d.B), 128, 0, st>>>(
+      part, ntiles, prefix, d, G, static_cast<__nv_bfloat16*>(a.out), a.lse);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace specv

@@ -81,7 +81,9 @@ __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { r
 struct WsLayout {
   size_t status_off;      // uint32 status word
   size_t attn_ok_off;     // [B] int32 per-request verdict of the append
-  size_t attn_off;        // split-KV partials: [B, Hkv, max_splits, R, D+1] f32
+  size_t tc_ntiles_off;   // [B] int32 64-key tiles per (request, head)
+  size_t tc_prefix_off;   // [B+1] int32 exclusive prefix of tiles over (request, head)
+  size_t attn_off;        // split-KV partials of either attention path (f32)
   size_t attn_bytes;
   int split_keys;         // keys per split (multiple of 16)
   int max_splits;

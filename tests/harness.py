@@ -23,11 +23,22 @@ def to_dev(x, dt, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(x)).to(device=dev, dtype=dt)
 
 
-def dims_for(wl, B, max_blocks=1, num_blocks=1, V=None):
+def dims_for(wl, B, max_blocks=1, num_blocks=1, V=None, impl=0):
     return sv.make_dims(B=B, M=wl.M, Hq=wl.Hq, Hkv=wl.Hkv, D=wl.D,
                         max_blocks=max_blocks, num_blocks=num_blocks,
                         V=wl.V if V is None else V, kv_dtype=tdtype(wl),
-                        logits_dtype=tdtype(wl))
+                        logits_dtype=tdtype(wl), attn_impl=impl)
+
+
+def impls_for(wl):
+    """Attention kernels that support this shape (CUDA cores, tensor cores)."""
+    R = (wl.Hq // wl.Hkv) * wl.M
+    out = []
+    if R <= 64:
+        out.append(sv.ATTN_CUDA_CORES)
+    if wl.dtype == "bf16" and wl.D == 128 and R <= 128:
+        out.append(sv.ATTN_TENSOR_CORES)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -102,11 +113,11 @@ def compare_reject(g, o):
 # attention
 # ---------------------------------------------------------------------------
 
-def gpu_attn(wl, kv, parent=None, dims=None, ws=None):
+def gpu_attn(wl, kv, parent=None, dims=None, ws=None, impl=0):
     """kv: host dict from synth.kv_inputs_host.  Returns numpy outputs."""
     dt = tdtype(wl)
     B = kv["block_table"].shape[0]
-    dims = dims or dims_for(wl, B, kv["max_blocks"], kv["num_blocks"])
+    dims = dims or dims_for(wl, B, kv["max_blocks"], kv["num_blocks"], impl=impl)
     ws = sv.workspace(dims) if ws is None else ws
     q = to_dev(kv["q"], dt)
     kn = to_dev(kv["k_new"], dt)

@@ -2,9 +2,11 @@
 
 Outputs within 2e-2 absolute + 1e-2 relative of the fp64 oracle, log-sum-exp
 within 1e-3; the appended cache bit-exact (new rows at ctx..ctx+M-1, rest of
-the last block zero, everything else untouched).  Covers chains and trees,
-GQA groups 1/4/8, fp32 and bf16, contexts that are empty, ragged or cross a
-block boundary, long contexts, and the device-side failure paths.
+the last block zero, everything else untouched).  Every case runs on each
+kernel that supports its shape (CUDA cores; tcgen05 tensor cores).  Covers
+chains and trees, GQA groups 1/4/8, fp32 and bf16, contexts that are empty,
+ragged or cross a block boundary, long contexts, rows per KV head from 1 to
+128, more CTAs than tiles, and the device-side failure paths.
 """
 import numpy as np
 import pytest
@@ -15,19 +17,20 @@ pytestmark = [pytest.mark.gpu,
 
 import speculative_decoding_verification_19_gb300 as sv  # noqa: E402
 from harness import (assert_attn_close, dims_for, gpu_attn,  # noqa: E402
-                     oracle_attn)
-from oracle import oracle_kv_append  # noqa: E402
+                     impls_for, oracle_attn)
 from synth import kv_inputs_host, logits_inputs, workload  # noqa: E402
 
 
-def _check(wl, kv, parent=None):
-    g = gpu_attn(wl, kv, parent)
+def _check(wl, kv, parent=None, impls=None):
     o_out, o_lse, o_kc, o_vc = oracle_attn(wl, kv, parent)
-    assert g["status"] == 0
-    assert_attn_close(g["out"], o_out, g["lse"], o_lse)
-    assert np.array_equal(g["k_cache"], o_kc.astype(np.float32))
-    assert np.array_equal(g["v_cache"], o_vc.astype(np.float32))
-    return g
+    impls = impls_for(wl) if impls is None else impls
+    assert impls
+    for impl in impls:
+        g = gpu_attn(wl, kv, parent, impl=impl)
+        assert g["status"] == 0, impl
+        assert_attn_close(g["out"], o_out, g["lse"], o_lse)
+        assert np.array_equal(g["k_cache"], o_kc.astype(np.float32)), impl
+        assert np.array_equal(g["v_cache"], o_vc.astype(np.float32)), impl
 
 
 def test_tiny_chain_full():
@@ -56,10 +59,24 @@ def test_ragged_contexts(ctx, dtype):
     _check(wl, kv_inputs_host(wl, seed=3, B=len(ctx), ctx=np.array(ctx)))
 
 
-@pytest.mark.parametrize("Hq,Hkv,gamma", [(8, 8, 0), (8, 2, 7), (16, 2, 7), (4, 1, 15)])
+@pytest.mark.parametrize("Hq,Hkv,gamma", [(8, 8, 0), (8, 2, 7), (16, 2, 7), (4, 1, 15),
+                                          (16, 1, 7), (32, 2, 7)])
 def test_group_shapes(Hq, Hkv, gamma):
     wl = workload("chain_7b").scaled(Hq=Hq, Hkv=Hkv, gamma=gamma)
     _check(wl, kv_inputs_host(wl, seed=4, B=2, ctx=np.array([77, 300])))
+
+
+def test_more_ctas_than_tiles():
+    # a handful of 64-key tiles spread over one CTA per SM
+    wl = workload("chain_gqa_128k").scaled(Hq=8, Hkv=2)
+    _check(wl, kv_inputs_host(wl, seed=11, B=3, ctx=np.array([0, 60, 130])))
+
+
+def test_tree_rows_up_to_128():
+    wl = workload("tree_64").scaled(Hq=4, Hkv=2, tree_nodes=64, tree_width=4)
+    kv = kv_inputs_host(wl, seed=12, B=2, ctx=np.array([200, 1999]))
+    parent = logits_inputs(wl.scaled(V=16), seed=12, B=2)["parent"]
+    _check(wl, kv, parent, impls=[sv.ATTN_TENSOR_CORES])
 
 
 def test_small_head_dim_tree():
@@ -69,7 +86,8 @@ def test_small_head_dim_tree():
     _check(wl, kv, parent)
 
 
-def test_capacity_and_bad_block():
+@pytest.mark.parametrize("impl", [sv.ATTN_CUDA_CORES, sv.ATTN_TENSOR_CORES])
+def test_capacity_and_bad_block(impl):
     wl = workload("chain_7b").scaled(Hq=4, Hkv=4, gamma=3)
     kv = kv_inputs_host(wl, seed=6, B=3, ctx=np.array([20, 40, 60]))
     kv["ctx_lens"] = kv["ctx_lens"].copy()
@@ -78,7 +96,7 @@ def test_capacity_and_bad_block():
     kv["ctx_lens"][1] = kv["max_blocks"] * 16 - 2
     # request 2 points one of its blocks outside the cache
     kv["block_table"][2, 1] = kv["num_blocks"] + 5
-    g = gpu_attn(wl, kv)
+    g = gpu_attn(wl, kv, impl=impl)
     assert g["status"] == (1 << 2) | (1 << 6)
     assert np.all(g["out"][1:] == 0) and np.all(np.isneginf(g["lse"][1:]))
     # request 0 is unaffected; failed requests leave the cache untouched
@@ -107,4 +125,13 @@ def test_host_validation():
         sv.spec_verify_attn(t, kvn, kvn, cache, cache, bt, ctx, None, t, None, dims,
                             ws[: ws.numel() // 2])
     assert e.value.code == 1
+    # a shape no kernel supports: 200 rows per KV head
+    big = sv.make_dims(B=1, M=25, Hq=8, Hkv=1, D=128, max_blocks=4, num_blocks=4)
+    ws2 = sv.workspace(big)
+    q2 = torch.zeros(1, 25, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kv2 = torch.zeros(1, 25, 1, 128, dtype=torch.bfloat16, device="cuda")
+    c2 = torch.zeros(4, 1, 16, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sv.SpecError) as e:
+        sv.spec_verify_attn(q2, kv2, kv2, c2, c2, bt, ctx, None, q2, None, big, ws2)
+    assert e.value.code == 3
     assert sv.device_status(ws) == 0

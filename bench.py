@@ -457,11 +457,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests per step (default: the workload's batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed steps
     from synth import workload
     wl = workload(args.workload)
+    if args.batch is not None:
+        wl = wl.scaled(B=args.batch)
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, world, rank)

@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_split_kernel(
       const float mnew = fmaxf(mrow[j], warp_max(sj));
       float p = 0.f, corr = 1.f;
       if (mnew != -INFINITY) {
-        p = exp2f(sj - mnew);
+        p = fast_exp2(sj - mnew);
         corr = exp2f(mrow[j] - mnew);
       }
       lrow[j] = lrow[j] * corr + warp_sum(p);

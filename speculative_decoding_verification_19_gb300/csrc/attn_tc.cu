@@ -16,13 +16,15 @@
 // kernel merges by log-sum-exp.
 //
 // Per CTA, warp-specialised:
-//   warp 0      TMA producer: Q of each pair (two 64-column halves) and the
+//   warp 6      TMA producer: Q of each pair (two 64-column halves) and the
 //               K and V pages of each tile into a 4-stage ring (32 KB/stage)
-//   warp 1      MMA issuer: S = Q K^T into TMEM (double-buffered), then
+//   warp 7      MMA issuer: S = Q K^T into TMEM (double-buffered), then
 //               O += P V with P read back from TMEM (aliasing S)
-//   warps 2..5  softmax: one thread per query row (TMEM lane), mask, exp2,
+//   warps 0..3  softmax: one thread per query row (TMEM lane), mask, exp2,
 //               P written as bf16 into TMEM; O is rescaled in TMEM only when
-//               the running maximum grows by more than 2^8.
+//               the running maximum grows by more than 2^8
+//   warps 4, 5  idle (they keep the two issuing roles off the sub-partitions
+//               of the softmax warps for rows 0..63).
 // TMEM: S0 cols [0,64), S1 [64,128), O [128,256).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -38,7 +40,13 @@ namespace tc {
 constexpr int kTileKeys = 64;
 constexpr int kPages = kTileKeys / kBlock;  // 4
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+// Warp roles.  A warp may only touch the TMEM lanes of its sub-partition
+// (warp % 4), so the softmax warps are 0..3 (lanes 32w..32w+31); the
+// producer and the MMA issuer sit on sub-partitions 2 and 3, away from the
+// softmax warps that own rows 0..63 (the common case R <= 64).
+constexpr int kProducerWarp = 6;
+constexpr int kMmaWarp = 7;
 constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
 constexpr int kHalfBytes = kPages * kBoxBytes;  // 8 KB
 constexpr int kStageBytes = 4 * kHalfBytes;     // K lo, K hi, V lo, V hi
@@ -46,7 +54,7 @@ constexpr int kQHalfBytes = 128 * 128;          // 128 rows x 128 B
 constexpr int kQBytes = 2 * kQHalfBytes;
 constexpr int kTmemCols = 256;
 constexpr int kOCol = 128;
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
 
 struct __align__(8) Bars {
   uint64_t full[kStages];
@@ -55,7 +63,7 @@ struct __align__(8) Bars {
   uint64_t q_empty[2];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t o_done[2];  // completion of PV(t) lands on o_done[t & 1]
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -92,6 +100,20 @@ struct Cursor {
     nt = b < B ? ntiles[b] : 0;
   }
 };
+
+// Scaled score of tile column j (log2 units) or -inf where the key is not
+// visible to this row: past the tile's valid keys or the request's length,
+// or a new position that is not an ancestor-or-self of the row's node.
+__device__ __forceinline__ float score_of(uint32_t sbits, int j, int kpos0, int nkeys, int ctx,
+                                          int L, unsigned long long anc, bool real, bool plain,
+                                          float qscale2) {
+  const float x = __uint_as_float(sbits) * qscale2;
+  if (plain) return real ? x : -INFINITY;
+  const int pos = kpos0 + j;
+  bool vis = real && j < nkeys && pos < L;
+  if (vis && pos >= ctx) vis = (anc >> (pos - ctx)) & 1ull;
+  return vis ? x : -INFINITY;
+}
 
 __device__ __forceinline__ int tile_pages(int L, int tile) {
   const int keys = L - tile * kTileKeys;
@@ -136,12 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), n_sm_warps);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->o_done[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->o_done[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -151,53 +174,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA
+    // The whole warp walks the tiles; lane j holds the four block ids of
+    // tile (window start + j), fetched for 32 tiles at once, and lane 0
+    // issues the barrier operations and the copies.
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_q);
       ptx::prefetch_tmap(&tm_k);
       ptx::prefetch_tmap(&tm_v);
-      Cursor cu;
-      cu.seek(g0, ntiles, prefix, B);
-      int seg = -1;
-      int64_t t = 0;
-      for (int64_t g = g0; g < g1; ++g, ++t) {
-        const bool first = (g == g0) || cu.tile == 0;
-        if (first) {
-          ++seg;
+    }
+    Cursor cu;
+    cu.seek(g0, ntiles, prefix, B);
+    int seg = -1, L = 0, win = -1;
+    int ids[kPages] = {0, 0, 0, 0};
+    int64_t t = 0;
+    bool ok = true;
+    for (int64_t g = g0; g < g1 && ok; ++g, ++t) {
+      const bool first = (g == g0) || cu.tile == 0;
+      if (first) {
+        ++seg;
+        L = ctx_lens[cu.b] + M;
+        win = -1;
+        if (lane == 0) {
           const int qb = seg & 1;
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg >> 1) & 1) ^ 1, abort,
-                              kTimeoutNs))
-            break;
-          const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
-          ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
-          for (int half = 0; half < 2; ++half)
-            ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q, qf,
-                             half * 64, cu.h * group, 0, cu.b);
-        }
-        const int stage = (int)(t % kStages);
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
-                            abort, kTimeoutNs))
-          break;
-        const int L = ctx_lens[cu.b] + M;
-        const int np = tile_pages(L, cu.tile);
-        const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
-        ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * 4u * kBoxBytes);
-        uint8_t* sb = stages + stage * kStageBytes;
-        const int32_t* bt = block_table + (int64_t)cu.b * d.max_blocks + cu.tile * kPages;
-        for (int p = 0; p < np; ++p) {
-          const int blk = bt[p];
-          for (int half = 0; half < 2; ++half) {
-            ptx::tma_load_4d(ptx::smem_u32(sb + half * kHalfBytes + p * kBoxBytes), &tm_k, fb,
-                             half * 64, 0, cu.h, blk);
-            ptx::tma_load_4d(ptx::smem_u32(sb + (2 + half) * kHalfBytes + p * kBoxBytes), &tm_v,
-                             fb, half * 64, 0, cu.h, blk);
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg >> 1) & 1) ^ 1, abort,
+                              kTimeoutNs);
+          if (ok) {
+            const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
+            ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
+            for (int half = 0; half < 2; ++half)
+              ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q,
+                               qf, half * 64, cu.h * group, 0, cu.b);
           }
         }
-        cu.next(ntiles, B, Hkv);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
+      if ((cu.tile >> 5) != win) {  // next window of 32 tiles of this pair
+        win = cu.tile >> 5;
+        const int page0 = ((win << 5) + lane) * kPages;
+        const int32_t* bt = block_table + (int64_t)cu.b * d.max_blocks;
+#pragma unroll
+        for (int p = 0; p < kPages; ++p)
+          ids[p] = (page0 + p < d.max_blocks) ? bt[page0 + p] : 0;
+      }
+      const int np = tile_pages(L, cu.tile);
+      const int src = cu.tile & 31;
+      int blk[kPages];
+#pragma unroll
+      for (int p = 0; p < kPages; ++p) blk[p] = __shfl_sync(0xffffffffu, ids[p], src);
+      const int stage = (int)(t % kStages);
+      if (lane == 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
+                            abort, kTimeoutNs);
+        if (ok) {
+          const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * 4u * kBoxBytes);
+          uint8_t* sb = stages + stage * kStageBytes;
+#pragma unroll
+          for (int p = 0; p < kPages; ++p) {
+            if (p < np) {
+              for (int half = 0; half < 2; ++half) {
+                ptx::tma_load_4d(ptx::smem_u32(sb + half * kHalfBytes + p * kBoxBytes), &tm_k, fb,
+                                 half * 64, 0, cu.h, blk[p]);
+                ptx::tma_load_4d(ptx::smem_u32(sb + (2 + half) * kHalfBytes + p * kBoxBytes),
+                                 &tm_v, fb, half * 64, 0, cu.h, blk[p]);
+              }
+            }
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      cu.next(ntiles, B, Hkv);
+    }
+    if (lane == 0) {
       // every load issued must have landed before the CTA may exit
-      const int64_t issued = t;
+      const int64_t issued = t;  // a broken loop did not issue tile t
       for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
         ptx::mbar_wait(ptx::smem_u32(&bars->full[u % kStages]), (uint32_t)((u / kStages) & 1),
                        abort, kTimeoutNs);
@@ -205,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg & 1]), (uint32_t)((sg >> 1) & 1), abort,
                        kTimeoutNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       const uint32_t id_qk_full = ptx::idesc_bf16_f32(128, kTileKeys, false, false);
@@ -215,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       int seg = -1;
       int64_t t = 0;
       bool have_prev = false;
-      int prev_stage = 0, prev_np = 0, prev_first = 0;
+      int prev_stage = 0, prev_np = 0, prev_first = 0, L = 0;
       bool ok = true;
       auto issue_pv = [&](int64_t u) -> bool {
         const int sbuf = (int)(u & 1);
@@ -229,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           ptx::mma_ts(tmem + kOCol, tmem + sbuf * kTileKeys + j * 8, bdesc, id_pv,
                       (prev_first && j == 0) ? 0u : 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->o_done));
+        ptx::mma_commit(ptx::smem_u32(&bars->o_done[u & 1]));
         ptx::mma_commit(ptx::smem_u32(&bars->empty[prev_stage]));
         return true;
       };
@@ -245,11 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
                             abort, kTimeoutNs))
           break;
-        if (t >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)((t - 2) & 1), abort,
-                                      kTimeoutNs))
+        // PV(t-2) read P out of the S buffer this tile's QK writes
+        if (t >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t & 1]),
+                                      (uint32_t)(((t - 2) >> 1) & 1), abort, kTimeoutNs))
           break;
         ptx::tc_fence_after();
-        const int L = ctx_lens[cu.b] + M;
+        if (first) L = ctx_lens[cu.b] + M;
         const int np = tile_pages(L, cu.tile);
         const uint32_t idqk = np == kPages ? id_qk_full : ptx::idesc_bf16_f32(128, np * 16, false, false);
         const uint32_t qbase = ptx::smem_u32(qbufs + qb * kQBytes);
@@ -274,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, abort, kTimeoutNs);
     }
-  } else {
+  } else if (warp < 4) {
     // -------------------------------------------------------------- softmax
-    const int sp = warp & 3;  // TMEM sub-partition this warp may access
+    const int sp = warp;  // TMEM sub-partition this warp may access
     const int row = sp * 32 + lane;
     if (sp < n_sm_warps) {
       const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
@@ -315,22 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                             kTimeoutNs))
           break;
         ptx::tc_fence_after();
-        uint32_t s0[32], s1[32];
-        ptx::tmem_ld32(lane_base + sbuf * kTileKeys, s0);
-        ptx::tmem_ld32(lane_base + sbuf * kTileKeys + 32, s1);
-        ptx::tmem_wait_ld();
         const int kpos0 = cu.tile * kTileKeys;
         const int nkeys = tile_pages(L, cu.tile) * kBlock;
-        float x[64];
+        // tiles wholly inside the cached prefix need no mask
+        const bool plain = kpos0 + kTileKeys <= ctx && nkeys == kTileKeys;
+        const uint32_t scol = lane_base + sbuf * kTileKeys;
+        // pass 1: masked, scaled scores -> tile maximum (16 TMEM columns at a time)
         float mt = -INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
+          uint32_t sv[16];
+          ptx::tmem_ld16(scol + c0, sv);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int pos = kpos0 + j;
-          bool vis = real && j < nkeys && pos < L;
-          if (vis && pos >= ctx) vis = (anc >> (pos - ctx)) & 1ull;
-          const float sraw = __uint_as_float(j < 32 ? s0[j] : s1[j - 32]);
-          x[j] = vis ? sraw * qscale2 : -INFINITY;
-          mt = fmaxf(mt, x[j]);
+          for (int j = 0; j < 16; ++j) {
+            const float x = score_of(sv[j], c0 + j, kpos0, nkeys, ctx, L, anc, real, plain, qscale2);
+            mt = fmaxf(mt, x);
+          }
         }
         bool need = false;
         if (first) {
@@ -338,12 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         } else if (mt > m_used + 8.0f) {
           need = true;
         }
-        // PV(t-1) must be complete before O is touched (and keeps the
-        // o_done phase this warp tracks within one of the barrier's)
-        if (t >= 1 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)((t - 1) & 1), abort,
-                                      kTimeoutNs))
-          break;
         if (__any_sync(0xffffffffu, need)) {
+          // O is rescaled in place: PV(t-1) must have landed
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) & 1]),
+                              (uint32_t)(((t - 1) >> 1) & 1), abort, kTimeoutNs))
+            break;
           ptx::tc_fence_after();
           const float f = need ? exp2f(m_used - mt) : 1.f;
 #pragma unroll 1
@@ -361,23 +416,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             m_used = mt;
           }
         }
-        uint32_t pk[32];
+        // pass 2: probabilities, packed to bf16 pairs over the S columns
+        // already consumed (keys c0..c0+15 -> P columns c0/2..c0/2+7)
         float lsum = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
+          uint32_t sv[16];
+          ptx::tmem_ld16(scol + c0, sv);
+          ptx::tmem_wait_ld();
+          uint32_t pk[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float a = (x[2 * j] == -INFINITY) ? 0.f : exp2f(x[2 * j] - m_used);
-          const float b2 = (x[2 * j + 1] == -INFINITY) ? 0.f : exp2f(x[2 * j + 1] - m_used);
-          lsum += a + b2;
-          pk[j] = ptx::pack_bf16x2(a, b2);
+          for (int j = 0; j < 8; ++j) {
+            const float xa = score_of(sv[2 * j], c0 + 2 * j, kpos0, nkeys, ctx, L, anc, real, plain,
+                                      qscale2);
+            const float xb = score_of(sv[2 * j + 1], c0 + 2 * j + 1, kpos0, nkeys, ctx, L, anc, real,
+                                      plain, qscale2);
+            const float pa = xa == -INFINITY ? 0.f : fast_exp2(xa - m_used);
+            const float pb = xb == -INFINITY ? 0.f : fast_exp2(xb - m_used);
+            lsum += pa + pb;
+            pk[j] = ptx::pack_bf16x2(pa, pb);
+          }
+          ptx::tmem_st8(scol + (c0 >> 1), pk);
         }
         l += lsum;
-        ptx::tmem_st32(lane_base + sbuf * kTileKeys, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sbuf]));
         if (last) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done), (uint32_t)(t & 1), abort, kTimeoutNs))
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t & 1]), (uint32_t)((t >> 1) & 1), abort,
+                              kTimeoutNs))
             break;
           ptx::tc_fence_after();
           const int64_t slot = (int64_t)cu.b * Hkv + cu.h + c;
@@ -407,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 
   __syncthreads();
   if (tid == 0 && *abort) raise_status(status, SPEC_ERR_TIMEOUT);
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }

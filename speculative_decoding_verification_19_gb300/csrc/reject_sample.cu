@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
 #pragma unroll
     for (int v = 0; v < kRsVecs; ++v)
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) st += exp2f((f[v][i] - mc) * cs);
+      for (int i = 0; i < EPV; ++i) st += fast_exp2((f[v][i] - mc) * cs);
   }
   double sd = warp_sum((double)st);
   if (tid % kWarp == 0) s_sum[tid / kWarp] = sd;
@@ -146,9 +146,9 @@ struct DecideCtx {
 //   nrej >= 1:  max(0, P_{nrej-1} - q)                  (unnormalised residual)
 // with P_0 = p and P_j = max(0, P_{j-1} - q) / Z_j.
 __device__ __forceinline__ float weight_of(float zt, float zd, const DecideCtx& c, int nrej) {
-  const float et = exp2f((zt - c.mT) * c.cs);
+  const float et = fast_exp2((zt - c.mT) * c.cs);
   if (nrej == 0) return et;
-  const float qv = exp2f((zd - c.mD) * c.cs) * c.invSD;
+  const float qv = fast_exp2((zd - c.mD) * c.cs) * c.invSD;
   float P = et * c.invST;
   for (int j = 1; j < nrej; ++j) P = fmaxf(P - qv, 0.f) * c.invZ[j];
   return fmaxf(P - qv, 0.f);

@@ -64,7 +64,7 @@ typedef enum spec_dtype { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 
 /* Attention kernel selection (spec_dims.attn_impl). */
 typedef enum spec_attn_impl {
-  SPEC_ATTN_AUTO = 0,          /* tensor cores when group*M >= 16, else CUDA cores */
+  SPEC_ATTN_AUTO = 0,          /* tensor cores when the shape allows, else CUDA cores */
   SPEC_ATTN_CUDA_CORES = 1,    /* split-KV on CUDA cores: group*M <= 64, D 64/128, bf16/f32 */
   SPEC_ATTN_TENSOR_CORES = 2   /* tcgen05 + TMA: bf16, D = 128, group*M <= 128 */
 } spec_attn_impl;

@@ -132,8 +132,9 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
       !aligned16(v_cache) || !aligned16(out))
     return SPEC_ERR_INVALID_ARG;
   const int R = (dims->Hq / dims->Hkv) * dims->M;
-  // kernel choice: tensor cores when the rows that share a KV head fill
-  // enough of an M=128 MMA tile, CUDA cores otherwise
+  // kernel choice: the tensor-core kernel whenever it supports the shape
+  // (bf16, D = 128, up to 128 rows per KV head): even a few rows per KV head
+  // run faster there than on CUDA cores; CUDA cores otherwise
   const bool tc_ok = dims->kv_dtype == SPEC_BF16 && dims->D == 128 && R <= 128 &&
                      (int64_t)dims->B * dims->Hkv *
                              ceil_div64((int64_t)dims->max_blocks * kBlock, 64) <
@@ -147,7 +148,7 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
     if (!simt_ok) return SPEC_ERR_UNSUPPORTED;
     use_tc = false;
   } else if (dims->attn_impl == SPEC_ATTN_AUTO) {
-    use_tc = tc_ok && (R >= 16 || !simt_ok);
+    use_tc = tc_ok;
     if (!use_tc && !simt_ok) return SPEC_ERR_UNSUPPORTED;
   } else {
     return SPEC_ERR_INVALID_ARG;

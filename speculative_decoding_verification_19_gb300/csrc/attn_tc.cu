@@ -16,14 +16,16 @@
 // kernel merges by log-sum-exp.
 //
 // Per CTA, warp-specialised:
-//   warp 6      TMA producer: Q of each pair (two 64-column halves) and the
+//   warp 10     TMA producer: Q of each pair (two 64-column halves) and the
 //               K and V pages of each tile into a 4-stage ring (32 KB/stage)
-//   warp 7      MMA issuer: S = Q K^T into TMEM (double-buffered), then
+//   warp 11     MMA issuer: S = Q K^T into TMEM (double-buffered), then
 //               O += P V with P read back from TMEM (aliasing S)
-//   warps 0..3  softmax: one thread per query row (TMEM lane), mask, exp2,
-//               P written as bf16 into TMEM; O is rescaled in TMEM only when
-//               the running maximum grows by more than 2^8
-//   warps 4, 5  idle (they keep the two issuing roles off the sub-partitions
+//   warps 0..7  softmax: one thread per query row (TMEM lane) and per half
+//               tile (32 keys); the two halves of a row swap their maxima
+//               through shared memory, exp2, P written as bf16 into TMEM;
+//               O is rescaled in TMEM only when the running maximum grows by
+//               more than 2^8
+//   warps 8, 9  idle (they keep the two issuing roles off the sub-partitions
 //               of the softmax warps for rows 0..63).
 // TMEM: S0 cols [0,64), S1 [64,128), O [128,256).
 #include <cuda.h>
@@ -40,13 +42,15 @@ namespace tc {
 constexpr int kTileKeys = 64;
 constexpr int kPages = kTileKeys / kBlock;  // 4
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 // Warp roles.  A warp may only touch the TMEM lanes of its sub-partition
-// (warp % 4), so the softmax warps are 0..3 (lanes 32w..32w+31); the
-// producer and the MMA issuer sit on sub-partitions 2 and 3, away from the
-// softmax warps that own rows 0..63 (the common case R <= 64).
-constexpr int kProducerWarp = 6;
-constexpr int kMmaWarp = 7;
+// (warp % 4).  Softmax warps 0..7: warp w serves rows 32*(w%4).. and the
+// half w/4 of each tile's 64 keys.  The producer and the MMA issuer sit on
+// sub-partitions 2 and 3, away from the softmax warps of rows 0..63 (the
+// common case R <= 64); warps 8 and 9 stay idle.
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 10;
+constexpr int kMmaWarp = 11;
 constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
 constexpr int kHalfBytes = kPages * kBoxBytes;  // 8 KB
 constexpr int kStageBytes = 4 * kHalfBytes;     // K lo, K hi, V lo, V hi
@@ -65,6 +69,8 @@ struct __align__(8) Bars {
   uint64_t p_full[2];
   uint64_t o_done[2];  // completion of PV(t) lands on o_done[t & 1]
   uint64_t drain;
+  uint64_t xbar[4][2];       // per sub-partition, per tile parity: both halves' maxima
+  float xmax[2][2][128];     // [tile parity][half][row]
   uint32_t tmem_base;
   int abort;
 };
@@ -156,11 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::mbar_init(ptx::smem_u32(&bars->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), n_sm_warps);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 2 * n_sm_warps);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->o_done[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_done[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    for (int sp = 0; sp < 4; ++sp)
+      for (int i = 0; i < 2; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[sp][i]), 2);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -329,9 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, abort, kTimeoutNs);
     }
-  } else if (warp < 4) {
+  } else if (warp < kSoftmaxWarps) {
     // -------------------------------------------------------------- softmax
-    const int sp = warp;  // TMEM sub-partition this warp may access
+    const int sp = warp & 3;   // TMEM sub-partition this warp may access
+    const int half = warp >> 2;  // keys [32*half, 32*half + 32) of each tile
     const int row = sp * 32 + lane;
     if (sp < n_sm_warps) {
       const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
@@ -374,20 +383,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         const int nkeys = tile_pages(L, cu.tile) * kBlock;
         // tiles wholly inside the cached prefix need no mask
         const bool plain = kpos0 + kTileKeys <= ctx && nkeys == kTileKeys;
-        const uint32_t scol = lane_base + sbuf * kTileKeys;
-        // pass 1: masked, scaled scores -> tile maximum (16 TMEM columns at a time)
-        float mt = -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
-          uint32_t sv[16];
-          ptx::tmem_ld16(scol + c0, sv);
-          ptx::tmem_wait_ld();
+        const int jbase = half * 32;
+        uint32_t sv[32];
+        ptx::tmem_ld32(lane_base + sbuf * kTileKeys + jbase, sv);
+        ptx::tmem_wait_ld();
+        // maximum of this half (log2 units), then of the whole tile
+        float mh;
+        if (plain) {
+          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float x = score_of(sv[j], c0 + j, kpos0, nkeys, ctx, L, anc, real, plain, qscale2);
-            mt = fmaxf(mt, x);
+          for (int j = 0; j < 32; j += 4) {
+            a0 = fmaxf(a0, __uint_as_float(sv[j]));
+            a1 = fmaxf(a1, __uint_as_float(sv[j + 1]));
+            a2 = fmaxf(a2, __uint_as_float(sv[j + 2]));
+            a3 = fmaxf(a3, __uint_as_float(sv[j + 3]));
           }
+          mh = real ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * qscale2 : -INFINITY;
+        } else {
+          mh = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            mh = fmaxf(mh, score_of(sv[j], jbase + j, kpos0, nkeys, ctx, L, anc, real, false, qscale2));
         }
+        bars->xmax[sbuf][half][row] = mh;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xbar[sp][sbuf]));
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->xbar[sp][sbuf]), (uint32_t)((t >> 1) & 1), abort,
+                            kTimeoutNs))
+          break;
+        const float mt = fmaxf(bars->xmax[sbuf][0][row], bars->xmax[sbuf][1][row]);
         bool need = false;
         if (first) {
           m_used = mt;
@@ -395,20 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           need = true;
         }
         if (__any_sync(0xffffffffu, need)) {
-          // O is rescaled in place: PV(t-1) must have landed
+          // O is rescaled in place (this half's 64 columns): PV(t-1) must have landed
           if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) & 1]),
                               (uint32_t)(((t - 1) >> 1) & 1), abort, kTimeoutNs))
             break;
           ptx::tc_fence_after();
           const float f = need ? exp2f(m_used - mt) : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
-            ptx::tmem_ld32(lane_base + kOCol + cc * 32, o);
+            const uint32_t oc = lane_base + kOCol + half * 64 + cc * 32;
+            ptx::tmem_ld32(oc, o);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-            ptx::tmem_st32(lane_base + kOCol + cc * 32, o);
+            ptx::tmem_st32(oc, o);
           }
           ptx::tmem_wait_st();
           if (need) {
@@ -416,29 +441,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             m_used = mt;
           }
         }
-        // pass 2: probabilities, packed to bf16 pairs over the S columns
-        // already consumed (keys c0..c0+15 -> P columns c0/2..c0/2+7)
-        float lsum = 0.f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
-          uint32_t sv[16];
-          ptx::tmem_ld16(scol + c0, sv);
-          ptx::tmem_wait_ld();
-          uint32_t pk[8];
+        // probabilities of this half, packed to bf16 pairs; keys
+        // 32*half.. land in P columns 16*half.. (S columns both halves have
+        // already read, by the exchange above)
+        uint32_t pk[16];
+        float l0 = 0.f, l1 = 0.f;
+        if (plain) {
+          const float nm = real ? -m_used : -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float xa = score_of(sv[2 * j], c0 + 2 * j, kpos0, nkeys, ctx, L, anc, real, plain,
-                                      qscale2);
-            const float xb = score_of(sv[2 * j + 1], c0 + 2 * j + 1, kpos0, nkeys, ctx, L, anc, real,
-                                      plain, qscale2);
-            const float pa = xa == -INFINITY ? 0.f : fast_exp2(xa - m_used);
-            const float pb = xb == -INFINITY ? 0.f : fast_exp2(xb - m_used);
-            lsum += pa + pb;
+          for (int j = 0; j < 16; ++j) {
+            const float pa = fast_exp2(fmaf(__uint_as_float(sv[2 * j]), qscale2, nm));
+            const float pb = fast_exp2(fmaf(__uint_as_float(sv[2 * j + 1]), qscale2, nm));
+            l0 += pa;
+            l1 += pb;
             pk[j] = ptx::pack_bf16x2(pa, pb);
           }
-          ptx::tmem_st8(scol + (c0 >> 1), pk);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float xa = score_of(sv[2 * j], jbase + 2 * j, kpos0, nkeys, ctx, L, anc, real,
+                                      false, qscale2);
+            const float xb = score_of(sv[2 * j + 1], jbase + 2 * j + 1, kpos0, nkeys, ctx, L, anc,
+                                      real, false, qscale2);
+            const float pa = xa == -INFINITY ? 0.f : fast_exp2(xa - m_used);
+            const float pb = xb == -INFINITY ? 0.f : fast_exp2(xb - m_used);
+            l0 += pa;
+            l1 += pb;
+            pk[j] = ptx::pack_bf16x2(pa, pb);
+          }
         }
-        l += lsum;
+        l += l0 + l1;
+        ptx::tmem_st16(lane_base + sbuf * kTileKeys + half * 16, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -448,24 +481,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                               kTimeoutNs))
             break;
           ptx::tc_fence_after();
+          // partial: unnormalised O (this half's 64 columns), the running
+          // maximum and this half's share of the row sum
           const int64_t slot = (int64_t)cu.b * Hkv + cu.h + c;
           float* prow = part + (slot * R + (real ? row : 0)) * (int64_t)tc_part_stride(d.D);
-          const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
-            ptx::tmem_ld32(lane_base + kOCol + cc * 32, o);
+            ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc * 32, o);
             ptx::tmem_wait_ld();
             if (real) {
 #pragma unroll
               for (int j = 0; j < 32; j += 4) {
-                float4 v = make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                                       __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-                *reinterpret_cast<float4*>(prow + cc * 32 + j) = v;
+                const float4 v = make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                                             __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                *reinterpret_cast<float4*>(prow + half * 64 + cc * 32 + j) = v;
               }
             }
           }
-          if (real) prow[d.D] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+          if (real) {
+            prow[d.D + 1 + half] = l;
+            if (half == 0) prow[d.D] = m_used;
+          }
           ptx::tc_fence_before();
         }
         cu.next(ntiles, B, Hkv);
@@ -542,22 +579,26 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   for (int r = warp; r < R; r += blockDim.x / kWarp) {
     const int i = r / group, hq = h * group + r % group;
-    // CTAs with an empty tile range wrote nothing (their slot may belong to
-    // a neighbouring pair), so they are skipped
+    // A partial row holds unnormalised O, the running maximum m (log2
+    // units) and the two half-tile shares of the row sum.  CTAs with an
+    // empty tile range wrote nothing (their slot may belong to a
+    // neighbouring pair), so they are skipped.
+    const int S = tc_part_stride(D);
     float m = -INFINITY;
     for (int cc = c_first; cc <= c_last; ++cc) {
       if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
-      m = fmaxf(m, part[((pair + cc) * R + r) * (int64_t)tc_part_stride(D) + D]);
+      const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
+      if (prow[D + 1] + prow[D + 2] > 0.f) m = fmaxf(m, prow[D]);
     }
     float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (m != -INFINITY) {
       for (int cc = c_first; cc <= c_last; ++cc) {
         if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
-        const float* prow = part + ((pair + cc) * R + r) * (int64_t)tc_part_stride(D);
-        const float ls = prow[D];
-        if (ls == -INFINITY) continue;
-        const float w = exp2f(ls - m);
-        wsum += w;
+        const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
+        const float lp = prow[D + 1] + prow[D + 2];
+        if (!(lp > 0.f)) continue;
+        const float w = exp2f(prow[D] - m);
+        wsum += w * lp;
         for (int k = 0; k < D / kWarp; ++k) acc[k] += w * prow[lane + k * kWarp];
       }
     }

@@ -85,6 +85,13 @@ def barrier(world):
         torch.distributed.barrier()
 
 
+def aggregate(ms_local: float, steps: int, world: int, device):
+    """Whole-job throughput: the steps of all ranks over the slowest rank's
+    time.  Returns (steps_per_s, ms_max)."""
+    ms_max = max_over_ranks(ms_local, world, device)
+    return world * steps / (ms_max / 1e3), ms_max
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -349,7 +356,7 @@ def run_native(args, wl, world, rank, local):
     barrier(world)
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    ms_max = max_over_ranks(ms_total, world, device)
+    steps_per_s, ms_max = aggregate(ms_total, K, world, device)
     attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     rej_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     com_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
@@ -369,7 +376,6 @@ def run_native(args, wl, world, rank, local):
         st.e2e_step(i, ins, outs)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
 
-    steps_per_s = world * K / (ms_max / 1e3)
     peaks = measured_peaks()
     achieved = attn_b / (attn_ms / 1e3) / 1e9
     traffic = TRAFFIC["bytes_per_call"] if TRAFFIC["digest"] == attn_sources_digest() else None

@@ -209,6 +209,44 @@ spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,
                       const spec_dims* dims, void* ws, size_t ws_bytes,
                       void* stream);
 
+/*
+ * spec_reject_sample_noalloc -- spec_reject_sample for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot provide a workspace: cudaMalloc may synchronise the whole device,
+ * is not allowed while a stream is being captured, and engines that hand all
+ * of HBM to a fixed KV-cache pool at start-up often have no allocator to call.
+ * Arguments, outputs and semantics are those of spec_reject_sample without
+ * ws / ws_bytes.  The scratch (row statistics of every request, row and
+ * 8192-logit chunk, 16 bytes each, plus a status word) lives in a 1 MiB array
+ * inside the library that every GPU loading the library holds until exit.
+ *   - Sizes whose statistics exceed that array (B * 2 * M * ceil(V / 8192)
+ *     > 65520 for bf16 logits, ceil(V / 4096) chunks for fp32) return
+ *     SPEC_ERR_UNSUPPORTED and launch nothing; use spec_reject_sample there.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - No memory is allocated or freed, by the library or any routine it
+ *     calls.  The status word is cleared at the start of each call with an
+ *     async memset on `stream`; device-side failures show as
+ *     accepted_len = -1 for the request, and the status word is not readable
+ *     through this call.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (different streams, or different host threads on one device) race and
+ *     must be serialised by the caller.
+ *   - It does not update spec_last_launch_count.
+ */
+spec_status spec_reject_sample_noalloc(const void* target_logits,
+                                       const void* draft_logits,
+                                       const int32_t* tokens,
+                                       const int32_t* parent,
+                                       const float* temperature, uint64_t seed,
+                                       uint64_t offset, uint64_t b_base,
+                                       int32_t* out_tokens, int32_t* path,
+                                       int32_t* accepted_len, float* probe,
+                                       const spec_dims* dims, void* stream);
+
 /* Host-side Philox4x64-10 block (the generator the kernels use), for
  * known-answer tests: out = Philox4x64-10(counter, key). */
 void spec_philox_block(const uint64_t key[2], const uint64_t counter[4],

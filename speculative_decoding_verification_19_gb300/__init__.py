@@ -27,6 +27,7 @@ from ._native import (  # noqa: F401
     make_dims,
     philox_block,
     spec_reject_sample,
+    spec_reject_sample_noalloc,
     spec_verify_attn,
     workspace,
     workspace_size,

@@ -28,7 +28,7 @@ ATTN_AUTO, ATTN_CUDA_CORES, ATTN_TENSOR_CORES = 0, 1, 2
 EXPORTS = (
     "spec_workspace_size", "spec_workspace_init", "spec_get_device_status",
     "spec_verify_attn", "spec_reject_sample", "kv_commit", "spec_philox_block",
-    "spec_status_string", "spec_last_launch_count",
+    "spec_status_string", "spec_last_launch_count", "spec_reject_sample_noalloc",
 )
 
 
@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
     L.spec_reject_sample.argtypes = [vp, vp, vp, vp, vp, u64, u64, u64, vp, vp, vp,
                                      vp, pd, vp, sz, vp]
     L.spec_reject_sample.restype = i32
+    L.spec_reject_sample_noalloc.argtypes = [vp, vp, vp, vp, vp, u64, u64, u64, vp, vp,
+                                             vp, vp, pd, vp]
+    L.spec_reject_sample_noalloc.restype = i32
     L.kv_commit.argtypes = [vp] * 7 + [pd, vp, sz, vp]
     L.kv_commit.restype = i32
     L.spec_philox_block.argtypes = [ctypes.POINTER(u64)] * 3
@@ -167,6 +170,21 @@ def spec_reject_sample(target_logits, draft_logits, tokens, parent, temperature,
         _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(stream))
     _check("spec_reject_sample", code)
     return lib().spec_last_launch_count()
+
+
+def spec_reject_sample_noalloc(target_logits, draft_logits, tokens, parent,
+                               temperature, seed, offset, out_tokens, path,
+                               accepted_len, probe, dims: SpecDims, b_base=0,
+                               stream=None) -> None:
+    """spec_reject_sample without a workspace, for callers that cannot
+    allocate device memory; its scratch is a fixed 1 MiB array inside the
+    library shared by every call, so overlapping calls race."""
+    code = lib().spec_reject_sample_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent),
+        _ptr(temperature), int(seed) % (1 << 64), int(offset) % (1 << 64),
+        int(b_base) % (1 << 64), _ptr(out_tokens), _ptr(path), _ptr(accepted_len),
+        _ptr(probe), ctypes.byref(dims), _stream(stream))
+    _check("spec_reject_sample_noalloc", code)
 
 
 def kv_commit(k_cache, v_cache, block_table, ctx_lens, new_ctx_lens, path,

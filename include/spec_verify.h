@@ -218,12 +218,15 @@ spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,
  * is not allowed while a stream is being captured, and engines that hand all
  * of HBM to a fixed KV-cache pool at start-up often have no allocator to call.
  * Arguments, outputs and semantics are those of spec_reject_sample without
- * ws / ws_bytes.  The scratch (row statistics of every request, row and
- * 8192-logit chunk, 16 bytes each, plus a status word) lives in a 1 MiB array
- * inside the library that every GPU loading the library holds until exit.
- *   - Sizes whose statistics exceed that array (B * 2 * M * ceil(V / 8192)
- *     > 65520 for bf16 logits, ceil(V / 4096) chunks for fp32) return
- *     SPEC_ERR_UNSUPPORTED and launch nothing; use spec_reject_sample there.
+ * ws / ws_bytes.  The scratch (a status word; 16 bytes of row statistics per
+ * request, row and 2048-logit chunk -- 1024 for fp32 logits; 8 bytes of
+ * residual mass per request and 8192-logit chunk -- 4096 for fp32; an
+ * 816-byte draw state per request) lives in a 1 MiB array inside the
+ * library that every GPU loading the library holds until exit.
+ *   - Sizes whose scratch exceeds that array (for bf16 logits, roughly
+ *     B * (32 * M * ceil(V / 2048) + 8 * ceil(V / 8192) + 816) > 1 MiB)
+ *     return SPEC_ERR_UNSUPPORTED and launch nothing; use
+ *     spec_reject_sample there.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
  *     any stream capture.

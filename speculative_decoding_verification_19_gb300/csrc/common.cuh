@@ -98,10 +98,14 @@ struct WsLayout {
   int split_keys;         // keys per split (multiple of 16)
   int max_splits;
   int rows;               // R = group * M
-  size_t rs_off;          // reject-sample chunk stats: [B, 2, M, n_chunks] float2
+  size_t rs_off;          // reject-sample chunk stats: [B, 2, M, n_chunks] RowStat
   size_t rs_bytes;
-  int rs_chunk;           // logits per chunk
-  int rs_chunks;          // chunks per row
+  size_t rs_draw_off;     // [B] DrawState: residual draws left for passes 3-4
+  size_t rs_zsum_off;     // [B, n_dchunks] f64: residual mass of each draw chunk
+  int rs_chunk;           // logits per statistics chunk
+  int rs_chunks;          // statistics chunks per row
+  int rs_dchunk;          // logits per draw chunk (residual passes)
+  int rs_dchunks;         // draw chunks per row
   size_t total;
 };
 

@@ -9,7 +9,7 @@
 // normalize(max(0, P - q)).  Draws use the inverse CDF in vocabulary order
 // (smallest k with C_k > u*Z).
 //
-// Two kernels:
+// Four kernels:
 //   rs_rowstats_kernel  one CTA per (chunk of 8192 logits, row, request):
 //                       chunk max m_c and s_c = sum exp2((z - m_c)*log2e/T)
 //                       (fp32 terms, fp64 sums), over every target row and
@@ -18,26 +18,37 @@
 //                       16-byte coalesced loads.
 //   rs_decide_kernel    one CTA per request: merges the chunk statistics into
 //                       row normalisers (fp64), runs the sequential accept
-//                       tests in fp64, and draws the replacement/bonus token
-//                       with a two-level inverse CDF (per-sweep sums, then a
-//                       block scan inside the selected sweep).
+//                       tests in fp64; a bonus draw (from p) locates its chunk
+//                       from the statistics and searches only that chunk; a
+//                       residual draw is left for the next two kernels.
+//   rs_residual_sums_kernel  one CTA per (chunk, request) with a pending
+//                       residual draw: mass of max(0, P - q) over the chunk.
+//   rs_residual_draw_kernel  one CTA per pending request: picks the chunk
+//                       from those masses and searches it element by element.
 #include <float.h>
 #include <math.h>
 
 #include "common.cuh"
 #include "philox.cuh"
 #include "reject_sample.cuh"
+#include "tc_ptx.cuh"
 
 namespace specv {
 
-constexpr int kRsThreads = 256;   // rowstats CTA size
-constexpr int kRsVecs = 4;        // 16-byte vectors per thread per chunk
+constexpr int kRsThreads = 256;   // rowstats / residual-sum CTA size
+constexpr int kRsVecs = 4;        // 16-byte vectors per thread per draw chunk (residual sums)
+constexpr int kStatVecs = 8;      // 16-byte vectors per lane per statistics chunk
 constexpr int kDecThreads = 512;  // decide CTA size
 constexpr int kDecWarps = kDecThreads / kWarp;
 constexpr int kMaxM = 64;
 constexpr int kMaxSweeps = 256;
 
+// Statistics chunk: one warp task, 32 lanes x 8 vectors (2048 bf16 / 1024 fp32 logits).
 int rs_chunk_elems(int logits_dtype) {
+  return kWarp * kStatVecs * (logits_dtype == SPEC_BF16 ? 8 : 4);
+}
+// Draw chunk of the residual passes: 256 threads x 4 vectors (8192 / 4096).
+int rs_draw_chunk_elems(int logits_dtype) {
   return kRsThreads * kRsVecs * (logits_dtype == SPEC_BF16 ? 8 : 4);
 }
 int rs_max_vocab(int logits_dtype) {
@@ -64,83 +75,357 @@ __device__ __forceinline__ void load_vec(const T* row, int64_t e, int V, float (
 // ---------------------------------------------------------------------------
 // pass 1: chunk statistics
 // ---------------------------------------------------------------------------
+// A draft row is read only if its node drafted children (for a tree: some
+// parent entry names it).  Warp-uniform.
+__device__ __forceinline__ bool row_needed(const int32_t* parent, int M, int b, int which, int n) {
+  if (which == 0) return true;
+  if (parent == nullptr) return n < M - 1;
+  const int lane = threadIdx.x % kWarp;
+  const int32_t* par = parent + (int64_t)b * M;
+  const int k1 = n + 1 + lane, k2 = n + 1 + kWarp + lane;
+  const bool f = (k1 < M && par[k1] == n) || (k2 < M && par[k2] == n);
+  return __any_sync(0xffffffffu, f);
+}
+
+struct StatTask {
+  int b, which, n, c;
+};
+__device__ __forceinline__ StatTask stat_task(int64_t t, int n_chunks, int M) {
+  StatTask k;
+  k.c = (int)(t % n_chunks);
+  const int row = (int)((t / n_chunks) % (2 * M));
+  k.b = (int)(t / ((int64_t)n_chunks * 2 * M));
+  k.which = row / M;
+  k.n = row % M;
+  return k;
+}
+
+// Next task at or after t (stride nw) whose row is needed, or >= ntask.
+__device__ __forceinline__ int64_t next_needed(int64_t t, int64_t nw, int64_t ntask, int n_chunks,
+                                               const int32_t* parent, int M) {
+  while (t < ntask) {
+    const StatTask k = stat_task(t, n_chunks, M);
+    if (row_needed(parent, M, k.b, k.which, k.n)) break;
+    t += nw;
+  }
+  return t;
+}
+
+// One warp per task (request, row, chunk of 2048 bf16 / 1024 fp32 logits):
+// chunk max m_c and s_c = sum exp2((z - m_c) * log2e / T), fp32 terms, fp64
+// warp sum.  Persistent grid; each warp loads the next task's logits before
+// reducing the current ones, so 2 x 4 KB per warp stay in flight.
 template <typename T, bool kAligned>
 __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ parent,
     const float* __restrict__ temperature, spec_dims d, int n_chunks, RowStat* __restrict__ stats) {
   constexpr int EPV = 16 / sizeof(T);
-  // flat task index over (request, row, chunk), chunks fastest
-  const int64_t task = blockIdx.x;
-  const int c = (int)(task % n_chunks);
-  const int row = (int)((task / n_chunks) % (2 * d.M));
-  const int b = (int)(task / ((int64_t)n_chunks * 2 * d.M));
-  const int which = row / d.M, n = row % d.M;
-  const int tid = threadIdx.x;
-  if (which == 1) {  // a draft row is read only if its node drafted children
-    int has_child;
-    if (parent == nullptr) {
-      has_child = n < d.M - 1;
-    } else {
-      const int k = n + 1 + tid;
-      has_child = __syncthreads_or(k < d.M && parent[(int64_t)b * d.M + k] == n);
-    }
-    if (!has_child) return;
-  }
-  const float temp = temperature[b];
-  const float cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
-  const T* rowp = (which == 0 ? target : draft) + ((int64_t)b * d.M + n) * d.V;
-  const int64_t e0 = (int64_t)c * (kRsThreads * kRsVecs * EPV);
+  constexpr int kChunk = kWarp * kStatVecs * EPV;
+  const int lane = threadIdx.x % kWarp;
+  const int64_t nw = (int64_t)gridDim.x * (kRsThreads / kWarp);
+  const int64_t ntask = (int64_t)d.B * 2 * d.M * n_chunks;
+  const int M = d.M, V = d.V;
+  int64_t t = next_needed((int64_t)blockIdx.x * (kRsThreads / kWarp) + threadIdx.x / kWarp, nw,
+                          ntask, n_chunks, parent, M);
 
-  float f[kRsVecs][EPV];
-  float mt = -INFINITY;
+  auto row_ptr = [&](const StatTask& k) {
+    return (k.which == 0 ? target : draft) + ((int64_t)k.b * M + k.n) * V;
+  };
+  // raw 16-byte vectors of a task (aligned rows); vectors past V stay unread
+  auto load = [&](int64_t tt, uint4 (&raw)[kStatVecs]) {
+    const StatTask k = stat_task(tt, n_chunks, M);
+    const T* rp = row_ptr(k);
+    const int64_t e0 = (int64_t)k.c * kChunk;
 #pragma unroll
-  for (int v = 0; v < kRsVecs; ++v) {
-    load_vec<T, kAligned>(rowp, e0 + ((int64_t)v * kRsThreads + tid) * EPV, d.V, f[v]);
+    for (int v = 0; v < kStatVecs; ++v) {
+      const int64_t e = e0 + ((int64_t)v * kWarp + lane) * EPV;
+      raw[v] = (e + EPV <= V) ? __ldg(reinterpret_cast<const uint4*>(rp + e)) : make_uint4(0, 0, 0, 0);
+    }
+  };
+
+  uint4 cur[kStatVecs], nxt[kStatVecs];
+  if (kAligned && t < ntask) load(t, cur);
+  while (t < ntask) {
+    const int64_t t2 = next_needed(t + nw, nw, ntask, n_chunks, parent, M);
+    if (kAligned && t2 < ntask) load(t2, nxt);
+    const StatTask k = stat_task(t, n_chunks, M);
+    const float temp = temperature[k.b];
+    const float cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+    const int64_t e0 = (int64_t)k.c * kChunk;
+    float f[kStatVecs][EPV];
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) mt = fmaxf(mt, f[v][i]);
-  }
-  __shared__ float s_max[kRsThreads / kWarp];
-  __shared__ double s_sum[kRsThreads / kWarp];
-  mt = warp_max(mt);
-  if (tid % kWarp == 0) s_max[tid / kWarp] = mt;
-  __syncthreads();
-  float mc = s_max[0];
+    for (int v = 0; v < kStatVecs; ++v) {
+      const int64_t e = e0 + ((int64_t)v * kWarp + lane) * EPV;
+      if (kAligned) {
+        if (e + EPV <= V) {
+          unpack16(cur[v], f[v]);
+        } else {
 #pragma unroll
-  for (int w = 1; w < kRsThreads / kWarp; ++w) mc = fmaxf(mc, s_max[w]);
-  float st = 0.f;
-  if (mc != -INFINITY) {
+          for (int i = 0; i < EPV; ++i) f[v][i] = -INFINITY;
+        }
+      } else {
+        load_vec<T, false>(row_ptr(k), e, V, f[v]);
+      }
+    }
+    float m = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < kRsVecs; ++v)
+    for (int v = 0; v < kStatVecs; ++v)
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) st += fast_exp2((f[v][i] - mc) * cs);
-  }
-  double sd = warp_sum((double)st);
-  if (tid % kWarp == 0) s_sum[tid / kWarp] = sd;
-  __syncthreads();
-  if (tid == 0) {
-    double s = 0.0;
+      for (int i = 0; i < EPV; ++i) m = fmaxf(m, f[v][i]);
+    m = warp_max(m);
+    float sl = 0.f;
+    if (m != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < kRsThreads / kWarp; ++w) s += s_sum[w];
-    RowStat r;
-    r.m = mc;
-    r.pad = 0.f;
-    r.s = s;
-    stats[(((int64_t)b * 2 + which) * d.M + n) * n_chunks + c] = r;
+      for (int v = 0; v < kStatVecs; ++v)
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) sl += fast_exp2((f[v][i] - m) * cs);
+    }
+    const double sd = warp_sum((double)sl);
+    if (lane == 0) {
+      RowStat r;
+      r.m = m;
+      r.pad = 0.f;
+      r.s = sd;
+      stats[(((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks + k.c] = r;
+    }
+#pragma unroll
+    for (int v = 0; v < kStatVecs; ++v) cur[v] = nxt[v];
+    t = t2;
   }
 }
 
-// ---------------------------------------------------------------------------
-// pass 2: decisions and the draw
-// ---------------------------------------------------------------------------
-struct DecideCtx {
-  float mT, mD;       // row maxima of the node's target / draft rows
-  float invST, invSD; // 1 / row sums (fp32)
-  float cs;           // log2(e) / T
-  int nrej;           // rejections so far at this node (working P = P_nrej)
-  float invZ[kMaxM];  // 1 / Z_j of the residuals taken so far (element path)
-  double Z[kMaxM];    // Z_j in fp64 (accept-test path)
+// The same statistics for rows whose starts are 16-byte aligned, fed by 1-D
+// bulk copies: each of 16 warps keeps a ring of 3 task slots (4 KB each) in
+// shared memory, so about 192 KB per SM is in flight while the warps reduce
+// earlier tasks.  One persistent CTA per SM.  Waits are bounded; a time-out
+// raises SPEC_ERR_TIMEOUT.
+constexpr int kBulkWarps = 16;
+constexpr int kBulkRing = 3;
+constexpr int kBulkSlot = kWarp * kStatVecs * 16;  // bytes per task
+constexpr uint64_t kBulkTimeout = 4000000000ull;   // SM clocks per wait
+constexpr size_t kBulkSmem = (size_t)kBulkWarps * kBulkRing * kBulkSlot +
+                             sizeof(uint64_t) * kBulkWarps * kBulkRing + 64 + 1024;
+
+// Walks a contiguous range of statistics tasks (request, row, chunk; chunks
+// fastest) without divisions, skipping rows that are not read.
+struct StatCursor {
+  int t, end;           // current flat task and end of the range
+  int b, which, n, c;   // decoded position
+  int nc, M;
+  const int32_t* parent;
+  __device__ void start(int t0, int t1, int n_chunks, int M_, const int32_t* par) {
+    t = t0;
+    end = t1;
+    nc = n_chunks;
+    M = M_;
+    parent = par;
+    c = t0 % nc;
+    const int row = (t0 / nc) % (2 * M);
+    b = t0 / (nc * 2 * M);
+    which = row / M;
+    n = row % M;
+    skip();
+  }
+  __device__ bool valid() const { return t < end; }
+  // move off rows that are not needed (whole rows at a time)
+  __device__ void skip() {
+    while (t < end && !row_needed(parent, M, b, which, n)) {
+      t += nc - c;
+      c = 0;
+      next_row();
+    }
+  }
+  __device__ void next_row() {
+    if (++n == M) {
+      n = 0;
+      if (++which == 2) {
+        which = 0;
+        ++b;
+      }
+    }
+  }
+  __device__ void next() {
+    ++t;
+    if (++c == nc) {
+      c = 0;
+      next_row();
+      skip();
+    }
+  }
 };
 
+template <typename T>
+__global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ parent,
+    const float* __restrict__ temperature, spec_dims d, int n_chunks, RowStat* __restrict__ stats,
+    uint32_t* __restrict__ status) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int kChunk = kWarp * kStatVecs * EPV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)kBulkWarps * kBulkRing * kBulkSlot);
+  int* abort_flag = reinterpret_cast<int*>(bars + kBulkWarps * kBulkRing);
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kBulkWarps * kBulkRing; ++i) ptx::mbar_init(ptx::smem_u32(&bars[i]), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort = abort_flag;
+  const int M = d.M, V = d.V;
+  const int nw = gridDim.x * kBulkWarps;
+  const int ntask = d.B * 2 * M * n_chunks;
+  const int gw = blockIdx.x * kBulkWarps + warp;
+  const int per = (ntask + nw - 1) / nw;
+  const int t0 = min(ntask, gw * per), t1 = min(ntask, t0 + per);
+  uint8_t* myring = ring + (size_t)warp * kBulkRing * kBulkSlot;
+  uint64_t* mybars = bars + warp * kBulkRing;
+
+  auto row_ptr = [&](int b, int which, int n) {
+    return (which == 0 ? target : draft) + ((int64_t)b * M + n) * V;
+  };
+  auto issue = [&](const StatCursor& k, int slot) {
+    if (lane == 0) {
+      const int64_t e0 = (int64_t)k.c * kChunk;
+      const int64_t left = (int64_t)V - e0;
+      const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
+      const uint32_t bar = ptx::smem_u32(&mybars[slot]);
+      ptx::mbar_arrive_expect_tx(bar, bytes);
+      ptx::bulk_g2s(ptx::smem_u32(myring + slot * kBulkSlot), row_ptr(k.b, k.which, k.n) + e0,
+                    bytes, bar);
+    }
+  };
+
+  StatCursor cp, ci;  // the task being reduced / the next task to fetch
+  cp.start(t0, t1, n_chunks, M, parent);
+  ci = cp;
+  int issued = 0, done = 0;
+  for (int k = 0; k < kBulkRing && ci.valid(); ++k) {
+    issue(ci, k);
+    ++issued;
+    ci.next();
+  }
+  bool ok = true;
+  int cur_b = -1;
+  float cs = 1.0f;
+  while (cp.valid()) {
+    const int slot = done % kBulkRing;
+    if (!ptx::mbar_wait(ptx::smem_u32(&mybars[slot]), (uint32_t)((done / kBulkRing) & 1), abort,
+                        kBulkTimeout)) {
+      ok = false;
+      break;
+    }
+    if (cp.b != cur_b) {
+      cur_b = cp.b;
+      const float temp = temperature[cur_b];
+      cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+    }
+    const int e0 = cp.c * kChunk;
+    const int nvalid = V - e0;  // elements of this chunk inside the row (may exceed kChunk)
+    const uint4* sv = reinterpret_cast<const uint4*>(myring + slot * kBulkSlot);
+    uint4 raw[kStatVecs];
+#pragma unroll
+    for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
+    if (sizeof(T) == 2 && nvalid >= kChunk) {
+      // full bf16 chunk: exact packed maximum, then four partial sums
+      __nv_bfloat162 mx2 = *reinterpret_cast<const __nv_bfloat162*>(&raw[0].x);
+#pragma unroll
+      for (int v = 0; v < kStatVecs; ++v) {
+        const uint32_t w4[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+      }
+      const float m = warp_max(fmaxf(__low2float(mx2), __high2float(mx2)));
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int v = 0; v < kStatVecs; ++v) {
+          const uint32_t w4[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+          s0 += fast_exp2((__uint_as_float(w4[0] << 16) - m) * cs);
+          s1 += fast_exp2((__uint_as_float(w4[0] & 0xffff0000u) - m) * cs);
+          s2 += fast_exp2((__uint_as_float(w4[1] << 16) - m) * cs);
+          s3 += fast_exp2((__uint_as_float(w4[1] & 0xffff0000u) - m) * cs);
+          s0 += fast_exp2((__uint_as_float(w4[2] << 16) - m) * cs);
+          s1 += fast_exp2((__uint_as_float(w4[2] & 0xffff0000u) - m) * cs);
+          s2 += fast_exp2((__uint_as_float(w4[3] << 16) - m) * cs);
+          s3 += fast_exp2((__uint_as_float(w4[3] & 0xffff0000u) - m) * cs);
+        }
+      }
+      const double sd = warp_sum((double)((s0 + s1) + (s2 + s3)));
+      if (lane == 0) {
+        RowStat r;
+        r.m = m;
+        r.pad = 0.f;
+        r.s = sd;
+        stats[(((int64_t)cp.b * 2 + cp.which) * M + cp.n) * n_chunks + cp.c] = r;
+      }
+      ++done;
+      __syncwarp();
+      if (ci.valid()) {
+        ptx::fence_proxy_async_smem();
+        issue(ci, slot);
+        ++issued;
+        ci.next();
+      }
+      cp.next();
+      continue;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < kStatVecs; ++v) {
+      if ((v * kWarp + lane) * EPV < nvalid) {
+        float f[EPV];
+        unpack16(raw[v], f);
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) m = fmaxf(m, f[i]);
+      }
+    }
+    m = warp_max(m);
+    float sl = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int v = 0; v < kStatVecs; ++v) {
+        if ((v * kWarp + lane) * EPV < nvalid) {
+          float f[EPV];
+          unpack16(raw[v], f);
+#pragma unroll
+          for (int i = 0; i < EPV; ++i) sl += fast_exp2((f[i] - m) * cs);  // z - m is exact
+        }
+      }
+    }
+    const double sd = warp_sum((double)sl);
+    if (lane == 0) {
+      RowStat r;
+      r.m = m;
+      r.pad = 0.f;
+      r.s = sd;
+      stats[(((int64_t)cp.b * 2 + cp.which) * M + cp.n) * n_chunks + cp.c] = r;
+    }
+    ++done;
+    __syncwarp();
+    if (ci.valid()) {
+      // the slot's reads are done before the async proxy refills it
+      ptx::fence_proxy_async_smem();
+      issue(ci, slot);
+      ++issued;
+      ci.next();
+    }
+    cp.next();
+  }
+  // copies issued but not consumed (only after a time-out) land before exit
+  if (lane == 0)
+    for (int u = done; u < issued; ++u)
+      ptx::mbar_wait(ptx::smem_u32(&mybars[u % kBulkRing]), (uint32_t)((u / kBulkRing) & 1), abort,
+                     kBulkTimeout);
+  if (!ok && lane == 0) raise_status(status, SPEC_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: decisions (and bonus draws); passes 3-4: residual draws
+// ---------------------------------------------------------------------------
 // Weight of element e of the node's sampling / residual law:
 //   nrej == 0:  exp2((z - mT) * cs)                     (unnormalised p)
 //   nrej >= 1:  max(0, P_{nrej-1} - q)                  (unnormalised residual)
@@ -154,15 +439,22 @@ __device__ __forceinline__ float weight_of(float zt, float zd, const DecideCtx& 
   return fmaxf(P - qv, 0.f);
 }
 
+// Weights of the EPV elements starting at e (elements at or past `lim`
+// weigh 0 and are not read).
 template <typename T, bool kAligned>
-__device__ __forceinline__ float vec_weights(const T* trow, const T* drow, int64_t e, int V,
+__device__ __forceinline__ float vec_weights(const T* trow, const T* drow, int64_t e, int lim,
                                              const DecideCtx& c, int nrej,
                                              float (&w)[16 / sizeof(T)]) {
   constexpr int EPV = 16 / sizeof(T);
   float zt[EPV], zd[EPV];
-  load_vec<T, kAligned>(trow, e, V, zt);
+  if (e >= lim) {
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) w[i] = 0.f;
+    return 0.f;
+  }
+  load_vec<T, kAligned>(trow, e, lim, zt);
   if (nrej > 0) {
-    load_vec<T, kAligned>(drow, e, V, zd);
+    load_vec<T, kAligned>(drow, e, lim, zd);
   } else {
 #pragma unroll
     for (int i = 0; i < EPV; ++i) zd[i] = 0.f;
@@ -170,7 +462,7 @@ __device__ __forceinline__ float vec_weights(const T* trow, const T* drow, int64
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < EPV; ++i) {
-    w[i] = (e + i < V) ? weight_of(zt[i], zd[i], c, nrej) : 0.f;
+    w[i] = (e + i < lim) ? weight_of(zt[i], zd[i], c, nrej) : 0.f;
     s += w[i];
   }
   return s;
@@ -189,13 +481,146 @@ __device__ __forceinline__ double block_sum(double v, double* scratch) {
   return t;
 }
 
+// Mass of chunk c of the node's target row under exp2((z - mT) * cs), from
+// the chunk statistics of pass 1.
+__device__ __forceinline__ double chunk_mass(const RowStat& r, float mT, float cs) {
+  return r.m == -INFINITY ? 0.0 : r.s * (double)fast_exp2((r.m - mT) * cs);
+}
+
+// Shared state of the block-wide in-chunk search.
+struct DrawScratch {
+  double wtot[kDecWarps];
+  int claim, last;
+  int token;
+  float w;
+};
+
+// Inverse CDF inside one chunk [e0, e0 + len) (len <= kDecThreads * E):
+// every thread takes E consecutive elements starting at e0 + tid*E, sums
+// their weights (fp32), the block scans the sums in fp64, and the thread
+// whose interval holds `trel` walks its elements in fp64 to the first one
+// whose running sum exceeds trel.  The result lands in ds->token / ds->w
+// (the weight of the drawn element).  Rounding gaps fall back to the last
+// element of positive weight.
+template <typename T, bool kAligned>
+__device__ void chunk_draw(const T* trow, const T* drow, int64_t e0, int len, int V,
+                           const DecideCtx& c, int nrej, double trel, DrawScratch* ds) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int E = 2 * EPV;
+  const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+  const int64_t e = e0 + (int64_t)tid * E;
+  const int lim = (int)min((int64_t)V, e0 + len);
+  float w[E];
+  float vsf = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    float wk[EPV];
+    vsf += vec_weights<T, kAligned>(trow, drow, e + k * EPV, lim, c, nrej, wk);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) w[k * EPV + i] = wk[i];
+  }
+  const double vs = (double)vsf;
+  double incl = vs;
+#pragma unroll
+  for (int o = 1; o < kWarp; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == kWarp - 1) ds->wtot[warp] = incl;
+  if (tid == 0) {
+    ds->claim = kDecThreads;
+    ds->last = -1;
+  }
+  __syncthreads();
+  double wpre = 0.0;
+  for (int i = 0; i < warp; ++i) wpre += ds->wtot[i];
+  const double excl = wpre + incl - vs;
+  if (vs > 0.0) atomicMax(&ds->last, tid);
+  if (vs > 0.0 && excl <= trel && trel < excl + vs) atomicMin(&ds->claim, tid);
+  __syncthreads();
+  int owner = ds->claim;
+  if (owner == kDecThreads) owner = ds->last;
+  if (owner < 0) owner = 0;
+  if (tid == owner) {
+    double cum = excl;
+    int k = -1, lastpos = -1;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if (w[i] > 0.f) lastpos = i;
+      cum += (double)w[i];
+      if (k < 0 && cum > trel) k = i;
+    }
+    if (k < 0 || w[k] <= 0.f) k = lastpos;
+    if (k < 0) k = 0;
+    ds->token = (int)(e + k);
+    ds->w = w[k];
+  }
+  __syncthreads();
+}
+
+// The draw from p of `node` (a bonus draw, or the fallback after a residual
+// of zero mass): the chunk is located from the pass-1 statistics, then
+// searched element by element.  Returns the chunk masses' total Z through
+// *zsum.  Called by the whole block.
+template <typename T, bool kAligned>
+__device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int chunk, int V,
+                            const DecideCtx& c, double u, DrawScratch* ds, double* s_trel,
+                            int* s_chunk, double* zsum) {
+  // warp 0 scans the chunk masses (fp64) 32 at a time and picks the chunk
+  if (threadIdx.x < kWarp) {
+    const int lane = threadIdx.x;
+    double Z = 0.0;
+    for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(st[k], c.mT, c.cs);
+    Z = warp_sum(Z);
+    const double t = u * Z;
+    double base = 0.0;
+    int sel = -1, lastpos = -1;
+    double sel_pre = 0.0;
+    for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
+      const int k = k0 + lane;
+      const double wk = k < n_chunks ? chunk_mass(st[k], c.mT, c.cs) : 0.0;
+      double incl = wk;
+#pragma unroll
+      for (int o = 1; o < kWarp; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const double excl = base + incl - wk;
+      const unsigned hit = __ballot_sync(0xffffffffu, wk > 0.0 && excl + wk > t);
+      const unsigned pos = __ballot_sync(0xffffffffu, wk > 0.0);
+      if (pos) lastpos = k0 + 31 - __clz(pos);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        sel = k0 + l;
+        sel_pre = __shfl_sync(0xffffffffu, excl, l);
+      }
+      base += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+    }
+    if (sel < 0) {  // rounding at the very top: the last chunk with mass
+      sel = lastpos < 0 ? 0 : lastpos;
+      double pre = 0.0;
+      for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(st[k], c.mT, c.cs);
+      sel_pre = warp_sum(pre);
+    }
+    if (lane == 0) {
+      *s_chunk = sel;
+      *s_trel = t - sel_pre;
+      *zsum = Z;
+    }
+  }
+  __syncthreads();
+  chunk_draw<T, kAligned>(trow, trow, (int64_t)(*s_chunk) * chunk, chunk, V, c, 0, *s_trel, ds);
+}
+
 template <typename T, bool kAligned>
 __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
     const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    const RowStat* __restrict__ stats, uint32_t* __restrict__ status) {
+    int chunk, const RowStat* __restrict__ stats, DrawState* __restrict__ draws,
+    uint32_t* __restrict__ status) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kSweep = kDecThreads * EPV;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -205,12 +630,14 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   __shared__ int first_child[kMaxM], next_sib[kMaxM], tok[kMaxM];
   __shared__ float rowM[2][kMaxM];
   __shared__ double rowS[2][kMaxM];
+  __shared__ float gzt[kMaxM], gzd[kMaxM];  // logits of each drafted token in its parent's rows
+  __shared__ double px[kMaxM], qx[kMaxM];   // p(x_c), q(x_c) under the parent's rows (fp64)
+  __shared__ double uacc[kMaxM], usmp[kMaxM];
   __shared__ double red[kDecWarps];
-  __shared__ double warp_part[kMaxSweeps][kDecWarps];
-  __shared__ double sweep_sum[kMaxSweeps];
   __shared__ DecideCtx ctx;
-  __shared__ int s_node, s_child, s_accept, s_sweep, s_claim, s_a;
-  __shared__ double s_t;
+  __shared__ DrawScratch ds;
+  __shared__ int s_node, s_child, s_accept, s_a, s_chunk;
+  __shared__ double s_trel, s_z;
 
   // defined outputs first
   for (int i = tid; i < M; i += kDecThreads) {
@@ -219,6 +646,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   }
   if (probe != nullptr)
     for (int i = tid; i < 4 * M; i += kDecThreads) probe[(int64_t)b * M * 4 + i] = -1.f;
+  if (tid == 0) draws[b].pending = 0;
 
   // ---- validation --------------------------------------------------------
   const float temp = temperature[b];
@@ -246,6 +674,13 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   __syncthreads();
   const float cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
 
+  // gather the logits every accept test will read, all at once
+  if (!bad_arg && !bad_tok && tid >= 1 && tid < M) {
+    const int p = parent ? parent[(int64_t)b * M + tid] : tid - 1;
+    const int64_t o = ((int64_t)b * M + p) * V + tok[tid];
+    gzt[tid] = to_f32(target[o]);
+    gzd[tid] = to_f32(draft[o]);
+  }
   // ---- row normalisers ---------------------------------------------------
   int bad_row = 0;
   if (!bad_arg) {
@@ -259,7 +694,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       double s = 0.0;
       for (int c = lane; c < n_chunks; c += kWarp) {
         const RowStat x = st[c];
-        s += x.s * (double)exp2f((x.m - m) * cs);
+        if (x.m != -INFINITY) s += x.s * (double)fast_exp2((x.m - m) * cs);
       }
       s = warp_sum(s);
       if (lane == 0) {
@@ -270,6 +705,20 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     }
   }
   bad_row = __syncthreads_or(bad_row);
+  const uint64_t bglob = b_base + (uint64_t)b;
+  const double cs64 = (double)cs;
+  if (!(bad_arg || bad_tok || bad_row) && tid < M) {
+    // everything the sequential walk needs per node, computed in parallel
+    const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
+    uacc[tid] = (double)u24(r.w[0]);
+    usmp[tid] = (double)u24(r.w[1]);
+    if (tid >= 1) {
+      const int p = parent ? parent[(int64_t)b * M + tid] : tid - 1;
+      px[tid] = exp2(((double)gzt[tid] - (double)rowM[0][p]) * cs64) / rowS[0][p];
+      qx[tid] = exp2(((double)gzd[tid] - (double)rowM[1][p]) * cs64) / rowS[1][p];
+    }
+  }
+  __syncthreads();
   if (bad_arg || bad_tok || bad_row) {
     if (tid == 0) {
       accepted_len[b] = -1;
@@ -281,8 +730,6 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   }
 
   // ---- the walk ----------------------------------------------------------
-  const uint64_t bglob = b_base + (uint64_t)b;
-  const double cs64 = (double)cs;
   if (tid == 0) {
     s_node = 0;
     s_a = 0;
@@ -313,14 +760,10 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       const int child = s_child;
       if (tid == 0) {
         // accept test of `child` in fp64
-        const int x = tok[child];
-        const double zt = (double)to_f32(trow[x]);
-        const double zd = (double)to_f32(drow[x]);
-        const double Q = exp2((zd - (double)ctx.mD) * cs64) / rowS[1][node];
-        double P = exp2((zt - (double)ctx.mT) * cs64) / rowS[0][node];
+        const double Q = qx[child];
+        double P = px[child];
         for (int j = 1; j <= ctx.nrej; ++j) P = fmax(P - Q, 0.0) / ctx.Z[j];
-        const Philox4 r = philox4x64_10((uint64_t)child + 1, bglob, offset, 0, seed, 0);
-        const double u = (double)u24(r.w[0]);
+        const double u = uacc[child];
         s_accept = (u * Q < P);
         if (probe != nullptr) {
           probe[((int64_t)b * M + child) * 4 + 0] = (float)P;
@@ -332,14 +775,14 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
         moved = true;
         break;
       }
-      const bool more = next_sib[child] >= 0;
-      if (more) {
+      if (next_sib[child] >= 0) {
         // mass of the next residual, needed by the next sibling's test
+        // (trees only: a chain node has a single child)
         const int nrej_next = ctx.nrej + 1;
         double acc = 0.0;
         for (int64_t e = (int64_t)tid * EPV; e < V; e += kSweep) {
           float w[EPV];
-          acc += (double)vec_weights<T, kAligned>(trow, drow, e, V, ctx, nrej_next, w);
+          acc += (double)vec_weights<T, kAligned>(trow, drow, e, V, ctx, nrej_next, w);  // lim = V
         }
         const double Z = block_sum(acc, red);
         if (tid == 0) {
@@ -369,108 +812,150 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       continue;
     }
 
-    // ---- draw at `node` from the working law (inverse CDF) ---------------
-    const Philox4 r = philox4x64_10((uint64_t)node + 1, bglob, offset, 0, seed, 0);
-    const double u = (double)u24(r.w[1]);
-    const int n_sweeps = ceil_div(V, kSweep);
-    for (int attempt = 0; attempt < 2; ++attempt) {
-      __syncthreads();
-      const int nrej_now = ctx.nrej;
-      for (int s = 0; s < n_sweeps; ++s) {
-        float w[EPV];
-        const float vs = vec_weights<T, kAligned>(trow, drow, (int64_t)s * kSweep + (int64_t)tid * EPV,
-                                                  V, ctx, nrej_now, w);
-        const double ws = warp_sum((double)vs);
-        if (lane == 0) warp_part[s][warp] = ws;
-      }
-      __syncthreads();
-      for (int s = tid; s < n_sweeps; s += kDecThreads) {
-        double t = 0.0;
-#pragma unroll
-        for (int i = 0; i < kDecWarps; ++i) t += warp_part[s][i];
-        sweep_sum[s] = t;
-      }
-      __syncthreads();
+    // ---- the draw at `node` ----------------------------------------------
+    const double u = usmp[node];
+    if (tid == 0) accepted_len[b] = s_a;
+    if (ctx.nrej > 0) {
+      // residual: its chunk masses need a pass over two rows, spread over
+      // the whole GPU by the next kernel
+      DrawState& st = draws[b];
+      for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
+        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&ctx)[i];
       if (tid == 0) {
-        double Z = 0.0;
-        for (int s = 0; s < n_sweeps; ++s) Z += sweep_sum[s];
-        s_t = Z;
+        st.node = node;
+        st.a = s_a;
+        st.u = u;
+        st.pending = 1;
       }
-      __syncthreads();
-      if (s_t > 0.0 || attempt == 1) break;
-      if (tid == 0) ctx.nrej = 0;  // zero-mass residual: draw from p of the node
+      return;
     }
+    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, ctx, u, &ds, &s_trel, &s_chunk, &s_z);
     if (tid == 0) {
-      const double Z = s_t;
-      const double t = u * Z;
-      double pre = 0.0;
-      int sel = -1, last_pos = 0;
-      for (int s = 0; s < n_sweeps; ++s) {
-        if (sweep_sum[s] > 0.0) last_pos = s;
-        if (sel < 0 && pre + sweep_sum[s] > t) {
-          sel = s;
-          break;
-        }
-        pre += sweep_sum[s];
-      }
-      if (sel < 0) {  // rounding at the very top: take the last non-empty sweep
-        sel = last_pos;
-        pre = 0.0;
-        for (int s = 0; s < sel; ++s) pre += sweep_sum[s];
-      }
-      s_sweep = sel;
-      red[0] = t - pre;  // target inside the sweep
-      red[1] = Z;
-      s_claim = kDecThreads;
-    }
-    __syncthreads();
-    const double trel = red[0];
-    const double Ztot = red[1];
-    // block exclusive scan of the per-thread vector sums of the selected sweep
-    const int nrej_fin = ctx.nrej;
-    const int64_t e = (int64_t)s_sweep * kSweep + (int64_t)tid * EPV;
-    float w[EPV];
-    const double vs = (double)vec_weights<T, kAligned>(trow, drow, e, V, ctx, nrej_fin, w);
-    double incl = vs;
-#pragma unroll
-    for (int o = 1; o < kWarp; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    __shared__ double wtot[kDecWarps];
-    __shared__ int last_nonzero;
-    if (lane == kWarp - 1) wtot[warp] = incl;
-    if (tid == 0) last_nonzero = -1;
-    __syncthreads();
-    double wpre = 0.0;
-    for (int i = 0; i < warp; ++i) wpre += wtot[i];
-    const double excl = wpre + incl - vs;
-    if (vs > 0.0) atomicMax(&last_nonzero, tid);
-    if (vs > 0.0 && excl <= trel && trel < excl + vs) atomicMin(&s_claim, tid);
-    __syncthreads();
-    int owner = s_claim;
-    if (owner == kDecThreads) owner = last_nonzero;  // rounding gap: take the last mass
-    if (owner < 0) owner = 0;
-    if (tid == owner) {
-      double cum = excl;
-      int k = -1, lastpos = -1;
-      for (int i = 0; i < EPV; ++i) {
-        if (w[i] > 0.f) lastpos = i;
-        cum += (double)w[i];
-        if (k < 0 && cum > trel) k = i;
-      }
-      if (k < 0 || w[k] <= 0.f) k = lastpos;
-      if (k < 0) k = 0;
-      const int token = (int)(e + k);
-      const int a = s_a;
-      out_tokens[(int64_t)b * M + a] = token;
-      accepted_len[b] = a;
+      out_tokens[(int64_t)b * M + s_a] = ds.token;
       if (probe != nullptr) {
-        probe[((int64_t)b * M + node) * 4 + 2] = nrej_fin == 0 ? 1.0f : (float)Ztot;
-        probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w[k] / Ztot);
+        probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
+        probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)ds.w / s_z);
       }
     }
     return;
+  }
+}
+
+// Pass 3: mass of each chunk of the pending residual laws, one CTA per
+// (chunk, request).
+template <typename T, bool kAligned>
+__global__ void __launch_bounds__(kRsThreads) rs_residual_sums_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
+    int chunk, const DrawState* __restrict__ draws, double* __restrict__ zsum) {
+  // n_chunks / chunk: the draw chunks (kRsThreads * kRsVecs vectors)
+  constexpr int EPV = 16 / sizeof(T);
+  const int c = (int)(blockIdx.x % n_chunks), b = (int)(blockIdx.x / n_chunks), tid = threadIdx.x;
+  __shared__ DecideCtx ctx;
+  __shared__ int s_node, s_pending;
+  __shared__ double s_red[kRsThreads / kWarp];
+  if (tid == 0) {
+    s_pending = draws[b].pending;
+    s_node = draws[b].node;
+  }
+  __syncthreads();
+  if (!s_pending) return;
+  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kRsThreads)
+    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&draws[b].c)[i];
+  __syncthreads();
+  const T* trow = target + ((int64_t)b * d.M + s_node) * d.V;
+  const T* drow = draft + ((int64_t)b * d.M + s_node) * d.V;
+  const int nrej = ctx.nrej;
+  float acc = 0.f;
+  const int64_t e0 = (int64_t)c * chunk;
+#pragma unroll
+  for (int v = 0; v < kRsVecs; ++v) {
+    float w[EPV];
+    acc += vec_weights<T, kAligned>(trow, drow, e0 + ((int64_t)v * kRsThreads + tid) * EPV, d.V,
+                                    ctx, nrej, w);
+  }
+  double s = warp_sum((double)acc);
+  if (tid % kWarp == 0) s_red[tid / kWarp] = s;
+  __syncthreads();
+  if (tid == 0) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < kRsThreads / kWarp; ++w) t += s_red[w];
+    zsum[(int64_t)b * n_chunks + c] = t;
+  }
+}
+
+// Pass 4: the residual draw of each pending request.
+template <typename T, bool kAligned>
+__global__ void __launch_bounds__(kDecThreads) rs_residual_draw_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
+    int chunk, int n_dchunks, int dchunk, const RowStat* __restrict__ stats,
+    const DrawState* __restrict__ draws, const double* __restrict__ zsum,
+    int32_t* __restrict__ out_tokens, float* __restrict__ probe) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ DecideCtx ctx;
+  __shared__ DrawScratch ds;
+  __shared__ int s_pending, s_node, s_a, s_chunk, s_fallback;
+  __shared__ double s_trel, s_z, s_u;
+  if (tid == 0) {
+    s_pending = draws[b].pending;
+    s_node = draws[b].node;
+    s_a = draws[b].a;
+    s_u = draws[b].u;
+  }
+  __syncthreads();
+  if (!s_pending) return;
+  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
+    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&draws[b].c)[i];
+  const double* zs = zsum + (int64_t)b * n_dchunks;
+  if (tid == 0) {
+    double Z = 0.0;
+    for (int k = 0; k < n_dchunks; ++k) Z += zs[k];
+    s_z = Z;
+    s_fallback = !(Z > 0.0);
+    if (!s_fallback) {
+      const double t = s_u * Z;
+      double pre = 0.0;
+      int sel = -1, lastpos = 0;
+      for (int k = 0; k < n_dchunks; ++k) {
+        if (zs[k] > 0.0) lastpos = k;
+        if (sel < 0 && pre + zs[k] > t) {
+          sel = k;
+          break;
+        }
+        pre += zs[k];
+      }
+      if (sel < 0) {
+        sel = lastpos;
+        pre = 0.0;
+        for (int k = 0; k < sel; ++k) pre += zs[k];
+      }
+      s_chunk = sel;
+      s_trel = t - pre;
+    }
+  }
+  __syncthreads();
+  const int M = d.M, node = s_node;
+  const T* trow = target + ((int64_t)b * M + node) * d.V;
+  const T* drow = draft + ((int64_t)b * M + node) * d.V;
+  double Zrep;
+  if (s_fallback) {
+    // a residual of zero mass: draw from p of the node instead
+    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, d.V, ctx, s_u, &ds, &s_trel, &s_chunk,
+                             &s_z);
+    Zrep = 1.0;
+  } else {
+    chunk_draw<T, kAligned>(trow, drow, (int64_t)s_chunk * dchunk, dchunk, d.V, ctx, ctx.nrej,
+                            s_trel, &ds);
+    Zrep = s_z;
+  }
+  if (tid == 0) {
+    out_tokens[(int64_t)b * M + s_a] = ds.token;
+    if (probe != nullptr) {
+      probe[((int64_t)b * M + node) * 4 + 2] = (float)Zrep;
+      probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)ds.w / s_z);
+    }
   }
 }
 
@@ -480,18 +965,41 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
 template <typename T, bool kAligned>
 static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
   const spec_dims& d = a.d;
-  RowStat* stats = reinterpret_cast<RowStat*>(static_cast<char*>(a.ws) + lay.rs_off);
-  uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(a.ws) + lay.status_off);
-  const unsigned g1 = (unsigned)((int64_t)lay.rs_chunks * 2 * d.M * d.B);
-  rs_rowstats_kernel<T, kAligned><<<g1, kRsThreads, 0, st>>>(
-      static_cast<const T*>(a.target), static_cast<const T*>(a.draft), a.parent, a.temperature, d,
-      lay.rs_chunks, stats);
-  ++*launches;
+  char* ws = static_cast<char*>(a.ws);
+  RowStat* stats = reinterpret_cast<RowStat*>(ws + lay.rs_off);
+  DrawState* draws = reinterpret_cast<DrawState*>(ws + lay.rs_draw_off);
+  double* zsum = reinterpret_cast<double*>(ws + lay.rs_zsum_off);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
+  const T* tgt = static_cast<const T*>(a.target);
+  const T* dft = static_cast<const T*>(a.draft);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t ntask = (int64_t)lay.rs_chunks * 2 * d.M * d.B;
+  const int64_t want = (ntask + kRsThreads / kWarp - 1) / (kRsThreads / kWarp);
+  if (kAligned) {
+    const int64_t wantb = (ntask + kBulkWarps - 1) / kBulkWarps;
+    const unsigned gb = (unsigned)(wantb < sms ? wantb : sms);
+    cudaError_t e = cudaFuncSetAttribute(rs_rowstats_bulk_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kBulkSmem);
+    if (e != cudaSuccess) return e;
+    rs_rowstats_bulk_kernel<T><<<gb, kBulkWarps * kWarp, kBulkSmem, st>>>(
+        tgt, dft, a.parent, a.temperature, d, lay.rs_chunks, stats, status);
+  } else {
+    const unsigned g1 = (unsigned)(want < 2 * sms ? want : 2 * sms);
+    rs_rowstats_kernel<T, false><<<g1, kRsThreads, 0, st>>>(tgt, dft, a.parent, a.temperature, d,
+                                                          lay.rs_chunks, stats);
+  }
   rs_decide_kernel<T, kAligned><<<d.B, kDecThreads, 0, st>>>(
-      static_cast<const T*>(a.target), static_cast<const T*>(a.draft), a.tokens, a.parent,
-      a.temperature, a.seed, a.offset, a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d,
-      lay.rs_chunks, stats, status);
-  ++*launches;
+      tgt, dft, a.tokens, a.parent, a.temperature, a.seed, a.offset, a.b_base, a.out_tokens, a.path,
+      a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk, stats, draws, status);
+  rs_residual_sums_kernel<T, kAligned><<<(unsigned)((int64_t)lay.rs_dchunks * d.B), kRsThreads, 0,
+                                         st>>>(tgt, dft, d, lay.rs_dchunks, lay.rs_dchunk, draws,
+                                               zsum);
+  rs_residual_draw_kernel<T, kAligned><<<d.B, kDecThreads, 0, st>>>(
+      tgt, dft, d, lay.rs_chunks, lay.rs_chunk, lay.rs_dchunks, lay.rs_dchunk, stats, draws, zsum,
+      a.out_tokens, a.probe);
+  *launches += 4;
   return cudaGetLastError();
 }
 

@@ -13,6 +13,27 @@ struct RowStat {
   double s;
 };
 
+constexpr int kRsMaxM = 64;
+
+// Law at the node where a request draws: row maxima and normalisers of the
+// node's target / draft rows, and the masses of the residuals taken so far.
+struct DecideCtx {
+  float mT, mD;          // row maxima of the node's target / draft rows
+  float invST, invSD;    // 1 / row sums (fp32)
+  float cs;              // log2(e) / T
+  int nrej;              // rejections so far at this node (working P = P_nrej)
+  float invZ[kRsMaxM];   // 1 / Z_j of the residuals taken so far (element path)
+  double Z[kRsMaxM];     // Z_j in fp64 (accept-test path)
+};
+
+// A draw left for the residual kernels: the law, the node, the number of
+// accepted drafts and the uniform.
+struct DrawState {
+  DecideCtx c;
+  double u;
+  int node, a, pending, pad;
+};
+
 struct RsArgs {
   const void* target;
   const void* draft;
@@ -28,7 +49,8 @@ struct RsArgs {
   void* ws;
 };
 
-int rs_chunk_elems(int logits_dtype);
+int rs_chunk_elems(int logits_dtype);       // statistics chunk (one warp task)
+int rs_draw_chunk_elems(int logits_dtype);  // chunk of the residual passes
 int rs_max_vocab(int logits_dtype);
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
 

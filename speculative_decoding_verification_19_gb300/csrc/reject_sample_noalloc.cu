@@ -18,8 +18,9 @@
 
 namespace specv {
 
-// Scratch of the no-allocation path: a 256-byte status area followed by the
-// chunk statistics.  Every GPU that loads the library holds it until exit.
+// Scratch of the no-allocation path: a 256-byte status area, the chunk
+// statistics, the per-request draw states and the residual chunk masses.
+// Every GPU that loads the library holds it until exit.
 constexpr size_t kNoAllocScratchBytes = (size_t)1 << 20;  // 1 MiB
 constexpr size_t kNoAllocStatusBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -65,15 +66,19 @@ extern "C" spec_status spec_reject_sample_noalloc(
   lay.rs_off = kNoAllocStatusBytes;
   lay.rs_chunk = rs_chunk_elems(dims->logits_dtype);
   lay.rs_chunks = (int)ceil_div64(dims->V, lay.rs_chunk);
+  lay.rs_dchunk = rs_draw_chunk_elems(dims->logits_dtype);
+  lay.rs_dchunks = (int)ceil_div64(dims->V, lay.rs_dchunk);
   lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
-  if (lay.rs_bytes > kNoAllocScratchBytes - kNoAllocStatusBytes) return SPEC_ERR_UNSUPPORTED;
-  lay.total = lay.rs_off + lay.rs_bytes;
+  lay.rs_draw_off = (lay.rs_off + lay.rs_bytes + 255) / 256 * 256;
+  lay.rs_zsum_off = (lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B + 255) / 256 * 256;
+  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_dchunks;
+  if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;
   const spec_status s = noalloc_scratch(&scratch);
   if (s != SPEC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word starts each call at zero; the statistics need no clearing
+  // the status word starts each call at zero; the rest needs no clearing
   // (every entry read is written earlier in the same call)
   if (cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
 

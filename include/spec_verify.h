@@ -220,11 +220,11 @@ spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,
  * Arguments, outputs and semantics are those of spec_reject_sample without
  * ws / ws_bytes.  The scratch (a status word; 16 bytes of row statistics per
  * request, row and 2048-logit chunk -- 1024 for fp32 logits; 8 bytes of
- * residual mass per request and 8192-logit chunk -- 4096 for fp32; an
- * 816-byte draw state per request) lives in a 1 MiB array inside the
- * library that every GPU loading the library holds until exit.
+ * residual mass per request and chunk; an 816-byte draw state per
+ * request) lives in a 1 MiB array inside the library that every GPU loading
+ * the library holds until exit.
  *   - Sizes whose scratch exceeds that array (for bf16 logits, roughly
- *     B * (32 * M * ceil(V / 2048) + 8 * ceil(V / 8192) + 816) > 1 MiB)
+ *     B * ((32 * M + 8) * ceil(V / 2048) + 816) > 1 MiB)
  *     return SPEC_ERR_UNSUPPORTED and launch nothing; use
  *     spec_reject_sample there.
  *   - The first call on a device looks up the array's device address (once

@@ -50,12 +50,10 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.attn_off = take(L.attn_bytes);
   L.rs_chunk = rs_chunk_elems(d.logits_dtype);
   L.rs_chunks = (int)ceil_div64(d.V, L.rs_chunk);
-  L.rs_dchunk = rs_draw_chunk_elems(d.logits_dtype);
-  L.rs_dchunks = (int)ceil_div64(d.V, L.rs_dchunk);
   L.rs_bytes = sizeof(RowStat) * (size_t)d.B * 2 * d.M * L.rs_chunks;
   L.rs_off = take(L.rs_bytes);
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
-  L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_dchunks);
+  L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
   L.total = off;
   return L;
 }

@@ -100,12 +100,10 @@ struct WsLayout {
   int rows;               // R = group * M
   size_t rs_off;          // reject-sample chunk stats: [B, 2, M, n_chunks] RowStat
   size_t rs_bytes;
-  size_t rs_draw_off;     // [B] DrawState: residual draws left for passes 3-4
-  size_t rs_zsum_off;     // [B, n_dchunks] f64: residual mass of each draw chunk
+  size_t rs_draw_off;     // [B] DrawState: residual draws left for pass 3
+  size_t rs_zsum_off;     // [B, n_chunks] f64: residual mass of each statistics chunk
   int rs_chunk;           // logits per statistics chunk
   int rs_chunks;          // statistics chunks per row
-  int rs_dchunk;          // logits per draw chunk (residual passes)
-  int rs_dchunks;         // draw chunks per row
   size_t total;
 };
 

@@ -9,20 +9,23 @@
 // normalize(max(0, P - q)).  Draws use the inverse CDF in vocabulary order
 // (smallest k with C_k > u*Z).
 //
-// Four kernels:
-//   rs_rowstats_kernel  one CTA per (chunk of 8192 logits, row, request):
+// Four kernels, each after the first launched as a programmatic dependent of
+// the one before (it starts while its predecessor drains and waits for its
+// results in-kernel):
+//   rs_rowstats(_bulk)_kernel  every (request, row, 2048-logit chunk):
 //                       chunk max m_c and s_c = sum exp2((z - m_c)*log2e/T)
-//                       (fp32 terms, fp64 sums), over every target row and
-//                       every draft row that drafted children.  This is the
-//                       HBM-streaming pass: each logit is read once, with
-//                       16-byte coalesced loads.
-//   rs_decide_kernel    one CTA per request: merges the chunk statistics into
-//                       row normalisers (fp64), runs the sequential accept
-//                       tests in fp64; a bonus draw (from p) locates its chunk
-//                       from the statistics and searches only that chunk; a
-//                       residual draw is left for the next two kernels.
-//   rs_residual_sums_kernel  one CTA per (chunk, request) with a pending
-//                       residual draw: mass of max(0, P - q) over the chunk.
+//                       (fp32), over every target row and every draft row
+//                       that drafted children.  This is the HBM-streaming
+//                       pass: each logit is read once (1-D bulk copies into
+//                       shared memory for 16-byte aligned rows).
+//   rs_decide_kernel    one CTA per request: row normalisers from the chunk
+//                       statistics (fp64); a chain's accept tests all at once
+//                       (one thread per draft), a tree's walk in order; a
+//                       bonus draw (from p) locates its chunk from the
+//                       statistics and searches only that chunk; a residual
+//                       draw is left for passes 3 and 4.
+//   rs_residual_sums_kernel  one CTA per (2 statistics chunks, request) with a
+//                       pending residual: mass of max(0, P - q) per chunk.
 //   rs_residual_draw_kernel  one CTA per pending request: picks the chunk
 //                       from those masses and searches it element by element.
 #include <float.h>
@@ -31,13 +34,12 @@
 #include "common.cuh"
 #include "philox.cuh"
 #include "reject_sample.cuh"
+#include "rs_device.cuh"
 #include "tc_ptx.cuh"
 
 namespace specv {
 
-constexpr int kRsThreads = 256;   // rowstats / residual-sum CTA size
-constexpr int kRsVecs = 4;        // 16-byte vectors per thread per draw chunk (residual sums)
-constexpr int kStatVecs = 8;      // 16-byte vectors per lane per statistics chunk
+constexpr int kRsThreads = 256;   // CTA size of the statistics kernel for unaligned rows
 constexpr int kDecThreads = 512;  // decide CTA size
 constexpr int kDecWarps = kDecThreads / kWarp;
 constexpr int kMaxM = 64;
@@ -47,29 +49,8 @@ constexpr int kMaxSweeps = 256;
 int rs_chunk_elems(int logits_dtype) {
   return kWarp * kStatVecs * (logits_dtype == SPEC_BF16 ? 8 : 4);
 }
-// Draw chunk of the residual passes: 256 threads x 4 vectors (8192 / 4096).
-int rs_draw_chunk_elems(int logits_dtype) {
-  return kRsThreads * kRsVecs * (logits_dtype == SPEC_BF16 ? 8 : 4);
-}
 int rs_max_vocab(int logits_dtype) {
   return kMaxSweeps * kDecThreads * (logits_dtype == SPEC_BF16 ? 8 : 4);
-}
-
-__device__ __forceinline__ bool temperature_ok(float T) {
-  return T >= FLT_MIN && T <= FLT_MAX;  // normal, positive, finite (NaN fails)
-}
-
-// Load EPV consecutive logits starting at element e (-inf past the row end).
-template <typename T, bool kAligned>
-__device__ __forceinline__ void load_vec(const T* row, int64_t e, int V, float (&f)[16 / sizeof(T)]) {
-  constexpr int EPV = 16 / sizeof(T);
-  if (kAligned && e + EPV <= V) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4*>(row + e));
-    unpack16(r, f);
-  } else {
-#pragma unroll
-    for (int i = 0; i < EPV; ++i) f[i] = (e + i < V) ? to_f32(row[e + i]) : -INFINITY;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -125,6 +106,7 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
   const int64_t nw = (int64_t)gridDim.x * (kRsThreads / kWarp);
   const int64_t ntask = (int64_t)d.B * 2 * d.M * n_chunks;
   const int M = d.M, V = d.V;
+  asm volatile("griddepcontrol.launch_dependents;");
   int64_t t = next_needed((int64_t)blockIdx.x * (kRsThreads / kWarp) + threadIdx.x / kWarp, nw,
                           ntask, n_chunks, parent, M);
 
@@ -328,80 +310,13 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     uint4 raw[kStatVecs];
 #pragma unroll
     for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
-    if (sizeof(T) == 2 && nvalid >= kChunk) {
-      // full bf16 chunk: exact packed maximum, then four partial sums
-      __nv_bfloat162 mx2 = *reinterpret_cast<const __nv_bfloat162*>(&raw[0].x);
-#pragma unroll
-      for (int v = 0; v < kStatVecs; ++v) {
-        const uint32_t w4[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
-      }
-      const float m = warp_max(fmaxf(__low2float(mx2), __high2float(mx2)));
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      if (m != -INFINITY) {
-#pragma unroll
-        for (int v = 0; v < kStatVecs; ++v) {
-          const uint32_t w4[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-          s0 += fast_exp2((__uint_as_float(w4[0] << 16) - m) * cs);
-          s1 += fast_exp2((__uint_as_float(w4[0] & 0xffff0000u) - m) * cs);
-          s2 += fast_exp2((__uint_as_float(w4[1] << 16) - m) * cs);
-          s3 += fast_exp2((__uint_as_float(w4[1] & 0xffff0000u) - m) * cs);
-          s0 += fast_exp2((__uint_as_float(w4[2] << 16) - m) * cs);
-          s1 += fast_exp2((__uint_as_float(w4[2] & 0xffff0000u) - m) * cs);
-          s2 += fast_exp2((__uint_as_float(w4[3] << 16) - m) * cs);
-          s3 += fast_exp2((__uint_as_float(w4[3] & 0xffff0000u) - m) * cs);
-        }
-      }
-      const double sd = warp_sum((double)((s0 + s1) + (s2 + s3)));
-      if (lane == 0) {
-        RowStat r;
-        r.m = m;
-        r.pad = 0.f;
-        r.s = sd;
-        stats[(((int64_t)cp.b * 2 + cp.which) * M + cp.n) * n_chunks + cp.c] = r;
-      }
-      ++done;
-      __syncwarp();
-      if (ci.valid()) {
-        ptx::fence_proxy_async_smem();
-        issue(ci, slot);
-        ++issued;
-        ci.next();
-      }
-      cp.next();
-      continue;
-    }
-    float m = -INFINITY;
-#pragma unroll
-    for (int v = 0; v < kStatVecs; ++v) {
-      if ((v * kWarp + lane) * EPV < nvalid) {
-        float f[EPV];
-        unpack16(raw[v], f);
-#pragma unroll
-        for (int i = 0; i < EPV; ++i) m = fmaxf(m, f[i]);
-      }
-    }
-    m = warp_max(m);
-    float sl = 0.f;
-    if (m != -INFINITY) {
-#pragma unroll
-      for (int v = 0; v < kStatVecs; ++v) {
-        if ((v * kWarp + lane) * EPV < nvalid) {
-          float f[EPV];
-          unpack16(raw[v], f);
-#pragma unroll
-          for (int i = 0; i < EPV; ++i) sl += fast_exp2((f[i] - m) * cs);  // z - m is exact
-        }
-      }
-    }
-    const double sd = warp_sum((double)sl);
+    float sd;
+    const float m = chunk_stat<T>(raw, nvalid, cs, &sd);
     if (lane == 0) {
       RowStat r;
       r.m = m;
       r.pad = 0.f;
-      r.s = sd;
+      r.s = (double)sd;
       stats[(((int64_t)cp.b * 2 + cp.which) * M + cp.n) * n_chunks + cp.c] = r;
     }
     ++done;
@@ -426,19 +341,6 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
 // ---------------------------------------------------------------------------
 // pass 2: decisions (and bonus draws); passes 3-4: residual draws
 // ---------------------------------------------------------------------------
-// Weight of element e of the node's sampling / residual law:
-//   nrej == 0:  exp2((z - mT) * cs)                     (unnormalised p)
-//   nrej >= 1:  max(0, P_{nrej-1} - q)                  (unnormalised residual)
-// with P_0 = p and P_j = max(0, P_{j-1} - q) / Z_j.
-__device__ __forceinline__ float weight_of(float zt, float zd, const DecideCtx& c, int nrej) {
-  const float et = fast_exp2((zt - c.mT) * c.cs);
-  if (nrej == 0) return et;
-  const float qv = fast_exp2((zd - c.mD) * c.cs) * c.invSD;
-  float P = et * c.invST;
-  for (int j = 1; j < nrej; ++j) P = fmaxf(P - qv, 0.f) * c.invZ[j];
-  return fmaxf(P - qv, 0.f);
-}
-
 // Weights of the EPV elements starting at e (elements at or past `lim`
 // weigh 0 and are not read).
 template <typename T, bool kAligned>
@@ -481,12 +383,6 @@ __device__ __forceinline__ double block_sum(double v, double* scratch) {
   return t;
 }
 
-// Mass of chunk c of the node's target row under exp2((z - mT) * cs), from
-// the chunk statistics of pass 1.
-__device__ __forceinline__ double chunk_mass(const RowStat& r, float mT, float cs) {
-  return r.m == -INFINITY ? 0.0 : r.s * (double)fast_exp2((r.m - mT) * cs);
-}
-
 // Shared state of the block-wide in-chunk search.
 struct DrawScratch {
   double wtot[kDecWarps];
@@ -495,7 +391,7 @@ struct DrawScratch {
   float w;
 };
 
-// Inverse CDF inside one chunk [e0, e0 + len) (len <= kDecThreads * E):
+// Inverse CDF inside one chunk [e0, e0 + len) (len <= blockDim.x * E):
 // every thread takes E consecutive elements starting at e0 + tid*E, sums
 // their weights (fp32), the block scans the sums in fp64, and the thread
 // whose interval holds `trel` walks its elements in fp64 to the first one
@@ -529,7 +425,7 @@ __device__ void chunk_draw(const T* trow, const T* drow, int64_t e0, int len, in
   __syncthreads();
   if (lane == kWarp - 1) ds->wtot[warp] = incl;
   if (tid == 0) {
-    ds->claim = kDecThreads;
+    ds->claim = (int)blockDim.x;
     ds->last = -1;
   }
   __syncthreads();
@@ -540,7 +436,7 @@ __device__ void chunk_draw(const T* trow, const T* drow, int64_t e0, int len, in
   if (vs > 0.0 && excl <= trel && trel < excl + vs) atomicMin(&ds->claim, tid);
   __syncthreads();
   int owner = ds->claim;
-  if (owner == kDecThreads) owner = ds->last;
+  if (owner == (int)blockDim.x) owner = ds->last;
   if (owner < 0) owner = 0;
   if (tid == owner) {
     double cum = excl;
@@ -613,6 +509,197 @@ __device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int 
   chunk_draw<T, kAligned>(trow, trow, (int64_t)(*s_chunk) * chunk, chunk, V, c, 0, *s_trel, ds);
 }
 
+// ---- one-warp draw inside a statistics chunk (16-byte aligned rows) ------
+// Lane l takes the kStatVecs consecutive 16-byte vectors starting at element
+// e0 + l * E of the chunk; the lanes' fp32 weight sums are scanned as
+// double-floats, and the owning lane's elements are spread over the warp
+// (one 32-bit word per lane) and scanned again.  Same law and rounding-gap
+// rule as chunk_draw.
+template <typename T>
+__device__ __forceinline__ float lane_weights(const T* trow, const T* drow, int64_t e0, int V,
+                                              const DecideCtx& c, int nrej,
+                                              uint4 (&raw_t)[kStatVecs], uint4 (&raw_d)[kStatVecs]) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int E = kStatVecs * EPV;
+  const int lane = threadIdx.x % kWarp;
+  const int64_t e = e0 + (int64_t)lane * E;
+#pragma unroll
+  for (int v = 0; v < kStatVecs; ++v) {
+    const bool in = e + (v + 1) * EPV <= V;  // rows are whole 16-byte vectors
+    raw_t[v] = in ? __ldg(reinterpret_cast<const uint4*>(trow + e) + v) : make_uint4(0, 0, 0, 0);
+    raw_d[v] = (in && nrej > 0) ? __ldg(reinterpret_cast<const uint4*>(drow + e) + v)
+                                : make_uint4(0, 0, 0, 0);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < kStatVecs; ++v) {
+    if (e + (v + 1) * EPV > V) continue;
+    float zt[EPV], zd[EPV];
+    unpack16(raw_t[v], zt);
+    unpack16(raw_d[v], zd);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) s += weight_of(zt[i], zd[i], c, nrej);
+  }
+  return s;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <typename T>
+__device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
+                               const DecideCtx& c, int nrej, dfloat trel, float* w_out) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int E = kStatVecs * EPV;  // elements per lane
+  constexpr int EW = 4 / sizeof(T);   // elements per 32-bit word
+  const int lane = threadIdx.x % kWarp;
+  uint4 raw_t[kStatVecs], raw_d[kStatVecs];
+  const float vs = lane_weights<T>(trow, drow, e0, V, c, nrej, raw_t, raw_d);
+  const dfloat incl = df_warp_scan(df_make(vs));
+  const dfloat excl = df_sub(incl, df_make(vs));
+  const unsigned hit =
+      __ballot_sync(0xffffffffu, vs > 0.f && !df_gt(excl, trel) && df_gt(incl, trel));
+  const unsigned pos = __ballot_sync(0xffffffffu, vs > 0.f);
+  const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+  const dfloat r = df_sub(trel, df_shfl(excl, owner));  // position inside the owner's segment
+  uint32_t wt = 0, wd = 0;  // lane l takes word l of the owner's segment
+#pragma unroll
+  for (int v = 0; v < kStatVecs; ++v)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t xt = __shfl_sync(0xffffffffu, word_of(raw_t[v], i), owner);
+      const uint32_t xd = __shfl_sync(0xffffffffu, word_of(raw_d[v], i), owner);
+      if (lane == v * 4 + i) {
+        wt = xt;
+        wd = xd;
+      }
+    }
+  const int64_t seg = e0 + (int64_t)owner * E;
+  float w[EW];
+  float ls = 0.f;
+#pragma unroll
+  for (int i = 0; i < EW; ++i) {
+    float zt, zd;
+    if (EW == 2) {
+      zt = __uint_as_float(i == 0 ? wt << 16 : wt & 0xffff0000u);
+      zd = __uint_as_float(i == 0 ? wd << 16 : wd & 0xffff0000u);
+    } else {
+      zt = __uint_as_float(wt);
+      zd = __uint_as_float(wd);
+    }
+    const bool in = seg + lane * EW + i < V;
+    w[i] = in ? weight_of(zt, zd, c, nrej) : 0.f;
+    ls += w[i];
+  }
+  const dfloat cum = df_warp_scan(df_make(ls));
+  const dfloat before = df_sub(cum, df_make(ls));
+  const unsigned h2 = __ballot_sync(0xffffffffu, ls > 0.f && df_gt(cum, r));
+  const unsigned p2 = __ballot_sync(0xffffffffu, ls > 0.f);
+  int k = 0;  // element inside the lane
+  if (EW == 2) {
+    if (h2) {
+      k = (w[0] > 0.f && df_gt(df_add(before, df_make(w[0])), r)) ? 0 : 1;
+      if (w[k] <= 0.f) k = 1 - k;
+    } else {
+      k = w[1] > 0.f ? 1 : 0;  // the last element of positive weight
+    }
+  }
+  const int l2 = h2 ? __ffs(h2) - 1 : (p2 ? 31 - __clz(p2) : 0);
+  const int tok = (int)(seg + lane * EW + k);
+  const float wk = w[EW == 2 ? (k & 1) : 0];
+  *w_out = __shfl_sync(0xffffffffu, wk, l2);
+  return __shfl_sync(0xffffffffu, tok, l2);
+}
+
+// Picks the chunk holding t from per-chunk masses zs[0..n) (fp64, read
+// through L2), by one warp: the smallest k with a positive mass and an
+// inclusive prefix above t, else the last chunk of positive mass.  Returns
+// the chunk; *pre = the masses before it.
+__device__ __forceinline__ int warp_select_chunk(const double* zs, int n, double t, double* pre) {
+  const int lane = threadIdx.x % kWarp;
+  double base = 0.0;
+  int sel = -1, lastpos = -1;
+  double sel_pre = 0.0, last_pre = 0.0;
+  for (int k0 = 0; k0 < n && sel < 0; k0 += kWarp) {
+    const int k = k0 + lane;
+    const double wk = k < n ? __ldcg(zs + k) : 0.0;
+    double incl = wk;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double excl = base + incl - wk;
+    const unsigned hit = __ballot_sync(0xffffffffu, wk > 0.0 && excl + wk > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, wk > 0.0);
+    if (pos) {
+      const int l = 31 - __clz(pos);
+      lastpos = k0 + l;
+      last_pre = __shfl_sync(0xffffffffu, excl, l);
+    }
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      sel = k0 + l;
+      sel_pre = __shfl_sync(0xffffffffu, excl, l);
+    }
+    base += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+  }
+  if (sel < 0) {  // rounding at the very top: the last chunk with mass
+    sel = lastpos < 0 ? 0 : lastpos;
+    sel_pre = lastpos < 0 ? 0.0 : last_pre;
+  }
+  *pre = sel_pre;
+  return sel;
+}
+
+// The draw from p of `node` by one warp (aligned rows): the statistics
+// chunk is located as in draw_from_p (fp64), then searched by
+// warp_chunk_draw.  Returns the token; *w its weight, *zsum the total.
+template <typename T>
+__device__ int warp_draw_from_p(const T* trow, const RowStat* st, int n_chunks, int chunk, int V,
+                                const DecideCtx& c, double u, float* w, double* zsum) {
+  const int lane = threadIdx.x % kWarp;
+  double Z = 0.0;
+  for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(st[k], c.mT, c.cs);
+  Z = warp_sum(Z);
+  const double t = u * Z;
+  double base = 0.0;
+  int sel = -1, lastpos = -1;
+  double sel_pre = 0.0;
+  for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
+    const int k = k0 + lane;
+    const double wk = k < n_chunks ? chunk_mass(st[k], c.mT, c.cs) : 0.0;
+    double incl = wk;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double excl = base + incl - wk;
+    const unsigned hit = __ballot_sync(0xffffffffu, wk > 0.0 && excl + wk > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, wk > 0.0);
+    if (pos) lastpos = k0 + 31 - __clz(pos);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      sel = k0 + l;
+      sel_pre = __shfl_sync(0xffffffffu, excl, l);
+    }
+    base += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+  }
+  if (sel < 0) {  // rounding at the very top: the last chunk with mass
+    sel = lastpos < 0 ? 0 : lastpos;
+    double pre = 0.0;
+    for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(st[k], c.mT, c.cs);
+    sel_pre = warp_sum(pre);
+  }
+  *zsum = Z;
+  const double trel = t - sel_pre;
+  const float th = (float)trel;
+  return warp_chunk_draw<T>(trow, trow, (int64_t)sel * chunk, V, c, 0,
+                            dfloat{th, (float)(trel - (double)th)}, w);
+}
+
 template <typename T, bool kAligned>
 __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
@@ -638,6 +725,12 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   __shared__ DrawScratch ds;
   __shared__ int s_node, s_child, s_accept, s_a, s_chunk;
   __shared__ double s_trel, s_z;
+  __shared__ int chain_rej[kMaxM];  // chain: the accept test of node n failed
+  __shared__ float chain_p[kMaxM], chain_q[kMaxM];
+
+  asm volatile("griddepcontrol.launch_dependents;");
+  // the statistics come from the previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // defined outputs first
   for (int i = tid; i < M; i += kDecThreads) {
@@ -688,14 +781,30 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       const int which = r / M, n = r % M;
       if (which == 1 && first_child[n] < 0) continue;
       const RowStat* st = stats + (((int64_t)b * 2 + which) * M + n) * n_chunks;
+      // the row's chunk statistics, all loads in flight together
+      constexpr int kItems = 16;  // n_chunks <= 512
+      float im[kItems];
+      double is[kItems];
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int c = lane + j * kWarp;
+        if (c < n_chunks) {
+          const RowStat x = st[c];
+          im[j] = x.m;
+          is[j] = x.s;
+        } else {
+          im[j] = -INFINITY;
+          is[j] = 0.0;
+        }
+      }
       float m = -INFINITY;
-      for (int c = lane; c < n_chunks; c += kWarp) m = fmaxf(m, st[c].m);
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) m = fmaxf(m, im[j]);
       m = warp_max(m);
       double s = 0.0;
-      for (int c = lane; c < n_chunks; c += kWarp) {
-        const RowStat x = st[c];
-        if (x.m != -INFINITY) s += x.s * (double)fast_exp2((x.m - m) * cs);
-      }
+#pragma unroll
+      for (int j = 0; j < kItems; ++j)
+        if (im[j] != -INFINITY) s += is[j] * (double)fast_exp2((im[j] - m) * cs);
       s = warp_sum(s);
       if (lane == 0) {
         rowM[which][n] = m;
@@ -712,8 +821,33 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
     uacc[tid] = (double)u24(r.w[0]);
     usmp[tid] = (double)u24(r.w[1]);
-    if (tid >= 1) {
-      const int p = parent ? parent[(int64_t)b * M + tid] : tid - 1;
+    if (tid >= 1 && parent == nullptr) {
+      // chain: every draft's test at once.  The exponent of p(x)/q(x) is
+      // formed in fp64 and split into integer and fraction, so that one fp32
+      // exp2 gives the ratio to about 3e-7 relative.
+      const int p = tid - 1;
+      const double et = ((double)gzt[tid] - (double)rowM[0][p]) * cs64;  // log2 unnormalised p(x)
+      const double ed = ((double)gzd[tid] - (double)rowM[1][p]) * cs64;  // log2 unnormalised q(x)
+      const float st_f = (float)rowS[0][p], sd_f = (float)rowS[1][p];
+      bool acc;
+      if (ed == -INFINITY) {
+        acc = et != -INFINITY;  // q(x) = 0: accepted iff p(x) > 0
+      } else if (et == -INFINITY) {
+        acc = false;            // p(x) = 0 < u q(x)
+      } else {
+        const double e = et - ed;
+        const double ei = rint(e);
+        const float ratio =
+            ldexpf(fast_exp2((float)(e - ei)), (int)fmax(fmin(ei, 300.0), -300.0)) * (sd_f / st_f);
+        acc = (float)uacc[tid] < ratio;  // u < p(x) / q(x)
+      }
+      chain_rej[tid] = !acc;
+      if (probe != nullptr) {
+        chain_p[tid] = exp2f((float)et) / st_f;
+        chain_q[tid] = exp2f((float)ed) / sd_f;
+      }
+    } else if (tid >= 1) {
+      const int p = parent[(int64_t)b * M + tid];
       px[tid] = exp2(((double)gzt[tid] - (double)rowM[0][p]) * cs64) / rowS[0][p];
       qx[tid] = exp2(((double)gzd[tid] - (double)rowM[1][p]) * cs64) / rowS[1][p];
     }
@@ -729,7 +863,88 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     return;
   }
 
-  // ---- the walk ----------------------------------------------------------
+  if (parent == nullptr) {
+    // ---- a chain: the walk stops at the first rejected draft ---------------
+    if (tid == 0) {
+      int fr = M;
+      for (int n = 1; n < M; ++n)
+        if (chain_rej[n]) {
+          fr = n;
+          break;
+        }
+      s_child = fr;
+    }
+    __syncthreads();
+    const int fr = s_child;              // first rejected node, M if none
+    const int a = fr < M ? fr - 1 : M - 1;  // accepted drafts = the draw node
+    for (int n = tid; n < M; n += kDecThreads) {
+      path[(int64_t)b * M + n] = n <= a ? n : -1;
+      if (n < a) out_tokens[(int64_t)b * M + n] = tok[n + 1];
+      if (probe != nullptr && n >= 1 && n <= min(fr, M - 1)) {
+        probe[((int64_t)b * M + n) * 4 + 0] = chain_p[n];
+        probe[((int64_t)b * M + n) * 4 + 1] = chain_q[n];
+      }
+    }
+    if (tid == 0) {
+      accepted_len[b] = a;
+      ctx.mT = rowM[0][a];
+      ctx.invST = (float)(1.0 / rowS[0][a]);
+      ctx.cs = cs;
+      ctx.nrej = fr < M ? 1 : 0;
+      if (fr < M) {
+        ctx.mD = rowM[1][a];
+        ctx.invSD = (float)(1.0 / rowS[1][a]);
+      } else {
+        ctx.mD = 0.f;
+        ctx.invSD = 0.f;
+      }
+    }
+    __syncthreads();
+    const double u = usmp[a];
+    if (fr < M) {
+      // the residual of node a: its chunk masses need a pass over two rows,
+      // spread over the whole GPU by the next kernel
+      DrawState& st = draws[b];
+      for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
+        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&ctx)[i];
+      if (tid == 0) {
+        st.node = a;
+        st.a = a;
+        st.u = u;
+        st.pending = 1;
+      }
+      return;
+    }
+    // the bonus token from p of the last node
+    const T* trow = target + ((int64_t)b * M + a) * V;
+    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
+    if (kAligned) {
+      if (warp == 0) {
+        float w;
+        double z;
+        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, ctx, u, &w, &z);
+        if (lane == 0) {
+          out_tokens[(int64_t)b * M + a] = tk;
+          if (probe != nullptr) {
+            probe[((int64_t)b * M + a) * 4 + 2] = 1.0f;
+            probe[((int64_t)b * M + a) * 4 + 3] = (float)((double)w / z);
+          }
+        }
+      }
+      return;
+    }
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, ctx, u, &ds, &s_trel, &s_chunk, &s_z);
+    if (tid == 0) {
+      out_tokens[(int64_t)b * M + a] = ds.token;
+      if (probe != nullptr) {
+        probe[((int64_t)b * M + a) * 4 + 2] = 1.0f;
+        probe[((int64_t)b * M + a) * 4 + 3] = (float)((double)ds.w / s_z);
+      }
+    }
+    return;
+  }
+
+  // ---- the walk of a tree ------------------------------------------------
   if (tid == 0) {
     s_node = 0;
     s_a = 0;
@@ -830,6 +1045,21 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       return;
     }
     const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
+    if (kAligned) {
+      if (warp == 0) {
+        float w;
+        double z;
+        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, ctx, u, &w, &z);
+        if (lane == 0) {
+          out_tokens[(int64_t)b * M + s_a] = tk;
+          if (probe != nullptr) {
+            probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
+            probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / z);
+          }
+        }
+      }
+      return;
+    }
     draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, ctx, u, &ds, &s_trel, &s_chunk, &s_z);
     if (tid == 0) {
       out_tokens[(int64_t)b * M + s_a] = ds.token;
@@ -842,116 +1072,139 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   }
 }
 
-// Pass 3: mass of each chunk of the pending residual laws, one CTA per
-// (chunk, request).
+// Passes 3 and 4: the residual draws.
+// Pass 3, one CTA per (kResSpan statistics chunks, request) with a pending
+// residual: the mass of max(0, P - q) over each of its chunks, all loads in
+// flight together (fp32 within a warp, fp64 across warps).
+constexpr int kResThreads = 256;
+// statistics chunks per CTA (one 16-byte vector per thread each); small spans
+// (many short CTAs) measured faster than long ones at 128 requests x 152k
+constexpr int kResSpan = 2;
+static_assert(kResThreads * 8 == 2048, "a statistics chunk is kResThreads vectors");
+
+__host__ __device__ __forceinline__ int rs_res_spans(int n_chunks) {
+  return (n_chunks + kResSpan - 1) / kResSpan;
+}
+
 template <typename T, bool kAligned>
-__global__ void __launch_bounds__(kRsThreads) rs_residual_sums_kernel(
+__global__ void __launch_bounds__(kResThreads) rs_residual_sums_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
     int chunk, const DrawState* __restrict__ draws, double* __restrict__ zsum) {
-  // n_chunks / chunk: the draw chunks (kRsThreads * kRsVecs vectors)
   constexpr int EPV = 16 / sizeof(T);
-  const int c = (int)(blockIdx.x % n_chunks), b = (int)(blockIdx.x / n_chunks), tid = threadIdx.x;
+  const int n_spans = rs_res_spans(n_chunks);
+  const int sp = (int)(blockIdx.x % n_spans), b = (int)(blockIdx.x / n_spans), tid = threadIdx.x;
+  const int warp = tid / kWarp, lane = tid % kWarp;
   __shared__ DecideCtx ctx;
-  __shared__ int s_node, s_pending;
-  __shared__ double s_red[kRsThreads / kWarp];
-  if (tid == 0) {
-    s_pending = draws[b].pending;
-    s_node = draws[b].node;
-  }
+  __shared__ float s_red[kResThreads / kWarp][kResSpan];
+  asm volatile("griddepcontrol.launch_dependents;");
+  // the decisions come from the previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the draw state in one round trip: the scalars to registers, the law to
+  // shared memory
+  const DrawState* dsb = draws + b;
+  const int pending = dsb->pending, node = dsb->node;
+  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kResThreads)
+    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&dsb->c)[i];
+  if (!pending) return;
   __syncthreads();
-  if (!s_pending) return;
-  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kRsThreads)
-    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&draws[b].c)[i];
-  __syncthreads();
-  const T* trow = target + ((int64_t)b * d.M + s_node) * d.V;
-  const T* drow = draft + ((int64_t)b * d.M + s_node) * d.V;
-  const int nrej = ctx.nrej;
-  float acc = 0.f;
-  const int64_t e0 = (int64_t)c * chunk;
+  const T* trow = target + ((int64_t)b * d.M + node) * d.V;
+  const T* drow = draft + ((int64_t)b * d.M + node) * d.V;
+  // thread t takes vector t of each chunk of the span
+  float acc[kResSpan];
 #pragma unroll
-  for (int v = 0; v < kRsVecs; ++v) {
+  for (int j = 0; j < kResSpan; ++j) {
+    const int k = sp * kResSpan + j;
     float w[EPV];
-    acc += vec_weights<T, kAligned>(trow, drow, e0 + ((int64_t)v * kRsThreads + tid) * EPV, d.V,
-                                    ctx, nrej, w);
+    acc[j] = k < n_chunks ? vec_weights<T, kAligned>(trow, drow,
+                                                     (int64_t)k * chunk + (int64_t)tid * EPV, d.V,
+                                                     ctx, ctx.nrej, w)
+                          : 0.f;
   }
-  double s = warp_sum((double)acc);
-  if (tid % kWarp == 0) s_red[tid / kWarp] = s;
+#pragma unroll
+  for (int j = 0; j < kResSpan; ++j) {
+    const float sj = warp_sum(acc[j]);
+    if (lane == 0) s_red[warp][j] = sj;
+  }
   __syncthreads();
-  if (tid == 0) {
+  if (tid < kResSpan && sp * kResSpan + tid < n_chunks) {
     double t = 0.0;
 #pragma unroll
-    for (int w = 0; w < kRsThreads / kWarp; ++w) t += s_red[w];
-    zsum[(int64_t)b * n_chunks + c] = t;
+    for (int w = 0; w < kResThreads / kWarp; ++w) t += (double)s_red[w][tid];
+    zsum[(int64_t)b * n_chunks + sp * kResSpan + tid] = t;
   }
 }
 
-// Pass 4: the residual draw of each pending request.
+// Pass 4, one CTA per request with a pending residual: picks the chunk from
+// the masses and searches it element by element (one warp for aligned rows).
 template <typename T, bool kAligned>
-__global__ void __launch_bounds__(kDecThreads) rs_residual_draw_kernel(
+__global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
-    int chunk, int n_dchunks, int dchunk, const RowStat* __restrict__ stats,
-    const DrawState* __restrict__ draws, const double* __restrict__ zsum,
-    int32_t* __restrict__ out_tokens, float* __restrict__ probe) {
+    int chunk, const RowStat* __restrict__ stats, const DrawState* __restrict__ draws,
+    const double* __restrict__ zsum, int32_t* __restrict__ out_tokens, float* __restrict__ probe) {
   const int b = blockIdx.x, tid = threadIdx.x;
+  const int warp = tid / kWarp, lane = tid % kWarp;
   __shared__ DecideCtx ctx;
   __shared__ DrawScratch ds;
-  __shared__ int s_pending, s_node, s_a, s_chunk, s_fallback;
-  __shared__ double s_trel, s_z, s_u;
-  if (tid == 0) {
-    s_pending = draws[b].pending;
-    s_node = draws[b].node;
-    s_a = draws[b].a;
-    s_u = draws[b].u;
-  }
+  __shared__ int s_chunk;
+  __shared__ double s_trel, s_z;
+  asm volatile("griddepcontrol.launch_dependents;");
+  // the chunk masses come from the previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const DrawState* dsb = draws + b;
+  const int pending = dsb->pending, node = dsb->node, a_acc = dsb->a;
+  const double u = dsb->u;
+  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kResThreads)
+    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&dsb->c)[i];
+  if (!pending) return;
   __syncthreads();
-  if (!s_pending) return;
-  for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
-    reinterpret_cast<uint32_t*>(&ctx)[i] = reinterpret_cast<const uint32_t*>(&draws[b].c)[i];
-  const double* zs = zsum + (int64_t)b * n_dchunks;
-  if (tid == 0) {
-    double Z = 0.0;
-    for (int k = 0; k < n_dchunks; ++k) Z += zs[k];
-    s_z = Z;
-    s_fallback = !(Z > 0.0);
-    if (!s_fallback) {
-      const double t = s_u * Z;
-      double pre = 0.0;
-      int sel = -1, lastpos = 0;
-      for (int k = 0; k < n_dchunks; ++k) {
-        if (zs[k] > 0.0) lastpos = k;
-        if (sel < 0 && pre + zs[k] > t) {
-          sel = k;
-          break;
-        }
-        pre += zs[k];
-      }
-      if (sel < 0) {
-        sel = lastpos;
-        pre = 0.0;
-        for (int k = 0; k < sel; ++k) pre += zs[k];
-      }
-      s_chunk = sel;
-      s_trel = t - pre;
-    }
-  }
-  __syncthreads();
-  const int M = d.M, node = s_node;
+  const int M = d.M;
   const T* trow = target + ((int64_t)b * M + node) * d.V;
   const T* drow = draft + ((int64_t)b * M + node) * d.V;
+  const double* zs = zsum + (int64_t)b * n_chunks;
+  if (warp == 0) {
+    double Z = 0.0;
+    for (int k = lane; k < n_chunks; k += kWarp) Z += zs[k];
+    Z = warp_sum(Z);
+    if (Z > 0.0) {
+      double pre;
+      const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
+      if (kAligned) {
+        const double trel = u * Z - pre;
+        const float th = (float)trel;
+        float w;
+        const int tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, d.V, ctx, ctx.nrej,
+                                          dfloat{th, (float)(trel - (double)th)}, &w);
+        if (lane == 0) {
+          out_tokens[(int64_t)b * M + a_acc] = tk;
+          if (probe != nullptr) {
+            probe[((int64_t)b * M + node) * 4 + 2] = (float)Z;
+            probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / Z);
+          }
+        }
+      }
+      if (lane == 0) {
+        s_chunk = sel;
+        s_trel = u * Z - pre;
+      }
+    }
+    if (lane == 0) s_z = Z;
+  }
+  __syncthreads();
+  if (s_z > 0.0 && kAligned) return;
   double Zrep;
-  if (s_fallback) {
+  if (!(s_z > 0.0)) {
     // a residual of zero mass: draw from p of the node instead
     const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
-    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, d.V, ctx, s_u, &ds, &s_trel, &s_chunk,
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, d.V, ctx, u, &ds, &s_trel, &s_chunk,
                              &s_z);
     Zrep = 1.0;
   } else {
-    chunk_draw<T, kAligned>(trow, drow, (int64_t)s_chunk * dchunk, dchunk, d.V, ctx, ctx.nrej,
+    chunk_draw<T, kAligned>(trow, drow, (int64_t)s_chunk * chunk, chunk, d.V, ctx, ctx.nrej,
                             s_trel, &ds);
     Zrep = s_z;
   }
   if (tid == 0) {
-    out_tokens[(int64_t)b * M + s_a] = ds.token;
+    out_tokens[(int64_t)b * M + a_acc] = ds.token;
     if (probe != nullptr) {
       probe[((int64_t)b * M + node) * 4 + 2] = (float)Zrep;
       probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)ds.w / s_z);
@@ -990,15 +1243,34 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
     rs_rowstats_kernel<T, false><<<g1, kRsThreads, 0, st>>>(tgt, dft, a.parent, a.temperature, d,
                                                           lay.rs_chunks, stats);
   }
-  rs_decide_kernel<T, kAligned><<<d.B, kDecThreads, 0, st>>>(
-      tgt, dft, a.tokens, a.parent, a.temperature, a.seed, a.offset, a.b_base, a.out_tokens, a.path,
-      a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk, stats, draws, status);
-  rs_residual_sums_kernel<T, kAligned><<<(unsigned)((int64_t)lay.rs_dchunks * d.B), kRsThreads, 0,
-                                         st>>>(tgt, dft, d, lay.rs_dchunks, lay.rs_dchunk, draws,
-                                               zsum);
-  rs_residual_draw_kernel<T, kAligned><<<d.B, kDecThreads, 0, st>>>(
-      tgt, dft, d, lay.rs_chunks, lay.rs_chunk, lay.rs_dchunks, lay.rs_dchunk, stats, draws, zsum,
-      a.out_tokens, a.probe);
+  // passes 2 and 3 start while their predecessor drains (programmatic
+  // dependent launch); each waits for its predecessor's results in-kernel
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)d.B);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, rs_decide_kernel<T, kAligned>, tgt, dft, a.tokens,
+                                     a.parent, a.temperature, a.seed, a.offset, a.b_base,
+                                     a.out_tokens, a.path, a.accepted_len, a.probe, d,
+                                     lay.rs_chunks, lay.rs_chunk, (const RowStat*)stats, draws,
+                                     status);
+  if (e != cudaSuccess) return e;
+  cfg.blockDim = dim3(kResThreads);
+  cfg.gridDim = dim3((unsigned)((int64_t)rs_res_spans(lay.rs_chunks) * d.B));
+  e = cudaLaunchKernelEx(&cfg, rs_residual_sums_kernel<T, kAligned>, tgt, dft, d, lay.rs_chunks,
+                         lay.rs_chunk, (const DrawState*)draws, zsum);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)d.B);
+  e = cudaLaunchKernelEx(&cfg, rs_residual_draw_kernel<T, kAligned>, tgt, dft, d, lay.rs_chunks,
+                         lay.rs_chunk, (const RowStat*)stats, (const DrawState*)draws,
+                         (const double*)zsum, a.out_tokens, a.probe);
+  if (e != cudaSuccess) return e;
   *launches += 4;
   return cudaGetLastError();
 }

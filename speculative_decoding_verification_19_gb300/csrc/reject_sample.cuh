@@ -50,7 +50,6 @@ struct RsArgs {
 };
 
 int rs_chunk_elems(int logits_dtype);       // statistics chunk (one warp task)
-int rs_draw_chunk_elems(int logits_dtype);  // chunk of the residual passes
 int rs_max_vocab(int logits_dtype);
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
 

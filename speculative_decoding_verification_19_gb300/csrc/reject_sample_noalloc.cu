@@ -66,12 +66,10 @@ extern "C" spec_status spec_reject_sample_noalloc(
   lay.rs_off = kNoAllocStatusBytes;
   lay.rs_chunk = rs_chunk_elems(dims->logits_dtype);
   lay.rs_chunks = (int)ceil_div64(dims->V, lay.rs_chunk);
-  lay.rs_dchunk = rs_draw_chunk_elems(dims->logits_dtype);
-  lay.rs_dchunks = (int)ceil_div64(dims->V, lay.rs_dchunk);
   lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
   lay.rs_draw_off = (lay.rs_off + lay.rs_bytes + 255) / 256 * 256;
   lay.rs_zsum_off = (lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B + 255) / 256 * 256;
-  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_dchunks;
+  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;

@@ -40,17 +40,20 @@ METRIC = "verify steps/s and accepted tokens/s at 1 GB300; achieved HBM TB/s vs 
 UNIT = "verify steps/s"
 DEFAULT_WORKLOAD = "stress_gqa_152k"
 
-# DRAM traffic of one spec_verify_attn call measured by ncu on the workload
-# below (profiles/verify_attn_stress_gqa_152k.md), valid only for the kernel
-# sources whose digest is recorded with it.
-TRAFFIC = {"digest": None, "bytes_per_call": None}
+# DRAM traffic of one spec_verify_attn call (append + plan + split + combine
+# kernels) measured by ncu on 16 of the 128 requests of the default workload
+# and scaled to 128 by the algorithmic bytes (traffic grows with the KV
+# bytes read): profiles/attn_tc_kernel_stress_gqa_152k_b16.md.  Valid only
+# for the attention kernel sources whose digest is recorded with it.
+TRAFFIC = {"digest": "adfe9889876a3cc3", "bytes_per_call": 10137161312}
+TRAFFIC_ALG_BYTES = 10051956736  # algorithmic bytes per call of that workload (seed 0)
 
 
 def attn_sources_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_19_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("attn") or f in ("api.cu", "common.cuh", "tc_ptx.cuh"):
+        if f.startswith("attn") or f in ("common.cuh", "tc_ptx.cuh"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]
@@ -378,7 +381,11 @@ def run_native(args, wl, world, rank, local):
 
     peaks = measured_peaks()
     achieved = attn_b / (attn_ms / 1e3) / 1e9
-    traffic = TRAFFIC["bytes_per_call"] if TRAFFIC["digest"] == attn_sources_digest() else None
+    # the recorded traffic belongs to the default workload at its full size
+    # (the bytes per call of the run it was scaled to) and to these sources
+    traffic = (TRAFFIC["bytes_per_call"]
+               if TRAFFIC["digest"] == attn_sources_digest() and attn_b == TRAFFIC_ALG_BYTES
+               else None)
     line = {
         "metric": METRIC, "value": round(steps_per_s, 3), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": W,

@@ -563,10 +563,14 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(
     const float* __restrict__ part, const int32_t* __restrict__ ntiles,
     const int32_t* __restrict__ prefix, spec_dims d, int G, T* __restrict__ out,
     float* __restrict__ lse) {
-  const int h = blockIdx.x, b = blockIdx.y;
+  // one warp per query row: blockIdx.x = group of 4 rows, y = KV head, z = request
+  const int h = blockIdx.y, b = blockIdx.z;
   const int group = d.Hq / d.Hkv;
   const int R = group * d.M;
   const int D = d.D;
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  const int r = blockIdx.x * (blockDim.x / kWarp) + warp;
+  if (r >= R) return;
   const int64_t Ttot = prefix[d.B];
   const int nt = ntiles[b];
   int c_first = 1, c_last = 0;
@@ -576,39 +580,42 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(
     c_last = (int)((pe * G - 1) / Ttot);
   }
   const int64_t pair = (int64_t)b * d.Hkv + h;
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  for (int r = warp; r < R; r += blockDim.x / kWarp) {
-    const int i = r / group, hq = h * group + r % group;
-    // A partial row holds unnormalised O, the running maximum m (log2
-    // units) and the two half-tile shares of the row sum.  CTAs with an
-    // empty tile range wrote nothing (their slot may belong to a
-    // neighbouring pair), so they are skipped.
-    const int S = tc_part_stride(D);
-    float m = -INFINITY;
+  const int i = r / group, hq = h * group + r % group;
+  // A partial row holds unnormalised O, the running maximum m (log2 units)
+  // and the two half-tile shares of the row sum.  CTAs with an empty tile
+  // range wrote nothing (their slot may belong to a neighbouring pair), so
+  // they are skipped.  Lane c reads the scalars of partial c_first + c (all
+  // partials in one round trip), then every lane its D / 32 values of each.
+  const int S = tc_part_stride(D);
+  const int np = c_last - c_first + 1;
+  float m = -INFINITY;
+  for (int c0 = 0; c0 < np; c0 += kWarp) {
+    const int cc = c_first + c0 + lane;
+    float mc = -INFINITY;
+    if (c0 + lane < np && (int64_t)cc * Ttot / G != (int64_t)(cc + 1) * Ttot / G) {
+      const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
+      if (prow[D + 1] + prow[D + 2] > 0.f) mc = prow[D];
+    }
+    m = fmaxf(m, warp_max(mc));
+  }
+  float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (m != -INFINITY) {
     for (int cc = c_first; cc <= c_last; ++cc) {
       if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
       const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
-      if (prow[D + 1] + prow[D + 2] > 0.f) m = fmaxf(m, prow[D]);
+      const float lp = prow[D + 1] + prow[D + 2];
+      if (!(lp > 0.f)) continue;
+      const float w = exp2f(prow[D] - m);
+      wsum += w * lp;
+      for (int k = 0; k < D / kWarp; ++k) acc[k] += w * prow[lane + k * kWarp];
     }
-    float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (m != -INFINITY) {
-      for (int cc = c_first; cc <= c_last; ++cc) {
-        if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
-        const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
-        const float lp = prow[D + 1] + prow[D + 2];
-        if (!(lp > 0.f)) continue;
-        const float w = exp2f(prow[D] - m);
-        wsum += w * lp;
-        for (int k = 0; k < D / kWarp; ++k) acc[k] += w * prow[lane + k * kWarp];
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    T* orow = out + (((int64_t)b * d.M + i) * d.Hq + hq) * D;
-    for (int k = 0; k < D / kWarp; ++k) orow[lane + k * kWarp] = from_f32<T>(acc[k] * inv);
-    if (lse != nullptr && lane == 0)
-      lse[((int64_t)b * d.M + i) * d.Hq + hq] =
-          wsum > 0.f ? (m + log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  T* orow = out + (((int64_t)b * d.M + i) * d.Hq + hq) * D;
+  for (int k = 0; k < D / kWarp; ++k) orow[lane + k * kWarp] = from_f32<T>(acc[k] * inv);
+  if (lse != nullptr && lane == 0)
+    lse[((int64_t)b * d.M + i) * d.Hq + hq] =
+        wsum > 0.f ? (m + log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -690,8 +697,11 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
                                                    a.parent, ntiles, prefix, d, qscale2, part,
                                                    status);
   ++*launches;
-  attn_tc_combine_kernel<__nv_bfloat16><<<dim3(d.Hkv, d.B), 128, 0, st>>>(
-      part, ntiles, prefix, d, G, static_cast<__nv_bfloat16*>(a.out), a.lse);
+  {
+    const int R = (d.Hq / d.Hkv) * d.M;
+    attn_tc_combine_kernel<__nv_bfloat16><<<dim3((R + 3) / 4, d.Hkv, d.B), 128, 0, st>>>(
+        part, ntiles, prefix, d, G, static_cast<__nv_bfloat16*>(a.out), a.lse);
+  }
   ++*launches;
   return cudaGetLastError();
 }

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     T* __restrict__ v_cache, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ parent, spec_dims d,
     int32_t* __restrict__ req_ok, uint32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // the inputs and the cache may come from the previous kernel
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int ctx = ctx_lens[b];
@@ -332,19 +334,22 @@ cudaError_t kv_append_launch(const AttnArgs& a, const WsLayout& lay, cudaStream_
   const spec_dims& d = a.d;
   int32_t* req_ok = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + lay.attn_ok_off);
   uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(a.ws) + lay.status_off);
+  PdlLaunch L(dim3(d.B), dim3(256), 0, st);
+  cudaError_t e;
   if (d.kv_dtype == SPEC_BF16) {
     using T = __nv_bfloat16;
-    kv_append_kernel<T><<<d.B, 256, 0, st>>>(
-        static_cast<const T*>(a.k_new), static_cast<const T*>(a.v_new), static_cast<T*>(a.k_cache),
-        static_cast<T*>(a.v_cache), a.block_table, a.ctx_lens, a.parent, d, req_ok, status);
+    e = cudaLaunchKernelEx(&L.cfg, kv_append_kernel<T>, static_cast<const T*>(a.k_new),
+                           static_cast<const T*>(a.v_new), static_cast<T*>(a.k_cache),
+                           static_cast<T*>(a.v_cache), a.block_table, a.ctx_lens, a.parent, d,
+                           req_ok, status);
   } else {
-    kv_append_kernel<float><<<d.B, 256, 0, st>>>(
-        static_cast<const float*>(a.k_new), static_cast<const float*>(a.v_new),
-        static_cast<float*>(a.k_cache), static_cast<float*>(a.v_cache), a.block_table, a.ctx_lens,
-        a.parent, d, req_ok, status);
+    e = cudaLaunchKernelEx(&L.cfg, kv_append_kernel<float>, static_cast<const float*>(a.k_new),
+                           static_cast<const float*>(a.v_new), static_cast<float*>(a.k_cache),
+                           static_cast<float*>(a.v_cache), a.block_table, a.ctx_lens, a.parent,
+                           d, req_ok, status);
   }
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>

@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const int group = d.Hq / d.Hkv;
   const int R = group * M;
   const int G = gridDim.x, c = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the tile plan and the appended rows come from the previous kernels
   const int64_t T = prefix[B];
   const int64_t g0 = (int64_t)c * T / G, g1 = (int64_t)(c + 1) * T / G;
   if (g0 >= g1) return;  // uniform: nothing allocated yet
@@ -527,6 +529,8 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ prefix) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
+  pdl_trigger();
+  pdl_wait();  // the append's per-request verdicts
   const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
   if (tid == 0) carry = 0;
   __syncthreads();
@@ -570,6 +574,8 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(
   const int D = d.D;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int r = blockIdx.x * (blockDim.x / kWarp) + warp;
+  pdl_trigger();
+  pdl_wait();  // the partials come from the previous kernel
   if (r >= R) return;
   const int64_t Ttot = prefix[d.B];
   const int nt = ntiles[b];
@@ -687,20 +693,32 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   const int G = sms < kMaxAttnCtas ? sms : kMaxAttnCtas;
 
   kv_append_launch(a, lay, st, launches);
-  attn_plan_kernel<<<1, 1024, 0, st>>>(a.ctx_lens, req_ok, d, ntiles, prefix);
+  {
+    PdlLaunch L(dim3(1), dim3(1024), 0, st);
+    e = cudaLaunchKernelEx(&L.cfg, attn_plan_kernel, a.ctx_lens, (const int32_t*)req_ok, d, ntiles,
+                           prefix);
+    if (e != cudaSuccess) return e;
+  }
   ++*launches;
   e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const float qscale2 = a.scale * 1.4426950408889634f;
-  attn_tc_kernel<<<G, kThreads, kSmemBytes, st>>>(tm_q, tm_k, tm_v, a.block_table, a.ctx_lens,
-                                                   a.parent, ntiles, prefix, d, qscale2, part,
-                                                   status);
+  {
+    PdlLaunch L(dim3(G), dim3(kThreads), kSmemBytes, st);
+    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q, tm_k, tm_v, a.block_table, a.ctx_lens,
+                           a.parent, (const int32_t*)ntiles, (const int32_t*)prefix, d, qscale2,
+                           part, status);
+    if (e != cudaSuccess) return e;
+  }
   ++*launches;
   {
     const int R = (d.Hq / d.Hkv) * d.M;
-    attn_tc_combine_kernel<__nv_bfloat16><<<dim3((R + 3) / 4, d.Hkv, d.B), 128, 0, st>>>(
-        part, ntiles, prefix, d, G, static_cast<__nv_bfloat16*>(a.out), a.lse);
+    PdlLaunch L(dim3((R + 3) / 4, d.Hkv, d.B), dim3(128), 0, st);
+    e = cudaLaunchKernelEx(&L.cfg, attn_tc_combine_kernel<__nv_bfloat16>, (const float*)part,
+                           (const int32_t*)ntiles, (const int32_t*)prefix, d, G,
+                           static_cast<__nv_bfloat16*>(a.out), a.lse);
+    if (e != cudaSuccess) return e;
   }
   ++*launches;
   return cudaGetLastError();

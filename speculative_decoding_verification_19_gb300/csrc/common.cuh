@@ -82,6 +82,33 @@ __device__ __forceinline__ int warp_or(int v) {
   return __reduce_or_sync(0xffffffffu, (unsigned)v);
 }
 
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with PdlLaunch may start
+// while its predecessor on the stream drains; it must call pdl_wait() before
+// touching memory a predecessor writes (which also keeps the chain
+// transitive), and calls pdl_trigger() early to let its own dependents launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+struct PdlLaunch {  // use in place: cfg points at attr
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg;
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+  }
+  PdlLaunch(const PdlLaunch&) = delete;
+  PdlLaunch& operator=(const PdlLaunch&) = delete;
+};
+
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     T* __restrict__ k_cache, T* __restrict__ v_cache, const int32_t* __restrict__ block_table,
     const int32_t* ctx_lens, int32_t* new_ctx_lens, const int32_t* __restrict__ path,
     const int32_t* __restrict__ accepted_len, spec_dims d, uint32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // path and accepted_len come from the previous kernel
   const int b = blockIdx.x, tid = threadIdx.x;
   const int ctx = ctx_lens[b];
   const int a = accepted_len[b];
@@ -72,11 +74,12 @@ template <typename T>
 static cudaError_t launch_commit_t(const CommitArgs& a, const WsLayout& lay, cudaStream_t st,
                                    int* launches) {
   uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<char*>(a.ws) + lay.status_off);
-  kv_commit_kernel<T><<<a.d.B, 256, 0, st>>>(static_cast<T*>(a.k_cache), static_cast<T*>(a.v_cache),
-                                            a.block_table, a.ctx_lens, a.new_ctx_lens, a.path,
-                                            a.accepted_len, a.d, status);
+  PdlLaunch L(dim3(a.d.B), dim3(256), 0, st);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kv_commit_kernel<T>, static_cast<T*>(a.k_cache),
+                                           static_cast<T*>(a.v_cache), a.block_table, a.ctx_lens,
+                                           a.new_ctx_lens, a.path, a.accepted_len, a.d, status);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t commit_launch(const CommitArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {

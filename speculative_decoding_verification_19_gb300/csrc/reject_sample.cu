@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
   const int64_t nw = (int64_t)gridDim.x * (kRsThreads / kWarp);
   const int64_t ntask = (int64_t)d.B * 2 * d.M * n_chunks;
   const int M = d.M, V = d.V;
-  asm volatile("griddepcontrol.launch_dependents;");
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
   int64_t t = next_needed((int64_t)blockIdx.x * (kRsThreads / kWarp) + threadIdx.x / kWarp, nw,
                           ntask, n_chunks, parent, M);
 
@@ -243,6 +244,8 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     uint32_t* __restrict__ status) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kChunk = kWarp * kStatVecs * EPV;
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -728,9 +731,8 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   __shared__ int chain_rej[kMaxM];  // chain: the accept test of node n failed
   __shared__ float chain_p[kMaxM], chain_q[kMaxM];
 
-  asm volatile("griddepcontrol.launch_dependents;");
-  // the statistics come from the previous kernel on the stream
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();  // the statistics come from the previous kernel
 
   // defined outputs first
   for (int i = tid; i < M; i += kDecThreads) {
@@ -1096,9 +1098,8 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_sums_kernel(
   const int warp = tid / kWarp, lane = tid % kWarp;
   __shared__ DecideCtx ctx;
   __shared__ float s_red[kResThreads / kWarp][kResSpan];
-  asm volatile("griddepcontrol.launch_dependents;");
-  // the decisions come from the previous kernel on the stream
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();  // the decisions come from the previous kernel
   // the draw state in one round trip: the scalars to registers, the law to
   // shared memory
   const DrawState* dsb = draws + b;
@@ -1147,9 +1148,8 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
   __shared__ DrawScratch ds;
   __shared__ int s_chunk;
   __shared__ double s_trel, s_z;
-  asm volatile("griddepcontrol.launch_dependents;");
-  // the chunk masses come from the previous kernel on the stream
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();  // the chunk masses come from the previous kernel
   const DrawState* dsb = draws + b;
   const int pending = dsb->pending, node = dsb->node, a_acc = dsb->a;
   const double u = dsb->u;
@@ -1236,12 +1236,16 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kBulkSmem);
     if (e != cudaSuccess) return e;
-    rs_rowstats_bulk_kernel<T><<<gb, kBulkWarps * kWarp, kBulkSmem, st>>>(
-        tgt, dft, a.parent, a.temperature, d, lay.rs_chunks, stats, status);
+    PdlLaunch L(dim3(gb), dim3(kBulkWarps * kWarp), kBulkSmem, st);
+    e = cudaLaunchKernelEx(&L.cfg, rs_rowstats_bulk_kernel<T>, tgt, dft, a.parent, a.temperature,
+                           d, lay.rs_chunks, stats, status);
+    if (e != cudaSuccess) return e;
   } else {
     const unsigned g1 = (unsigned)(want < 2 * sms ? want : 2 * sms);
-    rs_rowstats_kernel<T, false><<<g1, kRsThreads, 0, st>>>(tgt, dft, a.parent, a.temperature, d,
-                                                          lay.rs_chunks, stats);
+    PdlLaunch L(dim3(g1), dim3(kRsThreads), 0, st);
+    const cudaError_t e = cudaLaunchKernelEx(&L.cfg, rs_rowstats_kernel<T, false>, tgt, dft,
+                                             a.parent, a.temperature, d, lay.rs_chunks, stats);
+    if (e != cudaSuccess) return e;
   }
   // passes 2 and 3 start while their predecessor drains (programmatic
   // dependent launch); each waits for its predecessor's results in-kernel

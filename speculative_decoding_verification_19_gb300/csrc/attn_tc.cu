@@ -18,16 +18,21 @@
 // Per CTA, warp-specialised:
 //   warp 10     TMA producer: Q of each pair (two 64-column halves) and the
 //               K and V pages of each tile into a 4-stage ring (32 KB/stage)
-//   warp 11     MMA issuer: S = Q K^T into TMEM (double-buffered), then
-//               O += P V with P read back from TMEM (aliasing S)
+//   warp 11     MMA issuer of S = Q K^T into TMEM (four buffers)
+//   warp 9      MMA issuer of O += P V, P read back from TMEM (aliasing S);
+//               two issuing threads because each tcgen05.mma takes about 90
+//               cycles to issue, and one thread issuing both products of a
+//               tile was the kernel's bottleneck
 //   warps 0..7  softmax: one thread per query row (TMEM lane) and per half
 //               tile (32 keys); the two halves of a row swap their maxima
 //               through shared memory, exp2, P written as bf16 into TMEM;
 //               O is rescaled in TMEM only when the running maximum grows by
 //               more than 2^8
-//   warps 8, 9  idle (they keep the two issuing roles off the sub-partitions
-//               of the softmax warps for rows 0..63).
-// TMEM: S0 cols [0,64), S1 [64,128), O [128,256).
+//   warp 8      idle.
+// TMEM: S0..S3 cols [0,64) .. [192,256), O [256,384).  Four S buffers let
+// Q K^T of tile t wait only for P V of tile t-4: the hand-off chain QK ->
+// softmax -> PV -> QK of a buffer is spread over four tiles in flight (the
+// K/V ring of four stages bounds the look-ahead to about three).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -42,40 +47,43 @@ namespace tc {
 constexpr int kTileKeys = 64;
 constexpr int kPages = kTileKeys / kBlock;  // 4
 constexpr int kStages = 4;
+constexpr int kQBufs = 2;  // Q buffers (two: the next pair's Q loads while the current one runs)
 constexpr int kThreads = 384;
 // Warp roles.  A warp may only touch the TMEM lanes of its sub-partition
 // (warp % 4).  Softmax warps 0..7: warp w serves rows 32*(w%4).. and the
-// half w/4 of each tile's 64 keys.  The producer and the MMA issuer sit on
+// half w/4 of each tile's 64 keys.  The producer and the Q K^T issuer sit on
 // sub-partitions 2 and 3, away from the softmax warps of rows 0..63 (the
-// common case R <= 64); warps 8 and 9 stay idle.
+// common case R <= 64); the P V issuer is warp 9; warp 8 stays idle.
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 10;
-constexpr int kMmaWarp = 11;
+constexpr int kMmaWarp = 11;  // issues Q K^T
+constexpr int kPvWarp = 9;    // issues P V
 constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
 constexpr int kHalfBytes = kPages * kBoxBytes;  // 8 KB
 constexpr int kStageBytes = 4 * kHalfBytes;     // K lo, K hi, V lo, V hi
 constexpr int kQHalfBytes = 128 * 128;          // 128 rows x 128 B
 constexpr int kQBytes = 2 * kQHalfBytes;
-constexpr int kTmemCols = 256;
-constexpr int kOCol = 128;
+constexpr int kSBufs = 4;  // S buffers in TMEM
+constexpr int kTmemCols = 512;
+constexpr int kOCol = kSBufs * kTileKeys;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
 
 struct __align__(8) Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];  // completion of PV(t) lands on o_done[t & 1]
-  uint64_t drain;
+  uint64_t q_full[kQBufs];
+  uint64_t q_empty[kQBufs];
+  uint64_t s_full[kSBufs];
+  uint64_t p_full[kSBufs];
+  uint64_t o_done[kSBufs];  // completion of PV(t) lands on o_done[t % kSBufs]
+  uint64_t drain[2];  // the Q K^T issuer's and the P V issuer's last completion
   uint64_t xbar[4][2];       // per sub-partition, per tile parity: both halves' maxima
   float xmax[2][2][128];     // [tile parity][half][row]
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 2 * kQBytes + sizeof(Bars) + 1024;
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kQBufs * kQBytes + sizeof(Bars) + 1024;
 
 size_t smem_bytes() { return kSmemBytes; }
 
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                                              ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint8_t* qbufs = smem + kStages * kStageBytes;
-  Bars* bars = reinterpret_cast<Bars*>(qbufs + 2 * kQBytes);
+  Bars* bars = reinterpret_cast<Bars*>(qbufs + kQBufs * kQBytes);
 
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int B = d.B, Hkv = d.Hkv, M = d.M;
@@ -151,8 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   if (g0 >= g1) return;  // uniform: nothing allocated yet
   const int n_sm_warps = ceil_div(R, 32);
 
-  // zero both Q buffers once: rows R..127 stay zero padding
-  for (int i = tid; i < 2 * kQBytes / 16; i += kThreads)
+  // zero the Q buffers once: rows R..127 stay zero padding
+  for (int i = tid; i < kQBufs * kQBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(qbufs)[i] = make_uint4(0, 0, 0, 0);
   ptx::fence_proxy_async_smem();
   if (tid == 0) {
@@ -160,15 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::mbar_init(ptx::smem_u32(&bars->full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQBufs; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 2 * n_sm_warps);
+      ptx::mbar_init(ptx::smem_u32(&bars->o_done[i]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->o_done[0]), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->o_done[1]), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain[1]), 1);
     for (int sp = 0; sp < 4; ++sp)
       for (int i = 0; i < 2; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[sp][i]), 2);
     bars->abort = 0;
@@ -207,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         L = ctx_lens[cu.b] + M;
         win = -1;
         if (lane == 0) {
-          const int qb = seg & 1;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg >> 1) & 1) ^ 1, abort,
+          const int qb = seg % kQBufs;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
                               kTimeoutNs);
           if (ok) {
             const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
@@ -265,79 +275,99 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
         ptx::mbar_wait(ptx::smem_u32(&bars->full[u % kStages]), (uint32_t)((u / kStages) & 1),
                        abort, kTimeoutNs);
-      for (int sg = seg > 0 ? seg - 1 : 0; sg <= seg; ++sg)
-        ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg & 1]), (uint32_t)((sg >> 1) & 1), abort,
-                       kTimeoutNs);
+      for (int sg = seg >= kQBufs ? seg - kQBufs + 1 : 0; sg <= seg; ++sg)
+        ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg % kQBufs]), (uint32_t)((sg / kQBufs) & 1),
+                       abort, kTimeoutNs);
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA
+    // ------------------------------------------------------------- MMA: Q K^T
     if (lane == 0) {
       const uint32_t id_qk_full = ptx::idesc_bf16_f32(128, kTileKeys, false, false);
-      const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
       Cursor cu;
       cu.seek(g0, ntiles, prefix, B);
-      int seg = -1;
+      int seg = -1, L = 0;
       int64_t t = 0;
-      bool have_prev = false;
-      int prev_stage = 0, prev_np = 0, prev_first = 0, L = 0;
-      bool ok = true;
-      auto issue_pv = [&](int64_t u) -> bool {
-        const int sbuf = (int)(u & 1);
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u >> 1) & 1), abort,
-                            kTimeoutNs))
-          return false;
-        ptx::tc_fence_after();
-        const uint32_t vbase = ptx::smem_u32(stages + prev_stage * kStageBytes + 2 * kHalfBytes);
-        for (int j = 0; j < prev_np; ++j) {
-          const uint64_t bdesc = ptx::sdesc_sw128(vbase + j * 2 * 1024, kHalfBytes, 1024);
-          ptx::mma_ts(tmem + kOCol, tmem + sbuf * kTileKeys + j * 8, bdesc, id_pv,
-                      (prev_first && j == 0) ? 0u : 1u);
-        }
-        ptx::mma_commit(ptx::smem_u32(&bars->o_done[u & 1]));
-        ptx::mma_commit(ptx::smem_u32(&bars->empty[prev_stage]));
-        return true;
-      };
-      for (int64_t g = g0; g < g1 && ok; ++g, ++t) {
+      // Shared-memory descriptors built once; an operand at byte offset o
+      // from a base is the base descriptor plus o >> 4 in the start-address
+      // field (shared addresses stay below 2^18, so the 14-bit field never
+      // carries).
+      const uint64_t dq0 = ptx::sdesc_sw128(ptx::smem_u32(qbufs), 16, 1024);
+      const uint64_t dk0 = ptx::sdesc_sw128(ptx::smem_u32(stages), 16, 1024);
+      for (int64_t g = g0; g < g1; ++g, ++t) {
         const bool first = (g == g0) || cu.tile == 0;
         const bool last = (g == g1 - 1) || cu.tile == cu.nt - 1;
         if (first) ++seg;
-        const int qb = seg & 1;
-        if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), (uint32_t)((seg >> 1) & 1),
-                                     abort, kTimeoutNs))
+        const int qb = seg % kQBufs;
+        if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]),
+                                     (uint32_t)((seg / kQBufs) & 1), abort, kTimeoutNs))
           break;
         const int stage = (int)(t % kStages);
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
                             abort, kTimeoutNs))
           break;
-        // PV(t-2) read P out of the S buffer this tile's QK writes
-        if (t >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t & 1]),
-                                      (uint32_t)(((t - 2) >> 1) & 1), abort, kTimeoutNs))
+        // PV(t - kSBufs) read P out of the S buffer this tile's QK writes
+        if (t >= kSBufs && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t % kSBufs]),
+                                           (uint32_t)(((t - kSBufs) / kSBufs) & 1), abort,
+                                           kTimeoutNs))
           break;
         ptx::tc_fence_after();
         if (first) L = ctx_lens[cu.b] + M;
         const int np = tile_pages(L, cu.tile);
         const uint32_t idqk = np == kPages ? id_qk_full : ptx::idesc_bf16_f32(128, np * 16, false, false);
-        const uint32_t qbase = ptx::smem_u32(qbufs + qb * kQBytes);
-        const uint32_t kbase = ptx::smem_u32(stages + stage * kStageBytes);
-        const int sbuf = (int)(t & 1);
+        const uint64_t dq = dq0 + (uint64_t)((qb * kQBytes) >> 4);
+        const uint64_t dk = dk0 + (uint64_t)((stage * kStageBytes) >> 4);
+        const int sbuf = (int)(t % kSBufs);
+        const uint32_t scol = tmem + sbuf * kTileKeys;
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = ptx::sdesc_sw128(qbase + (k >> 2) * kQHalfBytes + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(kbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          ptx::mma_ss(tmem + sbuf * kTileKeys, ad, bd, idqk, k > 0 ? 1u : 0u);
+          const uint64_t ad = dq + (uint64_t)(((k >> 2) * kQHalfBytes + (k & 3) * 32) >> 4);
+          const uint64_t bd = dk + (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+          ptx::mma_ss(scol, ad, bd, idqk, k > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[sbuf]));
         if (last) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qb]));
-        if (have_prev) ok = issue_pv(t - 1);
-        have_prev = true;
-        prev_stage = stage;
-        prev_np = np;
-        prev_first = first ? 1 : 0;
         cu.next(ntiles, B, Hkv);
       }
-      if (ok && have_prev && !*abort) issue_pv(t - 1);
       // all MMAs issued by this thread complete before TMEM is released
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, abort, kTimeoutNs);
+      ptx::mma_commit(ptx::smem_u32(&bars->drain[0]));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain[0]), 0, abort, kTimeoutNs);
+    }
+  } else if (warp == kPvWarp) {
+    // ---------------------------------------------------------------- MMA: P V
+    // A second issuing thread, so that the two products of a tile are issued
+    // side by side.  PV(u) follows the softmax of tile u (p_full) and frees the
+    // tile's stage and its S buffer when it completes.
+    if (lane == 0) {
+      const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+      const uint64_t dv0 = ptx::sdesc_sw128(ptx::smem_u32(stages + 2 * kHalfBytes), kHalfBytes, 1024);
+      Cursor cu;
+      cu.seek(g0, ntiles, prefix, B);
+      int L = 0;
+      int64_t u = 0;
+      for (int64_t g = g0; g < g1; ++g, ++u) {
+        const bool first = (g == g0) || cu.tile == 0;
+        if (first) L = ctx_lens[cu.b] + M;
+        const int np = tile_pages(L, cu.tile);
+        const int sbuf = (int)(u % kSBufs);
+        const int stage = (int)(u % kStages);
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u / kSBufs) & 1), abort,
+                            kTimeoutNs))
+          break;
+        ptx::tc_fence_after();
+        const uint64_t dv = dv0 + (uint64_t)((stage * kStageBytes) >> 4);
+        const uint32_t pcol = tmem + sbuf * kTileKeys;
+#pragma unroll
+        for (int j = 0; j < kPages; ++j) {
+          if (j < np)
+            ptx::mma_ts(tmem + kOCol, pcol + j * 8, dv + (uint64_t)((j * 2 * 1024) >> 4), id_pv,
+                        (first && j == 0) ? 0u : 1u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->o_done[sbuf]));
+        ptx::mma_commit(ptx::smem_u32(&bars->empty[stage]));
+        cu.next(ntiles, B, Hkv);
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->drain[1]));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain[1]), 0, abort, kTimeoutNs);
     }
   } else if (warp < kSoftmaxWarps) {
     // -------------------------------------------------------------- softmax
@@ -376,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             }
           }
         }
-        const int sbuf = (int)(t & 1);
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]), (uint32_t)((t >> 1) & 1), abort,
+        const int sbuf = (int)(t % kSBufs);  // S / P buffer in TMEM
+        const int xb = (int)(t & 1);          // maxima exchange buffer
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]), (uint32_t)((t / kSBufs) & 1), abort,
                             kTimeoutNs))
           break;
         ptx::tc_fence_after();
@@ -407,13 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           for (int j = 0; j < 32; ++j)
             mh = fmaxf(mh, score_of(sv[j], jbase + j, kpos0, nkeys, ctx, L, anc, real, false, qscale2));
         }
-        bars->xmax[sbuf][half][row] = mh;
+        bars->xmax[xb][half][row] = mh;
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xbar[sp][sbuf]));
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->xbar[sp][sbuf]), (uint32_t)((t >> 1) & 1), abort,
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xbar[sp][xb]));
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->xbar[sp][xb]), (uint32_t)((t >> 1) & 1), abort,
                             kTimeoutNs))
           break;
-        const float mt = fmaxf(bars->xmax[sbuf][0][row], bars->xmax[sbuf][1][row]);
+        const float mt = fmaxf(bars->xmax[xb][0][row], bars->xmax[xb][1][row]);
         bool need = false;
         if (first) {
           m_used = mt;
@@ -422,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
         if (__any_sync(0xffffffffu, need)) {
           // O is rescaled in place (this half's 64 columns): PV(t-1) must have landed
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) & 1]),
-                              (uint32_t)(((t - 1) >> 1) & 1), abort, kTimeoutNs))
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) % kSBufs]),
+                              (uint32_t)(((t - 1) / kSBufs) & 1), abort, kTimeoutNs))
             break;
           ptx::tc_fence_after();
           const float f = need ? exp2f(m_used - mt) : 1.f;
@@ -479,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sbuf]));
         if (last) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t & 1]), (uint32_t)((t >> 1) & 1), abort,
-                              kTimeoutNs))
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[sbuf]), (uint32_t)((t / kSBufs) & 1),
+                              abort, kTimeoutNs))
             break;
           ptx::tc_fence_after();
           // partial: unnormalised O (this half's 64 columns), the running

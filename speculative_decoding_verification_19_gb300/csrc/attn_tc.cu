@@ -152,13 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const int group = d.Hq / d.Hkv;
   const int R = group * M;
   const int G = gridDim.x, c = blockIdx.x;
-  pdl_trigger();
-  pdl_wait();  // the tile plan and the appended rows come from the previous kernels
-  const int64_t T = prefix[B];
-  const int64_t g0 = (int64_t)c * T / G, g1 = (int64_t)(c + 1) * T / G;
-  if (g0 >= g1) return;  // uniform: nothing allocated yet
   const int n_sm_warps = ceil_div(R, 32);
+  pdl_trigger();
 
+  // Set-up that needs nothing from the previous kernels runs while they
+  // drain: Q padding, barriers, TMEM, tensor-map prefetch.
   // zero the Q buffers once: rows R..127 stay zero padding
   for (int i = tid; i < kQBufs * kQBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(qbufs)[i] = make_uint4(0, 0, 0, 0);
@@ -184,6 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
@@ -194,16 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
+  pdl_wait();  // the tile plan and the appended rows come from the previous kernels
+  const int64_t T = prefix[B];
+  const int64_t g0 = (int64_t)c * T / G, g1 = (int64_t)(c + 1) * T / G;
+  if (g0 >= g1) {  // uniform: no tiles for this CTA
+    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA
     // The whole warp walks the tiles; lane j holds the four block ids of
     // tile (window start + j), fetched for 32 tiles at once, and lane 0
     // issues the barrier operations and the copies.
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tm_q);
-      ptx::prefetch_tmap(&tm_k);
-      ptx::prefetch_tmap(&tm_v);
-    }
     Cursor cu;
     cu.seek(g0, ntiles, prefix, B);
     int seg = -1, L = 0, win = -1;
@@ -248,25 +254,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       if (lane == 0) {
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
                             abort, kTimeoutNs);
-        if (ok) {
-          const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
-          ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * 4u * kBoxBytes);
-          uint8_t* sb = stages + stage * kStageBytes;
-#pragma unroll
-          for (int p = 0; p < kPages; ++p) {
-            if (p < np) {
-              for (int half = 0; half < 2; ++half) {
-                ptx::tma_load_4d(ptx::smem_u32(sb + half * kHalfBytes + p * kBoxBytes), &tm_k, fb,
-                                 half * 64, 0, cu.h, blk[p]);
-                ptx::tma_load_4d(ptx::smem_u32(sb + (2 + half) * kHalfBytes + p * kBoxBytes),
-                                 &tm_v, fb, half * 64, 0, cu.h, blk[p]);
-              }
-            }
-          }
-        }
+        if (ok)
+          ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars->full[stage]),
+                                     (uint32_t)np * 4u * kBoxBytes);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      // the tile's loads (page p = lane / 4; K lo, K hi, V lo, V hi) go out
+      // from lanes 0..15 in one warp instruction instead of sixteen from one
+      // thread: a single thread's bulk-tensor issue rate bounded the kernel
+      {
+        const int p = lane >> 2, part = lane & 3;  // part: bit 1 = V, bit 0 = high half of D
+        if (lane < 4 * kPages && p < np) {
+          const int bp = p == 0 ? blk[0] : p == 1 ? blk[1] : p == 2 ? blk[2] : blk[3];
+          const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
+          uint8_t* sb = stages + stage * kStageBytes;
+          ptx::tma_load_4d(ptx::smem_u32(sb + part * kHalfBytes + p * kBoxBytes),
+                           (part & 2) ? &tm_v : &tm_k, fb, (part & 1) * 64, 0, cu.h, bp);
+        }
+      }
       cu.next(ntiles, B, Hkv);
     }
     if (lane == 0) {

@@ -16,8 +16,10 @@
 // kernel merges by log-sum-exp.
 //
 // Per CTA, warp-specialised:
-//   warp 10     TMA producer: Q of each pair (two 64-column halves) and the
-//               K and V pages of each tile into a 4-stage ring (32 KB/stage)
+//   warps 10 and 7 (8 when R > 64)  producers: Q of each pair by TMA;
+//               the K and V pages of each tile into a 4-stage ring (32 KB per
+//               stage) by 16-byte cp.async copies placed in the swizzled
+//               operand layout
 //   warp 11     MMA issuer of S = Q K^T into TMEM (four buffers)
 //   warp 9      MMA issuer of O += P V, P read back from TMEM (aliasing S);
 //               two issuing threads because each tcgen05.mma takes about 90
@@ -28,7 +30,7 @@
 //               through shared memory, exp2, P written as bf16 into TMEM;
 //               O is rescaled in TMEM only when the running maximum grows by
 //               more than 2^8
-//   warp 8      idle.
+
 // TMEM: S0..S3 cols [0,64) .. [192,256), O [256,384).  Four S buffers let
 // Q K^T of tile t wait only for P V of tile t-4: the hand-off chain QK ->
 // softmax -> PV -> QK of a buffer is spread over four tiles in flight (the
@@ -53,9 +55,15 @@ constexpr int kThreads = 384;
 // (warp % 4).  Softmax warps 0..7: warp w serves rows 32*(w%4).. and the
 // half w/4 of each tile's 64 keys.  The producer and the Q K^T issuer sit on
 // sub-partitions 2 and 3, away from the softmax warps of rows 0..63 (the
-// common case R <= 64); the P V issuer is warp 9; warp 8 stays idle.
+// common case R <= 64); the P V issuer is warp 9; warp 7 (R <= 64) or 8
+// copies K/V with the producer.
 constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 10;
+constexpr int kProducerWarp = 10;  // Q (TMA) and half of the K/V copies
+// the other half of the K/V copies: warp 7 (sub-partition 3, away from the
+// softmax warps) when rows 64..127 are padding, else warp 8
+constexpr int kCopyWarpSmallR = 7;
+constexpr int kCopyWarpLargeR = 8;
+constexpr int kCopyThreads = 64;    // threads issuing K/V copies (warps 8 and 10)
 constexpr int kMmaWarp = 11;  // issues Q K^T
 constexpr int kPvWarp = 9;    // issues P V
 constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
@@ -136,7 +144,8 @@ __device__ __forceinline__ int tile_pages(int L, int tile) {
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ block_table,
+    const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ k_cache,
+    const __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ parent,
     const int32_t* __restrict__ ntiles, const int32_t* __restrict__ prefix, spec_dims d,
     float qscale2, float* __restrict__ part, uint32_t* __restrict__ status) {
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   ptx::fence_proxy_async_smem();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->full[s]), kCopyThreads);
       ptx::mbar_init(ptx::smem_u32(&bars->empty[s]), 1);
     }
     for (int i = 0; i < kQBufs; ++i) {
@@ -205,11 +214,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     return;
   }
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA
-    // The whole warp walks the tiles; lane j holds the four block ids of
-    // tile (window start + j), fetched for 32 tiles at once, and lane 0
-    // issues the barrier operations and the copies.
+  const int copy_warp = n_sm_warps <= 2 ? kCopyWarpSmallR : kCopyWarpLargeR;
+  if (warp == kProducerWarp || warp == copy_warp) {
+    // ------------------------------------------------------------ producers
+    // Both warps walk the tiles; lane j holds the four block ids of tile
+    // (window start + j), fetched for 32 tiles at once.  Q comes by TMA
+    // (warp 10, lane 0).  K and V come by 16-byte cp.async copies from all
+    // 64 threads, each placed where the 128-byte-swizzled layout of the MMA
+    // operands wants it (chunk j of row r of a page at j ^ (r % 8)): one
+    // tensor-TMA box per page half and tensor bounded the kernel at about
+    // 16 boxes per tile, whatever their size.
+    const int ct = (warp == copy_warp ? 0 : kWarp) + lane;  // copy thread 0..63
+    const int c16 = ct & 15;                                 // 16-byte chunk of a 256-byte row
+    const int r0 = ct >> 4;                                  // rows r0, r0 + 4, r0 + 8, r0 + 12
+    const uint32_t swz_half = (uint32_t)(c16 >> 3) * kHalfBytes;
     Cursor cu;
     cu.seek(g0, ntiles, prefix, B);
     int seg = -1, L = 0, win = -1;
@@ -222,20 +240,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         ++seg;
         L = ctx_lens[cu.b] + M;
         win = -1;
-        if (lane == 0) {
-          const int qb = seg % kQBufs;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
-                              kTimeoutNs);
-          if (ok) {
-            const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
-            ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
-            for (int half = 0; half < 2; ++half)
-              ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q,
-                               qf, half * 64, cu.h * group, 0, cu.b);
+        if (warp == kProducerWarp) {
+          if (lane == 0) {
+            const int qb = seg % kQBufs;
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
+                                kTimeoutNs);
+            if (ok) {
+              const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
+              ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
+              for (int half = 0; half < 2; ++half)
+                ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q,
+                                 qf, half * 64, cu.h * group, 0, cu.b);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
       }
       if ((cu.tile >> 5) != win) {  // next window of 32 tiles of this pair
         win = cu.tile >> 5;
@@ -251,31 +271,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 #pragma unroll
       for (int p = 0; p < kPages; ++p) blk[p] = __shfl_sync(0xffffffffu, ids[p], src);
       const int stage = (int)(t % kStages);
-      if (lane == 0) {
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
-                            abort, kTimeoutNs);
-        if (ok)
-          ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars->full[stage]),
-                                     (uint32_t)np * 4u * kBoxBytes);
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
+                          abort, kTimeoutNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      // the tile's loads (page p = lane / 4; K lo, K hi, V lo, V hi) go out
-      // from lanes 0..15 in one warp instruction instead of sixteen from one
-      // thread: a single thread's bulk-tensor issue rate bounded the kernel
-      {
-        const int p = lane >> 2, part = lane & 3;  // part: bit 1 = V, bit 0 = high half of D
-        if (lane < 4 * kPages && p < np) {
-          const int bp = p == 0 ? blk[0] : p == 1 ? blk[1] : p == 2 ? blk[2] : blk[3];
-          const uint32_t fb = ptx::smem_u32(&bars->full[stage]);
-          uint8_t* sb = stages + stage * kStageBytes;
-          ptx::tma_load_4d(ptx::smem_u32(sb + part * kHalfBytes + p * kBoxBytes),
-                           (part & 2) ? &tm_v : &tm_k, fb, (part & 1) * 64, 0, cu.h, bp);
+      const uint32_t sb = ptx::smem_u32(stages + stage * kStageBytes);
+#pragma unroll
+      for (int p = 0; p < kPages; ++p) {
+        if (p < np) {
+          const int64_t page = ((int64_t)blk[p] * Hkv + cu.h) * kBlock;  // row of slot 0
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = r0 + 4 * k;
+            const int64_t e = (page + r) * 128 + c16 * 8;  // element offset in the cache
+            const uint32_t so = swz_half + (uint32_t)p * kBoxBytes + (uint32_t)r * 128u +
+                                ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
+            ptx::cp_async16(sb + so, k_cache + e);
+            ptx::cp_async16(sb + 2 * kHalfBytes + so, v_cache + e);
+          }
         }
       }
+      ptx::cp_async_arrive_noinc(ptx::smem_u32(&bars->full[stage]));
       cu.next(ntiles, B, Hkv);
     }
-    if (lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
       // every load issued must have landed before the CTA may exit
       const int64_t issued = t;  // a broken loop did not issue tile t
       for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
@@ -285,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg % kQBufs]), (uint32_t)((sg / kQBufs) & 1),
                        abort, kTimeoutNs);
     }
+    // the copies of a thread that stopped early land before the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA: Q K^T
     if (lane == 0) {
@@ -743,7 +766,9 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   const float qscale2 = a.scale * 1.4426950408889634f;
   {
     PdlLaunch L(dim3(G), dim3(kThreads), kSmemBytes, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q, tm_k, tm_v, a.block_table, a.ctx_lens,
+    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q, tm_k, tm_v,
+                           static_cast<const __nv_bfloat16*>(a.k_cache),
+                           static_cast<const __nv_bfloat16*>(a.v_cache), a.block_table, a.ctx_lens,
                            a.parent, (const int32_t*)ntiles, (const int32_t*)prefix, d, qscale2,
                            part, status);
     if (e != cudaSuccess) return e;

@@ -45,7 +45,7 @@ DEFAULT_WORKLOAD = "stress_gqa_152k"
 # and scaled to 128 by the algorithmic bytes (traffic grows with the KV
 # bytes read): profiles/attn_tc_kernel_stress_gqa_152k_b16.md.  Valid only
 # for the attention kernel sources whose digest is recorded with it.
-TRAFFIC = {"digest": "be1ae79bad15dfb2", "bytes_per_call": 10137184791}
+TRAFFIC = {"digest": "da5849afd4c4a790", "bytes_per_call": 10137078340}
 TRAFFIC_ALG_BYTES = 10051956736  # algorithmic bytes per call of that workload (seed 0)
 
 

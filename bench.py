@@ -252,14 +252,51 @@ class NativeStep:
         return ins, outs
 
     def e2e_step(self, i, ins, outs):
-        for k, v in ins.items():
-            getattr(self, k).copy_(v, non_blocking=True)
-        n = self.step(i)
+        """One step through the public API with this step's inputs copied
+        from pinned host memory and its results read back, all inside the
+        timed region.  The attention's inputs go first on the compute
+        stream; the logits and the decision inputs, which only
+        reject-sample reads, come over on two copy streams (in chunks)
+        while the attention runs, and reject-sample waits for them.
+        Nothing is fetched ahead of its own step."""
+        sv = self.sv
+        cs = torch.cuda.current_stream()
+        if not hasattr(self, "_copy_streams"):
+            self._copy_streams = [torch.cuda.Stream() for _ in range(2)]
+            self._copy_events = [torch.cuda.Event() for _ in range(2)]
+        for k in ("q", "k_new", "v_new", "block_table", "ctx_lens"):
+            getattr(self, k).copy_(ins[k], non_blocking=True)
+        late = [k for k in ("target", "draft", "tokens", "temperature", "parent") if k in ins]
+        for s_, e_ in zip(self._copy_streams, self._copy_events):
+            s_.wait_stream(cs)  # the buffers are free once the previous step's work is done
+        j = 0
+        for k in late:
+            dst = getattr(self, k).view(-1)
+            src = ins[k].view(-1)
+            n = 4 if dst.numel() >= (1 << 20) else 1
+            step_ = (dst.numel() + n - 1) // n
+            for c in range(n):
+                with torch.cuda.stream(self._copy_streams[j % 2]):
+                    dst[c * step_:(c + 1) * step_].copy_(src[c * step_:(c + 1) * step_],
+                                                       non_blocking=True)
+                j += 1
+        for s_, e_ in zip(self._copy_streams, self._copy_events):
+            e_.record(s_)
+        n = sv.spec_verify_attn(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                self.block_table, self.ctx_lens, self.parent, self.out,
+                                self.lse, self.dims, self.ws)
+        for e_ in self._copy_events:
+            cs.wait_event(e_)
+        n += sv.spec_reject_sample(self.target, self.draft, self.tokens, self.parent,
+                                   self.temperature, 20261202, i, self.out_tokens, self.path,
+                                   self.acc[i], None, self.dims, self.ws)
+        n += sv.kv_commit(self.k_cache, self.v_cache, self.block_table, self.ctx_lens,
+                          self.new_ctx, self.path, self.acc[i], self.dims, self.ws)
         outs["out_tokens"].copy_(self.out_tokens, non_blocking=True)
         outs["path"].copy_(self.path, non_blocking=True)
         outs["acc"].copy_(self.acc[i], non_blocking=True)
         outs["new_ctx"].copy_(self.new_ctx, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        cs.synchronize()
         return n
 
 

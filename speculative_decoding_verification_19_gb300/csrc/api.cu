@@ -39,7 +39,12 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.status_off = take(16);
   L.attn_ok_off = take(sizeof(int32_t) * (size_t)d.B);
   L.tc_ntiles_off = take(sizeof(int32_t) * (size_t)d.B);
-  L.tc_prefix_off = take(sizeof(int32_t) * ((size_t)d.B + 1));
+  L.tc_pre_off = take(sizeof(int64_t) * 2 * ((size_t)d.B + 1));
+  L.tc_rq_off = take(16 * (size_t)d.B);
+  L.tc_start_off = take(32 * ((size_t)kMaxAttnCtas + 1));
+  L.tc_pair_off = take(sizeof(int32_t) * (size_t)d.B * (size_t)(d.Hkv > 0 ? d.Hkv : 0));
+  L.tc_anc_off = take(sizeof(uint64_t) * (size_t)d.B * d.M);
+  L.tc_sync_off = take(16);
   const int group = d.Hkv > 0 ? d.Hq / d.Hkv : 0;
   L.rows = group * d.M;
   L.split_keys = attn_split_keys(d);

@@ -1,5 +1,5 @@
 // Verify attention on the 5th-generation tensor cores (tcgen05 + TMEM),
-// with TMA-staged paged K/V tiles.
+// with cp.async-staged paged K/V tiles.
 //
 // What is computed is the same as the CUDA-core kernels in attn.cu (page 1
 // §2.1, page 2 §3.3, page 3 tree-attention section): every new row attends
@@ -11,15 +11,30 @@
 // arithmetic intensity is R flop/byte, above what CUDA cores can serve at
 // HBM speed for R >= ~16 and far below the tensor-core ridge.  The key axis
 // of all (b, h) pairs is cut into 64-key tiles (4 blocks of 16), and the
-// tiles of the whole batch are split evenly over one persistent CTA per SM;
-// a pair that straddles two CTAs yields two partial results that a small
-// kernel merges by log-sum-exp.
+// tiles of the whole batch are split over one persistent CTA per SM.
+//
+// Two launches per call:
+//   attn_prep_kernel  one CTA per request: checks it (capacity, block ids,
+//                     topology), appends its new K/V rows, and for a tree
+//                     the ancestor-or-self mask of every row.  The last CTA
+//                     to finish plans the split: per-request records (ctx,
+//                     tiles, next request with tiles) and each CTA's first
+//                     tile, balancing tiles plus a fixed cost per (b, h)
+//                     segment a CTA starts (a segment start costs about as
+//                     much as a few tiles: new Q, new masks, a drain of the
+//                     MMA pipeline).
+//   attn_tc_kernel    the attention.  A (b, h) pair wholly inside one CTA
+//                     writes its normalised output directly; a pair split
+//                     over CTAs leaves one partial per CTA, and the CTA that
+//                     completes the pair's tile count merges them by
+//                     log-sum-exp.
 //
 // Per CTA, warp-specialised:
 //   warps 10 and 7 (8 when R > 64)  producers: Q of each pair by TMA;
 //               the K and V pages of each tile into a 4-stage ring (32 KB per
 //               stage) by 16-byte cp.async copies placed in the swizzled
-//               operand layout
+//               operand layout; the block ids of the next 32 tiles are
+//               fetched one window ahead
 //   warp 11     MMA issuer of S = Q K^T into TMEM (four buffers)
 //   warp 9      MMA issuer of O += P V, P read back from TMEM (aliasing S);
 //               two issuing threads because each tcgen05.mma takes about 90
@@ -29,8 +44,8 @@
 //               tile (32 keys); the two halves of a row swap their maxima
 //               through shared memory, exp2, P written as bf16 into TMEM;
 //               O is rescaled in TMEM only when the running maximum grows by
-//               more than 2^8
-
+//               more than 2^8; at the end of a pair, the output or partial
+//
 // TMEM: S0..S3 cols [0,64) .. [192,256), O [256,384).  Four S buffers let
 // Q K^T of tile t wait only for P V of tile t-4: the hand-off chain QK ->
 // softmax -> PV -> QK of a buffer is spread over four tiles in flight (the
@@ -75,6 +90,10 @@ constexpr int kSBufs = 4;  // S buffers in TMEM
 constexpr int kTmemCols = 512;
 constexpr int kOCol = kSBufs * kTileKeys;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
+// Split cost of one (request, head) segment, in tiles: the Q load, the
+// masks and the drain of the pipeline at a pair's end cost about this much.
+constexpr int kSegCost = 2;
+constexpr int kPrepThreads = 256;
 
 struct __align__(8) Bars {
   uint64_t full[kStages];
@@ -86,7 +105,10 @@ struct __align__(8) Bars {
   uint64_t o_done[kSBufs];  // completion of PV(t) lands on o_done[t % kSBufs]
   uint64_t drain[2];  // the Q K^T issuer's and the P V issuer's last completion
   uint64_t xbar[4][2];       // per sub-partition, per tile parity: both halves' maxima
+  uint64_t lbar[4];          // per sub-partition: both halves' row sums of a whole pair
+  uint64_t ebar;             // every softmax warp wrote its rows of a partial
   float xmax[2][2][128];     // [tile parity][half][row]
+  float xl[2][128];          // [half][row] row sums at the end of a whole pair
   uint32_t tmem_base;
   int abort;
 };
@@ -95,46 +117,55 @@ constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kQBufs * kQBytes +
 
 size_t smem_bytes() { return kSmemBytes; }
 
-// Position in the flat tile sequence: request b, KV head h, tile of the pair.
+// Position in the flat tile sequence: request b, KV head h, tile of the
+// pair, with the request's record (ctx, tiles per head, next request with
+// tiles) and the next request's record loaded one request ahead, so that no
+// role waits for a global load when it crosses into a new request.
 struct Cursor {
-  int b, h, tile, nt;
-  __device__ void seek(int64_t g, const int32_t* ntiles, const int32_t* prefix, int B) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((int64_t)prefix[mid] <= g) lo = mid;
-      else hi = mid - 1;
-    }
-    b = lo;
-    nt = ntiles[b];
-    const int64_t off = g - prefix[b];
-    h = (int)(off / nt);
-    tile = (int)(off % nt);
+  int b, h, tile, nt, ctx, next_b;
+  int4 nrec;
+  // st0 = (first tile, b, h, tile), st1 = (ctx, tiles, next request, end tile)
+  __device__ void start(int4 st0, int4 st1, const int4* rq, int B) {
+    b = st0.y;
+    h = st0.z;
+    tile = st0.w;
+    ctx = st1.x;
+    nt = st1.y;
+    next_b = st1.z;
+    nrec = make_int4(0, 0, B, 0);
+    if (next_b < B) nrec = rq[next_b];
   }
-  __device__ void next(const int32_t* ntiles, int B, int Hkv) {
+  __device__ void next(const int4* rq, int B, int Hkv) {
     if (++tile < nt) return;
     tile = 0;
     if (++h < Hkv) return;
     h = 0;
-    do {
-      ++b;
-    } while (b < B && ntiles[b] == 0);
-    nt = b < B ? ntiles[b] : 0;
+    b = next_b;
+    ctx = nrec.x;
+    nt = nrec.y;
+    next_b = nrec.z;
+    if (next_b < B) nrec = rq[next_b];
   }
 };
 
-// Scaled score of tile column j (log2 units) or -inf where the key is not
-// visible to this row: past the tile's valid keys or the request's length,
-// or a new position that is not an ancestor-or-self of the row's node.
-__device__ __forceinline__ float score_of(uint32_t sbits, int j, int kpos0, int nkeys, int ctx,
-                                          int L, unsigned long long anc, bool real, bool plain,
-                                          float qscale2) {
-  const float x = __uint_as_float(sbits) * qscale2;
-  if (plain) return real ? x : -INFINITY;
-  const int pos = kpos0 + j;
-  bool vis = real && j < nkeys && pos < L;
-  if (vis && pos >= ctx) vis = (anc >> (pos - ctx)) & 1ull;
-  return vis ? x : -INFINITY;
+// Keys of a tile visible to a row, bit j for tile column j: below the
+// tile's valid keys and the request's length L, and either in the cached
+// prefix (position < ctx) or a new position that is an ancestor-or-self of
+// the row's node (bit pos - ctx of anc).
+__device__ __forceinline__ unsigned long long tile_visibility(int kpos0, int nkeys, int ctx, int L,
+                                                              unsigned long long anc, bool real) {
+  if (!real) return 0ull;
+  const int lim = min(L - kpos0, nkeys);  // nkeys is 16..64
+  unsigned long long v = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1));
+  const int c0 = ctx - kpos0;  // tile columns in the cached prefix
+  unsigned long long vm;
+  if (c0 >= 64)
+    vm = ~0ull;
+  else if (c0 > 0)
+    vm = ((1ull << c0) - 1) | (anc << c0);
+  else
+    vm = -c0 >= 64 ? 0ull : (anc >> -c0);
+  return v & vm;
 }
 
 __device__ __forceinline__ int tile_pages(int L, int tile) {
@@ -142,13 +173,27 @@ __device__ __forceinline__ int tile_pages(int L, int tile) {
   return keys >= kTileKeys ? kPages : ceil_div(keys, kBlock);
 }
 
+// 32 fp32 values (as bits) scaled and stored as bf16: a quarter row of out.
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                             float scale) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) {
+    uint4 w;
+    w.x = ptx::pack_bf16x2(__uint_as_float(v[j]) * scale, __uint_as_float(v[j + 1]) * scale);
+    w.y = ptx::pack_bf16x2(__uint_as_float(v[j + 2]) * scale, __uint_as_float(v[j + 3]) * scale);
+    w.z = ptx::pack_bf16x2(__uint_as_float(v[j + 4]) * scale, __uint_as_float(v[j + 5]) * scale);
+    w.w = ptx::pack_bf16x2(__uint_as_float(v[j + 6]) * scale, __uint_as_float(v[j + 7]) * scale);
+    *reinterpret_cast<uint4*>(dst + j) = w;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ k_cache,
+    const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_cache,
     const __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ parent,
-    const int32_t* __restrict__ ntiles, const int32_t* __restrict__ prefix, spec_dims d,
-    float qscale2, float* __restrict__ part, uint32_t* __restrict__ status) {
+    const int4* __restrict__ rq, const int4* __restrict__ starts,
+    const unsigned long long* __restrict__ anc_ws, int* __restrict__ pairs, spec_dims d,
+    float qscale2, float* __restrict__ part, __nv_bfloat16* __restrict__ out,
+    float* __restrict__ lse, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -160,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const int B = d.B, Hkv = d.Hkv, M = d.M;
   const int group = d.Hq / d.Hkv;
   const int R = group * M;
-  const int G = gridDim.x, c = blockIdx.x;
+  const int c = blockIdx.x;
   const int n_sm_warps = ceil_div(R, 32);
   pdl_trigger();
 
@@ -186,16 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain[1]), 1);
-    for (int sp = 0; sp < 4; ++sp)
+    for (int sp = 0; sp < 4; ++sp) {
       for (int i = 0; i < 2; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[sp][i]), 2);
+      ptx::mbar_init(ptx::smem_u32(&bars->lbar[sp]), 2);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->ebar), 2 * n_sm_warps);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    ptx::prefetch_tmap(&tm_q);
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_v);
-  }
+  if (warp == kProducerWarp && lane == 0) ptx::prefetch_tmap(&tm_q);
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
@@ -206,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
-  pdl_wait();  // the tile plan and the appended rows come from the previous kernels
-  const int64_t T = prefix[B];
-  const int64_t g0 = (int64_t)c * T / G, g1 = (int64_t)(c + 1) * T / G;
+  pdl_wait();  // the plan and the appended rows come from the previous kernel
+  const int4 st0 = starts[2 * c], st1 = starts[2 * c + 1];
+  const int64_t g0 = st0.x, g1 = st1.w;
   if (g0 >= g1) {  // uniform: no tiles for this CTA
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
     return;
@@ -218,28 +262,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   if (warp == kProducerWarp || warp == copy_warp) {
     // ------------------------------------------------------------ producers
     // Both warps walk the tiles; lane j holds the four block ids of tile
-    // (window start + j), fetched for 32 tiles at once.  Q comes by TMA
-    // (warp 10, lane 0).  K and V come by 16-byte cp.async copies from all
-    // 64 threads, each placed where the 128-byte-swizzled layout of the MMA
+    // (window start + j) of a window of 32 tiles, and the ids of the next
+    // window are loaded when a window starts.  Q comes by TMA (warp 10,
+    // lane 0).  K and V come by 16-byte cp.async copies from all 64
+    // threads, each placed where the 128-byte-swizzled layout of the MMA
     // operands wants it (chunk j of row r of a page at j ^ (r % 8)): one
-    // tensor-TMA box per page half and tensor bounded the kernel at about
-    // 16 boxes per tile, whatever their size.
+    // tensor-TMA box per page half bounded the kernel at about 16 boxes per
+    // tile, whatever their size.
     const int ct = (warp == copy_warp ? 0 : kWarp) + lane;  // copy thread 0..63
     const int c16 = ct & 15;                                 // 16-byte chunk of a 256-byte row
     const int r0 = ct >> 4;                                  // rows r0, r0 + 4, r0 + 8, r0 + 12
     const uint32_t swz_half = (uint32_t)(c16 >> 3) * kHalfBytes;
     Cursor cu;
-    cu.seek(g0, ntiles, prefix, B);
-    int seg = -1, L = 0, win = -1;
-    int ids[kPages] = {0, 0, 0, 0};
+    cu.start(st0, st1, rq, B);
+    int seg = -1, L = 0;
+    int wb = -1, ww = -1, nb = -1, nw = -1;  // window held in ids and window loaded into nids
+    int ids[kPages] = {0, 0, 0, 0}, nids[kPages] = {0, 0, 0, 0};
     int64_t t = 0;
     bool ok = true;
     for (int64_t g = g0; g < g1 && ok; ++g, ++t) {
       const bool first = (g == g0) || cu.tile == 0;
       if (first) {
         ++seg;
-        L = ctx_lens[cu.b] + M;
-        win = -1;
+        L = cu.ctx + M;
         if (warp == kProducerWarp) {
           if (lane == 0) {
             const int qb = seg % kQBufs;
@@ -249,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
               const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
               ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
               for (int half = 0; half < 2; ++half)
-                ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQHalfBytes), &tm_q,
+                ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQBytes / 2), &tm_q,
                                  qf, half * 64, cu.h * group, 0, cu.b);
             }
           }
@@ -257,13 +302,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           if (!ok) break;
         }
       }
-      if ((cu.tile >> 5) != win) {  // next window of 32 tiles of this pair
-        win = cu.tile >> 5;
-        const int page0 = ((win << 5) + lane) * kPages;
-        const int32_t* bt = block_table + (int64_t)cu.b * d.max_blocks;
+      const int w = cu.tile >> 5;
+      if (cu.b != wb || w != ww) {  // next window of 32 tiles
+        if (cu.b == nb && w == nw) {
 #pragma unroll
-        for (int p = 0; p < kPages; ++p)
-          ids[p] = (page0 + p < d.max_blocks) ? bt[page0 + p] : 0;
+          for (int p = 0; p < kPages; ++p) ids[p] = nids[p];
+        } else {
+          const int page0 = ((w << 5) + lane) * kPages;
+          const int32_t* bt = block_table + (int64_t)cu.b * d.max_blocks;
+#pragma unroll
+          for (int p = 0; p < kPages; ++p) ids[p] = (page0 + p < d.max_blocks) ? bt[page0 + p] : 0;
+        }
+        wb = cu.b;
+        ww = w;
+        // the next window with other ids: the pair's next window, else the
+        // first of the next head (same ids when the pair has one window:
+        // then the next request's first)
+        if ((w + 1) * 32 < cu.nt) {
+          nb = cu.b;
+          nw = w + 1;
+        } else {
+          nb = (cu.h + 1 < Hkv && w > 0) ? cu.b : cu.next_b;
+          nw = 0;
+        }
+        if (nb == wb && nw == ww) {
+#pragma unroll
+          for (int p = 0; p < kPages; ++p) nids[p] = ids[p];
+        } else if (nb < B) {
+          const int page0 = ((nw << 5) + lane) * kPages;
+          const int32_t* bt = block_table + (int64_t)nb * d.max_blocks;
+#pragma unroll
+          for (int p = 0; p < kPages; ++p) nids[p] = (page0 + p < d.max_blocks) ? bt[page0 + p] : 0;
+        }
       }
       const int np = tile_pages(L, cu.tile);
       const int src = cu.tile & 31;
@@ -294,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
       }
       ptx::cp_async_arrive_noinc(ptx::smem_u32(&bars->full[stage]));
-      cu.next(ntiles, B, Hkv);
+      cu.next(rq, B, Hkv);
     }
     if (warp == kProducerWarp && lane == 0) {
       // every load issued must have landed before the CTA may exit
@@ -313,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     if (lane == 0) {
       const uint32_t id_qk_full = ptx::idesc_bf16_f32(128, kTileKeys, false, false);
       Cursor cu;
-      cu.seek(g0, ntiles, prefix, B);
+      cu.start(st0, st1, rq, B);
       int seg = -1, L = 0;
       int64_t t = 0;
       // Shared-memory descriptors built once; an operand at byte offset o
@@ -325,7 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       for (int64_t g = g0; g < g1; ++g, ++t) {
         const bool first = (g == g0) || cu.tile == 0;
         const bool last = (g == g1 - 1) || cu.tile == cu.nt - 1;
-        if (first) ++seg;
+        if (first) {
+          ++seg;
+          L = cu.ctx + M;
+        }
         const int qb = seg % kQBufs;
         if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]),
                                      (uint32_t)((seg / kQBufs) & 1), abort, kTimeoutNs))
@@ -340,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                                            kTimeoutNs))
           break;
         ptx::tc_fence_after();
-        if (first) L = ctx_lens[cu.b] + M;
         const int np = tile_pages(L, cu.tile);
         const uint32_t idqk = np == kPages ? id_qk_full : ptx::idesc_bf16_f32(128, np * 16, false, false);
         const uint64_t dq = dq0 + (uint64_t)((qb * kQBytes) >> 4);
@@ -355,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[sbuf]));
         if (last) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qb]));
-        cu.next(ntiles, B, Hkv);
+        cu.next(rq, B, Hkv);
       }
       // all MMAs issued by this thread complete before TMEM is released
       ptx::mma_commit(ptx::smem_u32(&bars->drain[0]));
@@ -370,12 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
       const uint64_t dv0 = ptx::sdesc_sw128(ptx::smem_u32(stages + 2 * kHalfBytes), kHalfBytes, 1024);
       Cursor cu;
-      cu.seek(g0, ntiles, prefix, B);
+      cu.start(st0, st1, rq, B);
       int L = 0;
       int64_t u = 0;
       for (int64_t g = g0; g < g1; ++g, ++u) {
         const bool first = (g == g0) || cu.tile == 0;
-        if (first) L = ctx_lens[cu.b] + M;
+        if (first) L = cu.ctx + M;
         const int np = tile_pages(L, cu.tile);
         const int sbuf = (int)(u % kSBufs);
         const int stage = (int)(u % kStages);
@@ -393,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
         ptx::mma_commit(ptx::smem_u32(&bars->o_done[sbuf]));
         ptx::mma_commit(ptx::smem_u32(&bars->empty[stage]));
-        cu.next(ntiles, B, Hkv);
+        cu.next(rq, B, Hkv);
       }
       ptx::mma_commit(ptx::smem_u32(&bars->drain[1]));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain[1]), 0, abort, kTimeoutNs);
@@ -405,33 +477,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     const int row = sp * 32 + lane;
     if (sp < n_sm_warps) {
       const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+      const int S = tc_part_stride(d.D);
       Cursor cu;
-      cu.seek(g0, ntiles, prefix, B);
+      cu.start(st0, st1, rq, B);
       int64_t t = 0;
       float m_used = -INFINITY, l = 0.f;
-      unsigned long long anc = 0;
-      int ctx = 0, L = 0;
+      unsigned long long anc = 0, anc_n = 0;
+      int anc_b = -1, anc_nb = -1;  // requests whose masks anc and anc_n hold
+      int ctx = 0, L = 0, tile0 = 0;
+      int n_whole = 0, n_split = 0;  // pair ends of each kind so far (barrier phases)
       const bool real = row < R;
+      const int i = real ? row / group : 0;
       for (int64_t g = g0; g < g1; ++g, ++t) {
         const bool first = (g == g0) || cu.tile == 0;
         const bool last = (g == g1 - 1) || cu.tile == cu.nt - 1;
         if (first) {
-          ctx = ctx_lens[cu.b];
+          ctx = cu.ctx;
           L = ctx + M;
+          tile0 = cu.tile;
           m_used = -INFINITY;
           l = 0.f;
-          anc = 0;
-          if (real) {
-            const int i = row / group;
-            if (parent == nullptr) {
-              anc = (i >= 63) ? ~0ull : ((1ull << (i + 1)) - 1);
-            } else {
-              const int32_t* par = parent + (int64_t)cu.b * M;
-              int n = i;
-              for (int step = 0; step <= 64 && n >= 0; ++step) {
-                anc |= 1ull << n;
-                n = par[n];
-              }
+          if (anc_ws == nullptr) {
+            anc = (i >= 63) ? ~0ull : ((1ull << (i + 1)) - 1);
+          } else if (real && cu.b != anc_b) {
+            // tree masks come from the prep kernel; the next request's mask
+            // is loaded one request ahead
+            anc = cu.b == anc_nb ? anc_n : anc_ws[(int64_t)cu.b * M + i];
+            anc_b = cu.b;
+            if (cu.next_b < B) {
+              anc_n = anc_ws[(int64_t)cu.next_b * M + i];
+              anc_nb = cu.next_b;
             }
           }
         }
@@ -446,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         // tiles wholly inside the cached prefix need no mask
         const bool plain = kpos0 + kTileKeys <= ctx && nkeys == kTileKeys;
         const int jbase = half * 32;
+        uint32_t vh = 0xffffffffu;  // visible keys of this half (non-plain tiles)
         uint32_t sv[32];
         ptx::tmem_ld32(lane_base + sbuf * kTileKeys + jbase, sv);
         ptx::tmem_wait_ld();
@@ -462,10 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           }
           mh = real ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * qscale2 : -INFINITY;
         } else {
-          mh = -INFINITY;
+          // visibility of this half's 32 keys as a bitmask, then the same
+          // maximum as the plain path over the visible ones
+          vh = (uint32_t)(tile_visibility(kpos0, nkeys, ctx, L, anc, real) >> jbase);
+          float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            mh = fmaxf(mh, score_of(sv[j], jbase + j, kpos0, nkeys, ctx, L, anc, real, false, qscale2));
+          for (int j = 0; j < 32; j += 2) {
+            a0 = fmaxf(a0, (vh >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY);
+            a1 = fmaxf(a1, (vh >> (j + 1)) & 1u ? __uint_as_float(sv[j + 1]) : -INFINITY);
+          }
+          mh = fmaxf(a0, a1) * qscale2;
         }
         bars->xmax[xb][half][row] = mh;
         __syncwarp();
@@ -519,14 +601,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             pk[j] = ptx::pack_bf16x2(pa, pb);
           }
         } else {
+          const float nm = -m_used;  // finite whenever a key of the row is visible
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float xa = score_of(sv[2 * j], jbase + 2 * j, kpos0, nkeys, ctx, L, anc, real,
-                                      false, qscale2);
-            const float xb = score_of(sv[2 * j + 1], jbase + 2 * j + 1, kpos0, nkeys, ctx, L, anc,
-                                      real, false, qscale2);
-            const float pa = xa == -INFINITY ? 0.f : fast_exp2(xa - m_used);
-            const float pb = xb == -INFINITY ? 0.f : fast_exp2(xb - m_used);
+            const float pa = (vh >> (2 * j)) & 1u
+                                 ? fast_exp2(fmaf(__uint_as_float(sv[2 * j]), qscale2, nm))
+                                 : 0.f;
+            const float pb = (vh >> (2 * j + 1)) & 1u
+                                 ? fast_exp2(fmaf(__uint_as_float(sv[2 * j + 1]), qscale2, nm))
+                                 : 0.f;
             l0 += pa;
             l1 += pb;
             pk[j] = ptx::pack_bf16x2(pa, pb);
@@ -543,31 +626,118 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                               abort, kTimeoutNs))
             break;
           ptx::tc_fence_after();
-          // partial: unnormalised O (this half's 64 columns), the running
-          // maximum and this half's share of the row sum
-          const int64_t slot = (int64_t)cu.b * Hkv + cu.h + c;
-          float* prow = part + (slot * R + (real ? row : 0)) * (int64_t)tc_part_stride(d.D);
+          const int64_t pair = (int64_t)cu.b * Hkv + cu.h;
+          const int hq = cu.h * group + (real ? row % group : 0);
+          __nv_bfloat16* orow = out + (((int64_t)cu.b * M + i) * d.Hq + hq) * d.D + half * 64;
+          float* lrow = lse != nullptr ? lse + ((int64_t)cu.b * M + i) * d.Hq + hq : nullptr;
+          const int own = cu.tile - tile0 + 1;  // tiles of the pair run by this CTA
+          if (tile0 > 0) {
+            // ---- a later share of a split pair: a partial for the CTA that
+            // ran the pair's first tile (unnormalised O of this half's 64
+            // columns, the running maximum, this half's row sum, the tiles)
+            float* prow = part + ((pair + c) * R + (real ? row : 0)) * (int64_t)S;
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t o[32];
-            ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc * 32, o);
-            ptx::tmem_wait_ld();
-            if (real) {
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t o[32];
+              ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc * 32, o);
+              ptx::tmem_wait_ld();
+              if (real) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) {
-                const float4 v = make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
-                                             __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
-                *reinterpret_cast<float4*>(prow + half * 64 + cc * 32 + j) = v;
+                for (int j = 0; j < 32; j += 4) {
+                  const float4 v = make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                                               __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                  *reinterpret_cast<float4*>(prow + half * 64 + cc * 32 + j) = v;
+                }
               }
             }
-          }
-          if (real) {
-            prow[d.D + 1 + half] = l;
-            if (half == 0) prow[d.D] = m_used;
+            if (real) {
+              prow[d.D + 1 + half] = l;
+              if (half == 0) {
+                prow[d.D] = m_used;
+                prow[d.D + 3] = __int_as_float(own);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ebar));
+            const uint32_t ph = (uint32_t)(n_split & 1);
+            ++n_split;
+            if (warp == 0 && lane == 0 &&
+                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), ph, abort, kTimeoutNs)) {
+              // every row of the partial is written (the barrier above); the
+              // fence makes them visible GPU-wide before the tiles are counted
+              __threadfence();
+              atomicAdd(pairs + pair, own);
+            }
+          } else {
+            // ---- the pair's first CTA: its own rows from TMEM, merged with
+            // the partials of the CTAs that ran the rest of the pair (none
+            // when the whole pair ran here)
+            bars->xl[half][row] = l;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->lbar[sp]));
+            if (!ptx::mbar_wait(ptx::smem_u32(&bars->lbar[sp]), (uint32_t)(n_whole & 1), abort,
+                                kTimeoutNs))
+              break;
+            ++n_whole;
+            float ls = bars->xl[0][row] + bars->xl[1][row];
+            float mx = m_used;
+            const int rest = cu.nt - own;  // tiles run by the CTAs after this one
+            int c_end = c;                 // the last CTA with a share of the pair
+            if (rest > 0) {
+              bool okc = true;
+              if (lane == 0) okc = ptx::wait_count_geq(pairs + pair, rest, abort, kTimeoutNs);
+              __syncwarp();
+              if (!__shfl_sync(0xffffffffu, okc, 0)) break;
+              // walk up from CTA c+1 until the partials' tiles add up; CTAs
+              // with no tiles (more CTAs than split costs) wrote nothing
+              for (int got = 0, cc = c + 1; got < rest && cc < (int)gridDim.x; ++cc) {
+                if (starts[2 * cc].x == starts[2 * cc + 1].w) continue;
+                const float* q = part + ((pair + cc) * R + (real ? row : 0)) * (int64_t)S;
+                const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
+                got += __float_as_int(sc.w);
+                c_end = cc;
+                const float lq = sc.y + sc.z;
+                if (lq > 0.f) {
+                  const float mn = fmaxf(mx, sc.x);
+                  ls = (mx == -INFINITY ? 0.f : ls * exp2f(mx - mn)) + lq * exp2f(sc.x - mn);
+                  mx = mn;
+                }
+              }
+            }
+            const float inv = ls > 0.f ? 1.f / ls : 0.f;
+            const float wown = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mx);
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t o[32];
+              ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc * 32, o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * wown);
+              for (int cq = c + 1; cq <= c_end; ++cq) {
+                if (starts[2 * cq].x == starts[2 * cq + 1].w) continue;
+                const float* q = part + ((pair + cq) * R + (real ? row : 0)) * (int64_t)S;
+                const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
+                float4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  v[j] = __ldcg(reinterpret_cast<const float4*>(q + half * 64 + cc * 32) + j);
+                const float w = sc.y + sc.z > 0.f ? exp2f(sc.x - mx) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  o[4 * j] = __float_as_uint(fmaf(w, v[j].x, __uint_as_float(o[4 * j])));
+                  o[4 * j + 1] = __float_as_uint(fmaf(w, v[j].y, __uint_as_float(o[4 * j + 1])));
+                  o[4 * j + 2] = __float_as_uint(fmaf(w, v[j].z, __uint_as_float(o[4 * j + 2])));
+                  o[4 * j + 3] = __float_as_uint(fmaf(w, v[j].w, __uint_as_float(o[4 * j + 3])));
+                }
+              }
+              if (real) store32_bf16(orow + cc * 32, o, inv);
+            }
+            if (real && half == 0 && lrow != nullptr)
+              *lrow = ls > 0.f ? (mx + log2f(ls)) * 0.69314718055994530942f : -INFINITY;
           }
           ptx::tc_fence_before();
         }
-        cu.next(ntiles, B, Hkv);
+        cu.next(rq, B, Hkv);
       }
     }
   }
@@ -581,107 +751,230 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// plan: tiles per request and their exclusive prefix over (request, head)
+// request checks, append and the plan of the split
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) attn_plan_kernel(const int32_t* __restrict__ ctx_lens,
-                                                         const int32_t* __restrict__ req_ok,
-                                                         spec_dims d, int32_t* __restrict__ ntiles,
-                                                         int32_t* __restrict__ prefix) {
-  __shared__ int32_t warp_tot[32];
-  __shared__ int32_t carry;
-  pdl_trigger();
-  pdl_wait();  // the append's per-request verdicts
-  const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  for (int base = 0; base < d.B; base += 1024) {
-    const int b = base + tid;
-    int nt = 0;
-    if (b < d.B && req_ok[b]) nt = ceil_div(ctx_lens[b] + d.M, kTileKeys);
-    if (b < d.B) ntiles[b] = nt;
-    int v = nt * d.Hkv;
-    int incl = v;
+// Exclusive prefix over the CTA's threads of two int64 sums and an int max.
+__device__ __forceinline__ void block_scan(int64_t& a, int64_t& c, int& m, int64_t* sa,
+                                           int64_t* sc, int* sm, int64_t& ta, int64_t& tc_,
+                                           int& tm) {
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  const int nw = blockDim.x / kWarp;
+  int64_t ia = a, ic = c;
+  int im = m;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t ya = __shfl_up_sync(0xffffffffu, ia, o);
+    const int64_t yc = __shfl_up_sync(0xffffffffu, ic, o);
+    const int ym = __shfl_up_sync(0xffffffffu, im, o);
+    if (lane >= o) {
+      ia += ya;
+      ic += yc;
+      im = max(im, ym);
     }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int wpre = 0;
-    for (int i = 0; i < warp; ++i) wpre += warp_tot[i];
-    const int c0 = carry;
-    if (b < d.B) prefix[b] = c0 + wpre + incl - v;
-    __syncthreads();
-    if (tid == 1023) carry = c0 + wpre + incl;
-    __syncthreads();
   }
-  if (tid == 0) prefix[d.B] = carry;
+  if (lane == 31) {
+    sa[warp] = ia;
+    sc[warp] = ic;
+    sm[warp] = im;
+  }
+  __syncthreads();
+  int64_t pa = 0, pc = 0;
+  int pm = -1;
+  for (int w = 0; w < warp; ++w) {
+    pa += sa[w];
+    pc += sc[w];
+    pm = max(pm, sm[w]);
+  }
+  ta = tc_ = 0;
+  tm = -1;
+  for (int w = 0; w < nw; ++w) {
+    ta += sa[w];
+    tc_ += sc[w];
+    tm = max(tm, sm[w]);
+  }
+  // exclusive values: the prefix of the earlier warps plus the lanes before
+  const int xm = __shfl_up_sync(0xffffffffu, im, 1);
+  a = pa + ia - a;
+  c = pc + ic - c;
+  m = max(pm, lane > 0 ? xm : -1);
+  __syncthreads();
 }
 
-// ---------------------------------------------------------------------------
-// merge of the partials of each (request, KV head)
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(128) attn_tc_combine_kernel(
-    const float* __restrict__ part, const int32_t* __restrict__ ntiles,
-    const int32_t* __restrict__ prefix, spec_dims d, int G, T* __restrict__ out,
-    float* __restrict__ lse) {
-  // one warp per query row: blockIdx.x = group of 4 rows, y = KV head, z = request
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int group = d.Hq / d.Hkv;
-  const int R = group * d.M;
-  const int D = d.D;
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  const int r = blockIdx.x * (blockDim.x / kWarp) + warp;
+// One CTA per request.  Checks the request (capacity, the block ids of every
+// page it reads or writes, the tree topology), records it for the plan, and
+// appends its new rows: positions ctx .. end-1 where end = ceil(L/16)*16,
+// rows past ctx+M-1 cleared.  A request that fails gets out = 0, lse = -inf
+// and no tiles.  The CTA that arrives last plans the split of the tiles.
+__global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
+    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+    __nv_bfloat16* __restrict__ k_cache, __nv_bfloat16* __restrict__ v_cache,
+    const int32_t* __restrict__ block_table, const int32_t* __restrict__ ctx_lens,
+    const int32_t* __restrict__ parent, spec_dims d, int G, int32_t* __restrict__ ntiles,
+    int64_t* __restrict__ pre, int4* __restrict__ rq, int4* __restrict__ starts,
+    int* __restrict__ pairs, unsigned long long* __restrict__ anc_ws,
+    uint32_t* __restrict__ arrivals, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+    uint32_t* __restrict__ status) {
+  __shared__ int s_last;
+  __shared__ int s_blk[8];
+  __shared__ int64_t s_a[kPrepThreads / kWarp], s_c[kPrepThreads / kWarp];
+  __shared__ int s_m[kPrepThreads / kWarp];
   pdl_trigger();
-  pdl_wait();  // the partials come from the previous kernel
-  if (r >= R) return;
-  const int64_t Ttot = prefix[d.B];
-  const int nt = ntiles[b];
-  int c_first = 1, c_last = 0;
-  if (nt > 0) {
-    const int64_t ps = (int64_t)prefix[b] + (int64_t)h * nt, pe = ps + nt;
-    c_first = (int)(((ps + 1) * G - 1) / Ttot);
-    c_last = (int)((pe * G - 1) / Ttot);
-  }
-  const int64_t pair = (int64_t)b * d.Hkv + h;
-  const int i = r / group, hq = h * group + r % group;
-  // A partial row holds unnormalised O, the running maximum m (log2 units)
-  // and the two half-tile shares of the row sum.  CTAs with an empty tile
-  // range wrote nothing (their slot may belong to a neighbouring pair), so
-  // they are skipped.  Lane c reads the scalars of partial c_first + c (all
-  // partials in one round trip), then every lane its D / 32 values of each.
-  const int S = tc_part_stride(D);
-  const int np = c_last - c_first + 1;
-  float m = -INFINITY;
-  for (int c0 = 0; c0 < np; c0 += kWarp) {
-    const int cc = c_first + c0 + lane;
-    float mc = -INFINITY;
-    if (c0 + lane < np && (int64_t)cc * Ttot / G != (int64_t)(cc + 1) * Ttot / G) {
-      const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
-      if (prow[D + 1] + prow[D + 2] > 0.f) mc = prow[D];
-    }
-    m = fmaxf(m, warp_max(mc));
-  }
-  float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (m != -INFINITY) {
-    for (int cc = c_first; cc <= c_last; ++cc) {
-      if ((int64_t)cc * Ttot / G == (int64_t)(cc + 1) * Ttot / G) continue;
-      const float* prow = part + ((pair + cc) * R + r) * (int64_t)S;
-      const float lp = prow[D + 1] + prow[D + 2];
-      if (!(lp > 0.f)) continue;
-      const float w = exp2f(prow[D] - m);
-      wsum += w * lp;
-      for (int k = 0; k < D / kWarp; ++k) acc[k] += w * prow[lane + k * kWarp];
+  pdl_wait();  // the inputs and the cache may come from the previous kernel
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int B = d.B, M = d.M, Hkv = d.Hkv, D = d.D;
+  const int ctx = ctx_lens[b];
+  const int64_t L = (int64_t)ctx + M;
+  const int64_t cap = (int64_t)d.max_blocks * kBlock;
+  const int32_t* bt = block_table + (int64_t)b * d.max_blocks;
+
+  const bool cap_ok = ctx >= 0 && L <= cap;
+  int bad_block = 0;
+  if (cap_ok) {
+    const int pages = (int)ceil_div64(L, kBlock);
+#pragma unroll 4
+    for (int p = tid; p < pages; p += blockDim.x) {
+      const int id = bt[p];
+      bad_block |= (id < 0 || id >= d.num_blocks);
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  T* orow = out + (((int64_t)b * d.M + i) * d.Hq + hq) * D;
-  for (int k = 0; k < D / kWarp; ++k) orow[lane + k * kWarp] = from_f32<T>(acc[k] * inv);
-  if (lse != nullptr && lane == 0)
-    lse[((int64_t)b * d.M + i) * d.Hq + hq] =
-        wsum > 0.f ? (m + log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
+  int bad_topo = 0;
+  if (parent != nullptr) {
+    const int32_t* par = parent + (int64_t)b * M;
+    for (int n = tid; n < M; n += blockDim.x) {
+      const int pn = par[n];
+      bad_topo |= (n == 0) ? (pn != -1) : (pn < 0 || pn >= n);
+    }
+  }
+  bad_block = __syncthreads_or(bad_block);
+  bad_topo = __syncthreads_or(bad_topo);
+  const bool ok = cap_ok && !bad_block && !bad_topo;
+  // tile counts of the request's (request, head) pairs start at zero
+  for (int h = tid; h < Hkv; h += blockDim.x) pairs[(int64_t)b * Hkv + h] = 0;
+  if (ok && parent != nullptr) {
+    // ancestor-or-self mask of each tree row (the topology is valid here,
+    // so every walk ends at the root within M steps)
+    const int32_t* par = parent + (int64_t)b * M;
+    for (int n = tid; n < M; n += blockDim.x) {
+      unsigned long long a = 0;
+      for (int k = n; k >= 0; k = par[k]) a |= 1ull << k;
+      anc_ws[(int64_t)b * M + n] = a;
+    }
+  }
+  if (tid == 0) {
+    if (!cap_ok) raise_status(status, SPEC_ERR_CAPACITY);
+    if (bad_block) raise_status(status, SPEC_ERR_DEVICE_BOUNDS);
+    if (bad_topo) raise_status(status, SPEC_ERR_INVALID_ARG);
+    ntiles[b] = ok ? (int)ceil_div64(L, kTileKeys) : 0;
+    __threadfence();
+    s_last = atomicAdd(arrivals, 1u) == (uint32_t)(B - 1);
+  }
+  __syncthreads();
+
+  const int lanes = D / 8;  // 16-byte vectors per (position, head)
+  if (!ok) {
+    const int64_t n = (int64_t)M * d.Hq * lanes;
+    for (int64_t w = tid; w < n; w += blockDim.x)
+      reinterpret_cast<uint4*>(out + (int64_t)b * M * d.Hq * D)[w] = make_uint4(0, 0, 0, 0);
+    if (lse != nullptr)
+      for (int w = tid; w < M * d.Hq; w += blockDim.x) lse[(int64_t)b * M * d.Hq + w] = -INFINITY;
+  } else {
+    // block ids of the pages written, staged once (at most 5 for M <= 64)
+    const int64_t end = ceil_div64(L, kBlock) * kBlock;
+    const int p0 = ctx / kBlock;
+    if (tid < (int)(end / kBlock) - p0) s_blk[tid] = bt[p0 + tid];
+    __syncthreads();
+    const int npos = (int)(end - ctx);
+    const int work = npos * Hkv * lanes;
+#pragma unroll 4
+    for (int w = tid; w < work; w += blockDim.x) {
+      const int lane = w % lanes;
+      const int h = (w / lanes) % Hkv;
+      const int i = w / (lanes * Hkv);
+      const int64_t t = (int64_t)ctx + i;
+      const int64_t dst = (((int64_t)s_blk[t / kBlock - p0] * Hkv + h) * kBlock + t % kBlock) * D;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (i < M) {
+        const int64_t src = (((int64_t)b * M + i) * Hkv + h) * D;
+        kv = reinterpret_cast<const uint4*>(k_new + src)[lane];
+        vv = reinterpret_cast<const uint4*>(v_new + src)[lane];
+      }
+      reinterpret_cast<uint4*>(k_cache + dst)[lane] = kv;
+      reinterpret_cast<uint4*>(v_cache + dst)[lane] = vv;
+    }
+  }
+  if (!s_last) return;
+
+  // ---- the plan, by the last CTA to arrive.  Request r costs
+  // Hkv * (tiles + kSegCost) when it has tiles; a pair's fixed cost comes
+  // before its first tile, so tile j of a pair starts at cost
+  // base + kSegCost + j, and CTA k starts at the first tile whose cost
+  // reaches k * total / G.
+  __threadfence();
+  int64_t* tpre = pre;           // [B+1] tiles before request r
+  int64_t* cpre = pre + B + 1;   // [B+1] split cost before request r
+  int64_t carry_t = 0, carry_c = 0;
+  int carry_m = -1;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int r = base + tid;
+    const int nt = r < B ? __ldcg(ntiles + r) : 0;
+    int64_t vt = (int64_t)nt * Hkv, vc = nt > 0 ? (int64_t)Hkv * (nt + kSegCost) : 0;
+    int vm = nt > 0 ? r : -1;
+    int64_t tt, tcst;
+    int tm;
+    block_scan(vt, vc, vm, s_a, s_c, s_m, tt, tcst, tm);
+    const int prev = max(vm, carry_m);  // the last request with tiles before r
+    if (r < B) {
+      tpre[r] = carry_t + vt;
+      cpre[r] = carry_c + vc;
+      rq[r] = make_int4(ctx_lens[r], nt, B, 0);
+    }
+    __syncthreads();
+    if (r < B && nt > 0 && prev >= 0) reinterpret_cast<int*>(rq + prev)[2] = r;
+    carry_t += tt;
+    carry_c += tcst;
+    carry_m = max(carry_m, tm);
+    __syncthreads();
+  }
+  const int64_t T = carry_t, Ctot = carry_c;
+  if (tid == 0) {
+    tpre[B] = T;
+    cpre[B] = Ctot;
+    starts[2 * G] = make_int4((int)T, B, 0, 0);
+    starts[2 * G + 1] = make_int4(0, 0, B, (int)T);
+    *arrivals = 0;
+  }
+  __syncthreads();
+  if (Ctot == 0) {
+    for (int k = tid; k < G; k += blockDim.x) {
+      starts[2 * k] = make_int4(0, B, 0, 0);
+      starts[2 * k + 1] = make_int4(0, 0, B, 0);
+    }
+    return;
+  }
+  for (int r = tid; r < B; r += blockDim.x) {
+    const int64_t c0 = cpre[r], c1 = cpre[r + 1];
+    if (c1 == c0) continue;
+    const int nt = __ldcg(ntiles + r);
+    const int64_t per = nt + kSegCost;
+    // CTAs k with c0 <= floor(k * Ctot / G) < c1
+    const int k0 = (int)((c0 * G + Ctot - 1) / Ctot), k1 = (int)((c1 * G + Ctot - 1) / Ctot);
+    for (int k = k0; k < k1; ++k) {
+      int64_t rem = (int64_t)k * Ctot / G - c0;
+      const int h = (int)(rem / per);
+      rem -= h * per;
+      const int j = (int)max((int64_t)0, rem - kSegCost);  // rem < nt + kSegCost: j < nt
+      starts[2 * k] = make_int4((int)(tpre[r] + (int64_t)h * nt + j), r, h, j);
+    }
+  }
+  __syncthreads();
+  // second half of each start record: the first request's record and the
+  // CTA's end tile
+  for (int k = tid; k < G; k += blockDim.x) {
+    const int4 s0 = starts[2 * k];
+    const int4 r = rq[s0.y];  // a CTA with tiles starts inside a request
+    starts[2 * k + 1] = make_int4(r.x, r.y, r.z, starts[2 * k + 2].x);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -721,29 +1014,27 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   using namespace tc;
   const spec_dims& d = a.d;
   const int group = d.Hq / d.Hkv;
+  // flat tile indices are int32: every request's tiles of every head
+  if ((int64_t)d.B * d.Hkv * ceil_div64((int64_t)d.max_blocks * kBlock, kTileKeys) > INT32_MAX)
+    return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.ws);
-  int32_t* req_ok = reinterpret_cast<int32_t*>(ws + lay.attn_ok_off);
   int32_t* ntiles = reinterpret_cast<int32_t*>(ws + lay.tc_ntiles_off);
-  int32_t* prefix = reinterpret_cast<int32_t*>(ws + lay.tc_prefix_off);
+  int64_t* pre = reinterpret_cast<int64_t*>(ws + lay.tc_pre_off);
+  int4* rq = reinterpret_cast<int4*>(ws + lay.tc_rq_off);
+  int4* starts = reinterpret_cast<int4*>(ws + lay.tc_start_off);
+  int* pairs = reinterpret_cast<int*>(ws + lay.tc_pair_off);
+  unsigned long long* anc = reinterpret_cast<unsigned long long*>(ws + lay.tc_anc_off);
+  uint32_t* arrivals = reinterpret_cast<uint32_t*>(ws + lay.tc_sync_off);
   float* part = reinterpret_cast<float*>(ws + lay.attn_off);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
 
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)d.D, (cuuint64_t)d.Hq, (cuuint64_t)d.M, (cuuint64_t)d.B};
     const cuuint64_t strides[3] = {(cuuint64_t)d.D * 2, (cuuint64_t)d.Hq * d.D * 2,
                                    (cuuint64_t)d.M * d.Hq * d.D * 2};
     const cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)d.M, 1};
     if (!make_map(&tm_q, a.q, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[4] = {(cuuint64_t)d.D, (cuuint64_t)kBlock, (cuuint64_t)d.Hkv,
-                                (cuuint64_t)d.num_blocks};
-    const cuuint64_t strides[3] = {(cuuint64_t)d.D * 2, (cuuint64_t)kBlock * d.D * 2,
-                                   (cuuint64_t)d.Hkv * kBlock * d.D * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)kBlock, 1, 1};
-    if (!make_map(&tm_k, a.k_cache, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!make_map(&tm_v, a.v_cache, dims, strides, box)) return cudaErrorInvalidValue;
   }
 
   int dev = 0, sms = 0;
@@ -752,11 +1043,14 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   if (e != cudaSuccess) return e;
   const int G = sms < kMaxAttnCtas ? sms : kMaxAttnCtas;
 
-  kv_append_launch(a, lay, st, launches);
   {
-    PdlLaunch L(dim3(1), dim3(1024), 0, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_plan_kernel, a.ctx_lens, (const int32_t*)req_ok, d, ntiles,
-                           prefix);
+    PdlLaunch L(dim3(d.B), dim3(kPrepThreads), 0, st);
+    e = cudaLaunchKernelEx(&L.cfg, attn_prep_kernel, static_cast<const __nv_bfloat16*>(a.k_new),
+                           static_cast<const __nv_bfloat16*>(a.v_new),
+                           static_cast<__nv_bfloat16*>(a.k_cache),
+                           static_cast<__nv_bfloat16*>(a.v_cache), a.block_table, a.ctx_lens,
+                           a.parent, d, G, ntiles, pre, rq, starts, pairs, anc, arrivals,
+                           static_cast<__nv_bfloat16*>(a.out), a.lse, status);
     if (e != cudaSuccess) return e;
   }
   ++*launches;
@@ -766,20 +1060,12 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   const float qscale2 = a.scale * 1.4426950408889634f;
   {
     PdlLaunch L(dim3(G), dim3(kThreads), kSmemBytes, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q, tm_k, tm_v,
+    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q,
                            static_cast<const __nv_bfloat16*>(a.k_cache),
-                           static_cast<const __nv_bfloat16*>(a.v_cache), a.block_table, a.ctx_lens,
-                           a.parent, (const int32_t*)ntiles, (const int32_t*)prefix, d, qscale2,
-                           part, status);
-    if (e != cudaSuccess) return e;
-  }
-  ++*launches;
-  {
-    const int R = (d.Hq / d.Hkv) * d.M;
-    PdlLaunch L(dim3((R + 3) / 4, d.Hkv, d.B), dim3(128), 0, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_tc_combine_kernel<__nv_bfloat16>, (const float*)part,
-                           (const int32_t*)ntiles, (const int32_t*)prefix, d, G,
-                           static_cast<__nv_bfloat16*>(a.out), a.lse);
+                           static_cast<const __nv_bfloat16*>(a.v_cache), a.block_table,
+                           (const int4*)rq, (const int4*)starts,
+                           a.parent != nullptr ? (const unsigned long long*)anc : nullptr, pairs, d,
+                           qscale2, part, static_cast<__nv_bfloat16*>(a.out), a.lse, status);
     if (e != cudaSuccess) return e;
   }
   ++*launches;

@@ -119,7 +119,13 @@ struct WsLayout {
   size_t status_off;      // uint32 status word
   size_t attn_ok_off;     // [B] int32 per-request verdict of the append
   size_t tc_ntiles_off;   // [B] int32 64-key tiles per (request, head)
-  size_t tc_prefix_off;   // [B+1] int32 exclusive prefix of tiles over (request, head)
+  size_t tc_pre_off;      // [2][B+1] int64 prefixes of tiles and of split costs over requests
+  size_t tc_rq_off;       // [B] int4 per request: ctx, tiles per head, next request with tiles
+  size_t tc_start_off;    // [kMaxAttnCtas+1][2] int4 per CTA: first tile, its (request, head,
+                          // tile), the request's record and the end tile
+  size_t tc_pair_off;     // [B*Hkv] int32 per (request, KV head): tiles run by the later CTAs
+  size_t tc_anc_off;      // [B*M] u64 ancestor-or-self mask of every tree row
+  size_t tc_sync_off;     // uint32 arrival count of the request-check kernel
   size_t attn_off;        // split-KV partials of either attention path (f32)
   size_t attn_bytes;
   int split_keys;         // keys per split (multiple of 16)

@@ -64,6 +64,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait until the int at p (written by other CTAs, GPU scope) reaches
+// target, with the same give-up rules as mbar_wait.  The load is an acquire:
+// what the writers published before their count is visible afterwards.
+__device__ __forceinline__ bool wait_count_geq(const int* p, int target, volatile int* abort,
+                                               uint64_t timeout_cycles) {
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if ((uint64_t)(now - t0) > timeout_cycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 4-D tiled load, completion counted on an mbarrier (bytes)
 // ---------------------------------------------------------------------------

@@ -31,7 +31,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ k_cache,
     T* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ parent, spec_dims d,
+    const int32_t* ctx_lens, const int32_t* __restrict__ parent, spec_dims d,
     int32_t* __restrict__ req_ok, uint32_t* __restrict__ status) {
   pdl_trigger();
   pdl_wait();  // the inputs and the cache may come from the previous kernel

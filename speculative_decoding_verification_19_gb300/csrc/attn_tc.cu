@@ -15,15 +15,18 @@
 //
 // Two launches per call:
 //   attn_prep_kernel  one CTA per request: checks it (capacity, block ids,
-//                     topology), appends its new K/V rows, and for a tree
-//                     the ancestor-or-self mask of every row.  The last CTA
+//                     topology) and, for a tree, the ancestor-or-self mask
+//                     of every row.  The last CTA
 //                     to finish plans the split: per-request records (ctx,
 //                     tiles, next request with tiles) and each CTA's first
 //                     tile, balancing tiles plus a fixed cost per (b, h)
 //                     segment a CTA starts (a segment start costs about as
 //                     much as a few tiles: new Q, new masks, a drain of the
 //                     MMA pipeline).
-//   attn_tc_kernel    the attention.  A (b, h) pair wholly inside one CTA
+//   attn_tc_kernel    the append (an even share of the new rows per CTA,
+//                     written while the first tiles load; tiles that reach
+//                     the new positions take them from k_new / v_new) and
+//                     the attention.  A (b, h) pair wholly inside one CTA
 //                     writes its normalised output directly; a pair split
 //                     over CTAs leaves one partial per CTA, and the CTA that
 //                     completes the pair's tile count merges them by
@@ -133,7 +136,7 @@ struct Cursor {
     nt = st1.y;
     next_b = st1.z;
     nrec = make_int4(0, 0, B, 0);
-    if (next_b < B) nrec = rq[next_b];
+    if (next_b < B) nrec = __ldcg(rq + next_b);
   }
   __device__ void next(const int4* rq, int B, int Hkv) {
     if (++tile < nt) return;
@@ -144,7 +147,7 @@ struct Cursor {
     ctx = nrec.x;
     nt = nrec.y;
     next_b = nrec.z;
-    if (next_b < B) nrec = rq[next_b];
+    if (next_b < B) nrec = __ldcg(rq + next_b);
   }
 };
 
@@ -188,11 +191,11 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_cache,
-    const __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int4* __restrict__ rq, const int4* __restrict__ starts,
-    const unsigned long long* __restrict__ anc_ws, int* __restrict__ pairs, spec_dims d,
-    float qscale2, float* __restrict__ part, __nv_bfloat16* __restrict__ out,
+    const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_new,
+    const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ k_cache,
+    __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
+    const int4* rq, const int4* starts, const unsigned long long* anc_ws, int* pairs, spec_dims d,
+    float qscale2, float* part, __nv_bfloat16* __restrict__ out,
     float* __restrict__ lse, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -250,15 +253,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
 
-  pdl_wait();  // the plan and the appended rows come from the previous kernel
-  const int4 st0 = starts[2 * c], st1 = starts[2 * c + 1];
+  pdl_wait();  // the plan comes from the previous kernel
+  const int4 st0 = __ldcg(starts + 2 * c), st1 = __ldcg(starts + 2 * c + 1);
   const int64_t g0 = st0.x, g1 = st1.w;
-  if (g0 >= g1) {  // uniform: no tiles for this CTA
+  const bool idle = g0 >= g1;  // uniform: no tiles for this CTA
+  const int copy_warp = n_sm_warps <= 2 ? kCopyWarpSmallR : kCopyWarpLargeR;
+
+  // ------------------------------------------------------------------ append
+  // The new rows go into the cache while the first tiles load: every CTA
+  // writes an even share of all (request, position, head, 16-byte chunk)
+  // items, positions ctx .. end-1 with end = ceil(L/16)*16 (rows past
+  // ctx+M-1 cleared).  The attention itself reads the new rows from
+  // k_new / v_new, so nothing waits for these writes.  Writers: every thread
+  // of a CTA without tiles, else the warps without a role (softmax warps of
+  // padding sub-partitions, warp 8 when warp 7 copies), else, when R > 96
+  // leaves none, the softmax warps before their first tile.
+  uint32_t writers = 0;  // bit w: warp w writes
+  for (int w = 0; w <= kCopyWarpLargeR; ++w)
+    if (w != copy_warp && (w >= kSoftmaxWarps || (w & 3) >= n_sm_warps)) writers |= 1u << w;
+  if (writers == 0) writers = ((1u << kSoftmaxWarps) - 1) & ~(1u << copy_warp);
+  if (idle) writers = (1u << (kThreads / kWarp)) - 1;
+  if ((writers >> warp) & 1u) {
+    const int nthr = __popc(writers) * kWarp;
+    const int wtid = __popc(writers & ((1u << warp) - 1)) * kWarp + lane;
+    const int per_pos = Hkv * 16;  // items of one position (D = 128)
+    const int per_req = (M + kBlock - 1) * per_pos;
+    const int64_t n_items = (int64_t)B * per_req;
+    const int64_t i0 = (int64_t)c * n_items / gridDim.x, i1 = (int64_t)(c + 1) * n_items / gridDim.x;
+#pragma unroll 2
+    for (int64_t it = i0 + wtid; it < i1; it += nthr) {
+      const int b = (int)(it / per_req);
+      const int rem = (int)(it - (int64_t)b * per_req);
+      const int pi = rem / per_pos;
+      const int h = (rem / 16) % Hkv;
+      const int ch = rem % 16;
+      const int4 r = __ldcg(rq + b);  // (ctx, tiles, ...): no tiles means the request failed its checks
+      const int64_t tpos = (int64_t)r.x + pi;
+      if (r.y == 0 || tpos >= ceil_div64((int64_t)r.x + M, kBlock) * kBlock) continue;
+      const int64_t dst = (((int64_t)block_table[(int64_t)b * d.max_blocks + tpos / kBlock] * Hkv + h) *
+                               kBlock + tpos % kBlock) * 128 + ch * 8;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (pi < M) {
+        const int64_t src = (((int64_t)b * M + pi) * Hkv + h) * 128 + ch * 8;
+        kv = *reinterpret_cast<const uint4*>(k_new + src);
+        vv = *reinterpret_cast<const uint4*>(v_new + src);
+      }
+      *reinterpret_cast<uint4*>(k_cache + dst) = kv;
+      *reinterpret_cast<uint4*>(v_cache + dst) = vv;
+    }
+  }
+  if (idle) {
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
     return;
   }
 
-  const int copy_warp = n_sm_warps <= 2 ? kCopyWarpSmallR : kCopyWarpLargeR;
   if (warp == kProducerWarp || warp == copy_warp) {
     // ------------------------------------------------------------ producers
     // Both warps walk the tiles; lane j holds the four block ids of tile
@@ -348,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         break;
       }
       const uint32_t sb = ptx::smem_u32(stages + stage * kStageBytes);
+      const int kpos0 = cu.tile * kTileKeys;
+      if (kpos0 + kTileKeys <= cu.ctx) {  // all keys in the cached prefix
 #pragma unroll
-      for (int p = 0; p < kPages; ++p) {
-        if (p < np) {
+        for (int p = 0; p < kPages; ++p) {
           const int64_t page = ((int64_t)blk[p] * Hkv + cu.h) * kBlock;  // row of slot 0
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -360,6 +409,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
                                 ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
             ptx::cp_async16(sb + so, k_cache + e);
             ptx::cp_async16(sb + 2 * kHalfBytes + so, v_cache + e);
+          }
+        }
+      } else {
+        // the tile reaches the new rows: those come from k_new / v_new (the
+        // append into the cache runs concurrently), rows past L are zero
+#pragma unroll
+        for (int p = 0; p < kPages; ++p) {
+          if (p < np) {
+            const int64_t page = ((int64_t)blk[p] * Hkv + cu.h) * kBlock;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = r0 + 4 * k;
+              const int pos = kpos0 + p * kBlock + r;
+              const uint32_t so = swz_half + (uint32_t)p * kBoxBytes + (uint32_t)r * 128u +
+                                  ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
+              if (pos < cu.ctx) {
+                const int64_t e = (page + r) * 128 + c16 * 8;
+                ptx::cp_async16(sb + so, k_cache + e);
+                ptx::cp_async16(sb + 2 * kHalfBytes + so, v_cache + e);
+              } else {
+                const bool in = pos < L;
+                const int64_t e = in ? (((int64_t)cu.b * M + (pos - cu.ctx)) * Hkv + cu.h) * 128 + c16 * 8 : 0;
+                ptx::cp_async16_fill(sb + so, k_new + e, in ? 16u : 0u);
+                ptx::cp_async16_fill(sb + 2 * kHalfBytes + so, v_new + e, in ? 16u : 0u);
+              }
+            }
           }
         }
       }
@@ -502,10 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           } else if (real && cu.b != anc_b) {
             // tree masks come from the prep kernel; the next request's mask
             // is loaded one request ahead
-            anc = cu.b == anc_nb ? anc_n : anc_ws[(int64_t)cu.b * M + i];
+            anc = cu.b == anc_nb ? anc_n : __ldcg(anc_ws + (int64_t)cu.b * M + i);
             anc_b = cu.b;
             if (cu.next_b < B) {
-              anc_n = anc_ws[(int64_t)cu.next_b * M + i];
+              anc_n = __ldcg(anc_ws + (int64_t)cu.next_b * M + i);
               anc_nb = cu.next_b;
             }
           }
@@ -691,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
               // walk up from CTA c+1 until the partials' tiles add up; CTAs
               // with no tiles (more CTAs than split costs) wrote nothing
               for (int got = 0, cc = c + 1; got < rest && cc < (int)gridDim.x; ++cc) {
-                if (starts[2 * cc].x == starts[2 * cc + 1].w) continue;
+                if (__ldcg(&starts[2 * cc].x) == __ldcg(&starts[2 * cc + 1].w)) continue;
                 const float* q = part + ((pair + cc) * R + (real ? row : 0)) * (int64_t)S;
                 const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
                 got += __float_as_int(sc.w);
@@ -714,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 #pragma unroll
               for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * wown);
               for (int cq = c + 1; cq <= c_end; ++cq) {
-                if (starts[2 * cq].x == starts[2 * cq + 1].w) continue;
+                if (__ldcg(&starts[2 * cq].x) == __ldcg(&starts[2 * cq + 1].w)) continue;
                 const float* q = part + ((pair + cq) * R + (real ? row : 0)) * (int64_t)S;
                 const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
                 float4 v[8];
@@ -751,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// request checks, append and the plan of the split
+// request checks and the plan of the split
 // ---------------------------------------------------------------------------
 // Exclusive prefix over the CTA's threads of two int64 sums and an int max.
 __device__ __forceinline__ void block_scan(int64_t& a, int64_t& c, int& m, int64_t* sa,
@@ -801,21 +876,18 @@ __device__ __forceinline__ void block_scan(int64_t& a, int64_t& c, int& m, int64
 }
 
 // One CTA per request.  Checks the request (capacity, the block ids of every
-// page it reads or writes, the tree topology), records it for the plan, and
-// appends its new rows: positions ctx .. end-1 where end = ceil(L/16)*16,
-// rows past ctx+M-1 cleared.  A request that fails gets out = 0, lse = -inf
-// and no tiles.  The CTA that arrives last plans the split of the tiles.
+// page it reads or writes, the tree topology) and records it for the plan.
+// A request that fails gets out = 0, lse = -inf and no tiles (the attention
+// kernel then neither reads nor appends it).  The CTA that arrives last
+// plans the split of the tiles.
 __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
-    const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
-    __nv_bfloat16* __restrict__ k_cache, __nv_bfloat16* __restrict__ v_cache,
-    const int32_t* __restrict__ block_table, const int32_t* __restrict__ ctx_lens,
+    const int32_t* __restrict__ block_table, const int32_t* ctx_lens,
     const int32_t* __restrict__ parent, spec_dims d, int G, int32_t* __restrict__ ntiles,
     int64_t* __restrict__ pre, int4* __restrict__ rq, int4* __restrict__ starts,
     int* __restrict__ pairs, unsigned long long* __restrict__ anc_ws,
     uint32_t* __restrict__ arrivals, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
     uint32_t* __restrict__ status) {
   __shared__ int s_last;
-  __shared__ int s_blk[8];
   __shared__ int64_t s_a[kPrepThreads / kWarp], s_c[kPrepThreads / kWarp];
   __shared__ int s_m[kPrepThreads / kWarp];
   pdl_trigger();
@@ -871,37 +943,13 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
   }
   __syncthreads();
 
-  const int lanes = D / 8;  // 16-byte vectors per (position, head)
   if (!ok) {
+    const int lanes = D / 8;  // 16-byte vectors per (position, head)
     const int64_t n = (int64_t)M * d.Hq * lanes;
     for (int64_t w = tid; w < n; w += blockDim.x)
       reinterpret_cast<uint4*>(out + (int64_t)b * M * d.Hq * D)[w] = make_uint4(0, 0, 0, 0);
     if (lse != nullptr)
       for (int w = tid; w < M * d.Hq; w += blockDim.x) lse[(int64_t)b * M * d.Hq + w] = -INFINITY;
-  } else {
-    // block ids of the pages written, staged once (at most 5 for M <= 64)
-    const int64_t end = ceil_div64(L, kBlock) * kBlock;
-    const int p0 = ctx / kBlock;
-    if (tid < (int)(end / kBlock) - p0) s_blk[tid] = bt[p0 + tid];
-    __syncthreads();
-    const int npos = (int)(end - ctx);
-    const int work = npos * Hkv * lanes;
-#pragma unroll 4
-    for (int w = tid; w < work; w += blockDim.x) {
-      const int lane = w % lanes;
-      const int h = (w / lanes) % Hkv;
-      const int i = w / (lanes * Hkv);
-      const int64_t t = (int64_t)ctx + i;
-      const int64_t dst = (((int64_t)s_blk[t / kBlock - p0] * Hkv + h) * kBlock + t % kBlock) * D;
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (i < M) {
-        const int64_t src = (((int64_t)b * M + i) * Hkv + h) * D;
-        kv = reinterpret_cast<const uint4*>(k_new + src)[lane];
-        vv = reinterpret_cast<const uint4*>(v_new + src)[lane];
-      }
-      reinterpret_cast<uint4*>(k_cache + dst)[lane] = kv;
-      reinterpret_cast<uint4*>(v_cache + dst)[lane] = vv;
-    }
   }
   if (!s_last) return;
 
@@ -1045,10 +1093,7 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
 
   {
     PdlLaunch L(dim3(d.B), dim3(kPrepThreads), 0, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_prep_kernel, static_cast<const __nv_bfloat16*>(a.k_new),
-                           static_cast<const __nv_bfloat16*>(a.v_new),
-                           static_cast<__nv_bfloat16*>(a.k_cache),
-                           static_cast<__nv_bfloat16*>(a.v_cache), a.block_table, a.ctx_lens,
+    e = cudaLaunchKernelEx(&L.cfg, attn_prep_kernel, a.block_table, a.ctx_lens,
                            a.parent, d, G, ntiles, pre, rq, starts, pairs, anc, arrivals,
                            static_cast<__nv_bfloat16*>(a.out), a.lse, status);
     if (e != cudaSuccess) return e;
@@ -1061,8 +1106,10 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   {
     PdlLaunch L(dim3(G), dim3(kThreads), kSmemBytes, st);
     e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q,
-                           static_cast<const __nv_bfloat16*>(a.k_cache),
-                           static_cast<const __nv_bfloat16*>(a.v_cache), a.block_table,
+                           static_cast<const __nv_bfloat16*>(a.k_new),
+                           static_cast<const __nv_bfloat16*>(a.v_new),
+                           static_cast<__nv_bfloat16*>(a.k_cache),
+                           static_cast<__nv_bfloat16*>(a.v_cache), a.block_table,
                            (const int4*)rq, (const int4*)starts,
                            a.parent != nullptr ? (const unsigned long long*)anc : nullptr, pairs, d,
                            qscale2, part, static_cast<__nv_bfloat16*>(a.out), a.lse, status);

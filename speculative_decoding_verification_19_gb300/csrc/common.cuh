@@ -87,6 +87,9 @@ __device__ __forceinline__ int warp_or(int v) {
 // while its predecessor on the stream drains; it must call pdl_wait() before
 // touching memory a predecessor writes (which also keeps the chain
 // transitive), and calls pdl_trigger() early to let its own dependents launch.
+// Pointers to what a predecessor kernel of the chain writes are never
+// __restrict__: a restrict-qualified load may be moved above pdl_wait (or
+// served by the read-only path) and then see the memory before the write.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -15,9 +15,9 @@ namespace specv {
 
 template <typename T>
 __global__ void __launch_bounds__(256) kv_commit_kernel(
-    T* __restrict__ k_cache, T* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int32_t* ctx_lens, int32_t* new_ctx_lens, const int32_t* __restrict__ path,
-    const int32_t* __restrict__ accepted_len, spec_dims d, uint32_t* __restrict__ status) {
+    T* k_cache, T* v_cache, const int32_t* __restrict__ block_table, const int32_t* ctx_lens,
+    int32_t* new_ctx_lens, const int32_t* path, const int32_t* accepted_len, spec_dims d,
+    uint32_t* __restrict__ status) {
   pdl_trigger();
   pdl_wait();  // path and accepted_len come from the previous kernel
   const int b = blockIdx.x, tid = threadIdx.x;

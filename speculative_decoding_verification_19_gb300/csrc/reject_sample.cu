@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* __restrict__ stats, DrawState* __restrict__ draws,
+    int chunk, const RowStat* stats, DrawState* __restrict__ draws,
     uint32_t* __restrict__ status) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kSweep = kDecThreads * EPV;
@@ -1091,7 +1091,7 @@ __host__ __device__ __forceinline__ int rs_res_spans(int n_chunks) {
 template <typename T, bool kAligned>
 __global__ void __launch_bounds__(kResThreads) rs_residual_sums_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
-    int chunk, const DrawState* __restrict__ draws, double* __restrict__ zsum) {
+    int chunk, const DrawState* draws, double* __restrict__ zsum) {
   constexpr int EPV = 16 / sizeof(T);
   const int n_spans = rs_res_spans(n_chunks);
   const int sp = (int)(blockIdx.x % n_spans), b = (int)(blockIdx.x / n_spans), tid = threadIdx.x;
@@ -1140,8 +1140,8 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_sums_kernel(
 template <typename T, bool kAligned>
 __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, spec_dims d, int n_chunks,
-    int chunk, const RowStat* __restrict__ stats, const DrawState* __restrict__ draws,
-    const double* __restrict__ zsum, int32_t* __restrict__ out_tokens, float* __restrict__ probe) {
+    int chunk, const RowStat* stats, const DrawState* draws, const double* zsum,
+    int32_t* __restrict__ out_tokens, float* __restrict__ probe) {
   const int b = blockIdx.x, tid = threadIdx.x;
   const int warp = tid / kWarp, lane = tid % kWarp;
   __shared__ DecideCtx ctx;

@@ -114,6 +114,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
                "l"(reinterpret_cast<uint64_t>(src))
                : "memory");
 }
+// The same copy with only the first `src_bytes` (0 or 16) read from global
+// memory and the rest of the 16 bytes set to zero.
+__device__ __forceinline__ void cp_async16_fill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed;
 // the arrival counts toward the barrier's expected count (no increment).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -55,10 +55,11 @@ def gpu_reject(wl, lg, seed, offset, b_base=0, dims=None, ws=None, probe=True):
     tok = to_dev(lg["tokens"], torch.int32)
     par = None if lg["parent"] is None else to_dev(lg["parent"], torch.int32)
     temp = to_dev(lg["temperature"], torch.float32)
-    out_tokens = torch.empty(B, M, dtype=torch.int32, device="cuda")
-    path = torch.empty(B, M, dtype=torch.int32, device="cuda")
-    acc = torch.empty(B, dtype=torch.int32, device="cuda")
-    pr = torch.empty(B, M, 4, dtype=torch.float32, device="cuda") if probe else None
+    # sentinel-filled: anything the kernels leave unwritten fails the comparison
+    out_tokens = torch.full((B, M), -7, dtype=torch.int32, device="cuda")
+    path = torch.full((B, M), -7, dtype=torch.int32, device="cuda")
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    pr = torch.full((B, M, 4), float("nan"), dtype=torch.float32, device="cuda") if probe else None
     sv.spec_reject_sample(t, d, tok, par, temp, seed, offset, out_tokens, path,
                           acc, pr, dims, ws, b_base=b_base)
     torch.cuda.synchronize()
@@ -127,8 +128,9 @@ def gpu_attn(wl, kv, parent=None, dims=None, ws=None, impl=0):
     bt = to_dev(kv["block_table"], torch.int32)
     ctx = to_dev(kv["ctx_lens"], torch.int32)
     par = None if parent is None else to_dev(parent, torch.int32)
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    # NaN-filled: an output row the kernels never write fails the comparison
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
     sv.spec_verify_attn(q, kn, vn, kc, vc, bt, ctx, par, out, lse, dims, ws)
     torch.cuda.synchronize()
     return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy(),

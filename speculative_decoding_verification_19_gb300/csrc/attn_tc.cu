@@ -306,6 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
     return;
   }
+  // Only a CTA's first segment can be a later share of a split pair (it
+  // starts inside the pair).  Its tiles are counted for the merging CTA by a
+  // warp without a role, after the softmax warps have written the partial,
+  // so that the fence before the count stalls no softmax warp.
+  const int helper = n_sm_warps <= 2 ? kCopyWarpLargeR : (n_sm_warps == 3 ? 3 : -1);
+  if (warp == helper && lane == 0 && st0.w > 0) {
+    if (ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, kTimeoutNs)) {
+      __threadfence();
+      atomicAdd(pairs + (int64_t)st0.y * Hkv + st0.z, (int)min((int64_t)(st1.y - st0.w), g1 - g0));
+    }
+  }
 
   if (warp == kProducerWarp || warp == copy_warp) {
     // ------------------------------------------------------------ producers
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       unsigned long long anc = 0, anc_n = 0;
       int anc_b = -1, anc_nb = -1;  // requests whose masks anc and anc_n hold
       int ctx = 0, L = 0, tile0 = 0;
-      int n_whole = 0, n_split = 0;  // pair ends of each kind so far (barrier phases)
+      int n_whole = 0;  // pair ends with output so far (barrier phase)
       const bool real = row < R;
       const int i = real ? row / group : 0;
       for (int64_t g = g0; g < g1; ++g, ++t) {
@@ -734,10 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ebar));
-            const uint32_t ph = (uint32_t)(n_split & 1);
-            ++n_split;
-            if (warp == 0 && lane == 0 &&
-                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), ph, abort, kTimeoutNs)) {
+            if (helper < 0 && warp == 0 && lane == 0 &&
+                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, kTimeoutNs)) {
               // every row of the partial is written (the barrier above); the
               // fence makes them visible GPU-wide before the tiles are counted
               __threadfence();
@@ -757,55 +766,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             float ls = bars->xl[0][row] + bars->xl[1][row];
             float mx = m_used;
             const int rest = cu.nt - own;  // tiles run by the CTAs after this one
-            int c_end = c;                 // the last CTA with a share of the pair
+            bool okc = true;
             if (rest > 0) {
-              bool okc = true;
               if (lane == 0) okc = ptx::wait_count_geq(pairs + pair, rest, abort, kTimeoutNs);
               __syncwarp();
-              if (!__shfl_sync(0xffffffffu, okc, 0)) break;
-              // walk up from CTA c+1 until the partials' tiles add up; CTAs
-              // with no tiles (more CTAs than split costs) wrote nothing
-              for (int got = 0, cc = c + 1; got < rest && cc < (int)gridDim.x; ++cc) {
-                if (__ldcg(&starts[2 * cc].x) == __ldcg(&starts[2 * cc + 1].w)) continue;
-                const float* q = part + ((pair + cc) * R + (real ? row : 0)) * (int64_t)S;
-                const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
-                got += __float_as_int(sc.w);
-                c_end = cc;
-                const float lq = sc.y + sc.z;
-                if (lq > 0.f) {
-                  const float mn = fmaxf(mx, sc.x);
-                  ls = (mx == -INFINITY ? 0.f : ls * exp2f(mx - mn)) + lq * exp2f(sc.x - mn);
-                  mx = mn;
-                }
-              }
+              okc = __shfl_sync(0xffffffffu, okc, 0);
             }
-            const float inv = ls > 0.f ? 1.f / ls : 0.f;
-            const float wown = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mx);
+            if (!okc) break;
+            // Two passes over this half's 64 columns, 32 at a time.  Each walks
+            // up from CTA c+1 until the partials' tiles add up (CTAs with no
+            // tiles, possible when there are more CTAs than split costs, wrote
+            // nothing), loading a partial's scalars with its columns.  The
+            // first pass also finds the common maximum and the row sum; the
+            // second reuses them.
+            const float m_own = m_used;
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc2 = 0; cc2 < 2; ++cc2) {
               uint32_t o[32];
-              ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc * 32, o);
+              ptx::tmem_ld32(lane_base + kOCol + half * 64 + cc2 * 32, o);
               ptx::tmem_wait_ld();
+              // o holds sum w * O relative to the maximum mx; in the first pass
+              // mx grows as partials come in, in the second it is final
+              const float w_own = cc2 == 0 ? 1.f : (m_own == -INFINITY ? 0.f : exp2f(m_own - mx));
 #pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * wown);
-              for (int cq = c + 1; cq <= c_end; ++cq) {
-                if (__ldcg(&starts[2 * cq].x) == __ldcg(&starts[2 * cq + 1].w)) continue;
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * w_own);
+              for (int got = 0, cq = c + 1; got < rest && cq < (int)gridDim.x; ++cq) {
+                const int ga = __ldcg(&starts[2 * cq].x), gb = __ldcg(&starts[2 * cq + 1].w);
                 const float* q = part + ((pair + cq) * R + (real ? row : 0)) * (int64_t)S;
                 const float4 sc = __ldcg(reinterpret_cast<const float4*>(q + d.D));
                 float4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                  v[j] = __ldcg(reinterpret_cast<const float4*>(q + half * 64 + cc * 32) + j);
-                const float w = sc.y + sc.z > 0.f ? exp2f(sc.x - mx) : 0.f;
+                  v[j] = __ldcg(reinterpret_cast<const float4*>(q + half * 64 + cc2 * 32) + j);
+                if (ga == gb) continue;
+                got += __float_as_int(sc.w);
+                const float lq = sc.y + sc.z;
+                if (!(lq > 0.f)) continue;
+                float a = 1.f, w;
+                if (cc2 == 0) {
+                  const float mn = fmaxf(mx, sc.x);
+                  a = mx == -INFINITY ? 0.f : exp2f(mx - mn);
+                  w = exp2f(sc.x - mn);
+                  ls = ls * a + lq * w;
+                  mx = mn;
+                } else {
+                  w = exp2f(sc.x - mx);
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  o[4 * j] = __float_as_uint(fmaf(w, v[j].x, __uint_as_float(o[4 * j])));
-                  o[4 * j + 1] = __float_as_uint(fmaf(w, v[j].y, __uint_as_float(o[4 * j + 1])));
-                  o[4 * j + 2] = __float_as_uint(fmaf(w, v[j].z, __uint_as_float(o[4 * j + 2])));
-                  o[4 * j + 3] = __float_as_uint(fmaf(w, v[j].w, __uint_as_float(o[4 * j + 3])));
+                  o[4 * j] = __float_as_uint(fmaf(w, v[j].x, a * __uint_as_float(o[4 * j])));
+                  o[4 * j + 1] = __float_as_uint(fmaf(w, v[j].y, a * __uint_as_float(o[4 * j + 1])));
+                  o[4 * j + 2] = __float_as_uint(fmaf(w, v[j].z, a * __uint_as_float(o[4 * j + 2])));
+                  o[4 * j + 3] = __float_as_uint(fmaf(w, v[j].w, a * __uint_as_float(o[4 * j + 3])));
                 }
               }
-              if (real) store32_bf16(orow + cc * 32, o, inv);
+              if (real) store32_bf16(orow + cc2 * 32, o, ls > 0.f ? 1.f / ls : 0.f);
             }
             if (real && half == 0 && lrow != nullptr)
               *lrow = ls > 0.f ? (mx + log2f(ls)) * 0.69314718055994530942f : -INFINITY;

@@ -95,8 +95,9 @@ constexpr int kOCol = kSBufs * kTileKeys;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
 // Split cost of one (request, head) segment, in tiles: the Q load, the
 // masks and the drain of the pipeline at a pair's end cost about this much.
-constexpr int kSegCost = 2;
+constexpr int kSegCost = 3;
 constexpr int kPrepThreads = 256;
+constexpr int kPlanReqs = 1024;  // requests whose plan arrays fit the prep kernel's shared memory
 
 struct __align__(8) Bars {
   uint64_t full[kStages];
@@ -905,6 +906,10 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
   __shared__ int s_last;
   __shared__ int64_t s_a[kPrepThreads / kWarp], s_c[kPrepThreads / kWarp];
   __shared__ int s_m[kPrepThreads / kWarp];
+  // the plan's working arrays (used by the last CTA only)
+  __shared__ int64_t s_tpre[kPlanReqs + 1], s_cpre[kPlanReqs + 1];
+  __shared__ int s_nt[kPlanReqs], s_ctx[kPlanReqs], s_next[kPlanReqs];
+  __shared__ int s_g0[kMaxAttnCtas + 1], s_req[kMaxAttnCtas];
   pdl_trigger();
   pdl_wait();  // the inputs and the cache may come from the previous kernel
   const int b = blockIdx.x;
@@ -974,13 +979,18 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
   // base + kSegCost + j, and CTA k starts at the first tile whose cost
   // reaches k * total / G.
   __threadfence();
-  int64_t* tpre = pre;           // [B+1] tiles before request r
-  int64_t* cpre = pre + B + 1;   // [B+1] split cost before request r
+  // Up to kPlanReqs requests the plan's per-request arrays live in shared
+  // memory (no global round trips after the first load), beyond that in the
+  // workspace.
+  const bool small = B <= kPlanReqs;
+  int64_t* tpre = small ? s_tpre : pre;          // [B+1] tiles before request r
+  int64_t* cpre = small ? s_cpre : pre + B + 1;  // [B+1] split cost before request r
   int64_t carry_t = 0, carry_c = 0;
   int carry_m = -1;
   for (int base = 0; base < B; base += blockDim.x) {
     const int r = base + tid;
     const int nt = r < B ? __ldcg(ntiles + r) : 0;
+    const int cx = r < B ? ctx_lens[r] : 0;
     int64_t vt = (int64_t)nt * Hkv, vc = nt > 0 ? (int64_t)Hkv * (nt + kSegCost) : 0;
     int vm = nt > 0 ? r : -1;
     int64_t tt, tcst;
@@ -990,10 +1000,18 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
     if (r < B) {
       tpre[r] = carry_t + vt;
       cpre[r] = carry_c + vc;
-      rq[r] = make_int4(ctx_lens[r], nt, B, 0);
+      rq[r] = make_int4(cx, nt, B, 0);
+      if (small) {
+        s_nt[r] = nt;
+        s_ctx[r] = cx;
+        s_next[r] = B;
+      }
     }
     __syncthreads();
-    if (r < B && nt > 0 && prev >= 0) reinterpret_cast<int*>(rq + prev)[2] = r;
+    if (r < B && nt > 0 && prev >= 0) {
+      reinterpret_cast<int*>(rq + prev)[2] = r;
+      if (small) s_next[prev] = r;
+    }
     carry_t += tt;
     carry_c += tcst;
     carry_m = max(carry_m, tm);
@@ -1005,6 +1023,7 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
     cpre[B] = Ctot;
     starts[2 * G] = make_int4((int)T, B, 0, 0);
     starts[2 * G + 1] = make_int4(0, 0, B, (int)T);
+    s_g0[G] = (int)T;
     *arrivals = 0;
   }
   __syncthreads();
@@ -1018,7 +1037,7 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
   for (int r = tid; r < B; r += blockDim.x) {
     const int64_t c0 = cpre[r], c1 = cpre[r + 1];
     if (c1 == c0) continue;
-    const int nt = __ldcg(ntiles + r);
+    const int nt = small ? s_nt[r] : __ldcg(ntiles + r);
     const int64_t per = nt + kSegCost;
     // CTAs k with c0 <= floor(k * Ctot / G) < c1
     const int k0 = (int)((c0 * G + Ctot - 1) / Ctot), k1 = (int)((c1 * G + Ctot - 1) / Ctot);
@@ -1027,16 +1046,19 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
       const int h = (int)(rem / per);
       rem -= h * per;
       const int j = (int)max((int64_t)0, rem - kSegCost);  // rem < nt + kSegCost: j < nt
-      starts[2 * k] = make_int4((int)(tpre[r] + (int64_t)h * nt + j), r, h, j);
+      const int g0 = (int)(tpre[r] + (int64_t)h * nt + j);
+      starts[2 * k] = make_int4(g0, r, h, j);
+      s_g0[k] = g0;
+      s_req[k] = r;
     }
   }
   __syncthreads();
   // second half of each start record: the first request's record and the
-  // CTA's end tile
+  // CTA's end tile (a CTA with tiles starts inside a request)
   for (int k = tid; k < G; k += blockDim.x) {
-    const int4 s0 = starts[2 * k];
-    const int4 r = rq[s0.y];  // a CTA with tiles starts inside a request
-    starts[2 * k + 1] = make_int4(r.x, r.y, r.z, starts[2 * k + 2].x);
+    const int r = s_req[k];
+    const int4 rec = small ? make_int4(s_ctx[r], s_nt[r], s_next[r], 0) : rq[r];
+    starts[2 * k + 1] = make_int4(rec.x, rec.y, rec.z, s_g0[k + 1]);
   }
 }
 

@@ -72,6 +72,15 @@ def test_more_ctas_than_tiles():
     _check(wl, kv_inputs_host(wl, seed=11, B=3, ctx=np.array([0, 60, 130])))
 
 
+def test_many_requests():
+    # more requests than the tensor-core plan keeps in shared memory (1024),
+    # with mixed short contexts so that CTA ranges cross many requests
+    wl = workload("chain_gqa_128k").scaled(Hq=8, Hkv=2, gamma=3)
+    rng = np.random.default_rng(13)
+    ctx = rng.integers(0, 200, size=1100)
+    _check(wl, kv_inputs_host(wl, seed=13, B=1100, ctx=ctx), impls=[sv.ATTN_TENSOR_CORES])
+
+
 def test_tree_rows_up_to_128():
     wl = workload("tree_64").scaled(Hq=4, Hkv=2, tree_nodes=64, tree_width=4)
     kv = kv_inputs_host(wl, seed=12, B=2, ctx=np.array([200, 1999]))

@@ -40,12 +40,13 @@ METRIC = "verify steps/s and accepted tokens/s at 1 GB300; achieved HBM TB/s vs 
 UNIT = "verify steps/s"
 DEFAULT_WORKLOAD = "stress_gqa_152k"
 
-# DRAM traffic of one spec_verify_attn call (append + plan + split + combine
-# kernels) measured by ncu on 16 of the 128 requests of the default workload
-# and scaled to 128 by the algorithmic bytes (traffic grows with the KV
-# bytes read): profiles/attn_tc_kernel_stress_gqa_152k_b16.md.  Valid only
-# for the attention kernel sources whose digest is recorded with it.
-TRAFFIC = {"digest": "da5849afd4c4a790", "bytes_per_call": 10137078340}
+# DRAM traffic of one spec_verify_attn call (request-check/plan kernel and
+# the attention kernel with its append and merge) measured by ncu on 16 of
+# the 128 requests of the default workload and scaled to 128 by the
+# algorithmic bytes (traffic grows with the KV bytes read):
+# profiles/attn_tc_kernel_stress_gqa_152k_b16.md.  Valid only for the
+# attention kernel sources whose digest is recorded with it.
+TRAFFIC = {"digest": "5e6e47c41375e2bf", "bytes_per_call": 10104207911}
 TRAFFIC_ALG_BYTES = 10051956736  # algorithmic bytes per call of that workload (seed 0)
 
 
@@ -437,7 +438,7 @@ def run_native(args, wl, world, rank, local):
         "accepted_tokens_per_s": round(steps_per_s * emitted_per_step, 1),
         "emitted_tokens_per_step": round(emitted_per_step, 2),
         "hbm_tb_s": round((attn_b + rej_b) / (ms_max / K / 1e3) / 1e12, 3),
-        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (append+split+combine)",
+        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (request checks + plan, attention with append and merge)",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

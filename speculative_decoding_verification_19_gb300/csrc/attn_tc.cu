@@ -81,7 +81,7 @@ constexpr int kProducerWarp = 10;  // Q (TMA) and half of the K/V copies
 // softmax warps) when rows 64..127 are padding, else warp 8
 constexpr int kCopyWarpSmallR = 7;
 constexpr int kCopyWarpLargeR = 8;
-constexpr int kCopyThreads = 64;    // threads issuing K/V copies (warps 8 and 10)
+constexpr int kCopyThreads = 64;    // threads issuing K/V copies (the copy warp and warp 10)
 constexpr int kMmaWarp = 11;  // issues Q K^T
 constexpr int kPvWarp = 9;    // issues P V
 constexpr int kBoxBytes = kBlock * 128;       // one page x 64 of D, bf16: 2 KB
@@ -109,10 +109,10 @@ struct __align__(8) Bars {
   uint64_t o_done[kSBufs];  // completion of PV(t) lands on o_done[t % kSBufs]
   uint64_t drain[2];  // the Q K^T issuer's and the P V issuer's last completion
   uint64_t xbar[4][2];       // per sub-partition, per tile parity: both halves' maxima
-  uint64_t lbar[4];          // per sub-partition: both halves' row sums of a whole pair
+  uint64_t lbar[4];          // per sub-partition: both halves' row sums at a pair's output
   uint64_t ebar;             // every softmax warp wrote its rows of a partial
   float xmax[2][2][128];     // [tile parity][half][row]
-  float xl[2][128];          // [half][row] row sums at the end of a whole pair
+  float xl[2][128];          // [half][row] row sums at a pair's output
   uint32_t tmem_base;
   int abort;
 };

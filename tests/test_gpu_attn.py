@@ -81,6 +81,14 @@ def test_many_requests():
     _check(wl, kv_inputs_host(wl, seed=13, B=1100, ctx=ctx), impls=[sv.ATTN_TENSOR_CORES])
 
 
+def test_pairs_over_many_ctas():
+    # one long request: each (request, KV head) pair spans about twenty CTAs,
+    # so the CTA holding a pair's first tile merges many partials
+    wl = workload("chain_gqa_128k").scaled(gamma=3)
+    _check(wl, kv_inputs_host(wl, seed=14, B=1, ctx=np.array([40000])),
+           impls=[sv.ATTN_TENSOR_CORES])
+
+
 def test_tree_rows_up_to_128():
     wl = workload("tree_64").scaled(Hq=4, Hkv=2, tree_nodes=64, tree_width=4)
     kv = kv_inputs_host(wl, seed=12, B=2, ctx=np.array([200, 1999]))

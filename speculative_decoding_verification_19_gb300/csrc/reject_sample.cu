@@ -190,7 +190,10 @@ constexpr size_t kBulkSmem = (size_t)kBulkWarps * kBulkRing * kBulkSlot +
                              sizeof(uint64_t) * kBulkWarps * kBulkRing + 64 + 1024;
 
 // Walks a contiguous range of statistics tasks (request, row, chunk; chunks
-// fastest) without divisions, skipping rows that are not read.
+// fastest) without divisions, skipping rows that are not read.  For a chain
+// the tasks are numbered over the rows that are read (each request's M
+// target rows, then its first M-1 draft rows), so that equal ranges are
+// equal work; for a tree over all 2M rows, with the unread ones skipped.
 struct StatCursor {
   int t, end;           // current flat task and end of the range
   int b, which, n, c;   // decoded position
@@ -203,8 +206,9 @@ struct StatCursor {
     M = M_;
     parent = par;
     c = t0 % nc;
-    const int row = (t0 / nc) % (2 * M);
-    b = t0 / (nc * 2 * M);
+    const int rows = par == nullptr ? 2 * M - 1 : 2 * M;  // rows numbered per request
+    const int row = (t0 / nc) % rows;
+    b = t0 / (nc * rows);
     which = row / M;
     n = row % M;
     skip();
@@ -219,9 +223,10 @@ struct StatCursor {
     }
   }
   __device__ void next_row() {
-    if (++n == M) {
+    if (++n == M || (parent == nullptr && which == 1 && n == M - 1)) {
       n = 0;
-      if (++which == 2) {
+      // a chain of one node reads no draft row
+      if (++which == 2 || (parent == nullptr && M == 1)) {
         which = 0;
         ++b;
       }
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   volatile int* abort = abort_flag;
   const int M = d.M, V = d.V;
   const int nw = gridDim.x * kBulkWarps;
-  const int ntask = d.B * 2 * M * n_chunks;
+  const int ntask = d.B * (parent == nullptr ? 2 * M - 1 : 2 * M) * n_chunks;
   const int gw = blockIdx.x * kBulkWarps + warp;
   const int per = (ntask + nw - 1) / nw;
   const int t0 = min(ntask, gw * per), t1 = min(ntask, t0 + per);

@@ -44,7 +44,8 @@ def test_workload_full_size(name):
 
 
 @pytest.mark.parametrize("B,gamma,V", [(1, 1, 8), (3, 2, 32), (3, 8, 1000),
-                                       (2, 5, 32007), (4, 3, 4097), (2, 8, 50)])
+                                       (2, 5, 32007), (4, 3, 4097), (2, 8, 50),
+                                       (3, 0, 4096)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_shapes(B, gamma, V, dtype):
     wl = workload("chain_7b").scaled(B=B, gamma=gamma, V=V, dtype=dtype, T=0.9)

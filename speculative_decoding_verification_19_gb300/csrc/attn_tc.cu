@@ -44,15 +44,18 @@
 //               cycles to issue, and one thread issuing both products of a
 //               tile was the kernel's bottleneck
 //   warps 0..7  softmax: one thread per query row (TMEM lane) and per half
-//               tile (32 keys); the two halves of a row swap their maxima
-//               through shared memory, exp2, P written as bf16 into TMEM;
-//               O is rescaled in TMEM only when the running maximum grows by
-//               more than 2^8; at the end of a pair, the output or partial
+//               tile (32 keys); each half reads the other half's scores too
+//               for the tile maximum, so the two never wait for each other;
+//               exp2, P written as bf16 into TMEM; O is rescaled in TMEM only
+//               when the running maximum grows by more than 2^8; at a pair's
+//               end, its output or partial
 //
-// TMEM: S0..S3 cols [0,64) .. [192,256), O [256,384).  Four S buffers let
-// Q K^T of tile t wait only for P V of tile t-4: the hand-off chain QK ->
-// softmax -> PV -> QK of a buffer is spread over four tiles in flight (the
-// K/V ring of four stages bounds the look-ahead to about three).
+// TMEM: S0..S3 cols [0,64) .. [192,256), O [256,384), P0..P3 (bf16 pairs of
+// S0..S3) [384,416) .. [480,512).  Four S buffers let Q K^T of tile t wait
+// only for P V of tile t-4: the hand-off chain QK -> softmax -> PV -> QK of a
+// buffer is spread over four tiles in flight (the K/V ring of four stages
+// bounds the look-ahead to about three).  P has columns of its own so that
+// no half ever writes over scores the other half is still reading.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -92,6 +95,7 @@ constexpr int kQBytes = 2 * kQHalfBytes;
 constexpr int kSBufs = 4;  // S buffers in TMEM
 constexpr int kTmemCols = 512;
 constexpr int kOCol = kSBufs * kTileKeys;
+constexpr int kPCol = kOCol + 128;  // P of S buffer k (bf16 pairs) at kPCol + 32 k
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
 // Split cost of one (request, head) segment, in tiles: the Q load, the
 // masks and the drain of the pipeline at a pair's end cost about this much.
@@ -108,10 +112,8 @@ struct __align__(8) Bars {
   uint64_t p_full[kSBufs];
   uint64_t o_done[kSBufs];  // completion of PV(t) lands on o_done[t % kSBufs]
   uint64_t drain[2];  // the Q K^T issuer's and the P V issuer's last completion
-  uint64_t xbar[4][2];       // per sub-partition, per tile parity: both halves' maxima
   uint64_t lbar[4];          // per sub-partition: both halves' row sums at a pair's output
   uint64_t ebar;             // every softmax warp wrote its rows of a partial
-  float xmax[2][2][128];     // [tile parity][half][row]
   float xl[2][128];          // [half][row] row sums at a pair's output
   uint32_t tmem_base;
   int abort;
@@ -235,10 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain[1]), 1);
-    for (int sp = 0; sp < 4; ++sp) {
-      for (int i = 0; i < 2; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[sp][i]), 2);
-      ptx::mbar_init(ptx::smem_u32(&bars->lbar[sp]), 2);
-    }
+    for (int sp = 0; sp < 4; ++sp) ptx::mbar_init(ptx::smem_u32(&bars->lbar[sp]), 2);
     ptx::mbar_init(ptx::smem_u32(&bars->ebar), 2 * n_sm_warps);
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -543,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           break;
         ptx::tc_fence_after();
         const uint64_t dv = dv0 + (uint64_t)((stage * kStageBytes) >> 4);
-        const uint32_t pcol = tmem + sbuf * kTileKeys;
+        const uint32_t pcol = tmem + kPCol + sbuf * 32;
 #pragma unroll
         for (int j = 0; j < kPages; ++j) {
           if (j < np)
@@ -598,7 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           }
         }
         const int sbuf = (int)(t % kSBufs);  // S / P buffer in TMEM
-        const int xb = (int)(t & 1);          // maxima exchange buffer
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]), (uint32_t)((t / kSBufs) & 1), abort,
                             kTimeoutNs))
           break;
@@ -609,11 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         const bool plain = kpos0 + kTileKeys <= ctx && nkeys == kTileKeys;
         const int jbase = half * 32;
         uint32_t vh = 0xffffffffu;  // visible keys of this half (non-plain tiles)
-        uint32_t sv[32];
+        uint32_t sv[32], so[32];
         ptx::tmem_ld32(lane_base + sbuf * kTileKeys + jbase, sv);
+        ptx::tmem_ld32(lane_base + sbuf * kTileKeys + (jbase ^ 32), so);
         ptx::tmem_wait_ld();
-        // maximum of this half (log2 units), then of the whole tile
-        float mh;
+        // maximum of the whole tile (log2 units): this half's columns and the
+        // other half's, read straight from TMEM, so that both halves reach
+        // the same maximum without waiting for each other (P goes to its own
+        // columns, never over S)
+        float mt;
         if (plain) {
           float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
@@ -623,26 +625,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             a2 = fmaxf(a2, __uint_as_float(sv[j + 2]));
             a3 = fmaxf(a3, __uint_as_float(sv[j + 3]));
           }
-          mh = real ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * qscale2 : -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            a0 = fmaxf(a0, __uint_as_float(so[j]));
+            a1 = fmaxf(a1, __uint_as_float(so[j + 1]));
+            a2 = fmaxf(a2, __uint_as_float(so[j + 2]));
+            a3 = fmaxf(a3, __uint_as_float(so[j + 3]));
+          }
+          mt = real ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * qscale2 : -INFINITY;
         } else {
-          // visibility of this half's 32 keys as a bitmask, then the same
-          // maximum as the plain path over the visible ones
-          vh = (uint32_t)(tile_visibility(kpos0, nkeys, ctx, L, anc, real) >> jbase);
+          // visibility of the tile's keys as a bitmask, then the same maximum
+          // as the plain path over the visible ones
+          const unsigned long long vis = tile_visibility(kpos0, nkeys, ctx, L, anc, real);
+          vh = (uint32_t)(vis >> jbase);
+          const uint32_t vo = (uint32_t)(vis >> (jbase ^ 32));
           float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             a0 = fmaxf(a0, (vh >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY);
             a1 = fmaxf(a1, (vh >> (j + 1)) & 1u ? __uint_as_float(sv[j + 1]) : -INFINITY);
           }
-          mh = fmaxf(a0, a1) * qscale2;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            a0 = fmaxf(a0, (vo >> j) & 1u ? __uint_as_float(so[j]) : -INFINITY);
+            a1 = fmaxf(a1, (vo >> (j + 1)) & 1u ? __uint_as_float(so[j + 1]) : -INFINITY);
+          }
+          mt = fmaxf(a0, a1) * qscale2;
         }
-        bars->xmax[xb][half][row] = mh;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xbar[sp][xb]));
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->xbar[sp][xb]), (uint32_t)((t >> 1) & 1), abort,
-                            kTimeoutNs))
-          break;
-        const float mt = fmaxf(bars->xmax[xb][0][row], bars->xmax[xb][1][row]);
         bool need = false;
         if (first) {
           m_used = mt;
@@ -672,9 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             m_used = mt;
           }
         }
-        // probabilities of this half, packed to bf16 pairs; keys
-        // 32*half.. land in P columns 16*half.. (S columns both halves have
-        // already read, by the exchange above)
+        // probabilities of this half, packed to bf16 pairs: keys 32*half..
+        // land in columns 16*half.. of the buffer's P columns
         uint32_t pk[16];
         float l0 = 0.f, l1 = 0.f;
         if (plain) {
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           }
         }
         l += l0 + l1;
-        ptx::tmem_st16(lane_base + sbuf * kTileKeys + half * 16, pk);
+        ptx::tmem_st16(lane_base + kPCol + sbuf * 32 + half * 16, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();

@@ -86,13 +86,15 @@ def test_all_accept_and_all_reject():
     assert np.all(g["out_tokens"][:, 0] != x1)
 
 
-def test_failed_requests():
-    wl = workload("chain_7b").scaled(B=5, V=300)
+@pytest.mark.parametrize("V", [300, 4096])
+def test_failed_requests(V):
+    # V = 300: rows not 16-byte aligned (four-kernel path); 4096: one kernel
+    wl = workload("chain_7b").scaled(B=5, V=V)
     lg = logits_inputs(wl, seed=6)
     lg["target"][1, 2, 7] = np.nan
     lg["draft"][2, 0, 3] = np.inf
     lg["temperature"][3] = 0.0
-    lg["tokens"][4, 2] = 300
+    lg["tokens"][4, 2] = V
     g, o, _ = _run(wl, lg, seed=2, offset=0)
     assert list(g["accepted_len"][1:]) == [-1, -1, -1, -1]
     assert g["accepted_len"][0] >= 0

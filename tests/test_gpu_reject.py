@@ -54,6 +54,19 @@ def test_ragged_shapes(B, gamma, V, dtype):
         _run(wl, lg, seed=99, offset=offset, b_base=5)
 
 
+@pytest.mark.parametrize("B,gamma,V,dtype", [
+    (2, 63, 1000, "bf16"),      # the longest chain: M = 64 rows
+    (2, 3, 1 << 20, "bf16"),    # the largest vocabulary: 512 statistics chunks per row
+    (2, 3, 1 << 19, "f32"),     # the same in fp32 (1024-logit chunks)
+])
+def test_maximum_sizes(B, gamma, V, dtype):
+    wl = workload("chain_7b").scaled(B=B, gamma=gamma, V=V, dtype=dtype)
+    lg = logits_inputs(wl, seed=gamma + V % 97)
+    for offset in range(2):
+        g, _, _ = _run(wl, lg, seed=41, offset=offset)
+        assert g["status"] == 0
+
+
 @pytest.mark.parametrize("V", [64, 32000])
 def test_trees(V):
     wl = workload("tree_64").scaled(B=6, V=V)

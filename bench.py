@@ -46,7 +46,7 @@ DEFAULT_WORKLOAD = "stress_gqa_152k"
 # algorithmic bytes (traffic grows with the KV bytes read):
 # profiles/attn_tc_kernel_stress_gqa_152k_b16.md.  Valid only for the
 # attention kernel sources whose digest is recorded with it.
-TRAFFIC = {"digest": "5bf30e21445a46d0", "bytes_per_call": 10104004126}
+TRAFFIC = {"digest": "125e7226bd61e1b3", "bytes_per_call": 10104052907}
 TRAFFIC_ALG_BYTES = 10051956736  # algorithmic bytes per call of that workload (seed 0)
 
 

@@ -905,7 +905,7 @@ __device__ __forceinline__ void block_scan(int64_t& a, int64_t& c, int& m, int64
 // kernel then neither reads nor appends it).  The CTA that arrives last
 // plans the split of the tiles.
 __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
-    const int32_t* __restrict__ block_table, const int32_t* ctx_lens,
+    const int32_t* block_table, const int32_t* ctx_lens,
     const int32_t* __restrict__ parent, spec_dims d, int G, int32_t* __restrict__ ntiles,
     int64_t* __restrict__ pre, int4* __restrict__ rq, int4* __restrict__ starts,
     int* __restrict__ pairs, unsigned long long* __restrict__ anc_ws,
@@ -923,18 +923,31 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int B = d.B, M = d.M, Hkv = d.Hkv, D = d.D;
-  const int ctx = ctx_lens[b];
+  const int32_t* bt = block_table + (int64_t)b * d.max_blocks;
+  // The table's first kPrepPages * kPrepThreads entries are loaded together
+  // with the context length (all in bounds of the table), so the check does
+  // not wait for the length before its loads.
+  constexpr int kPrepPages = 8;
+  int ids[kPrepPages];
+#pragma unroll
+  for (int k = 0; k < kPrepPages; ++k) {
+    const int p = tid + k * kPrepThreads;
+    ids[k] = p < d.max_blocks ? __ldcg(bt + p) : 0;
+  }
+  const int ctx = __ldcg(ctx_lens + b);
   const int64_t L = (int64_t)ctx + M;
   const int64_t cap = (int64_t)d.max_blocks * kBlock;
-  const int32_t* bt = block_table + (int64_t)b * d.max_blocks;
 
   const bool cap_ok = ctx >= 0 && L <= cap;
   int bad_block = 0;
   if (cap_ok) {
     const int pages = (int)ceil_div64(L, kBlock);
+#pragma unroll
+    for (int k = 0; k < kPrepPages; ++k)
+      if (tid + k * kPrepThreads < pages) bad_block |= (ids[k] < 0 || ids[k] >= d.num_blocks);
 #pragma unroll 4
-    for (int p = tid; p < pages; p += blockDim.x) {
-      const int id = bt[p];
+    for (int p = tid + kPrepPages * kPrepThreads; p < pages; p += kPrepThreads) {
+      const int id = __ldcg(bt + p);
       bad_block |= (id < 0 || id >= d.num_blocks);
     }
   }

@@ -18,8 +18,14 @@
  *     row-major in the stated shape.  The library never allocates, never
  *     frees and never synchronises (except spec_get_device_status).  All work
  *     is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
- *     legacy default stream).  Calls are re-entrant; the only state kept
- *     between calls is a per-thread count of launches (spec_last_launch_count).
+ *     legacy default stream).  Calls are re-entrant; the state kept between
+ *     calls is a per-thread count of launches (spec_last_launch_count),
+ *     cached driver entry points, and the scratch array of
+ *     spec_reject_sample_noalloc with its device address per CUDA context.
+ *   - Every device-side wait is bounded (spec_dims.wait_limit_kcycles); one
+ *     that gives up raises SPEC_ERR_TIMEOUT.  After that bit is seen, clear
+ *     the status word and zero the workspace again (spec_workspace_init)
+ *     before the next call: counters inside it may be left mid-way.
  *   - B requests, M query rows per request (row 0 = the pending root token
  *     whose K/V is not cached yet, rows 1.. = drafts or tree nodes), Hq query
  *     heads, Hkv KV heads (Hq % Hkv == 0), head size D, vocabulary V.
@@ -69,6 +75,16 @@ typedef enum spec_attn_impl {
   SPEC_ATTN_TENSOR_CORES = 2   /* tcgen05 + TMA: bf16, D = 128, group*M <= 128 */
 } spec_attn_impl;
 
+/* Reject-sample kernel selection (spec_dims.reject_impl). */
+typedef enum spec_reject_impl {
+  SPEC_REJECT_AUTO = 0,        /* the fused kernel when the shape allows, else the staged one */
+  SPEC_REJECT_STAGED = 1,      /* four kernels: logit statistics, decisions, residual
+                                  masses, residual draws; any vocabulary up to 2^20 */
+  SPEC_REJECT_FUSED = 2        /* one kernel on 4-CTA clusters: statistics, tests and draws
+                                  of every (request, node) as the logits stream in;
+                                  16-byte aligned rows, V <= 4 * 64 chunks of 2048 (bf16) */
+} spec_reject_impl;
+
 typedef struct spec_dims {
   int32_t B;            /* requests in the batch */
   int32_t M;            /* query rows per request: gamma+1, or tree nodes incl. root */
@@ -83,6 +99,13 @@ typedef struct spec_dims {
   int32_t logits_dtype; /* spec_dtype of target and draft logits */
   float softmax_scale;  /* attention score scale; 0 selects 1/sqrt(D) */
   int32_t attn_impl;    /* spec_attn_impl; 0 = automatic choice */
+  int32_t reject_impl;  /* spec_reject_impl; 0 = automatic choice */
+  int32_t wait_limit_kcycles; /* every bounded device wait gives up after this
+                                 many thousand SM clocks and raises
+                                 SPEC_ERR_TIMEOUT; 0 = the default, 4e6
+                                 (about 2 s at 2 GHz).  Work already issued
+                                 (copies, MMAs) is always waited for before a
+                                 CTA exits, whatever this limit. */
 } spec_dims;
 
 /* Bytes of caller-owned device workspace every call with these dims needs
@@ -175,7 +198,10 @@ spec_status spec_verify_attn(const void* q, const void* k_new,
  *                 was drawn from (1 for a bonus draw) and the probability of
  *                 the drawn token (cols 2, 3); -1 elsewhere.
  * A failed request (bad temperature, token, topology, or a needed row with
- * no distribution) gets accepted_len = -1 and -1 rows.
+ * no distribution) gets accepted_len = -1 and -1 rows.  If a wait gave up
+ * (SPEC_ERR_TIMEOUT in the status word, from this call or an earlier one not
+ * yet cleared), every request of the call gets accepted_len = -1: no
+ * decision is made on statistics that may be incomplete.
  */
 spec_status spec_reject_sample(const void* target_logits,
                                const void* draft_logits,
@@ -227,9 +253,11 @@ spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,
  *     B * ((32 * M + 8) * ceil(V / 2048) + 816) > 1 MiB)
  *     return SPEC_ERR_UNSUPPORTED and launch nothing; use
  *     spec_reject_sample there.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     in that context (cudaGetSymbolAddress, once per context, with the
+ *     context current) and keeps it; make that first call before any stream
+ *     capture.  A new context on the same device (after cudaDeviceReset, or
+ *     another context made current) gets its own lookup.
  *   - No memory is allocated or freed, by the library or any routine it
  *     calls.  The status word is cleared at the start of each call with an
  *     async memset on `stream`; device-side failures show as

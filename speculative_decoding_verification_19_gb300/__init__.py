@@ -14,6 +14,9 @@ from ._native import (  # noqa: F401
     ATTN_AUTO,
     ATTN_CUDA_CORES,
     ATTN_TENSOR_CORES,
+    REJECT_AUTO,
+    REJECT_FUSED,
+    REJECT_STAGED,
     EXPORTS,
     LIB_PATH,
     SPEC_BF16,

@@ -23,6 +23,7 @@ STATUS_NAMES = {
     6: "SPEC_ERR_DEVICE_BOUNDS", 7: "SPEC_ERR_TIMEOUT",
 }
 ATTN_AUTO, ATTN_CUDA_CORES, ATTN_TENSOR_CORES = 0, 1, 2
+REJECT_AUTO, REJECT_STAGED, REJECT_FUSED = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = (
@@ -45,7 +46,8 @@ class SpecDims(ctypes.Structure):
         ("max_blocks", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
         ("V", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
         ("logits_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
-        ("attn_impl", ctypes.c_int32),
+        ("attn_impl", ctypes.c_int32), ("reject_impl", ctypes.c_int32),
+        ("wait_limit_kcycles", ctypes.c_int32),
     ]
 
 
@@ -120,10 +122,12 @@ def dtype_code(dt: torch.dtype) -> int:
 
 def make_dims(B, M, Hq=1, Hkv=1, D=128, max_blocks=1, num_blocks=1, V=1,
               kv_dtype=torch.bfloat16, logits_dtype=torch.bfloat16,
-              softmax_scale=0.0, block=16, attn_impl=0) -> SpecDims:
+              softmax_scale=0.0, block=16, attn_impl=0, reject_impl=0,
+              wait_limit_kcycles=0) -> SpecDims:
     return SpecDims(B, M, Hq, Hkv, D, block, max_blocks, num_blocks, V,
                     dtype_code(kv_dtype), dtype_code(logits_dtype),
-                    float(softmax_scale), int(attn_impl))
+                    float(softmax_scale), int(attn_impl), int(reject_impl),
+                    int(wait_limit_kcycles))
 
 
 def workspace_size(dims: SpecDims) -> int:

@@ -65,13 +65,16 @@ WsLayout workspace_layout(const spec_dims& d) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static spec_status check_common(const spec_dims* d) {
+spec_status check_common(const spec_dims* d) {
   if (d == nullptr) return SPEC_ERR_INVALID_ARG;
   if (d->B < 1 || d->M < 1) return SPEC_ERR_INVALID_ARG;
   if (d->M > 64) return SPEC_ERR_UNSUPPORTED;
   if (d->block != kBlock) return SPEC_ERR_UNSUPPORTED;
   if ((d->kv_dtype != SPEC_BF16 && d->kv_dtype != SPEC_F32) ||
       (d->logits_dtype != SPEC_BF16 && d->logits_dtype != SPEC_F32))
+    return SPEC_ERR_INVALID_ARG;
+  if (d->wait_limit_kcycles < 0) return SPEC_ERR_INVALID_ARG;
+  if (d->reject_impl < SPEC_REJECT_AUTO || d->reject_impl > SPEC_REJECT_FUSED)
     return SPEC_ERR_INVALID_ARG;
   return SPEC_OK;
 }

@@ -96,7 +96,6 @@ constexpr int kSBufs = 4;  // S buffers in TMEM
 constexpr int kTmemCols = 512;
 constexpr int kOCol = kSBufs * kTileKeys;
 constexpr int kPCol = kOCol + 128;  // P of S buffer k (bf16 pairs) at kPCol + 32 k
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // SM clocks per wait (about 2 s)
 // Split cost of one (request, head) segment, in tiles: the Q load, the
 // masks and the drain of the pipeline at a pair's end cost about this much.
 constexpr int kSegCost = 3;
@@ -117,6 +116,7 @@ struct __align__(8) Bars {
   float xl[2][128];          // [half][row] row sums at a pair's output
   uint32_t tmem_base;
   int abort;
+  int tiles_issued[2];       // K/V tiles each copy warp issued (its loop may stop early)
 };
 
 constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kQBufs * kQBytes + sizeof(Bars) + 1024;
@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   const int R = group * M;
   const int c = blockIdx.x;
   const int n_sm_warps = ceil_div(R, 32);
+  const uint64_t wait = wait_limit_cycles(d);
   pdl_trigger();
 
   // Set-up that needs nothing from the previous kernels runs while they
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   // so that the fence before the count stalls no softmax warp.
   const int helper = n_sm_warps <= 2 ? kCopyWarpLargeR : (n_sm_warps == 3 ? 3 : -1);
   if (warp == helper && lane == 0 && st0.w > 0) {
-    if (ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, kTimeoutNs)) {
+    if (ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
       __threadfence();
       atomicAdd(pairs + (int64_t)st0.y * Hkv + st0.z, (int)min((int64_t)(st1.y - st0.w), g1 - g0));
     }
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     int wb = -1, ww = -1, nb = -1, nw = -1;  // window held in ids and window loaded into nids
     int ids[kPages] = {0, 0, 0, 0}, nids[kPages] = {0, 0, 0, 0};
     int64_t t = 0;
+    int q_issued = 0;  // Q loads issued (warp 10, lane 0)
     bool ok = true;
     for (int64_t g = g0; g < g1 && ok; ++g, ++t) {
       const bool first = (g == g0) || cu.tile == 0;
@@ -348,13 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           if (lane == 0) {
             const int qb = seg % kQBufs;
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
-                                kTimeoutNs);
+                                wait);
             if (ok) {
               const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
               ptx::mbar_arrive_expect_tx(qf, 2u * R * 128u);
               for (int half = 0; half < 2; ++half)
                 ptx::tma_load_4d(ptx::smem_u32(qbufs + qb * kQBytes + half * kQBytes / 2), &tm_q,
                                  qf, half * 64, cu.h * group, 0, cu.b);
+              ++q_issued;
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       for (int p = 0; p < kPages; ++p) blk[p] = __shfl_sync(0xffffffffu, ids[p], src);
       const int stage = (int)(t % kStages);
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
-                          abort, kTimeoutNs);
+                          abort, wait);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -452,18 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       ptx::cp_async_arrive_noinc(ptx::smem_u32(&bars->full[stage]));
       cu.next(rq, B, Hkv);
     }
-    if (warp == kProducerWarp && lane == 0) {
-      // every load issued must have landed before the CTA may exit
-      const int64_t issued = t;  // a broken loop did not issue tile t
-      for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
-        ptx::mbar_wait(ptx::smem_u32(&bars->full[u % kStages]), (uint32_t)((u / kStages) & 1),
-                       abort, kTimeoutNs);
-      for (int sg = seg >= kQBufs ? seg - kQBufs + 1 : 0; sg <= seg; ++sg)
-        ptx::mbar_wait(ptx::smem_u32(&bars->q_full[sg % kQBufs]), (uint32_t)((sg / kQBufs) & 1),
-                       abort, kTimeoutNs);
-    }
-    // the copies of a thread that stopped early land before the CTA exits
+    // Every copy issued lands before the CTA may exit, also when a wait gave
+    // up and the two copy warps stopped at different tiles: each thread's
+    // own cp.async copies (wait_all), then the full barriers of the tiles
+    // both warps issued (their arrivals follow the copies), then the Q loads
+    // actually issued.  A barrier that only one warp arrived on is never
+    // waited for.
     asm volatile("cp.async.wait_all;" ::: "memory");
+    if (lane == 0) bars->tiles_issued[warp == kProducerWarp ? 1 : 0] = (int)t;
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // the two copy warps only
+    if (warp == kProducerWarp && lane == 0) {
+      const int64_t both = min(bars->tiles_issued[0], bars->tiles_issued[1]);
+      for (int64_t u = both > kStages ? both - kStages : 0; u < both; ++u)
+        ptx::mbar_drain(ptx::smem_u32(&bars->full[u % kStages]), (uint32_t)((u / kStages) & 1),
+                        kDefaultWaitCycles);
+      for (int sg = q_issued > kQBufs ? q_issued - kQBufs : 0; sg < q_issued; ++sg)
+        ptx::mbar_drain(ptx::smem_u32(&bars->q_full[sg % kQBufs]), (uint32_t)((sg / kQBufs) & 1),
+                        kDefaultWaitCycles);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA: Q K^T
     if (lane == 0) {
@@ -487,16 +496,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
         const int qb = seg % kQBufs;
         if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]),
-                                     (uint32_t)((seg / kQBufs) & 1), abort, kTimeoutNs))
+                                     (uint32_t)((seg / kQBufs) & 1), abort, wait))
           break;
         const int stage = (int)(t % kStages);
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
-                            abort, kTimeoutNs))
+                            abort, wait))
           break;
         // PV(t - kSBufs) read P out of the S buffer this tile's QK writes
         if (t >= kSBufs && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t % kSBufs]),
                                            (uint32_t)(((t - kSBufs) / kSBufs) & 1), abort,
-                                           kTimeoutNs))
+                                           wait))
           break;
         ptx::tc_fence_after();
         const int np = tile_pages(L, cu.tile);
@@ -517,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       }
       // all MMAs issued by this thread complete before TMEM is released
       ptx::mma_commit(ptx::smem_u32(&bars->drain[0]));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain[0]), 0, abort, kTimeoutNs);
+      ptx::mbar_drain(ptx::smem_u32(&bars->drain[0]), 0, kDefaultWaitCycles);
     }
   } else if (warp == kPvWarp) {
     // ---------------------------------------------------------------- MMA: P V
@@ -538,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         const int sbuf = (int)(u % kSBufs);
         const int stage = (int)(u % kStages);
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u / kSBufs) & 1), abort,
-                            kTimeoutNs))
+                            wait))
           break;
         ptx::tc_fence_after();
         const uint64_t dv = dv0 + (uint64_t)((stage * kStageBytes) >> 4);
@@ -554,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         cu.next(rq, B, Hkv);
       }
       ptx::mma_commit(ptx::smem_u32(&bars->drain[1]));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain[1]), 0, abort, kTimeoutNs);
+      ptx::mbar_drain(ptx::smem_u32(&bars->drain[1]), 0, kDefaultWaitCycles);
     }
   } else if (warp < kSoftmaxWarps) {
     // -------------------------------------------------------------- softmax
@@ -597,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           }
         }
         const int sbuf = (int)(t % kSBufs);  // S / P buffer in TMEM
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]), (uint32_t)((t / kSBufs) & 1), abort,
-                            kTimeoutNs))
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]),
+                                                     (uint32_t)((t / kSBufs) & 1), abort, wait)))
           break;
         ptx::tc_fence_after();
         const int kpos0 = cu.tile * kTileKeys;
@@ -660,8 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         }
         if (__any_sync(0xffffffffu, need)) {
           // O is rescaled in place (this half's 64 columns): PV(t-1) must have landed
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) % kSBufs]),
-                              (uint32_t)(((t - 1) / kSBufs) & 1), abort, kTimeoutNs))
+          if (!__all_sync(0xffffffffu,
+                          ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) % kSBufs]),
+                                         (uint32_t)(((t - 1) / kSBufs) & 1), abort, wait)))
             break;
           ptx::tc_fence_after();
           const float f = need ? exp2f(m_used - mt) : 1.f;
@@ -717,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sbuf]));
         if (last) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->o_done[sbuf]), (uint32_t)((t / kSBufs) & 1),
-                              abort, kTimeoutNs))
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->o_done[sbuf]),
+                                                       (uint32_t)((t / kSBufs) & 1), abort, wait)))
             break;
           ptx::tc_fence_after();
           const int64_t pair = (int64_t)cu.b * Hkv + cu.h;
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ebar));
             if (helper < 0 && warp == 0 && lane == 0 &&
-                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, kTimeoutNs)) {
+                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
               // every row of the partial is written (the barrier above); the
               // fence makes them visible GPU-wide before the tiles are counted
               __threadfence();
@@ -768,8 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             bars->xl[half][row] = l;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->lbar[sp]));
-            if (!ptx::mbar_wait(ptx::smem_u32(&bars->lbar[sp]), (uint32_t)(n_whole & 1), abort,
-                                kTimeoutNs))
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->lbar[sp]),
+                                                         (uint32_t)(n_whole & 1), abort, wait)))
               break;
             ++n_whole;
             float ls = bars->xl[0][row] + bars->xl[1][row];
@@ -777,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             const int rest = cu.nt - own;  // tiles run by the CTAs after this one
             bool okc = true;
             if (rest > 0) {
-              if (lane == 0) okc = ptx::wait_count_geq(pairs + pair, rest, abort, kTimeoutNs);
+              if (lane == 0) okc = ptx::wait_count_geq(pairs + pair, rest, abort, wait);
               __syncwarp();
               okc = __shfl_sync(0xffffffffu, okc, 0);
             }

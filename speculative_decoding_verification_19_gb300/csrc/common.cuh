@@ -59,6 +59,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ void raise_status(uint32_t* status, int code) {
   atomicOr(status, 1u << code);
 }
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
 
 // ---------------------------------------------------------------------------
 // warp reductions
@@ -112,6 +115,20 @@ struct PdlLaunch {  // use in place: cfg points at attr
   PdlLaunch& operator=(const PdlLaunch&) = delete;
 };
 
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+// Every spin-wait of the kernels gives up after a limit of SM clocks and
+// raises SPEC_ERR_TIMEOUT.  The caller may lower the limit
+// (spec_dims.wait_limit_kcycles, in thousands of clocks); waits for work a
+// CTA has already issued (copies into its shared memory, MMAs into its
+// tensor memory) keep the default limit whatever the caller asks, because
+// the CTA must not exit before that work lands.
+constexpr uint64_t kDefaultWaitCycles = 4000000000ull;  // about 2 s at 2 GHz
+__host__ __device__ __forceinline__ uint64_t wait_limit_cycles(const spec_dims& d) {
+  return d.wait_limit_kcycles > 0 ? (uint64_t)d.wait_limit_kcycles * 1000ull : kDefaultWaitCycles;
+}
+
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -144,5 +161,9 @@ struct WsLayout {
 };
 
 WsLayout workspace_layout(const spec_dims& d);
+
+// Checks of the dims every entry point shares (counts, M, block size,
+// dtypes, the wait limit and the kernel selectors).
+spec_status check_common(const spec_dims* d);
 
 }  // namespace specv

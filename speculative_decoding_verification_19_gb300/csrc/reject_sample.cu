@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
 constexpr int kBulkWarps = 16;
 constexpr int kBulkRing = 3;
 constexpr int kBulkSlot = kWarp * kStatVecs * 16;  // bytes per task
-constexpr uint64_t kBulkTimeout = 4000000000ull;   // SM clocks per wait
 constexpr size_t kBulkSmem = (size_t)kBulkWarps * kBulkRing * kBulkSlot +
                              sizeof(uint64_t) * kBulkWarps * kBulkRing + 64 + 1024;
 
@@ -264,6 +263,7 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   }
   __syncthreads();
   volatile int* abort = abort_flag;
+  const uint64_t wait = wait_limit_cycles(d);
   const int M = d.M, V = d.V;
   const int nw = gridDim.x * kBulkWarps;
   const int ntask = d.B * (parent == nullptr ? 2 * M - 1 : 2 * M) * n_chunks;
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   while (cp.valid()) {
     const int slot = done % kBulkRing;
     if (!ptx::mbar_wait(ptx::smem_u32(&mybars[slot]), (uint32_t)((done / kBulkRing) & 1), abort,
-                        kBulkTimeout)) {
+                        wait)) {
       ok = false;
       break;
     }
@@ -338,11 +338,13 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     }
     cp.next();
   }
-  // copies issued but not consumed (only after a time-out) land before exit
+  // Copies issued but not consumed (only after a wait gave up) land before
+  // the CTA exits: these waits ignore the abort flag and keep the default
+  // limit, since the copies complete on their own.
   if (lane == 0)
     for (int u = done; u < issued; ++u)
-      ptx::mbar_wait(ptx::smem_u32(&mybars[u % kBulkRing]), (uint32_t)((u / kBulkRing) & 1), abort,
-                     kBulkTimeout);
+      ptx::mbar_drain(ptx::smem_u32(&mybars[u % kBulkRing]), (uint32_t)((u / kBulkRing) & 1),
+                      kDefaultWaitCycles);
   if (!ok && lane == 0) raise_status(status, SPEC_ERR_TIMEOUT);
 }
 
@@ -714,8 +716,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* stats, DrawState* __restrict__ draws,
-    uint32_t* __restrict__ status) {
+    int chunk, const RowStat* stats, DrawState* __restrict__ draws, uint32_t* status) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kSweep = kDecThreads * EPV;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -738,6 +739,9 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
 
   pdl_trigger();
   pdl_wait();  // the statistics come from the previous kernel
+  // A wait of the statistics kernel that gave up left some statistics
+  // unwritten: then no request of the call is decided on them.
+  const bool stats_lost = (ld_volatile_u32(status) >> SPEC_ERR_TIMEOUT) & 1u;
 
   // defined outputs first
   for (int i = tid; i < M; i += kDecThreads) {
@@ -763,6 +767,13 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   }
   bad_arg = __syncthreads_or(bad_arg);
   bad_tok = __syncthreads_or(bad_tok);
+  if (stats_lost) {
+    if (tid == 0) {
+      accepted_len[b] = -1;
+      draws[b].pending = 0;
+    }
+    return;
+  }
   if (tid == 0 && !bad_arg) {
     for (int n = 0; n < M; ++n) first_child[n] = -1;
     for (int n = M - 1; n >= 1; --n) {  // ascending sibling lists
@@ -1285,6 +1296,7 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
 }
 
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
+  if (a.d.reject_impl == SPEC_REJECT_FUSED) return cudaErrorNotSupported;
   const int esz = a.d.logits_dtype == SPEC_BF16 ? 2 : 4;
   const bool aligned = ((size_t)a.d.V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 &&

@@ -9,9 +9,11 @@
 // word) in a fixed-size array in the library's own device memory instead of
 // a caller-provided workspace, and runs the same kernels as
 // spec_reject_sample.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <string.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "reject_sample.cuh"
@@ -25,21 +27,76 @@ constexpr size_t kNoAllocScratchBytes = (size_t)1 << 20;  // 1 MiB
 constexpr size_t kNoAllocStatusBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 256;
-static std::atomic<void*> g_noalloc_ptr[kMaxDevices];
+// Device address of the scratch array in the current CUDA context.  The
+// host-side symbol is not a device address, and the array's address belongs
+// to the context that loaded the module: after cudaDeviceReset, or under
+// another context on the same device, the module is loaded again elsewhere.
+// So the address is cached per context, keyed by the context's unique id,
+// and looked up (cudaGetSymbolAddress) the first time a context is seen.
+struct CtxAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+constexpr int kMaxContexts = 64;
+static std::mutex g_noalloc_mu;
+static CtxAddr g_noalloc_cache[kMaxContexts];
+static int g_noalloc_n = 0;
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is not a device address).
-static spec_status noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
-  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return SPEC_ERR_CUDA;
-    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+static PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
   }
+  return fn;
+}
+static PFN_cuCtxGetId_v12000 ctx_id_fn() {
+  static PFN_cuCtxGetId_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  }
+  return fn;
+}
+
+static spec_status noalloc_scratch(void** out) {
+  auto get_ctx = ctx_current_fn();
+  auto get_id = ctx_id_fn();
+  if (get_ctx == nullptr || get_id == nullptr) return SPEC_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return SPEC_ERR_CUDA;
+  if (ctx == nullptr) {
+    // no context is current yet: the runtime makes the device's primary
+    // context current on its first call that needs one, such as this lookup
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SPEC_ERR_CUDA;
+  }
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (int i = 0; i < g_noalloc_n; ++i)
+    if (g_noalloc_cache[i].ctx_id == id) {
+      *out = g_noalloc_cache[i].ptr;
+      return SPEC_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return SPEC_ERR_CUDA;
+  // a full table forgets its oldest entry (a context id is never reused)
+  if (g_noalloc_n == kMaxContexts) {
+    memmove(g_noalloc_cache, g_noalloc_cache + 1, sizeof(CtxAddr) * (kMaxContexts - 1));
+    --g_noalloc_n;
+  }
+  g_noalloc_cache[g_noalloc_n++] = CtxAddr{id, p};
   *out = p;
   return SPEC_OK;
 }
@@ -53,9 +110,11 @@ extern "C" spec_status spec_reject_sample_noalloc(
     const int32_t* parent, const float* temperature, uint64_t seed, uint64_t offset,
     uint64_t b_base, int32_t* out_tokens, int32_t* path, int32_t* accepted_len, float* probe,
     const spec_dims* dims, void* stream) {
-  if (dims == nullptr || dims->B < 1 || dims->M < 1 || dims->V < 1) return SPEC_ERR_INVALID_ARG;
-  if (dims->M > 64 || dims->V > rs_max_vocab(dims->logits_dtype)) return SPEC_ERR_UNSUPPORTED;
-  if (dims->logits_dtype != SPEC_BF16 && dims->logits_dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  // the same dims checks as spec_reject_sample
+  const spec_status chk = check_common(dims);
+  if (chk != SPEC_OK) return chk;
+  if (dims->V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dims->V > rs_max_vocab(dims->logits_dtype)) return SPEC_ERR_UNSUPPORTED;
   if (!target_logits || !draft_logits || !tokens || !temperature || !out_tokens || !path ||
       !accepted_len)
     return SPEC_ERR_INVALID_ARG;

@@ -41,17 +41,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Polls between two reads of the clock: 1024 for the default limits (a wait
+// that is satisfied quickly costs nothing but the polls), 16 for limits
+// below 2^20 clocks, so that a short limit is honoured.
+__device__ __forceinline__ uint32_t poll_mask(uint64_t timeout_cycles) {
+  return timeout_cycles < (1ull << 20) ? 15u : 1023u;
+}
+
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when
 // *abort is set by another role or after about `timeout_cycles` SM clocks,
 // setting *abort itself in the second case, so no wait can hang the GPU.
-// The clock is read only once a wait has polled 1024 times: a wait that is
-// satisfied quickly costs nothing but the polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_cycles) {
   long long t0 = 0;
+  const uint32_t mask = poll_mask(timeout_cycles);
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 1023u) {
+    if ((it & mask) == mask) {
       if (*abort) return false;
       const long long now = clock64();
       if (t0 == 0) {
@@ -64,17 +70,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for work this CTA already issued (bulk copies, MMAs) to complete
+// before it exits or frees what that work writes: the same polling as
+// mbar_wait, but the CTA's abort flag does not cut it short -- the work lands
+// on its own -- only its own limit does.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t timeout_cycles) {
+  int never = 0;
+  return mbar_wait(bar, parity, &never, timeout_cycles);
+}
+
 // Wait until the int at p (written by other CTAs, GPU scope) reaches
 // target, with the same give-up rules as mbar_wait.  The load is an acquire:
 // what the writers published before their count is visible afterwards.
 __device__ __forceinline__ bool wait_count_geq(const int* p, int target, volatile int* abort,
                                                uint64_t timeout_cycles) {
   long long t0 = 0;
+  const uint32_t mask = timeout_cycles < (1ull << 20) ? 3u : 63u;
   for (uint32_t it = 0;; ++it) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     if (v >= target) return true;
-    if ((it & 63u) == 63u) {
+    if ((it & mask) == mask) {
       if (*abort) return false;
       const long long now = clock64();
       if (t0 == 0) {

@@ -12,14 +12,17 @@ What is pinned, and against what (none of it re-types the oracle):
   children per node (page 1 §2.3 / §4.1, page 2 §2.2: the output law equals
   the target's).
 * Monte Carlo with the real Philox uniforms: chi-square of the first emitted
-  token against p; first-position acceptance rate against
+  token against p over 10^6 requests; first-position acceptance rate against
   alpha = sum min(p, q); mean emitted count against (1 - a^(g+1)) / (1 - a)
   (page 2 §2.3), including the pages' worked value a = 0.5, g = 4 -> 1.9375.
 * edge cases the pages ask to test first (page 2 §3.3): all accepted (draft
   equals target) and all rejected (target gives the first draft zero mass).
 * temperature softmax closed form for two tokens; non-finite rows.
 """
+import concurrent.futures
 import itertools
+import multiprocessing
+import os
 
 import numpy as np
 import pytest
@@ -262,7 +265,7 @@ def test_exact_law_detects_wrong_bonus():
 # Monte Carlo with the real uniforms
 # ---------------------------------------------------------------------------
 
-def _iid_batch(B, gamma, V, seed, same=False):
+def _iid_batch(B, gamma, V, seed, same=False, token_seed=None):
     rng = np.random.default_rng(seed)
     z = rng.normal(0, 1.5, V)
     d = z if same else z + rng.normal(0, 1.0, V)
@@ -270,18 +273,35 @@ def _iid_batch(B, gamma, V, seed, same=False):
     target = np.broadcast_to(z, (B, M, V)).copy()
     draft = np.broadcast_to(d, (B, M, V)).copy()
     q = softmax_rows(d[None], 1.0)[0]
+    if token_seed is not None:
+        rng = np.random.default_rng([seed, token_seed])
     tokens = rng.choice(V, size=(B, M), p=q).astype(np.int32)
     return target, draft, tokens, np.ones(B, dtype=np.float32)
 
 
-def test_mc_first_token_chi_square():
-    B, gamma, V = 100_000, 3, 8
-    target, draft, tokens, T = _iid_batch(B, gamma, V, seed=1)
+def _first_token_counts(shard):
+    """Counts of the first emitted token over one shard of the 10^6 trials
+    (its own requests, numbered from b_base, so its uniforms are its own)."""
+    b_base, B, gamma, V = shard
+    target, draft, tokens, T = _iid_batch(B, gamma, V, seed=1, token_seed=b_base)
     res = oracle_reject_sample(target, draft, tokens, None, T, seed=77,
-                               offset=0)
+                               offset=0, b_base=b_base)
+    return np.bincount(res["out_tokens"][:, 0], minlength=V)
+
+
+def test_mc_first_token_chi_square():
+    """10^6 independent requests through the oracle (in parallel processes,
+    each a shard of requests): the first emitted token follows p."""
+    B, gamma, V = 1_000_000, 3, 8
+    workers = max(1, min(8, os.cpu_count() or 1))
+    per = -(-B // (4 * workers))
+    shards = [(s, min(per, B - s), gamma, V) for s in range(0, B, per)]
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(workers, mp_context=ctx) as ex:
+        counts = sum(ex.map(_first_token_counts, shards))
+    assert counts.sum() == B
+    target, _, _, _ = _iid_batch(1, gamma, V, seed=1)
     p = softmax_rows(target[0, :1], 1.0)[0]
-    first = res["out_tokens"][:, 0]
-    counts = np.bincount(first, minlength=V)
     chi = stats.chisquare(counts, p * B)
     assert chi.pvalue > 1e-3
 

@@ -69,7 +69,8 @@ def test_same_inputs_twice():
 
 
 def test_refuses_sizes_beyond_its_scratch():
-    # 512 requests x 10 rows x 19 chunks of 8192 logits need more than 1 MiB
+    # 512 requests x 10 rows x 75 chunks of 2048 logits, 16 bytes of
+    # statistics each, need far more than 1 MiB
     dims = sv.make_dims(B=512, M=5, V=152064)
     t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     i = torch.zeros(16, dtype=torch.int32, device="cuda")

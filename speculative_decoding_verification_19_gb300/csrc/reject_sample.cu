@@ -302,8 +302,8 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   float cs = 1.0f;
   while (cp.valid()) {
     const int slot = done % kBulkRing;
-    if (!ptx::mbar_wait(ptx::smem_u32(&mybars[slot]), (uint32_t)((done / kBulkRing) & 1), abort,
-                        wait)) {
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&mybars[slot]),
+                                                 (uint32_t)((done / kBulkRing) & 1), abort, wait))) {
       ok = false;
       break;
     }

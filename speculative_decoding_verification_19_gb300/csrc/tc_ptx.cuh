@@ -41,11 +41,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Polls between two reads of the clock: 1024 for the default limits (a wait
-// that is satisfied quickly costs nothing but the polls), 16 for limits
-// below 2^20 clocks, so that a short limit is honoured.
+// Non-blocking probe of the phase (no hardware suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this many clocks are short: their waits poll without the
+// hardware suspension of try_wait and read the clock every 16 polls, so the
+// limit is honoured; longer limits read it every 1024 polls (a wait that is
+// satisfied quickly then costs nothing but the polls).
+constexpr uint64_t kShortWait = 1ull << 20;
 __device__ __forceinline__ uint32_t poll_mask(uint64_t timeout_cycles) {
-  return timeout_cycles < (1ull << 20) ? 15u : 1023u;
+  return timeout_cycles < kShortWait ? 15u : 1023u;
 }
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when
@@ -55,8 +70,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           uint64_t timeout_cycles) {
   long long t0 = 0;
   const uint32_t mask = poll_mask(timeout_cycles);
+  const bool short_wait = timeout_cycles < kShortWait;
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (short_wait ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & mask) == mask) {
       if (*abort) return false;
       const long long now = clock64();

@@ -59,6 +59,9 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_off = take(L.rs_bytes);
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
+  L.rsf_ctl_off = take(16);
+  L.rsf_req_off = take(sizeof(uint32_t) * (size_t)d.B);
+  L.rsf_rec_off = take(32 * (size_t)d.B * d.M);
   L.total = off;
   return L;
 }
@@ -223,6 +226,7 @@ spec_status spec_reject_sample(const void* target_logits, const void* draft_logi
   int launches = 0;
   const cudaError_t e = rs_launch(a, lay, static_cast<cudaStream_t>(stream), &launches);
   g_launches = launches;
+  if (e == cudaErrorNotSupported) return SPEC_ERR_UNSUPPORTED;
   return from_cuda(e);
 }
 

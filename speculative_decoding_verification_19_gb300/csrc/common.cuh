@@ -157,6 +157,9 @@ struct WsLayout {
   size_t rs_zsum_off;     // [B, n_chunks] f64: residual mass of each statistics chunk
   int rs_chunk;           // logits per statistics chunk
   int rs_chunks;          // statistics chunks per row
+  size_t rsf_ctl_off;     // fused reject kernel: item counter, CTAs done, epoch tag (u32 x 4)
+  size_t rsf_req_off;     // [B] u32 items finished per request
+  size_t rsf_rec_off;     // [B, M] 32-byte record per (request, node)
   size_t total;
 };
 

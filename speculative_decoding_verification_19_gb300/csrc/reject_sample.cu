@@ -1296,11 +1296,17 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
 }
 
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
-  if (a.d.reject_impl == SPEC_REJECT_FUSED) return cudaErrorNotSupported;
   const int esz = a.d.logits_dtype == SPEC_BF16 ? 2 : 4;
   const bool aligned = ((size_t)a.d.V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0;
+  const bool fused_ok = rsf_supported(a.d, aligned);
+  if (a.d.reject_impl == SPEC_REJECT_FUSED) {
+    if (!fused_ok) return cudaErrorNotSupported;
+    return rsf_launch(a, lay, st, launches);
+  }
+  if (a.d.reject_impl == SPEC_REJECT_AUTO && rsf_preferred(a.d, aligned))
+    return rsf_launch(a, lay, st, launches);
   if (a.d.logits_dtype == SPEC_BF16)
     return aligned ? launch_rs_t<__nv_bfloat16, true>(a, lay, st, launches)
                    : launch_rs_t<__nv_bfloat16, false>(a, lay, st, launches);

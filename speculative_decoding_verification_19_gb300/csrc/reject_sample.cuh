@@ -51,6 +51,14 @@ struct RsArgs {
 
 int rs_chunk_elems(int logits_dtype);       // statistics chunk (one warp task)
 int rs_max_vocab(int logits_dtype);
+// rs_launch picks the kernels (spec_dims.reject_impl): the fused one-kernel
+// path (reject_fused.cu) when the shape allows it, else the staged four.
+// Returns cudaErrorNotSupported when the fused path is asked for and the
+// shape does not allow it.
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
+int rsf_max_vocab(int logits_dtype);
+bool rsf_supported(const spec_dims& d, bool aligned);
+bool rsf_preferred(const spec_dims& d, bool aligned);
+cudaError_t rsf_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
 
 }  // namespace specv

@@ -118,26 +118,56 @@ extern "C" spec_status spec_reject_sample_noalloc(
   if (!target_logits || !draft_logits || !tokens || !temperature || !out_tokens || !path ||
       !accepted_len)
     return SPEC_ERR_INVALID_ARG;
-  // the statistics of every (request, row, chunk) must fit the fixed scratch
+  // The call runs the kernels spec_reject_sample would run on these inputs:
+  // the fused kernel when the shape allows it, else the staged ones.  Each
+  // has its own scratch layout, which must fit the fixed array.
+  const int esz = dims->logits_dtype == SPEC_BF16 ? 2 : 4;
+  const bool aligned = ((size_t)dims->V * esz) % 16 == 0 &&
+                       (reinterpret_cast<uintptr_t>(target_logits) % 16) == 0 &&
+                       (reinterpret_cast<uintptr_t>(draft_logits) % 16) == 0;
+  const bool fused = dims->reject_impl == SPEC_REJECT_FUSED ? rsf_supported(*dims, aligned)
+                     : dims->reject_impl == SPEC_REJECT_AUTO  ? rsf_preferred(*dims, aligned)
+                                                              : false;
+  if (dims->reject_impl == SPEC_REJECT_FUSED && !fused) return SPEC_ERR_UNSUPPORTED;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   WsLayout lay;
   memset(&lay, 0, sizeof(lay));
   lay.status_off = 0;
-  lay.rs_off = kNoAllocStatusBytes;
   lay.rs_chunk = rs_chunk_elems(dims->logits_dtype);
   lay.rs_chunks = (int)ceil_div64(dims->V, lay.rs_chunk);
-  lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
-  lay.rs_draw_off = (lay.rs_off + lay.rs_bytes + 255) / 256 * 256;
-  lay.rs_zsum_off = (lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B + 255) / 256 * 256;
-  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
+  if (fused) {
+    // status, then the fused kernel's counters (item counter, CTAs done,
+    // epoch tag), items finished per request, one record per (request, node)
+    lay.rsf_ctl_off = kNoAllocStatusBytes;
+    lay.rsf_req_off = up(lay.rsf_ctl_off + 16);
+    lay.rsf_rec_off = up(lay.rsf_req_off + sizeof(uint32_t) * (size_t)dims->B);
+    lay.total = lay.rsf_rec_off + 32 * (size_t)dims->B * dims->M;
+  } else {
+    // status, then the chunk statistics, the draw states and the residual
+    // chunk masses
+    lay.rs_off = kNoAllocStatusBytes;
+    lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
+    lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
+    lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
+    lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
+  }
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;
   const spec_status s = noalloc_scratch(&scratch);
   if (s != SPEC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word starts each call at zero; the rest needs no clearing
-  // (every entry read is written earlier in the same call)
-  if (cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  // The status word and the counters start each call at zero, whatever an
+  // earlier call (one whose wait gave up, say) left there: the status area,
+  // the fused kernel's item counter and CTA count (not its epoch tag, which
+  // tells its records of one call from the last's), and its per-request
+  // counts.  Everything else read is written earlier in the same call.
+  char* sb = static_cast<char*>(scratch);
+  if (cudaMemsetAsync(sb, 0, fused ? lay.rsf_ctl_off + 8 : kNoAllocStatusBytes, st) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (fused && cudaMemsetAsync(sb + lay.rsf_req_off, 0, sizeof(uint32_t) * (size_t)dims->B, st) !=
+                   cudaSuccess)
+    return SPEC_ERR_CUDA;
 
   RsArgs a;
   a.target = target_logits;
@@ -153,6 +183,7 @@ extern "C" spec_status spec_reject_sample_noalloc(
   a.accepted_len = accepted_len;
   a.probe = probe;
   a.d = *dims;
+  a.d.reject_impl = fused ? SPEC_REJECT_FUSED : SPEC_REJECT_STAGED;
   a.ws = scratch;
   int launches = 0;
   return rs_launch(a, lay, st, &launches) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -15,13 +15,20 @@ from scipy import stats
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
 
-from harness import compare_reject, gpu_reject  # noqa: E402
+import speculative_decoding_verification_19_gb300 as sv  # noqa: E402
+from harness import compare_reject, dims_for, gpu_reject  # noqa: E402
 from oracle import oracle_reject_sample, softmax_rows  # noqa: E402
 from synth import logits_inputs, workload  # noqa: E402
 
 
-def _run(wl, lg, seed, offset, b_base=0):
-    g = gpu_reject(wl, lg, seed, offset, b_base=b_base)
+IMPLS = [sv.REJECT_FUSED, sv.REJECT_STAGED]
+
+
+def _run(wl, lg, seed, offset, b_base=0, impl=sv.REJECT_AUTO):
+    B, M, V = lg["target"].shape
+    dims = dims_for(wl, B, V=V)
+    dims.reject_impl = impl
+    g = gpu_reject(wl, lg, seed, offset, b_base=b_base, dims=dims)
     o = oracle_reject_sample(lg["target"], lg["draft"], lg["tokens"],
                              lg["parent"], lg["temperature"], seed, offset,
                              b_base=b_base)
@@ -29,14 +36,15 @@ def _run(wl, lg, seed, offset, b_base=0):
     return g, o, near
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("name", ["tiny_chain", "chain_7b", "chain_gqa_128k",
                                   "tree_64", "stress_gqa_152k"])
-def test_workload_full_size(name):
+def test_workload_full_size(name, impl):
     wl = workload(name)
     lg = logits_inputs(wl, seed=0)
     total_near = 0
     for offset in (0, 1, 2):
-        g, o, near = _run(wl, lg, seed=1234, offset=offset)
+        g, o, near = _run(wl, lg, seed=1234, offset=offset, impl=impl)
         total_near += near
         assert g["status"] == 0
     # near-threshold exclusions must stay rare
@@ -47,11 +55,15 @@ def test_workload_full_size(name):
                                        (2, 5, 32007), (4, 3, 4097), (2, 8, 50),
                                        (3, 0, 4096)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_ragged_shapes(B, gamma, V, dtype):
+@pytest.mark.parametrize("impl", [sv.REJECT_AUTO, sv.REJECT_STAGED])
+def test_ragged_shapes(B, gamma, V, dtype, impl):
+    # the automatic choice runs the fused kernel where the rows are 16-byte
+    # aligned (V a multiple of 8 for bf16, of 4 for fp32), the staged ones
+    # elsewhere
     wl = workload("chain_7b").scaled(B=B, gamma=gamma, V=V, dtype=dtype, T=0.9)
     lg = logits_inputs(wl, seed=B * 100 + gamma)
     for offset in range(3):
-        _run(wl, lg, seed=99, offset=offset, b_base=5)
+        _run(wl, lg, seed=99, offset=offset, b_base=5, impl=impl)
 
 
 @pytest.mark.parametrize("B,gamma,V,dtype", [
@@ -67,48 +79,53 @@ def test_maximum_sizes(B, gamma, V, dtype):
         assert g["status"] == 0
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("V", [64, 32000])
-def test_trees(V):
+def test_trees(V, impl):
     wl = workload("tree_64").scaled(B=6, V=V)
     lg = logits_inputs(wl, seed=3)
     for offset in range(4):
-        _run(wl, lg, seed=7, offset=offset)
+        _run(wl, lg, seed=7, offset=offset, impl=impl)
 
 
-def test_small_trees_many_rejections():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_small_trees_many_rejections(impl):
     # wide fan-out, noisy draft: several rejections per node
     wl = workload("tree_64").scaled(B=8, V=48, gamma=2, tree_width=8,
                                     tree_nodes=40, noise=3.0)
     lg = logits_inputs(wl, seed=4)
     for offset in range(6):
-        _run(wl, lg, seed=11, offset=offset)
+        _run(wl, lg, seed=11, offset=offset, impl=impl)
 
 
-def test_all_accept_and_all_reject():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_all_accept_and_all_reject(impl):
     wl = workload("chain_7b").scaled(B=16, V=4000)
     lg = logits_inputs(wl, seed=5)
     same = dict(lg, draft=lg["target"].copy())
-    g, o, _ = _run(wl, same, seed=1, offset=0)
+    g, o, _ = _run(wl, same, seed=1, offset=0, impl=impl)
     assert np.all(g["accepted_len"] == wl.gamma)
     assert np.allclose(g["probe"][:, wl.gamma, 2], 1.0)
     rej = dict(lg, target=lg["target"].copy())
     x1 = lg["tokens"][:, 1]
     rej["target"][np.arange(wl.B), 0, x1] = -np.inf
-    g, o, _ = _run(wl, rej, seed=1, offset=0)
+    g, o, _ = _run(wl, rej, seed=1, offset=0, impl=impl)
     assert np.all(g["accepted_len"] == 0)
     assert np.all(g["out_tokens"][:, 0] != x1)
 
 
-@pytest.mark.parametrize("V", [300, 4096])
-def test_failed_requests(V):
-    # V = 300: rows not 16-byte aligned (four-kernel path); 4096: one kernel
+@pytest.mark.parametrize("V,impl", [(300, sv.REJECT_AUTO), (4096, sv.REJECT_FUSED),
+                                    (4096, sv.REJECT_STAGED)])
+def test_failed_requests(V, impl):
+    # V = 300: rows not 16-byte aligned (the staged kernels' scalar path);
+    # 4096: the fused kernel and the staged kernels' bulk-copy path
     wl = workload("chain_7b").scaled(B=5, V=V)
     lg = logits_inputs(wl, seed=6)
     lg["target"][1, 2, 7] = np.nan
     lg["draft"][2, 0, 3] = np.inf
     lg["temperature"][3] = 0.0
     lg["tokens"][4, 2] = V
-    g, o, _ = _run(wl, lg, seed=2, offset=0)
+    g, o, _ = _run(wl, lg, seed=2, offset=0, impl=impl)
     assert list(g["accepted_len"][1:]) == [-1, -1, -1, -1]
     assert g["accepted_len"][0] >= 0
     assert g["status"] == (1 << 1) | (1 << 5) | (1 << 6)

@@ -36,6 +36,8 @@ from .reject_sample import (  # noqa: F401
     UniformChooser,
     inverse_cdf,
     softmax_rows,
+    greedy_rows,
+    row_law,
     NONFINITE,
     INVALID_ARG,
     BAD_TOKEN,

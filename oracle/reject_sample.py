@@ -34,6 +34,15 @@ What the pages fix, and the readings taken where they are silent:
 * Rows containing NaN or +inf, or only -inf, have no distribution: the whole
   request is reported as failed (accepted length -1).  -inf entries are
   allowed and have probability 0.
+* Temperature 0 is greedy decoding (page 1 §4.3, first point: at temperature
+  0, or under greedy decoding, the probabilistic test becomes an exact match
+  position by position).  Reading taken: the law of a row at T = 0 is the
+  point mass on its largest logit, the smallest index among equal largest
+  ones (the limit of softmax(z / T) as T -> 0 when the maximum is unique);
+  the same walk then accepts a draft exactly when it is that token, and
+  every draw -- after a rejection or at the end -- is that token, whatever
+  the uniforms.  Page 2 §5.1 asks for the same sampling rule on both sides,
+  so the draft row's law at T = 0 is its own point mass.
 """
 from __future__ import annotations
 
@@ -53,6 +62,21 @@ def softmax_rows(logits: np.ndarray, T: float) -> np.ndarray:
     m = z.max(axis=-1, keepdims=True)
     e = np.exp((z - m) / float(T))
     return e / e.sum(axis=-1, keepdims=True)
+
+
+def greedy_rows(logits: np.ndarray) -> np.ndarray:
+    """Point mass on the largest logit of each row (smallest index on ties)."""
+    z = np.asarray(logits, dtype=np.float64)
+    k = np.argmax(z, axis=-1)          # numpy returns the first maximum
+    out = np.zeros_like(z)
+    np.put_along_axis(out, k[..., None], 1.0, axis=-1)
+    return out
+
+
+def row_law(logits: np.ndarray, T: float) -> np.ndarray:
+    """The law of a row at temperature T: softmax(z / T), or the point mass
+    on the largest logit at T = 0."""
+    return greedy_rows(logits) if T == 0.0 else softmax_rows(logits, T)
 
 
 def row_has_distribution(row: np.ndarray) -> bool:
@@ -87,9 +111,10 @@ def inverse_cdf(weights: np.ndarray, u: float, tol: float = NEAR):
 class UniformChooser:
     """Decisions driven by one request's counter-based uniforms."""
 
-    def __init__(self, u_acc: np.ndarray, u_smp: np.ndarray):
+    def __init__(self, u_acc: np.ndarray, u_smp: np.ndarray, exact: bool = False):
         self.u_acc = u_acc
         self.u_smp = u_smp
+        self.exact = exact           # point-mass laws: no decision is near a threshold
         self.acc_margin = np.inf     # smallest |u - p/q| over the accept tests
         self.smp_margin = np.inf     # |u - nearest CDF step| of the draw
         self.band = None             # tokens a draw within NEAR could select
@@ -100,14 +125,15 @@ class UniformChooser:
 
     def accept(self, node: int, P_x: float, Q_x: float) -> bool:
         u = self.u_acc[node]
-        if Q_x > 0.0:
+        if Q_x > 0.0 and not self.exact:
             self.acc_margin = min(self.acc_margin, abs(u - P_x / Q_x))
         return u * Q_x < P_x
 
     def sample(self, node: int, weights: np.ndarray) -> int:
         k, dist, band = inverse_cdf(weights, self.u_smp[node])
-        self.smp_margin = min(self.smp_margin, dist)
-        self.band = band
+        if not self.exact:
+            self.smp_margin = min(self.smp_margin, dist)
+        self.band = (k, k) if self.exact else band
         return k
 
 
@@ -184,7 +210,7 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
     target, draft : [B, M, V] logits (row n = distribution over n's children)
     tokens        : [B, M] drafted tokens (tokens[b, 0] ignored)
     parent        : [B, M] parent indices (parent[b, 0] = -1) or None (chain)
-    temperature   : [B] positive normal finite fp32 values
+    temperature   : [B] fp32 values: positive normal finite, or 0 (greedy)
     seed, offset  : Philox key word and counter word 2; b_base + b is word 1
 
     Returns dict of numpy arrays:
@@ -218,9 +244,9 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
         par = None if parent is None else np.asarray(parent[b])
         kids = children_lists(par, M)
         T = float(np.float32(temperature[b]))
-        # temperature must be a positive, normal, finite fp32 value
-        if not (T >= float(np.finfo(np.float32).tiny) and np.isfinite(T)) or (
-                par is not None and not valid_topology(par)):
+        # temperature must be 0 (greedy) or a positive, normal, finite fp32 value
+        t_ok = T == 0.0 or (T >= float(np.finfo(np.float32).tiny) and np.isfinite(T))
+        if not t_ok or (par is not None and not valid_topology(par)):
             status[b] = INVALID_ARG
             continue
         if np.any((tokens[b, 1:] < 0) | (tokens[b, 1:] >= V)):
@@ -232,10 +258,10 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
             status[b] = NONFINITE
             continue
         u_acc, u_smp = uniforms_for(seed, offset, b_base + b, M)
-        chooser = UniformChooser(u_acc, u_smp)
+        chooser = UniformChooser(u_acc, u_smp, exact=(T == 0.0))
         res = verify_request(
-            lambda n: softmax_rows(target[b, n], T),
-            lambda n: softmax_rows(draft[b, n], T),
+            lambda n: row_law(target[b, n], T),
+            lambda n: row_law(draft[b, n], T),
             tokens[b], kids, chooser)
         a = len(res["path"]) - 1
         acc[b] = a

@@ -123,7 +123,7 @@ def test_failed_requests(V, impl):
     lg = logits_inputs(wl, seed=6)
     lg["target"][1, 2, 7] = np.nan
     lg["draft"][2, 0, 3] = np.inf
-    lg["temperature"][3] = 0.0
+    lg["temperature"][3] = -1.0
     lg["tokens"][4, 2] = V
     g, o, _ = _run(wl, lg, seed=2, offset=0, impl=impl)
     assert list(g["accepted_len"][1:]) == [-1, -1, -1, -1]

@@ -57,17 +57,18 @@ namespace rsf {
 constexpr int kC = 4;              // CTAs per cluster: quarters of each row
 constexpr int kThreads = 512;
 constexpr int kSchedWarp = 1;
-constexpr int kCtrlWarp = 2;
-constexpr int kFirstConsumer = 3;
-constexpr int kConsumers = kThreads / kWarp - kFirstConsumer;  // 13
-constexpr int kSlots = 24;         // ring slots
+constexpr int kCtrlWarp = 2;       // first of the control warps
+constexpr int kCtl = 6;            // control warps: items k, k + 6, ... go to control k mod 6
+constexpr int kFirstConsumer = kCtrlWarp + kCtl;
+constexpr int kConsumers = kThreads / kWarp - kFirstConsumer;  // 8
+constexpr int kSlots = 20;         // ring slots
 constexpr int kHalfSlot = 4096;    // one chunk of one row
 constexpr int kSlotBytes = 2 * kHalfSlot;
-constexpr int kNQ = 6;             // items in flight per CTA
-constexpr int kNE = 4;             // exchange buffers
+constexpr int kNQ = 2 * kCtl;      // items in flight per CTA (two per control)
+constexpr int kNE = 2;             // exchange buffers per control
 constexpr int kMaxQuarter = 32;    // chunks per quarter
 constexpr int kMaxKids = 63;
-constexpr int kReqQ = 8;           // control -> producer requests
+constexpr int kReqQ = 4;           // requests of one control to the producer
 
 enum : int { kTaskStats = 0, kTaskRes = 1, kTaskSearch = 2, kTaskStop = 3 };
 enum : int { kReqRes = 1, kReqSearch = 2 };
@@ -96,7 +97,8 @@ struct ItemState {
   int b, n, pair;           // request, node; pair: the node has children (its draft row is read)
   int nkids;
   uint32_t bad;             // spec_status bits found by the scheduler
-  float cs;                 // log2(e) / T
+  float cs;                 // log2(e) / T (1 for a greedy request)
+  int greedy;               // temperature 0: every law is the point mass on the row's argmax
   int par;                  // parent node (-1 for the root)
   int kid[kMaxKids];        // children, ascending
   int ktok[kMaxKids];       // their drafted tokens
@@ -119,6 +121,7 @@ struct __align__(16) XMsg {
   double s_t, s_d;
   unsigned long long have;
   uint32_t flags, path;
+  int amax_t, amax_d;       // greedy: the quarter's first maximum (element index), -1 if none
   float2 gz[kMaxKids + 1];
 };
 
@@ -138,13 +141,13 @@ struct __align__(8) Bars {
   uint64_t freed[kNQ];    // rank 0 only: the four controls are done with the slot
   uint64_t stats[kNQ], resd[kNQ], srch[kNQ];
   uint64_t drawn[kNQ];    // rank 0 only: the draw's result arrived
-  uint64_t xbar[kNE];
+  uint64_t xbar[kCtl][kNE];
   int bcast_item[kNQ];
   DrawMsg draw[kNQ];
   TaskDesc task[kSlots];
-  int req_type[kReqQ], req_q[kReqQ], req_c[kReqQ];
-  int req_tail;
-  int ctrl_done;
+  int req_type[kCtl][kReqQ], req_q[kCtl][kReqQ], req_c[kCtl][kReqQ];
+  int req_tail[kCtl];
+  int ctrl_done;          // controls that have finished
   int prod_items;         // items whose state the producer has taken (it may then be reused)
   int abort;
   uint32_t epoch_tag;
@@ -163,7 +166,7 @@ static_assert(sizeof(Rec) == 32, "record size");
 constexpr size_t kRingOff = 0;
 constexpr size_t kItemsOff = kRingOff + (size_t)kSlots * kSlotBytes;
 constexpr size_t kXbufOff = kItemsOff + (((sizeof(ItemState) * kNQ) + 15) / 16) * 16;
-constexpr size_t kBarsOff = kXbufOff + sizeof(XMsg) * kNE * kC;
+constexpr size_t kBarsOff = kXbufOff + sizeof(XMsg) * kCtl * kNE * kC;
 constexpr size_t kSmemBytes = kBarsOff + sizeof(Bars) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
                                              ~uintptr_t(1023));
   uint8_t* ring = smem + kRingOff;
   ItemState* items = reinterpret_cast<ItemState*>(smem + kItemsOff);
-  XMsg* xbuf = reinterpret_cast<XMsg*>(smem + kXbufOff);  // [kNE][kC]
+  XMsg* xbuf = reinterpret_cast<XMsg*>(smem + kXbufOff);  // [kCtl][kNE][kC]
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarsOff);
 
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -370,8 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       ptx::mbar_init(ptx::smem_u32(&bars->srch[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->drawn[i]), 1);
     }
-    for (int i = 0; i < kNE; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[i]), kC);
-    bars->req_tail = 0;
+    for (int j = 0; j < kCtl; ++j) {
+      for (int i = 0; i < kNE; ++i) ptx::mbar_init(ptx::smem_u32(&bars->xbar[j][i]), kC);
+      bars->req_tail[j] = 0;
+    }
     bars->ctrl_done = 0;
     bars->prod_items = 0;
     bars->abort = 0;
@@ -405,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       bool cur_pair = false;
       const T* cur_t = nullptr;
       const T* cur_d = nullptr;
-      int head = 0;               // next request of the control warp
+      int head[kCtl];             // next request of each control warp
+      for (int j = 0; j < kCtl; ++j) head[j] = 0;
+      int rr = 0;                 // control whose queue is looked at first
       int rq_type = 0, rq_q = 0, rq_c = 0, rq_end = 0;
       bool ok = true;
       long long t_idle = 0;
@@ -445,11 +452,19 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
           t_idle = 0;
           continue;
         }
-        if (head < *reinterpret_cast<volatile int*>(&bars->req_tail)) {
-          const int h = head % kReqQ;
-          rq_type = *reinterpret_cast<volatile int*>(&bars->req_type[h]);
-          rq_q = *reinterpret_cast<volatile int*>(&bars->req_q[h]);
-          const int c = *reinterpret_cast<volatile int*>(&bars->req_c[h]);
+        int jq = -1;  // a control with a request waiting, taken in turn
+        for (int jj = 0; jj < kCtl; ++jj) {
+          const int j = (rr + jj) % kCtl;
+          if (head[j] < *reinterpret_cast<volatile int*>(&bars->req_tail[j])) {
+            jq = j;
+            break;
+          }
+        }
+        if (jq >= 0) {
+          const int h = head[jq] % kReqQ;
+          rq_type = *reinterpret_cast<volatile int*>(&bars->req_type[jq][h]);
+          rq_q = *reinterpret_cast<volatile int*>(&bars->req_q[jq][h]);
+          const int c = *reinterpret_cast<volatile int*>(&bars->req_c[jq][h]);
           if (rq_type == kReqRes) {
             rq_c = q0;
             rq_end = q1;
@@ -457,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
             rq_c = c;
             rq_end = c + 1;
           }
-          ++head;
+          ++head[jq];
+          rr = (jq + 1) % kCtl;
           t_idle = 0;
           continue;
         }
@@ -487,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
             }
             continue;
           }
-        } else if (*reinterpret_cast<volatile int*>(&bars->ctrl_done)) {
+        } else if (*reinterpret_cast<volatile int*>(&bars->ctrl_done) == kCtl) {
           break;
         }
         // nothing to issue yet: bounded idle
@@ -511,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
     }
   } else if (warp == kSchedWarp) {
     // ----------------------------------------------------------- scheduler
+    // After the last item, one end marker per control (each control takes
+    // every kCtl-th slot).
+    int stops = 0;
     for (int k = 0;; ++k) {
       const int q = k % kNQ;
       const uint32_t par = (uint32_t)((k / kNQ) & 1);
@@ -553,13 +572,14 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
           it.item = -1;
           ptx::mbar_arrive(ptx::smem_u32(&bars->meta[q]));
         }
-        break;
+        if (++stops == kCtl) break;
+        continue;
       }
       const int b = i % B, n = i / B;
       // children of n (ascending), their tokens, the topology check
       uint32_t bad = 0;
       const float temp = temperature[b];
-      if (!temperature_ok(temp)) bad |= 1u << SPEC_ERR_INVALID_ARG;
+      if (!temperature_valid(temp)) bad |= 1u << SPEC_ERR_INVALID_ARG;
       int pn = n - 1;
       unsigned long long kids = 0;
       if (parent == nullptr) {
@@ -583,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         it.n = n;
         it.pair = nk > 0;
         it.nkids = nk;
-        it.cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+        it.cs = stat_scale(temp);
+        it.greedy = temp == 0.f;
         it.par = n == 0 ? -1 : pn;
         it.have = 0;
         it.s_done = 0;
@@ -610,9 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         ptx::mbar_arrive(ptx::smem_u32(&bars->meta[q]));  // releases the state to the CTA
       }
     }
-  } else if (warp == kCtrlWarp) {
+  } else if (warp < kCtrlWarp + kCtl) {
     // ------------------------------------------------------------- control
-    int e = 0;                  // exchange events so far
+    const int cj = warp - kCtrlWarp;  // this control's items: k = cj, cj + kCtl, ...
+    int e = 0;                  // exchange events of this control so far
     int res_uses[kNQ], srch_uses[kNQ], drawn_uses[kNQ];
     for (int q = 0; q < kNQ; ++q) res_uses[q] = srch_uses[q] = drawn_uses[q] = 0;
     int req_tail = 0;
@@ -622,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
     // of the cluster and wait for theirs: returns the four messages.
     auto exchange = [&](const XMsg& m, int words) -> const XMsg* {
       const int slot = e % kNE;
-      XMsg* dst = &xbuf[slot * kC + rank];
+      XMsg* chan = &xbuf[(cj * kNE + slot) * kC];
+      XMsg* dst = &chan[rank];
       const uint4* src = reinterpret_cast<const uint4*>(&m);
       for (int w = lane; w < words * kC; w += kWarp) {
         const int r = w / words, wi = w % words;
@@ -633,22 +656,22 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       if (lane == 0) {
         ptx::fence_acq_rel_cluster();
         for (uint32_t r = 0; r < kC; ++r)
-          ptx::mbar_arrive_cluster(ptx::map_rank(ptx::smem_u32(&bars->xbar[slot]), r));
+          ptx::mbar_arrive_cluster(ptx::map_rank(ptx::smem_u32(&bars->xbar[cj][slot]), r));
       }
       const bool got = __all_sync(0xffffffffu,
-                                  ptx::mbar_wait_cluster(ptx::smem_u32(&bars->xbar[slot]),
+                                  ptx::mbar_wait_cluster(ptx::smem_u32(&bars->xbar[cj][slot]),
                                                          (uint32_t)((e / kNE) & 1), abort, wait));
       ++e;
-      return got ? &xbuf[slot * kC] : nullptr;
+      return got ? chan : nullptr;
     };
     auto request = [&](int type, int q, int c) {
       if (lane == 0) {
         const int h = req_tail % kReqQ;
-        bars->req_type[h] = type;
-        bars->req_q[h] = q;
-        bars->req_c[h] = c;
+        bars->req_type[cj][h] = type;
+        bars->req_q[cj][h] = q;
+        bars->req_c[cj][h] = c;
         __threadfence_block();
-        *reinterpret_cast<volatile int*>(&bars->req_tail) = req_tail + 1;
+        *reinterpret_cast<volatile int*>(&bars->req_tail[cj]) = req_tail + 1;
       }
       ++req_tail;
       __syncwarp();
@@ -679,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       return true;
     };
 
-    for (int k = 0; ok; ++k) {
+    for (int k = cj; ok; k += kCtl) {
       const int q = k % kNQ;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->meta[q]),
                                                   (uint32_t)((k / kNQ) & 1), abort, wait))) {
@@ -690,8 +713,15 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       if (it.item < 0) break;
       const int b = it.b, n = it.n, nk = it.nkids;
       const float cs = it.cs;
-      // path state of the node from its parent's record (rank 0 reads it
-      // and sends it with its statistics, so all four agree)
+      // the quarter's statistics
+      if (nq > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->stats[q]),
+                                                            (uint32_t)((k / kNQ) & 1), abort, wait))) {
+        ok = false;
+        break;
+      }
+      // path state of the node from its parent's record (rank 0 reads it,
+      // as late as it can, and sends it with its statistics, so all four
+      // agree)
       uint32_t pstate = kPathUnknown;
       if (rank == 0 && lane == 0) {
         if (n == 0) {
@@ -710,12 +740,6 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         }
       }
       pstate = __shfl_sync(0xffffffffu, pstate, 0);
-      // the quarter's statistics
-      if (nq > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->stats[q]),
-                                                            (uint32_t)((k / kNQ) & 1), abort, wait))) {
-        ok = false;
-        break;
-      }
       XMsg m;
       quarter_stats(it.st_t, nq, cs, &m.m_t, &m.s_t);
       if (it.pair) {
@@ -727,6 +751,21 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       m.have = it.have;
       m.flags = it.bad;
       m.path = pstate;
+      m.amax_t = m.amax_d = -1;
+      if (it.greedy) {
+        // the quarter's first maximum of each row (exact comparisons)
+        for (int jj = 0; jj < nq; ++jj)
+          if (it.st_t[jj].m == m.m_t) {
+            m.amax_t = (q0 + jj) * CH + unpack_index(it.st_t[jj].pad);
+            break;
+          }
+        if (it.pair)
+          for (int jj = 0; jj < nq; ++jj)
+            if (it.st_d[jj].m == m.m_d) {
+              m.amax_d = (q0 + jj) * CH + unpack_index(it.st_d[jj].pad);
+              break;
+            }
+      }
       for (int j = 0; j < nk && j < kMaxKids; ++j) m.gz[j] = it.gz[j];
       const int words = (int)((offsetof(XMsg, gz) + sizeof(float2) * nk + 15) / 16);
       const XMsg* x = exchange(m, words);
@@ -758,6 +797,14 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
           if ((x[r].have >> j) & 1ull) gzk[j] = x[r].gz[j];
       }
       const bool decide = bad == 0 && state != kPathOff;
+      const bool greedy = it.greedy != 0;
+      int amaxT = -1, amaxD = -1;  // greedy: each row's first maximum
+      if (greedy) {
+        for (int r = 0; r < kC && amaxT < 0; ++r)
+          if (x[r].m_t == mT && x[r].amax_t >= 0) amaxT = x[r].amax_t;
+        for (int r = 0; r < kC && amaxD < 0; ++r)
+          if (x[r].m_d == mD && x[r].amax_d >= 0) amaxD = x[r].amax_d;
+      }
       // ---- the tests of the children, in order ---------------------------
       const uint64_t bglob = b_base + (uint64_t)b;
       const double cs64 = (double)cs;
@@ -767,7 +814,22 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       float pcs[kMaxKids], qcs[kMaxKids];
       for (int j = 0; j < nk; ++j) pcs[j] = qcs[j] = -1.f;
       bool drawn = false;  // the draw at n was arranged
-      if (decide) {
+      if (decide && greedy) {
+        // temperature 0: a child is accepted iff its token is the argmax;
+        // the draw at n is the argmax (residuals of point masses are that
+        // point mass, or empty and back to it)
+        for (int j = 0; j < nk; ++j) {
+          const bool acc = it.ktok[j] == amaxT;
+          pcs[j] = acc ? 1.f : 0.f;
+          qcs[j] = it.ktok[j] == amaxD ? 1.f : 0.f;
+          if (acc) {
+            acc_child = it.kid[j];
+            acc_tok = it.ktok[j];
+            break;
+          }
+        }
+        drawn = true;
+      } else if (decide) {
         const float st_f = (float)ST, sd_f = (float)SD;
         for (int j = 0; j < nk && ok; ++j) {
           const int child = it.kid[j];
@@ -976,7 +1038,9 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
       // ---- rank 0: the item's record, the children's tests, the request --
       if (rank == 0) {
         DrawMsg dm{-1, -1.f};
-        if (drew) {
+        if (drew && greedy) {
+          dm = DrawMsg{amaxT, 1.f};
+        } else if (drew) {
           if (!__all_sync(0xffffffffu, ptx::mbar_wait_cluster(ptx::smem_u32(&bars->drawn[q]),
                                                               (uint32_t)(drawn_uses[q] & 1), abort,
                                                               wait))) {
@@ -1097,7 +1161,7 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         break;
       }
     }
-    if (lane == 0) *reinterpret_cast<volatile int*>(&bars->ctrl_done) = 1;
+    if (lane == 0) atomicAdd(&bars->ctrl_done, 1);
     if (!ok && lane == 0) spread_abort();
   } else {
     // ----------------------------------------------------------- consumers
@@ -1121,11 +1185,15 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         for (int v = 0; v < kStatVecs; ++v) raw[v] = sv_t[v * kWarp + lane];
         float s_t;
         const float m_t = chunk_stat<T>(raw, nvalid, it.cs, &s_t);
+        const bool greedy = it.greedy != 0;
+        const int am_t = greedy ? chunk_argmax<T>(raw, nvalid, m_t) : 0;
         float m_d = -INFINITY, s_d = 0.f;
+        int am_d = 0;
         if (it.pair) {
 #pragma unroll
           for (int v = 0; v < kStatVecs; ++v) raw[v] = sv_d[v * kWarp + lane];
           m_d = chunk_stat<T>(raw, nvalid, it.cs, &s_d);
+          if (greedy) am_d = chunk_argmax<T>(raw, nvalid, m_d);
         }
         // the children's logits that fall in this chunk
         for (int j = lane; j < it.nkids; j += kWarp) {
@@ -1141,10 +1209,10 @@ __global__ void __launch_bounds__(kThreads, 1) rs_fused_kernel(
         if (lane == 0) {
           const int jj = td.c - q0;
           it.st_t[jj].m = m_t;
-          it.st_t[jj].pad = 0.f;
+          it.st_t[jj].pad = pack_index(am_t);
           it.st_t[jj].s = (double)s_t;
           it.st_d[jj].m = m_d;
-          it.st_d[jj].pad = 0.f;
+          it.st_d[jj].pad = pack_index(am_d);
           it.st_d[jj].s = (double)s_d;
           __threadfence_block();
           if (atomicAdd(&it.s_done, 1) == nq - 1) ptx::mbar_arrive(ptx::smem_u32(&bars->stats[td.q]));

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
     if (kAligned && t2 < ntask) load(t2, nxt);
     const StatTask k = stat_task(t, n_chunks, M);
     const float temp = temperature[k.b];
-    const float cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+    const float cs = stat_scale(temp);
     const int64_t e0 = (int64_t)k.c * kChunk;
     float f[kStatVecs][EPV];
 #pragma unroll
@@ -164,10 +164,22 @@ __global__ void __launch_bounds__(kRsThreads) rs_rowstats_kernel(
         for (int i = 0; i < EPV; ++i) sl += fast_exp2((f[v][i] - m) * cs);
     }
     const double sd = warp_sum((double)sl);
+    int am = 0;
+    if (temp == 0.f) {  // greedy: the chunk's first maximum
+      int best = 0x7fffffff;
+#pragma unroll
+      for (int v = 0; v < kStatVecs; ++v)
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) {
+          const int er = (v * kWarp + lane) * EPV + i;
+          if (e0 + er < V && f[v][i] == m && er < best) best = er;
+        }
+      am = __reduce_min_sync(0xffffffffu, best);
+    }
     if (lane == 0) {
       RowStat r;
       r.m = m;
-      r.pad = 0.f;
+      r.pad = pack_index(am);
       r.s = sd;
       stats[(((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks + k.c] = r;
     }
@@ -300,6 +312,7 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   bool ok = true;
   int cur_b = -1;
   float cs = 1.0f;
+  bool greedy = false;
   while (cp.valid()) {
     const int slot = done % kBulkRing;
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&mybars[slot]),
@@ -310,7 +323,8 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     if (cp.b != cur_b) {
       cur_b = cp.b;
       const float temp = temperature[cur_b];
-      cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+      cs = stat_scale(temp);
+      greedy = temp == 0.f;
     }
     const int e0 = cp.c * kChunk;
     const int nvalid = V - e0;  // elements of this chunk inside the row (may exceed kChunk)
@@ -320,10 +334,11 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
     float sd;
     const float m = chunk_stat<T>(raw, nvalid, cs, &sd);
+    const int am = greedy ? chunk_argmax<T>(raw, nvalid, m) : 0;
     if (lane == 0) {
       RowStat r;
       r.m = m;
-      r.pad = 0.f;
+      r.pad = pack_index(am);
       r.s = (double)sd;
       stats[(((int64_t)cp.b * 2 + cp.which) * M + cp.n) * n_chunks + cp.c] = r;
     }
@@ -736,6 +751,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   __shared__ double s_trel, s_z;
   __shared__ int chain_rej[kMaxM];  // chain: the accept test of node n failed
   __shared__ float chain_p[kMaxM], chain_q[kMaxM];
+  __shared__ int rowA[2][kMaxM];    // greedy: each row's largest logit (smallest index)
 
   pdl_trigger();
   pdl_wait();  // the statistics come from the previous kernel
@@ -754,7 +770,8 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
 
   // ---- validation --------------------------------------------------------
   const float temp = temperature[b];
-  int bad_arg = !temperature_ok(temp);
+  const bool greedy = temp == 0.f;
+  int bad_arg = !temperature_valid(temp);
   int bad_tok = 0;
   if (tid < M) {
     const int32_t x = tokens[(int64_t)b * M + tid];
@@ -783,7 +800,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     }
   }
   __syncthreads();
-  const float cs = temperature_ok(temp) ? 1.4426950408889634f / temp : 1.0f;
+  const float cs = stat_scale(temp);
 
   // gather the logits every accept test will read, all at once
   if (!bad_arg && !bad_tok && tid >= 1 && tid < M) {
@@ -824,6 +841,18 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       for (int j = 0; j < kItems; ++j)
         if (im[j] != -INFINITY) s += is[j] * (double)fast_exp2((im[j] - m) * cs);
       s = warp_sum(s);
+      if (greedy) {
+        // the row's first maximum: the first chunk holding m, then its index
+        int c_first = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+          const int c = lane + j * kWarp;
+          if (c < n_chunks && im[j] == m && c < c_first) c_first = c;
+        }
+        c_first = __reduce_min_sync(0xffffffffu, c_first);
+        if (lane == 0)
+          rowA[which][n] = c_first < n_chunks ? c_first * chunk + unpack_index(st[c_first].pad) : 0;
+      }
       if (lane == 0) {
         rowM[which][n] = m;
         rowS[which][n] = s;
@@ -877,6 +906,44 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       raise_status(status, bad_arg ? SPEC_ERR_INVALID_ARG
                            : bad_tok ? SPEC_ERR_DEVICE_BOUNDS
                                      : SPEC_ERR_NONFINITE);
+    }
+    return;
+  }
+
+  if (greedy) {
+    // ---- temperature 0: exact match with each row's largest logit -------
+    // A child is accepted iff its token is its parent's argmax; the first
+    // such child of a node is entered; the token drawn at the last node is
+    // its argmax (every residual of point masses is that point mass, or
+    // empty, which falls back to it).
+    if (tid == 0) {
+      int node = 0, a = 0;
+      path[(int64_t)b * M] = 0;
+      for (;;) {
+        int next = -1;
+        for (int c = first_child[node]; c >= 0; c = next_sib[c]) {
+          const bool acc = tok[c] == rowA[0][node];
+          if (probe != nullptr) {
+            probe[((int64_t)b * M + c) * 4 + 0] = acc ? 1.f : 0.f;
+            probe[((int64_t)b * M + c) * 4 + 1] = tok[c] == rowA[1][node] ? 1.f : 0.f;
+          }
+          if (acc) {
+            next = c;
+            break;
+          }
+        }
+        if (next < 0) break;
+        out_tokens[(int64_t)b * M + a] = tok[next];
+        ++a;
+        path[(int64_t)b * M + a] = next;
+        node = next;
+      }
+      out_tokens[(int64_t)b * M + a] = rowA[0][node];
+      accepted_len[b] = a;
+      if (probe != nullptr) {
+        probe[((int64_t)b * M + node) * 4 + 2] = 1.f;
+        probe[((int64_t)b * M + node) * 4 + 3] = 1.f;
+      }
     }
     return;
   }

@@ -76,6 +76,39 @@ __device__ __forceinline__ dfloat df_warp_scan(dfloat x) {
 __device__ __forceinline__ bool temperature_ok(float T) {
   return T >= FLT_MIN && T <= FLT_MAX;  // normal, positive, finite (NaN fails)
 }
+// A request's temperature is valid when it is 0 (greedy: every row's law is
+// the point mass on its largest logit, the smallest index among ties) or a
+// positive normal finite value.
+__device__ __forceinline__ bool temperature_valid(float T) { return T == 0.0f || temperature_ok(T); }
+// log2(e) / T for the statistics; rows of a greedy request are still reduced
+// (with a scale of 1) so that rows without a distribution are found.
+__device__ __forceinline__ float stat_scale(float T) {
+  return temperature_ok(T) ? 1.4426950408889634f / T : 1.0f;
+}
+
+// Index inside a chunk of the first element equal to the chunk's maximum m,
+// the chunk held as chunk_stat holds it (lane l: vectors v * 32 + l).
+// Comparisons are exact, so the smallest index among equal maxima wins.
+template <typename T>
+__device__ __forceinline__ int chunk_argmax(const uint4 (&raw)[kStatVecs], int nvalid, float m) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int lane = threadIdx.x % kWarp;
+  int best = 0x7fffffff;
+#pragma unroll
+  for (int v = 0; v < kStatVecs; ++v) {
+    float f[EPV];
+    unpack16(raw[v], f);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      const int e = (v * kWarp + lane) * EPV + i;
+      if (e < nvalid && f[i] == m && e < best) best = e;
+    }
+  }
+  return __reduce_min_sync(0xffffffffu, best);
+}
+// The chunk statistics keep the argmax index in RowStat's spare word.
+__device__ __forceinline__ float pack_index(int i) { return __int_as_float(i); }
+__device__ __forceinline__ int unpack_index(float f) { return __float_as_int(f); }
 
 // Load EPV consecutive logits starting at element e (-inf past the row end).
 template <typename T, bool kAligned>

@@ -18,7 +18,7 @@ pytestmark = [pytest.mark.gpu,
 import speculative_decoding_verification_19_gb300 as sv  # noqa: E402
 from harness import compare_reject, dims_for, gpu_reject  # noqa: E402
 from oracle import oracle_reject_sample, softmax_rows  # noqa: E402
-from synth import logits_inputs, workload  # noqa: E402
+from synth import bf16_round, logits_inputs, workload  # noqa: E402
 
 
 IMPLS = [sv.REJECT_FUSED, sv.REJECT_STAGED]
@@ -155,3 +155,43 @@ def test_gpu_output_law_chi_square():
     emitted = g["accepted_len"] + 1
     expect = (1 - alpha ** (gamma + 1)) / (1 - alpha)
     assert abs(emitted.mean() - expect) < 4 * emitted.std() / np.sqrt(B)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["chain_gqa_128k", "tree_64", "stress_gqa_152k"])
+def test_greedy_full_size(name, impl):
+    """Temperature 0 (page 1 §4.3): exact match with each row's argmax; the
+    drawn token is the argmax.  Bit-exact: no decision is near a threshold."""
+    wl = workload(name)
+    lg = logits_inputs(wl, seed=8)
+    lg["temperature"][:] = 0.0
+    # make some drafts the target's argmax so that acceptances happen
+    t = lg["target"]
+    for b in range(wl.B):
+        for c in range(1, wl.M):
+            par = c - 1 if lg["parent"] is None else lg["parent"][b, c]
+            if (b + c) % 3 != 0:
+                lg["tokens"][b, c] = int(np.argmax(t[b, par]))
+    g, o, near = _run(wl, lg, seed=3, offset=0, impl=impl)
+    assert near == 0 and g["status"] == 0
+    assert np.array_equal(g["out_tokens"], o["out_tokens"])
+    assert np.array_equal(g["path"], o["path"])
+    assert (o["accepted_len"] > 0).any()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_greedy_mixed_batch_and_ties(impl):
+    # half the requests greedy, half sampled, in one call; a greedy row with
+    # its maximum repeated (the smallest index must win)
+    wl = workload("chain_7b").scaled(B=12, V=16384)
+    lg = logits_inputs(wl, seed=9)
+    lg["temperature"][::2] = 0.0
+    t = lg["target"]
+    top = bf16_round(np.array([t[0, 0].max() + 1.0], np.float32))[0]
+    t[0, 0, 100] = top
+    t[0, 0, 9000] = top
+    lg["tokens"][0, 1] = 9000          # a tie, but not the first maximum: rejected
+    g, o, _ = _run(wl, lg, seed=4, offset=2, impl=impl)
+    assert g["accepted_len"][0] == 0 and g["out_tokens"][0, 0] == 100
+    greedy = lg["temperature"] == 0.0
+    assert np.array_equal(g["out_tokens"][greedy], o["out_tokens"][greedy])

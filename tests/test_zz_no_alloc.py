@@ -69,12 +69,27 @@ def test_same_inputs_twice():
 
 
 def test_refuses_sizes_beyond_its_scratch():
-    # 512 requests x 10 rows x 75 chunks of 2048 logits, 16 bytes of
-    # statistics each, need far more than 1 MiB
-    dims = sv.make_dims(B=512, M=5, V=152064)
-    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
-    i = torch.zeros(16, dtype=torch.int32, device="cuda")
-    f = torch.ones(16, dtype=torch.float32, device="cuda")
+    # 16384 requests x 5 rows of a 16-logit vocabulary: the kernels these
+    # sizes run on (the staged ones: the rows are too short for the fused
+    # kernel) need 16 MB of scratch, far beyond the 1 MiB array.  The
+    # buffers have the full sizes, so nothing could be read out of bounds
+    # even if the call went ahead.
+    B, M, V = 16384, 5, 16
+    dims = sv.make_dims(B=B, M=M, V=V)
+    t = torch.zeros(B, M, V, dtype=torch.bfloat16, device="cuda")
+    i = torch.zeros(B, M, dtype=torch.int32, device="cuda")
+    f = torch.ones(B, dtype=torch.float32, device="cuda")
+    a = torch.zeros(B, dtype=torch.int32, device="cuda")
     with pytest.raises(sv.SpecError) as e:
-        sv.spec_reject_sample_noalloc(t, t, i, None, f, 1, 0, i, i, i, None, dims)
+        sv.spec_reject_sample_noalloc(t, t, i, None, f, 1, 0, i, i.clone(), a, None, dims)
+    assert e.value.code == 3
+    # the fused kernel's records: 40000 requests x 5 nodes x 32 bytes
+    B = 40000
+    dims = sv.make_dims(B=B, M=M, V=64, reject_impl=sv.REJECT_FUSED)
+    t = torch.zeros(B, M, 64, dtype=torch.bfloat16, device="cuda")
+    i = torch.zeros(B, M, dtype=torch.int32, device="cuda")
+    f = torch.ones(B, dtype=torch.float32, device="cuda")
+    a = torch.zeros(B, dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpecError) as e:
+        sv.spec_reject_sample_noalloc(t, t, i, None, f, 1, 0, i, i.clone(), a, None, dims)
     assert e.value.code == 3

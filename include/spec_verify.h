@@ -77,15 +77,15 @@ typedef enum spec_attn_impl {
 
 /* Reject-sample kernel selection (spec_dims.reject_impl). */
 typedef enum spec_reject_impl {
-  SPEC_REJECT_AUTO = 0,        /* the fused kernel for 16-byte aligned rows of 4 to 128
-                                  statistics chunks (8192..262144 bf16 logits,
-                                  4096..131072 fp32), else the staged kernels */
+  SPEC_REJECT_AUTO = 0,        /* the fused kernel for 16-byte aligned rows, else the
+                                  staged kernels */
   SPEC_REJECT_STAGED = 1,      /* four kernels: logit statistics, decisions, residual
-                                  masses, residual draws; any vocabulary up to 2^20 */
-  SPEC_REJECT_FUSED = 2        /* one kernel on 4-CTA clusters: statistics, tests and draws
-                                  of every (request, node) as the logits stream in;
-                                  16-byte aligned rows, V <= 128 chunks of 2048 bf16
-                                  (1024 fp32) logits; SPEC_ERR_UNSUPPORTED otherwise */
+                                  masses, residual draws; any alignment, V up to 2^20 */
+  SPEC_REJECT_FUSED = 2        /* one kernel: most SMs stream the logit statistics while
+                                  a few decide each request as soon as its rows are
+                                  done; 16-byte aligned rows (V * element size a
+                                  multiple of 16, aligned row pointers), V up to 2^20;
+                                  SPEC_ERR_UNSUPPORTED otherwise */
 } spec_reject_impl;
 
 typedef struct spec_dims {

@@ -725,39 +725,43 @@ __device__ int warp_draw_from_p(const T* trow, const RowStat* st, int n_chunks, 
                             dfloat{th, (float)(trel - (double)th)}, w);
 }
 
+// Shared state of the decisions of one request (one CTA of kDecThreads).
+struct DecideSmem {
+  int first_child[kMaxM], next_sib[kMaxM], tok[kMaxM];
+  float rowM[2][kMaxM];
+  double rowS[2][kMaxM];
+  float gzt[kMaxM], gzd[kMaxM];  // logits of each drafted token in its parent's rows
+  double px[kMaxM], qx[kMaxM];   // p(x_c), q(x_c) under the parent's rows (fp64)
+  double uacc[kMaxM], usmp[kMaxM];
+  double red[kDecWarps];
+  DecideCtx ctx;
+  DrawScratch ds;
+  int s_node, s_child, s_accept, s_a, s_chunk;
+  double s_trel, s_z;
+  int chain_rej[kMaxM];  // chain: the accept test of node n failed
+  float chain_p[kMaxM], chain_q[kMaxM];
+  int rowA[2][kMaxM];    // greedy: each row's largest logit (smallest index)
+};
+
+// The decisions of request b from its rows' chunk statistics, by one CTA of
+// kDecThreads threads: validation, row normalisers, the accept tests (a
+// chain's all at once, a tree walked in order with its residual updates),
+// and the draw from p; a draw from a residual is left in draws[b]
+// (pending = 1) for the caller.  stats_lost: a statistics wait gave up,
+// so the request is failed without being decided.
 template <typename T, bool kAligned>
-__global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
+__device__ void decide_request(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
     const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
-    int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* stats, DrawState* __restrict__ draws, uint32_t* status) {
+    int32_t* __restrict__ accepted_len, float* __restrict__ probe, const spec_dims& d, int n_chunks,
+    int chunk, const RowStat* stats, DrawState* draws, uint32_t* status, int b, bool stats_lost,
+    DecideSmem& sh) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kSweep = kDecThreads * EPV;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int warp = tid / kWarp, lane = tid % kWarp;
   const int M = d.M, V = d.V;
-
-  __shared__ int first_child[kMaxM], next_sib[kMaxM], tok[kMaxM];
-  __shared__ float rowM[2][kMaxM];
-  __shared__ double rowS[2][kMaxM];
-  __shared__ float gzt[kMaxM], gzd[kMaxM];  // logits of each drafted token in its parent's rows
-  __shared__ double px[kMaxM], qx[kMaxM];   // p(x_c), q(x_c) under the parent's rows (fp64)
-  __shared__ double uacc[kMaxM], usmp[kMaxM];
-  __shared__ double red[kDecWarps];
-  __shared__ DecideCtx ctx;
-  __shared__ DrawScratch ds;
-  __shared__ int s_node, s_child, s_accept, s_a, s_chunk;
-  __shared__ double s_trel, s_z;
-  __shared__ int chain_rej[kMaxM];  // chain: the accept test of node n failed
-  __shared__ float chain_p[kMaxM], chain_q[kMaxM];
-  __shared__ int rowA[2][kMaxM];    // greedy: each row's largest logit (smallest index)
-
-  pdl_trigger();
-  pdl_wait();  // the statistics come from the previous kernel
-  // A wait of the statistics kernel that gave up left some statistics
-  // unwritten: then no request of the call is decided on them.
-  const bool stats_lost = (ld_volatile_u32(status) >> SPEC_ERR_TIMEOUT) & 1u;
 
   // defined outputs first
   for (int i = tid; i < M; i += kDecThreads) {
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   int bad_tok = 0;
   if (tid < M) {
     const int32_t x = tokens[(int64_t)b * M + tid];
-    tok[tid] = x;
+    sh.tok[tid] = x;
     if (tid > 0) bad_tok = (x < 0 || x >= V);
     if (parent != nullptr) {
       const int32_t pn = parent[(int64_t)b * M + tid];
@@ -792,11 +796,11 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     return;
   }
   if (tid == 0 && !bad_arg) {
-    for (int n = 0; n < M; ++n) first_child[n] = -1;
+    for (int n = 0; n < M; ++n) sh.first_child[n] = -1;
     for (int n = M - 1; n >= 1; --n) {  // ascending sibling lists
       const int p = parent ? parent[(int64_t)b * M + n] : n - 1;
-      next_sib[n] = first_child[p];
-      first_child[p] = n;
+      sh.next_sib[n] = sh.first_child[p];
+      sh.first_child[p] = n;
     }
   }
   __syncthreads();
@@ -805,16 +809,16 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   // gather the logits every accept test will read, all at once
   if (!bad_arg && !bad_tok && tid >= 1 && tid < M) {
     const int p = parent ? parent[(int64_t)b * M + tid] : tid - 1;
-    const int64_t o = ((int64_t)b * M + p) * V + tok[tid];
-    gzt[tid] = to_f32(target[o]);
-    gzd[tid] = to_f32(draft[o]);
+    const int64_t o = ((int64_t)b * M + p) * V + sh.tok[tid];
+    sh.gzt[tid] = to_f32(target[o]);
+    sh.gzd[tid] = to_f32(draft[o]);
   }
   // ---- row normalisers ---------------------------------------------------
   int bad_row = 0;
   if (!bad_arg) {
     for (int r = warp; r < 2 * M; r += kDecWarps) {
       const int which = r / M, n = r % M;
-      if (which == 1 && first_child[n] < 0) continue;
+      if (which == 1 && sh.first_child[n] < 0) continue;
       const RowStat* st = stats + (((int64_t)b * 2 + which) * M + n) * n_chunks;
       // the row's chunk statistics, all loads in flight together
       constexpr int kItems = 16;  // n_chunks <= 512
@@ -851,11 +855,11 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
         }
         c_first = __reduce_min_sync(0xffffffffu, c_first);
         if (lane == 0)
-          rowA[which][n] = c_first < n_chunks ? c_first * chunk + unpack_index(st[c_first].pad) : 0;
+          sh.rowA[which][n] = c_first < n_chunks ? c_first * chunk + unpack_index(st[c_first].pad) : 0;
       }
       if (lane == 0) {
-        rowM[which][n] = m;
-        rowS[which][n] = s;
+        sh.rowM[which][n] = m;
+        sh.rowS[which][n] = s;
       }
       bad_row |= !(m > -INFINITY && m < INFINITY && s > 0.0 && s < INFINITY);
     }
@@ -866,16 +870,16 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
   if (!(bad_arg || bad_tok || bad_row) && tid < M) {
     // everything the sequential walk needs per node, computed in parallel
     const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
-    uacc[tid] = (double)u24(r.w[0]);
-    usmp[tid] = (double)u24(r.w[1]);
+    sh.uacc[tid] = (double)u24(r.w[0]);
+    sh.usmp[tid] = (double)u24(r.w[1]);
     if (tid >= 1 && parent == nullptr) {
       // chain: every draft's test at once.  The exponent of p(x)/q(x) is
       // formed in fp64 and split into integer and fraction, so that one fp32
       // exp2 gives the ratio to about 3e-7 relative.
       const int p = tid - 1;
-      const double et = ((double)gzt[tid] - (double)rowM[0][p]) * cs64;  // log2 unnormalised p(x)
-      const double ed = ((double)gzd[tid] - (double)rowM[1][p]) * cs64;  // log2 unnormalised q(x)
-      const float st_f = (float)rowS[0][p], sd_f = (float)rowS[1][p];
+      const double et = ((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64;  // log2 unnormalised p(x)
+      const double ed = ((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64;  // log2 unnormalised q(x)
+      const float st_f = (float)sh.rowS[0][p], sd_f = (float)sh.rowS[1][p];
       bool acc;
       if (ed == -INFINITY) {
         acc = et != -INFINITY;  // q(x) = 0: accepted iff p(x) > 0
@@ -886,17 +890,17 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
         const double ei = rint(e);
         const float ratio =
             ldexpf(fast_exp2((float)(e - ei)), (int)fmax(fmin(ei, 300.0), -300.0)) * (sd_f / st_f);
-        acc = (float)uacc[tid] < ratio;  // u < p(x) / q(x)
+        acc = (float)sh.uacc[tid] < ratio;  // u < p(x) / q(x)
       }
-      chain_rej[tid] = !acc;
+      sh.chain_rej[tid] = !acc;
       if (probe != nullptr) {
-        chain_p[tid] = exp2f((float)et) / st_f;
-        chain_q[tid] = exp2f((float)ed) / sd_f;
+        sh.chain_p[tid] = exp2f((float)et) / st_f;
+        sh.chain_q[tid] = exp2f((float)ed) / sd_f;
       }
     } else if (tid >= 1) {
       const int p = parent[(int64_t)b * M + tid];
-      px[tid] = exp2(((double)gzt[tid] - (double)rowM[0][p]) * cs64) / rowS[0][p];
-      qx[tid] = exp2(((double)gzd[tid] - (double)rowM[1][p]) * cs64) / rowS[1][p];
+      sh.px[tid] = exp2(((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64) / sh.rowS[0][p];
+      sh.qx[tid] = exp2(((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64) / sh.rowS[1][p];
     }
   }
   __syncthreads();
@@ -921,11 +925,11 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       path[(int64_t)b * M] = 0;
       for (;;) {
         int next = -1;
-        for (int c = first_child[node]; c >= 0; c = next_sib[c]) {
-          const bool acc = tok[c] == rowA[0][node];
+        for (int c = sh.first_child[node]; c >= 0; c = sh.next_sib[c]) {
+          const bool acc = sh.tok[c] == sh.rowA[0][node];
           if (probe != nullptr) {
             probe[((int64_t)b * M + c) * 4 + 0] = acc ? 1.f : 0.f;
-            probe[((int64_t)b * M + c) * 4 + 1] = tok[c] == rowA[1][node] ? 1.f : 0.f;
+            probe[((int64_t)b * M + c) * 4 + 1] = sh.tok[c] == sh.rowA[1][node] ? 1.f : 0.f;
           }
           if (acc) {
             next = c;
@@ -933,12 +937,12 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
           }
         }
         if (next < 0) break;
-        out_tokens[(int64_t)b * M + a] = tok[next];
+        out_tokens[(int64_t)b * M + a] = sh.tok[next];
         ++a;
         path[(int64_t)b * M + a] = next;
         node = next;
       }
-      out_tokens[(int64_t)b * M + a] = rowA[0][node];
+      out_tokens[(int64_t)b * M + a] = sh.rowA[0][node];
       accepted_len[b] = a;
       if (probe != nullptr) {
         probe[((int64_t)b * M + node) * 4 + 2] = 1.f;
@@ -953,45 +957,45 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     if (tid == 0) {
       int fr = M;
       for (int n = 1; n < M; ++n)
-        if (chain_rej[n]) {
+        if (sh.chain_rej[n]) {
           fr = n;
           break;
         }
-      s_child = fr;
+      sh.s_child = fr;
     }
     __syncthreads();
-    const int fr = s_child;              // first rejected node, M if none
+    const int fr = sh.s_child;              // first rejected node, M if none
     const int a = fr < M ? fr - 1 : M - 1;  // accepted drafts = the draw node
     for (int n = tid; n < M; n += kDecThreads) {
       path[(int64_t)b * M + n] = n <= a ? n : -1;
-      if (n < a) out_tokens[(int64_t)b * M + n] = tok[n + 1];
+      if (n < a) out_tokens[(int64_t)b * M + n] = sh.tok[n + 1];
       if (probe != nullptr && n >= 1 && n <= min(fr, M - 1)) {
-        probe[((int64_t)b * M + n) * 4 + 0] = chain_p[n];
-        probe[((int64_t)b * M + n) * 4 + 1] = chain_q[n];
+        probe[((int64_t)b * M + n) * 4 + 0] = sh.chain_p[n];
+        probe[((int64_t)b * M + n) * 4 + 1] = sh.chain_q[n];
       }
     }
     if (tid == 0) {
       accepted_len[b] = a;
-      ctx.mT = rowM[0][a];
-      ctx.invST = (float)(1.0 / rowS[0][a]);
-      ctx.cs = cs;
-      ctx.nrej = fr < M ? 1 : 0;
+      sh.ctx.mT = sh.rowM[0][a];
+      sh.ctx.invST = (float)(1.0 / sh.rowS[0][a]);
+      sh.ctx.cs = cs;
+      sh.ctx.nrej = fr < M ? 1 : 0;
       if (fr < M) {
-        ctx.mD = rowM[1][a];
-        ctx.invSD = (float)(1.0 / rowS[1][a]);
+        sh.ctx.mD = sh.rowM[1][a];
+        sh.ctx.invSD = (float)(1.0 / sh.rowS[1][a]);
       } else {
-        ctx.mD = 0.f;
-        ctx.invSD = 0.f;
+        sh.ctx.mD = 0.f;
+        sh.ctx.invSD = 0.f;
       }
     }
     __syncthreads();
-    const double u = usmp[a];
+    const double u = sh.usmp[a];
     if (fr < M) {
       // the residual of node a: its chunk masses need a pass over two rows,
       // spread over the whole GPU by the next kernel
       DrawState& st = draws[b];
       for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
-        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&ctx)[i];
+        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&sh.ctx)[i];
       if (tid == 0) {
         st.node = a;
         st.a = a;
@@ -1007,7 +1011,7 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       if (warp == 0) {
         float w;
         double z;
-        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, ctx, u, &w, &z);
+        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &w, &z);
         if (lane == 0) {
           out_tokens[(int64_t)b * M + a] = tk;
           if (probe != nullptr) {
@@ -1018,12 +1022,12 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       }
       return;
     }
-    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, ctx, u, &ds, &s_trel, &s_chunk, &s_z);
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &sh.ds, &sh.s_trel, &sh.s_chunk, &sh.s_z);
     if (tid == 0) {
-      out_tokens[(int64_t)b * M + a] = ds.token;
+      out_tokens[(int64_t)b * M + a] = sh.ds.token;
       if (probe != nullptr) {
         probe[((int64_t)b * M + a) * 4 + 2] = 1.0f;
-        probe[((int64_t)b * M + a) * 4 + 3] = (float)((double)ds.w / s_z);
+        probe[((int64_t)b * M + a) * 4 + 3] = (float)((double)sh.ds.w / sh.s_z);
       }
     }
     return;
@@ -1031,99 +1035,99 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
 
   // ---- the walk of a tree ------------------------------------------------
   if (tid == 0) {
-    s_node = 0;
-    s_a = 0;
+    sh.s_node = 0;
+    sh.s_a = 0;
     path[(int64_t)b * M] = 0;
   }
   for (;;) {
     __syncthreads();
-    const int node = s_node;
+    const int node = sh.s_node;
     const T* trow = target + ((int64_t)b * M + node) * V;
     const T* drow = draft + ((int64_t)b * M + node) * V;
     if (tid == 0) {
-      ctx.mT = rowM[0][node];
-      ctx.invST = (float)(1.0 / rowS[0][node]);
-      ctx.cs = cs;
-      ctx.nrej = 0;
-      if (first_child[node] >= 0) {
-        ctx.mD = rowM[1][node];
-        ctx.invSD = (float)(1.0 / rowS[1][node]);
+      sh.ctx.mT = sh.rowM[0][node];
+      sh.ctx.invST = (float)(1.0 / sh.rowS[0][node]);
+      sh.ctx.cs = cs;
+      sh.ctx.nrej = 0;
+      if (sh.first_child[node] >= 0) {
+        sh.ctx.mD = sh.rowM[1][node];
+        sh.ctx.invSD = (float)(1.0 / sh.rowS[1][node]);
       } else {
-        ctx.mD = 0.f;
-        ctx.invSD = 0.f;
+        sh.ctx.mD = 0.f;
+        sh.ctx.invSD = 0.f;
       }
-      s_child = first_child[node];
+      sh.s_child = sh.first_child[node];
     }
     __syncthreads();
     bool moved = false;
-    while (s_child >= 0) {
-      const int child = s_child;
+    while (sh.s_child >= 0) {
+      const int child = sh.s_child;
       if (tid == 0) {
         // accept test of `child` in fp64
-        const double Q = qx[child];
-        double P = px[child];
-        for (int j = 1; j <= ctx.nrej; ++j) P = fmax(P - Q, 0.0) / ctx.Z[j];
-        const double u = uacc[child];
-        s_accept = (u * Q < P);
+        const double Q = sh.qx[child];
+        double P = sh.px[child];
+        for (int j = 1; j <= sh.ctx.nrej; ++j) P = fmax(P - Q, 0.0) / sh.ctx.Z[j];
+        const double u = sh.uacc[child];
+        sh.s_accept = (u * Q < P);
         if (probe != nullptr) {
           probe[((int64_t)b * M + child) * 4 + 0] = (float)P;
           probe[((int64_t)b * M + child) * 4 + 1] = (float)Q;
         }
       }
       __syncthreads();
-      if (s_accept) {
+      if (sh.s_accept) {
         moved = true;
         break;
       }
-      if (next_sib[child] >= 0) {
+      if (sh.next_sib[child] >= 0) {
         // mass of the next residual, needed by the next sibling's test
         // (trees only: a chain node has a single child)
-        const int nrej_next = ctx.nrej + 1;
+        const int nrej_next = sh.ctx.nrej + 1;
         double acc = 0.0;
         for (int64_t e = (int64_t)tid * EPV; e < V; e += kSweep) {
           float w[EPV];
-          acc += (double)vec_weights<T, kAligned>(trow, drow, e, V, ctx, nrej_next, w);  // lim = V
+          acc += (double)vec_weights<T, kAligned>(trow, drow, e, V, sh.ctx, nrej_next, w);  // lim = V
         }
-        const double Z = block_sum(acc, red);
+        const double Z = block_sum(acc, sh.red);
         if (tid == 0) {
           if (Z > 0.0) {
-            ctx.nrej = ctx.nrej + 1;
-            ctx.invZ[ctx.nrej] = (float)(1.0 / Z);
-            ctx.Z[ctx.nrej] = Z;
+            sh.ctx.nrej = sh.ctx.nrej + 1;
+            sh.ctx.invZ[sh.ctx.nrej] = (float)(1.0 / Z);
+            sh.ctx.Z[sh.ctx.nrej] = Z;
           } else {
-            ctx.nrej = 0;  // zero-mass residual: fall back to p of the node
+            sh.ctx.nrej = 0;  // zero-mass residual: fall back to p of the node
           }
         }
       } else if (tid == 0) {
-        ctx.nrej = ctx.nrej + 1;
+        sh.ctx.nrej = sh.ctx.nrej + 1;
       }
-      if (tid == 0) s_child = next_sib[child];
+      if (tid == 0) sh.s_child = sh.next_sib[child];
       __syncthreads();
     }
     if (moved) {
       if (tid == 0) {
-        const int child = s_child;
-        const int a = s_a + 1;
-        s_a = a;
+        const int child = sh.s_child;
+        const int a = sh.s_a + 1;
+        sh.s_a = a;
         path[(int64_t)b * M + a] = child;
-        out_tokens[(int64_t)b * M + a - 1] = tok[child];
-        s_node = child;
+        out_tokens[(int64_t)b * M + a - 1] = sh.tok[child];
+        sh.s_node = child;
       }
       continue;
     }
 
     // ---- the draw at `node` ----------------------------------------------
-    const double u = usmp[node];
-    if (tid == 0) accepted_len[b] = s_a;
-    if (ctx.nrej > 0) {
+    const double u = sh.usmp[node];
+    if (tid == 0) accepted_len[b] = sh.s_a;
+    if (sh.ctx.nrej > 0) {
       // residual: its chunk masses need a pass over two rows, spread over
       // the whole GPU by the next kernel
       DrawState& st = draws[b];
       for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
-        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&ctx)[i];
+        reinterpret_cast<uint32_t*>(&st.c)[i] = reinterpret_cast<const uint32_t*>(&sh.ctx)[i];
       if (tid == 0) {
         st.node = node;
-        st.a = s_a;
+        st.a = sh.s_a;
         st.u = u;
         st.pending = 1;
       }
@@ -1134,9 +1138,9 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       if (warp == 0) {
         float w;
         double z;
-        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, ctx, u, &w, &z);
+        const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &w, &z);
         if (lane == 0) {
-          out_tokens[(int64_t)b * M + s_a] = tk;
+          out_tokens[(int64_t)b * M + sh.s_a] = tk;
           if (probe != nullptr) {
             probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
             probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / z);
@@ -1145,16 +1149,34 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
       }
       return;
     }
-    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, ctx, u, &ds, &s_trel, &s_chunk, &s_z);
+    draw_from_p<T, kAligned>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &sh.ds, &sh.s_trel, &sh.s_chunk, &sh.s_z);
     if (tid == 0) {
-      out_tokens[(int64_t)b * M + s_a] = ds.token;
+      out_tokens[(int64_t)b * M + sh.s_a] = sh.ds.token;
       if (probe != nullptr) {
         probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
-        probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)ds.w / s_z);
+        probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)sh.ds.w / sh.s_z);
       }
     }
     return;
   }
+}
+
+template <typename T, bool kAligned>
+__global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
+    const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
+    uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
+    int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
+    int chunk, const RowStat* stats, DrawState* __restrict__ draws, uint32_t* status) {
+  __shared__ DecideSmem sh;
+  pdl_trigger();
+  pdl_wait();  // the statistics come from the previous kernel
+  // A wait of the statistics kernel that gave up left some statistics
+  // unwritten: then no request of the call is decided on them.
+  const bool stats_lost = (ld_volatile_u32(status) >> SPEC_ERR_TIMEOUT) & 1u;
+  decide_request<T, kAligned>(target, draft, tokens, parent, temperature, seed, offset, b_base,
+                              out_tokens, path, accepted_len, probe, d, n_chunks, chunk, stats,
+                              draws, status, blockIdx.x, stats_lost, sh);
 }
 
 // Passes 3 and 4: the residual draws.
@@ -1296,6 +1318,347 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// One kernel, two roles: the logit stream on most SMs, the decisions on the
+// others, at the same time.
+//
+// Stream CTAs (blockIdx < n_stream) claim batches of statistics tasks from a
+// global counter, in request-major order (request b's rows, chunks fastest),
+// copy each task's 4 KB chunk into a ring of shared-memory slots with 1-D
+// bulk copies (one issuing lane), and reduce it on 15 consumer warps, as
+// rs_rowstats_bulk_kernel does; after each chunk's statistics are written
+// the count of finished tasks of its request goes up (a release).  They
+// never wait on the deciders, so the stream runs at the rate of HBM.
+//
+// Decider CTAs take requests in order from a second counter, wait until the
+// request's count is complete (acquire; the stream reaches requests in order,
+// so this is soon), and run the decisions of rs_decide_kernel; a draw from a
+// residual is finished in the same CTA: the residual's mass over every
+// statistics chunk of the node's two rows (re-read while still in L2, all
+// warps, several chunks in flight), the chunk picked by the masses, and the
+// element found inside it.  Only the last requests' decisions come after the
+// stream ends.
+// ---------------------------------------------------------------------------
+constexpr int kOvWarps = 16;      // per CTA: stream = producer warp + 15 consumers
+constexpr int kOvConsumers = kOvWarps - 1;
+constexpr int kOvSlots = 48;      // 4 KB ring slots of a stream CTA
+constexpr int kOvBatch = 32;      // tasks per claim
+constexpr int kOvMaxDeciders = 24;
+constexpr size_t kOvSmem = (size_t)kOvSlots * kBulkSlot + 1024;
+static_assert(kOvWarps * kWarp == kDecThreads, "a decider CTA is a decide CTA");
+
+struct OvTask {
+  int b, which, n, c;
+  float cs;
+  int greedy, stop, pad;
+};
+
+// ctl: [0] next task batch, [1] next request to decide, [2] CTAs finished,
+// [3] the call failed (a wait gave up)
+template <typename T>
+__global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
+    const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
+    uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
+    int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
+    int chunk, RowStat* stats, DrawState* draws, double* zsum, uint32_t* ctl, uint32_t* req_done,
+    int n_stream, uint32_t* status) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int kChunk = kWarp * kStatVecs * EPV;
+  __shared__ DecideSmem sh;
+  __shared__ OvTask desc[kOvSlots];
+  __shared__ uint64_t full[kOvSlots], empty[kOvSlots];
+  __shared__ int s_abort, s_req;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  const int B = d.B, M = d.M, V = d.V;
+  const uint64_t wait = wait_limit_cycles(d);
+  volatile int* abort = &s_abort;
+  const int rows = parent == nullptr ? 2 * M - 1 : 2 * M;  // rows numbered per request
+  const int64_t per_req = (int64_t)rows * n_chunks;
+  const int64_t ntask = per_req * B;
+  volatile uint32_t* failed = ctl + 3;
+
+  if (tid == 0) {
+    for (int i = 0; i < kOvSlots; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty[i]), 1);
+    }
+    s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
+
+  if ((int)blockIdx.x < n_stream) {
+    // ================================================================ stream
+    if (warp == 0) {
+      // producer: the whole warp walks the tasks, lane 0 issues the copies
+      int64_t task = 0;  // tasks issued by this CTA
+      bool ok = true;
+      int cur_b = -1;
+      unsigned long long kids = 0;  // nodes of request cur_b that have children
+      float cur_cs = 1.f;
+      int cur_greedy = 0;
+      uint32_t next = 0;
+      if (lane == 0) next = atomicAdd(ctl + 0, 1u);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      while (ok) {
+        const int64_t t0 = (int64_t)next * kOvBatch;
+        if (t0 >= ntask) break;
+        // claim the next batch now: its index is needed only after this one
+        uint32_t after = 0;
+        if (lane == 0) after = atomicAdd(ctl + 0, 1u);
+        const int64_t t1 = t0 + kOvBatch < ntask ? t0 + kOvBatch : ntask;
+        for (int64_t t = t0; t < t1 && ok; ++t) {
+          const int b = (int)(t / per_req);
+          const int rem = (int)(t - (int64_t)b * per_req);
+          const int row = rem / n_chunks, c = rem - row * n_chunks;
+          const int which = row < M ? 0 : 1, n = row < M ? row : row - M;
+          if (b != cur_b) {
+            cur_b = b;
+            const float temp = temperature[b];
+            cur_cs = stat_scale(temp);
+            cur_greedy = temp == 0.f;
+            kids = 0;
+            if (parent != nullptr) {
+              // bit n: some node names n as its parent (its draft row is read)
+              const int32_t* pr = parent + (int64_t)b * M;
+              unsigned lo = 0, hi = 0;
+              for (int k = 1 + lane; k < M; k += kWarp) {
+                const int pn = pr[k];
+                if (pn >= 0 && pn < 32) lo |= 1u << pn;
+                else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
+              }
+              lo = __reduce_or_sync(0xffffffffu, lo);
+              hi = __reduce_or_sync(0xffffffffu, hi);
+              kids = ((unsigned long long)hi << 32) | lo;
+            }
+          }
+          if (which == 1 && parent != nullptr && !((kids >> n) & 1ull)) continue;  // a leaf's draft row
+          const int slot = (int)(task % kOvSlots);
+          if (lane == 0) {
+            if (task >= kOvSlots &&
+                !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
+                                abort, wait))
+              ok = false;
+            if (ok) {
+              desc[slot] = OvTask{b, which, n, c, cur_cs, cur_greedy, 0, 0};
+              const int64_t e0 = (int64_t)c * kChunk;
+              const int64_t left = (int64_t)V - e0;
+              const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
+              const uint32_t fb = ptx::smem_u32(&full[slot]);
+              ptx::mbar_arrive_expect_tx(fb, bytes);
+              ptx::bulk_g2s(ptx::smem_u32(ring + (size_t)slot * kBulkSlot),
+                            (which == 0 ? target : draft) + ((int64_t)b * M + n) * V + e0, bytes, fb);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++task;
+        }
+        next = __shfl_sync(0xffffffffu, after, 0);
+      }
+      // one stop task per consumer warp
+      for (int w = 0; w < kOvConsumers && ok; ++w) {
+        const int slot = (int)(task % kOvSlots);
+        if (lane == 0) {
+          if (task >= kOvSlots &&
+              !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
+                              abort, wait))
+            ok = false;
+          if (ok) {
+            desc[slot].stop = 1;
+            ptx::mbar_arrive(ptx::smem_u32(&full[slot]));
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++task;
+      }
+      // every copy issued lands before the CTA may exit
+      if (lane == 0)
+        for (int64_t u = task > kOvSlots ? task - kOvSlots : 0; u < task; ++u)
+          ptx::mbar_drain(ptx::smem_u32(&full[u % kOvSlots]), (uint32_t)((u / kOvSlots) & 1),
+                          kDefaultWaitCycles);
+    } else {
+      // consumers: task t on warp 1 + t mod 15
+      for (int64_t t = warp - 1;; t += kOvConsumers) {
+        const int slot = (int)(t % kOvSlots);
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&full[slot]),
+                                                    (uint32_t)((t / kOvSlots) & 1), abort, wait)))
+          break;
+        const OvTask k = desc[slot];
+        if (k.stop) break;
+        const int e0 = k.c * kChunk;
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kBulkSlot);
+        uint4 raw[kStatVecs];
+#pragma unroll
+        for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
+        float sd;
+        const float m = chunk_stat<T>(raw, V - e0, k.cs, &sd);
+        const int am = k.greedy ? chunk_argmax<T>(raw, V - e0, m) : 0;
+        __syncwarp();
+        if (lane == 0) {
+          RowStat r;
+          r.m = m;
+          r.pad = pack_index(am);
+          r.s = (double)sd;
+          stats[(((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks + k.c] = r;
+          // the request's count of finished tasks, released after the write
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(req_done + k.b) : "memory");
+          ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort) {
+      *failed = 1u;
+      raise_status(status, SPEC_ERR_TIMEOUT);
+    }
+  } else {
+    // =============================================================== deciders
+    for (;;) {
+      if (tid == 0) s_req = (int)atomicAdd(ctl + 1, 1u);
+      __syncthreads();
+      const int b = s_req;
+      __syncthreads();
+      if (b >= B) break;
+      // tasks of request b: its target rows and the draft rows it reads
+      int nrows = parent == nullptr ? 2 * M - 1 : M;
+      if (parent != nullptr) {
+        // nodes named as a parent read their draft rows (warps 0 and 1
+        // cover nodes 1..63; each sets the bits of the parents it sees)
+        unsigned lo = 0, hi = 0;
+        if (tid >= 1 && tid < M) {
+          const int pn = parent[(int64_t)b * M + tid];
+          if (pn >= 0 && pn < 32) lo = 1u << pn;
+          else if (pn >= 32 && pn < 64) hi = 1u << (pn - 32);
+        }
+        if (warp < 2) {
+          lo = __reduce_or_sync(0xffffffffu, lo);
+          hi = __reduce_or_sync(0xffffffffu, hi);
+          if (lane == 0) {
+            sh.chain_rej[2 * warp] = (int)lo;
+            sh.chain_rej[2 * warp + 1] = (int)hi;
+          }
+        }
+        __syncthreads();
+        const unsigned long long kd =
+            ((unsigned long long)((unsigned)sh.chain_rej[1] | (unsigned)sh.chain_rej[3]) << 32) |
+            ((unsigned)sh.chain_rej[0] | (unsigned)sh.chain_rej[2]);
+        nrows += __popcll(kd);
+        __syncthreads();
+      }
+      const uint32_t target_count = (uint32_t)((int64_t)nrows * n_chunks);
+      // wait for the stream to finish request b (bounded; a failed call stops it)
+      if (tid == 0) {
+        long long t0 = 0;
+        bool lost = false;
+        for (uint32_t it = 0;; ++it) {
+          uint32_t v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(req_done + b) : "memory");
+          if (v >= target_count) break;
+          if (*failed) {
+            lost = true;
+            break;
+          }
+          if ((it & 15u) == 15u) {
+            const long long now = clock64();
+            if (t0 == 0) {
+              t0 = now;
+            } else if ((uint64_t)(now - t0) > wait) {
+              lost = true;
+              *failed = 1u;
+              raise_status(status, SPEC_ERR_TIMEOUT);
+              break;
+            }
+          }
+          __nanosleep(128);
+        }
+        s_abort = lost;
+      }
+      __syncthreads();
+      const bool lost = s_abort != 0;
+      __syncthreads();
+      decide_request<T, true>(target, draft, tokens, parent, temperature, seed, offset, b_base,
+                              out_tokens, path, accepted_len, probe, d, n_chunks, chunk, stats,
+                              draws, status, b, lost, sh);
+      __syncthreads();
+      // a draw from a residual: the chunk masses (every warp, its chunks),
+      // then the chunk and the element, as rs_residual_sums_kernel and
+      // rs_residual_draw_kernel do
+      const DrawState* dsb = draws + b;
+      if (!lost && dsb->pending) {
+        const int node = dsb->node, a_acc = dsb->a;
+        const double u = dsb->u;
+        for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
+          reinterpret_cast<uint32_t*>(&sh.ctx)[i] = reinterpret_cast<const uint32_t*>(&dsb->c)[i];
+        __syncthreads();
+        const T* trow = target + ((int64_t)b * M + node) * V;
+        const T* drow = draft + ((int64_t)b * M + node) * V;
+        double* zs = zsum + (int64_t)b * n_chunks;
+        for (int c = warp; c < n_chunks; c += kOvWarps) {
+          uint4 rt[kStatVecs], rd[kStatVecs];
+          const float ls = lane_weights<T>(trow, drow, (int64_t)c * kChunk, V, sh.ctx, sh.ctx.nrej, rt, rd);
+          const dfloat tot = df_warp_sum(df_make(ls));
+          if (lane == 0) zs[c] = df_to_d(tot);
+        }
+        __syncthreads();
+        if (warp == 0) {
+          double Z = 0.0;
+          for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
+          Z = warp_sum(Z);
+          if (Z > 0.0) {
+            double pre;
+            const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
+            const double trel = u * Z - pre;
+            const float th = (float)trel;
+            float w;
+            const int tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, sh.ctx,
+                                              sh.ctx.nrej, dfloat{th, (float)(trel - (double)th)}, &w);
+            if (lane == 0) {
+              out_tokens[(int64_t)b * M + a_acc] = tk;
+              if (probe != nullptr) {
+                probe[((int64_t)b * M + node) * 4 + 2] = (float)Z;
+                probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / Z);
+              }
+            }
+          } else {
+            // a residual of zero mass: the draw from p of the node
+            const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
+            float w;
+            double z;
+            const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &w, &z);
+            if (lane == 0) {
+              out_tokens[(int64_t)b * M + a_acc] = tk;
+              if (probe != nullptr) {
+                probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
+                probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / z);
+              }
+            }
+          }
+        }
+      }
+      if (tid == 0) req_done[b] = 0u;  // ready for the next call
+      __syncthreads();
+    }
+  }
+
+  // the last CTA out puts the counters back for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(ctl + 2, 1u) == gridDim.x - 1) {
+      *reinterpret_cast<volatile uint32_t*>(ctl + 0) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(ctl + 1) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(ctl + 3) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(ctl + 2) = 0u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host launcher
 // ---------------------------------------------------------------------------
 template <typename T, bool kAligned>
@@ -1362,18 +1725,50 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_overlap_t(const RsArgs& a, const WsLayout& lay, cudaStream_t st,
+                                    int* launches) {
+  const spec_dims& d = a.d;
+  char* ws = static_cast<char*>(a.ws);
+  int dev = 0, sms = 148;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // deciders: enough to keep up with the stream's requests, at most one per
+  // request; every other SM streams
+  const int n_dec = d.B < kOvMaxDeciders ? d.B : kOvMaxDeciders;
+  const int n_stream = sms - n_dec > 1 ? sms - n_dec : 1;
+  e = cudaFuncSetAttribute(rs_overlap_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kOvSmem);
+  if (e != cudaSuccess) return e;
+  PdlLaunch L(dim3(n_stream + n_dec), dim3(kDecThreads), kOvSmem, st);
+  e = cudaLaunchKernelEx(&L.cfg, rs_overlap_kernel<T>, static_cast<const T*>(a.target),
+                         static_cast<const T*>(a.draft), a.tokens, a.parent, a.temperature, a.seed,
+                         a.offset, a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d,
+                         lay.rs_chunks, lay.rs_chunk, reinterpret_cast<RowStat*>(ws + lay.rs_off),
+                         reinterpret_cast<DrawState*>(ws + lay.rs_draw_off),
+                         reinterpret_cast<double*>(ws + lay.rs_zsum_off),
+                         reinterpret_cast<uint32_t*>(ws + lay.rsf_ctl_off),
+                         reinterpret_cast<uint32_t*>(ws + lay.rsf_req_off), n_stream,
+                         reinterpret_cast<uint32_t*>(ws + lay.status_off));
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  return cudaGetLastError();
+}
+
+bool rso_supported(const spec_dims& d, bool aligned) { return aligned && d.M <= kMaxM; }
+
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
   const int esz = a.d.logits_dtype == SPEC_BF16 ? 2 : 4;
   const bool aligned = ((size_t)a.d.V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0;
-  const bool fused_ok = rsf_supported(a.d, aligned);
-  if (a.d.reject_impl == SPEC_REJECT_FUSED) {
+  const bool fused_ok = rso_supported(a.d, aligned);
+  if (a.d.reject_impl == SPEC_REJECT_FUSED || (a.d.reject_impl == SPEC_REJECT_AUTO && fused_ok)) {
     if (!fused_ok) return cudaErrorNotSupported;
-    return rsf_launch(a, lay, st, launches);
+    return a.d.logits_dtype == SPEC_BF16 ? launch_overlap_t<__nv_bfloat16>(a, lay, st, launches)
+                                         : launch_overlap_t<float>(a, lay, st, launches);
   }
-  if (a.d.reject_impl == SPEC_REJECT_AUTO && rsf_preferred(a.d, aligned))
-    return rsf_launch(a, lay, st, launches);
   if (a.d.logits_dtype == SPEC_BF16)
     return aligned ? launch_rs_t<__nv_bfloat16, true>(a, lay, st, launches)
                    : launch_rs_t<__nv_bfloat16, false>(a, lay, st, launches);

@@ -56,9 +56,8 @@ int rs_max_vocab(int logits_dtype);
 // Returns cudaErrorNotSupported when the fused path is asked for and the
 // shape does not allow it.
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
-int rsf_max_vocab(int logits_dtype);
-bool rsf_supported(const spec_dims& d, bool aligned);
-bool rsf_preferred(const spec_dims& d, bool aligned);
-cudaError_t rsf_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
+// The fused kernel (statistics stream and decisions in one launch) takes
+// 16-byte aligned rows.
+bool rso_supported(const spec_dims& d, bool aligned);
 
 }  // namespace specv

@@ -125,31 +125,26 @@ extern "C" spec_status spec_reject_sample_noalloc(
   const bool aligned = ((size_t)dims->V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(target_logits) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(draft_logits) % 16) == 0;
-  const bool fused = dims->reject_impl == SPEC_REJECT_FUSED ? rsf_supported(*dims, aligned)
-                     : dims->reject_impl == SPEC_REJECT_AUTO  ? rsf_preferred(*dims, aligned)
-                                                              : false;
+  const bool fused = dims->reject_impl != SPEC_REJECT_STAGED && rso_supported(*dims, aligned);
   if (dims->reject_impl == SPEC_REJECT_FUSED && !fused) return SPEC_ERR_UNSUPPORTED;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  // status, the chunk statistics, the draw states, the residual chunk
+  // masses; for the fused kernel also its four counters and the finished
+  // tasks of each request
   WsLayout lay;
   memset(&lay, 0, sizeof(lay));
   lay.status_off = 0;
   lay.rs_chunk = rs_chunk_elems(dims->logits_dtype);
   lay.rs_chunks = (int)ceil_div64(dims->V, lay.rs_chunk);
+  lay.rs_off = kNoAllocStatusBytes;
+  lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
+  lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
+  lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
+  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
   if (fused) {
-    // status, then the fused kernel's counters (item counter, CTAs done,
-    // epoch tag), items finished per request, one record per (request, node)
-    lay.rsf_ctl_off = kNoAllocStatusBytes;
+    lay.rsf_ctl_off = up(lay.total);
     lay.rsf_req_off = up(lay.rsf_ctl_off + 16);
-    lay.rsf_rec_off = up(lay.rsf_req_off + sizeof(uint32_t) * (size_t)dims->B);
-    lay.total = lay.rsf_rec_off + 32 * (size_t)dims->B * dims->M;
-  } else {
-    // status, then the chunk statistics, the draw states and the residual
-    // chunk masses
-    lay.rs_off = kNoAllocStatusBytes;
-    lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
-    lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
-    lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
-    lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
+    lay.total = lay.rsf_req_off + sizeof(uint32_t) * (size_t)dims->B;
   }
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
@@ -158,14 +153,11 @@ extern "C" spec_status spec_reject_sample_noalloc(
   if (s != SPEC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status word and the counters start each call at zero, whatever an
-  // earlier call (one whose wait gave up, say) left there: the status area,
-  // the fused kernel's item counter and CTA count (not its epoch tag, which
-  // tells its records of one call from the last's), and its per-request
-  // counts.  Everything else read is written earlier in the same call.
+  // earlier call (one whose wait gave up, say) left there.  Everything else
+  // read is written earlier in the same call.
   char* sb = static_cast<char*>(scratch);
-  if (cudaMemsetAsync(sb, 0, fused ? lay.rsf_ctl_off + 8 : kNoAllocStatusBytes, st) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  if (fused && cudaMemsetAsync(sb + lay.rsf_req_off, 0, sizeof(uint32_t) * (size_t)dims->B, st) !=
+  if (cudaMemsetAsync(sb, 0, kNoAllocStatusBytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (fused && cudaMemsetAsync(sb + lay.rsf_ctl_off, 0, lay.total - lay.rsf_ctl_off, st) !=
                    cudaSuccess)
     return SPEC_ERR_CUDA;
 

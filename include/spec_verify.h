@@ -281,6 +281,86 @@ spec_status spec_reject_sample_noalloc(const void* target_logits,
                                        int32_t* accepted_len, float* probe,
                                        const spec_dims* dims, void* stream);
 
+/*
+ * Host-side controller and metrics (no GPU work; plain host memory).
+ *
+ * Page 3 ("推测解码的工程真相 2026"), dynamic scheduling and observability:
+ * the acceptance rate of a request's last `window` verify steps sets its
+ * next draft length (above high_acceptance: gamma_high; from
+ * low_acceptance to high_acceptance: gamma_mid; below: gamma_low); a
+ * temperature above hot_temperature sets gamma_hot at once; a request whose
+ * speculation does not pay over a full window falls back to plain decoding
+ * (gamma 0) and stays there.  Page 2 §5.1: log drafted and accepted counts
+ * and where the rejections fall.
+ *
+ * Speculative efficiency is read as page 2 §2.3's speedup of a verify step:
+ * emitted tokens per step (accepted + 1) / (1 + gamma * draft_cost); a
+ * request below min_efficiency falls back.  Requests the device failed
+ * (accepted_len = -1, e.g. SPEC_ERR_CAPACITY, the pages' fallback trigger)
+ * fall back too.
+ */
+#define SPEC_CTRL_MAX_WINDOW 64
+#define SPEC_CTRL_HIST_BINS 10
+#define SPEC_STEP_MAX_POS 65
+
+typedef struct spec_ctrl_config {
+  int32_t window;          /* steps the acceptance rate is taken over (<= 64); 16 */
+  float high_acceptance;   /* 0.6 */
+  float low_acceptance;    /* 0.3 */
+  int32_t gamma_high;      /* 8 */
+  int32_t gamma_mid;       /* 4 */
+  int32_t gamma_low;       /* 2 */
+  float hot_temperature;   /* 0.8 */
+  int32_t gamma_hot;       /* 1 */
+  float draft_cost;        /* draft forward / target forward, 0.02 */
+  float min_efficiency;    /* 1.0 */
+  int32_t max_gamma;       /* cap on any draft length (<= 63) */
+} spec_ctrl_config;
+
+/* Per-request state, caller-owned (zeroed by spec_ctrl_init). */
+typedef struct spec_ctrl_request {
+  int16_t drafted[SPEC_CTRL_MAX_WINDOW];  /* ring of the last steps */
+  int16_t accepted[SPEC_CTRL_MAX_WINDOW];
+  int32_t head, steps;
+  int32_t gamma;           /* draft length of the next step; 0 = plain decoding */
+  int32_t fallback;        /* 1 once the request fell back */
+  int32_t failed_steps;
+} spec_ctrl_request;
+
+typedef struct spec_ctrl_metrics_out {
+  int32_t requests;
+  int32_t acceptance_hist[SPEC_CTRL_HIST_BINS]; /* per-request window rates, 0.1-wide bins */
+  float acceptance_mean, acceptance_p50, acceptance_p95, acceptance_p99;
+  float emitted_per_step;
+  float speculative_efficiency;
+  float fallback_rate;
+} spec_ctrl_metrics_out;
+
+typedef struct spec_step_stats_out {
+  int32_t requests, failed;
+  int64_t accepted, emitted;
+  int32_t rejection_pos[SPEC_STEP_MAX_POS];  /* 1-based draft position of the first
+                                                rejection; index M: none rejected */
+  float tree_width_effective;  /* mean share of the tree's root-to-leaf paths through
+                                  the first accepted node (-1 for chains) */
+} spec_step_stats_out;
+
+void spec_ctrl_default_config(spec_ctrl_config* cfg);
+spec_status spec_ctrl_init(spec_ctrl_request* reqs, int32_t n, int32_t gamma0);
+/* Feed one verify step's accepted lengths (host copy of spec_reject_sample's
+ * output; temperature may be NULL) and get each request's next draft length. */
+spec_status spec_ctrl_update(const spec_ctrl_config* cfg, spec_ctrl_request* reqs, int32_t n,
+                             const int32_t* accepted_len, const float* temperature,
+                             int32_t* next_gamma);
+spec_status spec_ctrl_metrics(const spec_ctrl_config* cfg, const spec_ctrl_request* reqs,
+                              int32_t n, spec_ctrl_metrics_out* out);
+/* Statistics of one verify step from host copies of its outputs: accepted
+ * and emitted counts, the rejection-position histogram, and, for a tree
+ * (parent != NULL), the tree width effective. */
+spec_status spec_step_stats(const int32_t* accepted_len, const int32_t* path,
+                            const int32_t* parent, int32_t B, int32_t M,
+                            spec_step_stats_out* out);
+
 /* Host-side Philox4x64-10 block (the generator the kernels use), for
  * known-answer tests: out = Philox4x64-10(counter, key). */
 void spec_philox_block(const uint64_t key[2], const uint64_t counter[4],

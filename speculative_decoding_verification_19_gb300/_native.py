@@ -30,6 +30,8 @@ EXPORTS = (
     "spec_workspace_size", "spec_workspace_init", "spec_get_device_status",
     "spec_verify_attn", "spec_reject_sample", "kv_commit", "spec_philox_block",
     "spec_status_string", "spec_last_launch_count", "spec_reject_sample_noalloc",
+    "spec_ctrl_default_config", "spec_ctrl_init", "spec_ctrl_update", "spec_ctrl_metrics",
+    "spec_step_stats",
 )
 
 

@@ -1412,10 +1412,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
         uint32_t after = 0;
         if (lane == 0) after = atomicAdd(ctl + 0, 1u);
         const int64_t t1 = t0 + kOvBatch < ntask ? t0 + kOvBatch : ntask;
+        // the batch's first task decoded once, then walked (chunks fastest)
+        int b = (int)(t0 / per_req);
+        const int rem0 = (int)(t0 - (int64_t)b * per_req);
+        int row = rem0 / n_chunks, c = rem0 - row * n_chunks;
         for (int64_t t = t0; t < t1 && ok; ++t) {
-          const int b = (int)(t / per_req);
-          const int rem = (int)(t - (int64_t)b * per_req);
-          const int row = rem / n_chunks, c = rem - row * n_chunks;
+          if (t > t0 && ++c == n_chunks) {
+            c = 0;
+            if (++row == rows) {
+              row = 0;
+              ++b;
+            }
+          }
           const int which = row < M ? 0 : 1, n = row < M ? row : row - M;
           if (b != cur_b) {
             cur_b = b;

@@ -1340,17 +1340,52 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kOvWarps = 16;      // per CTA: stream = producer warp + 15 consumers
 constexpr int kOvConsumers = kOvWarps - 1;
-constexpr int kOvSlots = 48;      // 4 KB ring slots of a stream CTA
+constexpr int kOvSlots = 44;      // 4 KB ring slots (a decider pairs them: 22 of 8 KB)
+constexpr int kOvPairs = kOvSlots / 2;
 constexpr int kOvBatch = 32;      // tasks per claim
+constexpr int kOvGroups = 16;     // completion groups in flight per stream CTA
+constexpr int kOvMaxMeta = 2048;  // requests whose temperature and tree masks sit in shared memory
 constexpr int kOvMaxDeciders = 24;
-constexpr size_t kOvSmem = (size_t)kOvSlots * kBulkSlot + 1024;
+constexpr size_t kOvRingBytes = (size_t)kOvSlots * kBulkSlot;
+constexpr size_t kOvSmem = kOvRingBytes + kOvMaxMeta * (sizeof(float) + sizeof(uint64_t)) + 1024;
 static_assert(kOvWarps * kWarp == kDecThreads, "a decider CTA is a decide CTA");
+constexpr int kGroupOpen = 1 << 30;  // a group's count before its producer closes it
 
 struct OvTask {
   int b, which, n, c;
   float cs;
-  int greedy, stop, pad;
+  int greedy, stop, grp;
 };
+
+// Consecutive statistics tasks of one request on one stream CTA: the count
+// of finished tasks is published for the whole group at once (one fence and
+// one atomic), not per task.
+struct OvGroup {
+  int b, total;
+  int remaining;  // kGroupOpen - tasks finished - (kGroupOpen - total) once closed
+  int free;
+};
+
+// Weights of the residual law over one chunk held in shared memory (target
+// and draft chunks side by side), by one warp: lane l takes vectors v * 32 + l.
+template <typename T>
+__device__ __forceinline__ float smem_chunk_mass(const uint4* st, const uint4* sd, int e0, int V,
+                                                 const DecideCtx& c, int nrej) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int lane = threadIdx.x % kWarp;
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < kStatVecs; ++v) {
+    const int e = e0 + (v * kWarp + lane) * EPV;
+    if (e >= V) continue;
+    float zt[EPV], zd[EPV];
+    unpack16(st[v * kWarp + lane], zt);
+    unpack16(sd[v * kWarp + lane], zd);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) s += (e + i < V) ? weight_of(zt[i], zd[i], c, nrej) : 0.f;
+  }
+  return s;
+}
 
 // ctl: [0] next task batch, [1] next request to decide, [2] CTAs finished,
 // [3] the call failed (a wait gave up)
@@ -1366,11 +1401,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
   constexpr int kChunk = kWarp * kStatVecs * EPV;
   __shared__ DecideSmem sh;
   __shared__ OvTask desc[kOvSlots];
+  __shared__ OvGroup grp[kOvGroups];
   __shared__ uint64_t full[kOvSlots], empty[kOvSlots];
   __shared__ int s_abort, s_req;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  float* s_temp = reinterpret_cast<float*>(ring + kOvRingBytes);
+  unsigned long long* s_kids = reinterpret_cast<unsigned long long*>(s_temp + kOvMaxMeta);
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int B = d.B, M = d.M, V = d.V;
   const uint64_t wait = wait_limit_cycles(d);
@@ -1379,6 +1417,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
   const int64_t per_req = (int64_t)rows * n_chunks;
   const int64_t ntask = per_req * B;
   volatile uint32_t* failed = ctl + 3;
+  const bool meta_in_smem = B <= kOvMaxMeta;
 
   if (tid == 0) {
     for (int i = 0; i < kOvSlots; ++i) {
@@ -1388,20 +1427,55 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
     s_abort = 0;
     ptx::fence_mbar_init();
   }
+  for (int g = tid; g < kOvGroups; g += kDecThreads) grp[g].free = 1;
   __syncthreads();
   pdl_trigger();
   pdl_wait();  // the logits may come from the previous kernel
 
   if ((int)blockIdx.x < n_stream) {
     // ================================================================ stream
+    // the requests' temperatures and tree masks, once, before any copy is
+    // queued (a plain load behind queued bulk copies waits for all of them)
+    if (meta_in_smem) {
+      for (int i = tid; i < B; i += kDecThreads) s_temp[i] = temperature[i];
+      if (parent != nullptr)
+        for (int i = warp; i < B; i += kOvWarps) {
+          const int32_t* pr = parent + (int64_t)i * M;
+          unsigned lo = 0, hi = 0;
+          for (int k = 1 + lane; k < M; k += kWarp) {
+            const int pn = pr[k];
+            if (pn >= 0 && pn < 32) lo |= 1u << pn;
+            else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
+          }
+          lo = __reduce_or_sync(0xffffffffu, lo);
+          hi = __reduce_or_sync(0xffffffffu, hi);
+          if (lane == 0) s_kids[i] = ((unsigned long long)hi << 32) | lo;
+        }
+    }
+    __syncthreads();
     if (warp == 0) {
       // producer: the whole warp walks the tasks, lane 0 issues the copies
       int64_t task = 0;  // tasks issued by this CTA
+      int ngrp = 0;      // groups opened by this CTA
+      int g_open = -1, g_count = 0;
       bool ok = true;
       int cur_b = -1;
       unsigned long long kids = 0;  // nodes of request cur_b that have children
       float cur_cs = 1.f;
       int cur_greedy = 0;
+      auto close_group = [&]() {  // lane 0
+        if (g_open >= 0) {
+          grp[g_open].total = g_count;
+          __threadfence_block();
+          if (atomicSub(&grp[g_open].remaining, kGroupOpen - g_count) == kGroupOpen - g_count) {
+            // every task already finished: publish here
+            __threadfence();
+            atomicAdd(req_done + grp[g_open].b, (uint32_t)g_count);
+            *reinterpret_cast<volatile int*>(&grp[g_open].free) = 1;
+          }
+          g_open = -1;
+        }
+      };
       uint32_t next = 0;
       if (lane == 0) next = atomicAdd(ctl + 0, 1u);
       next = __shfl_sync(0xffffffffu, next, 0);
@@ -1427,33 +1501,63 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
           const int which = row < M ? 0 : 1, n = row < M ? row : row - M;
           if (b != cur_b) {
             cur_b = b;
-            const float temp = temperature[b];
+            float temp;
+            if (meta_in_smem) {
+              temp = s_temp[b];
+              kids = parent != nullptr ? s_kids[b] : 0;
+            } else {
+              temp = temperature[b];
+              kids = 0;
+              if (parent != nullptr) {
+                const int32_t* pr = parent + (int64_t)b * M;
+                unsigned lo = 0, hi = 0;
+                for (int k = 1 + lane; k < M; k += kWarp) {
+                  const int pn = pr[k];
+                  if (pn >= 0 && pn < 32) lo |= 1u << pn;
+                  else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
+                }
+                lo = __reduce_or_sync(0xffffffffu, lo);
+                hi = __reduce_or_sync(0xffffffffu, hi);
+                kids = ((unsigned long long)hi << 32) | lo;
+              }
+            }
             cur_cs = stat_scale(temp);
             cur_greedy = temp == 0.f;
-            kids = 0;
-            if (parent != nullptr) {
-              // bit n: some node names n as its parent (its draft row is read)
-              const int32_t* pr = parent + (int64_t)b * M;
-              unsigned lo = 0, hi = 0;
-              for (int k = 1 + lane; k < M; k += kWarp) {
-                const int pn = pr[k];
-                if (pn >= 0 && pn < 32) lo |= 1u << pn;
-                else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
-              }
-              lo = __reduce_or_sync(0xffffffffu, lo);
-              hi = __reduce_or_sync(0xffffffffu, hi);
-              kids = ((unsigned long long)hi << 32) | lo;
-            }
           }
           if (which == 1 && parent != nullptr && !((kids >> n) & 1ull)) continue;  // a leaf's draft row
           const int slot = (int)(task % kOvSlots);
           if (lane == 0) {
-            if (task >= kOvSlots &&
+            // a new group at the batch's first task and at every new request
+            if (g_open < 0 || grp[g_open].b != b || t == t0) {
+              close_group();
+              const int g = ngrp % kOvGroups;
+              long long w0 = 0;
+              while (!*reinterpret_cast<volatile int*>(&grp[g].free)) {  // bounded
+                const long long now = clock64();
+                if (w0 == 0) w0 = now;
+                else if ((uint64_t)(now - w0) > wait || *abort) {
+                  *abort = 1;
+                  ok = false;
+                  break;
+                }
+              }
+              if (ok) {
+                grp[g].free = 0;
+                grp[g].b = b;
+                grp[g].total = 0;
+                grp[g].remaining = kGroupOpen;
+                g_open = g;
+                g_count = 0;
+                ++ngrp;
+              }
+            }
+            if (ok && task >= kOvSlots &&
                 !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
                                 abort, wait))
               ok = false;
             if (ok) {
-              desc[slot] = OvTask{b, which, n, c, cur_cs, cur_greedy, 0, 0};
+              ++g_count;
+              desc[slot] = OvTask{b, which, n, c, cur_cs, cur_greedy, 0, g_open};
               const int64_t e0 = (int64_t)c * kChunk;
               const int64_t left = (int64_t)V - e0;
               const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
@@ -1468,6 +1572,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
         }
         next = __shfl_sync(0xffffffffu, after, 0);
       }
+      if (lane == 0 && ok) close_group();
       // one stop task per consumer warp
       for (int w = 0; w < kOvConsumers && ok; ++w) {
         const int slot = (int)(task % kOvSlots);
@@ -1513,9 +1618,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
           r.pad = pack_index(am);
           r.s = (double)sd;
           stats[(((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks + k.c] = r;
-          // the request's count of finished tasks, released after the write
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(req_done + k.b) : "memory");
           ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
+          // the last task of a closed group publishes the group's count
+          __threadfence_block();
+          if (atomicSub(&grp[k.grp].remaining, 1) == 1) {
+            __threadfence();
+            atomicAdd(req_done + grp[k.grp].b, (uint32_t)grp[k.grp].total);
+            *reinterpret_cast<volatile int*>(&grp[k.grp].free) = 1;
+          }
         }
       }
     }
@@ -1526,6 +1636,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
     }
   } else {
     // =============================================================== deciders
+    int64_t rtask = 0;  // chunk pairs this CTA has copied for residual passes
+    bool ring_ok = true;
     for (;;) {
       if (tid == 0) s_req = (int)atomicAdd(ctl + 1, 1u);
       __syncthreads();
@@ -1582,9 +1694,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
               break;
             }
           }
-          __nanosleep(128);
+          __nanosleep(64);
         }
-        s_abort = lost;
+        s_abort = lost || !ring_ok;
       }
       __syncthreads();
       const bool lost = s_abort != 0;
@@ -1593,9 +1705,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
                               out_tokens, path, accepted_len, probe, d, n_chunks, chunk, stats,
                               draws, status, b, lost, sh);
       __syncthreads();
-      // a draw from a residual: the chunk masses (every warp, its chunks),
-      // then the chunk and the element, as rs_residual_sums_kernel and
-      // rs_residual_draw_kernel do
+      // A draw from a residual, finished here: the residual's mass over each
+      // statistics chunk of the node's two rows (bulk copies of the chunk
+      // pairs into the ring, thread 0 issuing, warps 1..15 reducing), then
+      // the chunk and the element, as rs_residual_sums_kernel and
+      // rs_residual_draw_kernel do.
       const DrawState* dsb = draws + b;
       if (!lost && dsb->pending) {
         const int node = dsb->node, a_acc = dsb->a;
@@ -1606,14 +1720,48 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
         const T* trow = target + ((int64_t)b * M + node) * V;
         const T* drow = draft + ((int64_t)b * M + node) * V;
         double* zs = zsum + (int64_t)b * n_chunks;
-        for (int c = warp; c < n_chunks; c += kOvWarps) {
-          uint4 rt[kStatVecs], rd[kStatVecs];
-          const float ls = lane_weights<T>(trow, drow, (int64_t)c * kChunk, V, sh.ctx, sh.ctx.nrej, rt, rd);
-          const dfloat tot = df_warp_sum(df_make(ls));
-          if (lane == 0) zs[c] = df_to_d(tot);
+        if (tid == 0) {
+          for (int c = 0; c < n_chunks && ring_ok; ++c) {
+            const int64_t r = rtask + c;
+            const int p = (int)(r % kOvPairs);
+            if (r >= kOvPairs &&
+                !ptx::mbar_wait(ptx::smem_u32(&empty[p]), (uint32_t)(((r / kOvPairs) & 1) ^ 1), abort,
+                                wait)) {
+              ring_ok = false;
+              break;
+            }
+            const int64_t e0 = (int64_t)c * kChunk;
+            const int64_t left = (int64_t)V - e0;
+            const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
+            const uint32_t fb = ptx::smem_u32(&full[p]);
+            ptx::mbar_arrive_expect_tx(fb, 2 * bytes);
+            uint8_t* sp = ring + (size_t)p * 2 * kBulkSlot;
+            ptx::bulk_g2s(ptx::smem_u32(sp), trow + e0, bytes, fb);
+            ptx::bulk_g2s(ptx::smem_u32(sp + kBulkSlot), drow + e0, bytes, fb);
+          }
+        } else if (warp >= 1) {
+          for (int c = warp - 1; c < n_chunks; c += kOvConsumers) {
+            const int64_t r = rtask + c;
+            const int p = (int)(r % kOvPairs);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&full[p]),
+                                                        (uint32_t)((r / kOvPairs) & 1), abort, wait)))
+              break;
+            const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)p * 2 * kBulkSlot);
+            const float ls = smem_chunk_mass<T>(sp, sp + kBulkSlot / 16, c * kChunk, V, sh.ctx,
+                                                sh.ctx.nrej);
+            const dfloat tot = df_warp_sum(df_make(ls));
+            __syncwarp();
+            if (lane == 0) {
+              zs[c] = df_to_d(tot);
+              ptx::mbar_arrive(ptx::smem_u32(&empty[p]));
+            }
+          }
         }
+        rtask += n_chunks;
         __syncthreads();
-        if (warp == 0) {
+        if (*abort) {
+          ring_ok = false;
+        } else if (warp == 0) {
           double Z = 0.0;
           for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
           Z = warp_sum(Z);
@@ -1650,6 +1798,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
       }
       if (tid == 0) req_done[b] = 0u;  // ready for the next call
       __syncthreads();
+    }
+    // the residual copies issued have all been waited for by their readers;
+    // after a wait that gave up, drain what may still be in flight
+    if (tid == 0 && *abort)
+      for (int64_t r = rtask > kOvPairs ? rtask - kOvPairs : 0; r < rtask; ++r)
+        ptx::mbar_drain(ptx::smem_u32(&full[r % kOvPairs]), (uint32_t)((r / kOvPairs) & 1),
+                        kDefaultWaitCycles);
+    if (tid == 0 && *abort) {
+      *failed = 1u;
+      raise_status(status, SPEC_ERR_TIMEOUT);
     }
   }
 

@@ -54,13 +54,34 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Limits below this many clocks are short: their waits poll without the
-// hardware suspension of try_wait and read the clock every 16 polls, so the
-// limit is honoured; longer limits read it every 1024 polls (a wait that is
-// satisfied quickly then costs nothing but the polls).
+// Limits below this many clocks are short.  A wait under a short limit
+// polls without the hardware suspension of try_wait and reads the clock
+// every 16 polls, so that the limit is honoured; it lives in a function of
+// its own, reached by one branch after the first poll, so that the usual
+// waits (try_wait, the clock read every 1024 polls: a wait that is
+// satisfied quickly costs nothing but the polls) compile as they would
+// without it.
 constexpr uint64_t kShortWait = 1ull << 20;
 __device__ __forceinline__ uint32_t poll_mask(uint64_t timeout_cycles) {
   return timeout_cycles < kShortWait ? 15u : 1023u;
+}
+
+static __device__ __noinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             uint64_t timeout_cycles) {
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u) {
+      if (*abort) return false;
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if ((uint64_t)(now - t0) > timeout_cycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
 }
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when
@@ -68,12 +89,12 @@ __device__ __forceinline__ uint32_t poll_mask(uint64_t timeout_cycles) {
 // setting *abort itself in the second case, so no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_cycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (timeout_cycles < kShortWait) return mbar_wait_short(bar, parity, abort, timeout_cycles);
   long long t0 = 0;
-  const uint32_t mask = poll_mask(timeout_cycles);
-  const bool short_wait = timeout_cycles < kShortWait;
-  for (uint32_t it = 0;; ++it) {
-    if (short_wait ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((it & mask) == mask) {
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 1023u) {
       if (*abort) return false;
       const long long now = clock64();
       if (t0 == 0) {
@@ -117,91 +138,6 @@ __device__ __forceinline__ bool wait_count_geq(const int* p, int target, volatil
       }
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// thread-block clusters: rank, shared-memory addresses of the other CTAs,
-// stores and mbarrier arrivals into them, cluster-wide barrier
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The shared::cluster address of `local` (a shared::cta address of this
-// CTA) in the CTA of cluster rank `rank`.
-__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-// Arrive on an mbarrier of any CTA of the cluster, releasing at cluster scope
-// what this thread (and, cumulatively, what it has observed) wrote before.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait for a phase completed by arrivals from other CTAs of the cluster
-// (acquire at cluster scope), with the same give-up rules.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, uint64_t timeout_cycles) {
-  long long t0 = 0;
-  const uint32_t mask = poll_mask(timeout_cycles);
-  const bool short_wait = timeout_cycles < kShortWait;
-  for (uint32_t it = 0;; ++it) {
-    if (short_wait ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity))
-      return true;
-    if ((it & mask) == mask) {
-      if (*abort) return false;
-      const long long now = clock64();
-      if (t0 == 0) {
-        t0 = now;
-      } else if ((uint64_t)(now - t0) > timeout_cycles) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
 }
 
 // ---------------------------------------------------------------------------

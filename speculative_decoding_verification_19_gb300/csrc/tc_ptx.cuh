@@ -57,7 +57,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Limits below this many clocks are short.  A wait under a short limit
 // polls without the hardware suspension of try_wait and reads the clock
 // every 16 polls, so that the limit is honoured; it lives in a function of
-// its own, reached by one branch after the first poll, so that the usual
+// its own, reached by one branch on entry, so that the usual
 // waits (try_wait, the clock read every 1024 polls: a wait that is
 // satisfied quickly costs nothing but the polls) compile as they would
 // without it.
@@ -89,10 +89,9 @@ static __device__ __noinline__ bool mbar_wait_short(uint32_t bar, uint32_t parit
 // setting *abort itself in the second case, so no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
   if (timeout_cycles < kShortWait) return mbar_wait_short(bar, parity, abort, timeout_cycles);
   long long t0 = 0;
-  for (uint32_t it = 1;; ++it) {
+  for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 1023u) == 1023u) {
       if (*abort) return false;

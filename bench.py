@@ -321,6 +321,70 @@ def timed_steps(st, first, K):
             float(np.mean([e[2].elapsed_time(e[3]) for e in ev])))
 
 
+def verify_statistics(wl, acc, st, parent):
+    """The pages' observability figures over the timed steps, computed by the
+    library's host-side controller: the rejection-position histogram of every
+    step (page 2 §5.1), each request's acceptance rate over the steps with
+    its histogram and percentiles, and the speculative efficiency (page 3)."""
+    from speculative_decoding_verification_19_gb300.controller import Controller, step_stats
+    K, B = acc.shape
+    pos = np.zeros(wl.M + 1, dtype=np.int64)
+    twe = []
+    path = st.path.cpu().numpy()  # the last step's path (for the tree figure)
+    for k in range(K):
+        sst = step_stats(acc[k], path=path if k == K - 1 else None,
+                         parent=parent if k == K - 1 else None)
+        pos += np.asarray(sst["rejection_pos"][:wl.M + 1])
+        if k == K - 1 and parent is not None:
+            twe.append(sst["tree_width_effective"])
+    # a controller fed the steps at the workload's fixed draft length (its
+    # proposals are reported, not applied: the workload's shape is fixed)
+    from speculative_decoding_verification_19_gb300.controller import default_config
+    ctl = Controller(B, gamma0=wl.gamma if not wl.is_tree else wl.M - 1,
+                     cfg=default_config(window=min(16, K), max_gamma=63, min_efficiency=0.0))
+    proposed = None
+    for k in range(K):
+        # the draft length stays the workload's: feed each step as drafted at it
+        for r in ctl.reqs:
+            r.gamma = wl.gamma if not wl.is_tree else wl.M - 1
+        proposed = ctl.update(acc[k])
+    m = ctl.metrics()
+    out = {"rejection_position_hist": pos.tolist(),
+           "acceptance_hist": m["acceptance_hist"],
+           "acceptance_p50": round(m["acceptance_p50"], 4),
+           "acceptance_p95": round(m["acceptance_p95"], 4),
+           "acceptance_p99": round(m["acceptance_p99"], 4),
+           "speculative_efficiency": round(m["speculative_efficiency"], 4),
+           "proposed_gamma_hist": np.bincount(proposed, minlength=9).tolist()}
+    if twe:
+        out["tree_width_effective"] = round(float(np.mean(twe)), 4)
+    return out
+
+
+def greedy_reject(st, K, peak, rej_b):
+    """spec_reject_sample of the same batch at temperature 0 (greedy:
+    exact match with each row's argmax), timed alone on the same inputs."""
+    sv = st.sv
+    temp0 = torch.zeros_like(st.temperature)
+    for i in range(3):
+        sv.spec_reject_sample(st.target, st.draft, st.tokens, st.parent, temp0, 1, i,
+                              st.out_tokens, st.path, st.acc[0], None, st.dims, st.ws)
+    ts = []
+    for i in range(K):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        sv.spec_reject_sample(st.target, st.draft, st.tokens, st.parent, temp0, 1, i,
+                              st.out_tokens, st.path, st.acc[0], None, st.dims, st.ws)
+        b_.record()
+        torch.cuda.synchronize()
+        ts.append(a_.elapsed_time(b_))
+    ms = float(np.mean(ts))
+    a = st.acc[0].cpu().numpy()
+    assert np.all(a >= 0)
+    return {"reject_ms": round(ms, 4), "reject_frac": round(rej_b / (ms / 1e3) / 1e9 / peak, 4),
+            "emitted_tokens_per_step": int((a + 1).sum())}
+
+
 def second_workload(name, seed, device, K, W, peak):
     """The other workload the HBM bar is set on, timed the same way in the
     same process after the main timed region (its own inputs, K steps)."""
@@ -447,6 +511,7 @@ def run_native(args, wl, world, rank, local):
     acc = st.acc[W + 1:W + 1 + K].cpu().numpy()
     assert np.all(acc >= 0), "a request failed inside the timed region"
     emitted_per_step = float((acc + 1).sum(axis=1).mean())
+    verify_stats = verify_statistics(wl, acc, st, lg["parent"])
 
     # end to end through the public API with pinned host buffers
     ins, outs = st.host_inputs()
@@ -465,6 +530,7 @@ def run_native(args, wl, world, rank, local):
     # the timed region above, the other timed after it in this process
     workloads = {wl.name: {"attn_frac": round(attn_b / (attn_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                            "reject_frac": round(rej_b / (rej_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}}
+    workloads[wl.name + " (temperature 0)"] = greedy_reject(st, K, peaks["hbm_gbs"], rej_b)
     if not args.no_second and wl.name in BAR_WORKLOADS:
         for other in BAR_WORKLOADS:
             if other != wl.name:
@@ -500,6 +566,7 @@ def run_native(args, wl, world, rank, local):
                     "reject_frac": round(rej_b / (rej_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                     "reject_bytes": rej_b},
         "workloads": workloads,
+        "verify_stats": verify_stats,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * K / e2e_s, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -1340,21 +1340,28 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kOvWarps = 16;      // per CTA: stream = producer warp + 15 consumers
 constexpr int kOvConsumers = kOvWarps - 1;
-constexpr int kOvSlots = 44;      // 4 KB ring slots (a decider pairs them: 22 of 8 KB)
+// A stream task is a segment of up to four consecutive statistics chunks of
+// one row, copied by one 1-D bulk copy (16 KB): the copies one thread can
+// issue per microsecond, not the bytes, bounded 4 KB copies.
+constexpr int kSegChunks = 4;
+constexpr int kSegBytes = kSegChunks * kBulkSlot;
+constexpr int kOvSlots = 11;      // 16 KB ring slots (a decider pairs them: 5 of 32 KB)
 constexpr int kOvPairs = kOvSlots / 2;
 constexpr int kOvBatch = 32;      // tasks per claim
 constexpr int kOvGroups = 16;     // completion groups in flight per stream CTA
 constexpr int kOvMaxMeta = 2048;  // requests whose temperature and tree masks sit in shared memory
 constexpr int kOvMaxDeciders = 24;
-constexpr size_t kOvRingBytes = (size_t)kOvSlots * kBulkSlot;
+constexpr size_t kOvRingBytes = (size_t)kOvSlots * kSegBytes;
 constexpr size_t kOvSmem = kOvRingBytes + kOvMaxMeta * (sizeof(float) + sizeof(uint64_t)) + 1024;
 static_assert(kOvWarps * kWarp == kDecThreads, "a decider CTA is a decide CTA");
 constexpr int kGroupOpen = 1 << 30;  // a group's count before its producer closes it
 
 struct OvTask {
-  int b, which, n, c;
+  int b, which, n, c;  // request, target (0) or draft (1) row, node, first chunk
+  int nc;              // chunks in the segment
   float cs;
   int greedy, stop, grp;
+  int pad[3];
 };
 
 // Consecutive statistics tasks of one request on one stream CTA: the count
@@ -1486,10 +1493,64 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
         uint32_t after = 0;
         if (lane == 0) after = atomicAdd(ctl + 0, 1u);
         const int64_t t1 = t0 + kOvBatch < ntask ? t0 + kOvBatch : ntask;
+        bool sg_c_first_of_batch = true;  // the batch's first segment opens a group
         // the batch's first task decoded once, then walked (chunks fastest)
         int b = (int)(t0 / per_req);
         const int rem0 = (int)(t0 - (int64_t)b * per_req);
         int row = rem0 / n_chunks, c = rem0 - row * n_chunks;
+        // segments: consecutive chunks of one row, up to kSegChunks
+        int sg_b = -1, sg_which = 0, sg_n = 0, sg_c = 0, sg_nc = 0;
+        auto issue_segment = [&]() {  // whole warp; lane 0 issues
+          if (sg_nc == 0) return;
+          const int slot = (int)(task % kOvSlots);
+          if (lane == 0) {
+            // a new group at the batch's first segment and at every new request
+            if (g_open < 0 || grp[g_open].b != sg_b || sg_c_first_of_batch) {
+              close_group();
+              const int g = ngrp % kOvGroups;
+              long long w0 = 0;
+              while (!*reinterpret_cast<volatile int*>(&grp[g].free)) {  // bounded
+                const long long now = clock64();
+                if (w0 == 0) w0 = now;
+                else if ((uint64_t)(now - w0) > wait || *abort) {
+                  *abort = 1;
+                  ok = false;
+                  break;
+                }
+              }
+              if (ok) {
+                grp[g].free = 0;
+                grp[g].b = sg_b;
+                grp[g].total = 0;
+                grp[g].remaining = kGroupOpen;
+                g_open = g;
+                g_count = 0;
+                ++ngrp;
+              }
+            }
+            if (ok && task >= kOvSlots &&
+                !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
+                                abort, wait))
+              ok = false;
+            if (ok) {
+              g_count += sg_nc;
+              desc[slot] = OvTask{sg_b, sg_which, sg_n, sg_c, sg_nc, cur_cs, cur_greedy, 0, g_open, {0, 0, 0}};
+              const int64_t e0 = (int64_t)sg_c * kChunk;
+              const int64_t left = (int64_t)V - e0;
+              const int64_t want = (int64_t)sg_nc * kChunk;
+              const uint32_t bytes = (uint32_t)((left < want ? left : want) * sizeof(T));
+              const uint32_t fb = ptx::smem_u32(&full[slot]);
+              ptx::mbar_arrive_expect_tx(fb, bytes);
+              ptx::bulk_g2s(ptx::smem_u32(ring + (size_t)slot * kSegBytes),
+                            (sg_which == 0 ? target : draft) + ((int64_t)sg_b * M + sg_n) * V + e0, bytes,
+                            fb);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++task;
+          sg_nc = 0;
+          sg_c_first_of_batch = false;
+        };
         for (int64_t t = t0; t < t1 && ok; ++t) {
           if (t > t0 && ++c == n_chunks) {
             c = 0;
@@ -1500,6 +1561,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
           }
           const int which = row < M ? 0 : 1, n = row < M ? row : row - M;
           if (b != cur_b) {
+            issue_segment();
+            if (!ok) break;
             cur_b = b;
             float temp;
             if (meta_in_smem) {
@@ -1525,51 +1588,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
             cur_greedy = temp == 0.f;
           }
           if (which == 1 && parent != nullptr && !((kids >> n) & 1ull)) continue;  // a leaf's draft row
-          const int slot = (int)(task % kOvSlots);
-          if (lane == 0) {
-            // a new group at the batch's first task and at every new request
-            if (g_open < 0 || grp[g_open].b != b || t == t0) {
-              close_group();
-              const int g = ngrp % kOvGroups;
-              long long w0 = 0;
-              while (!*reinterpret_cast<volatile int*>(&grp[g].free)) {  // bounded
-                const long long now = clock64();
-                if (w0 == 0) w0 = now;
-                else if ((uint64_t)(now - w0) > wait || *abort) {
-                  *abort = 1;
-                  ok = false;
-                  break;
-                }
-              }
-              if (ok) {
-                grp[g].free = 0;
-                grp[g].b = b;
-                grp[g].total = 0;
-                grp[g].remaining = kGroupOpen;
-                g_open = g;
-                g_count = 0;
-                ++ngrp;
-              }
-            }
-            if (ok && task >= kOvSlots &&
-                !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
-                                abort, wait))
-              ok = false;
-            if (ok) {
-              ++g_count;
-              desc[slot] = OvTask{b, which, n, c, cur_cs, cur_greedy, 0, g_open};
-              const int64_t e0 = (int64_t)c * kChunk;
-              const int64_t left = (int64_t)V - e0;
-              const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
-              const uint32_t fb = ptx::smem_u32(&full[slot]);
-              ptx::mbar_arrive_expect_tx(fb, bytes);
-              ptx::bulk_g2s(ptx::smem_u32(ring + (size_t)slot * kBulkSlot),
-                            (which == 0 ? target : draft) + ((int64_t)b * M + n) * V + e0, bytes, fb);
-            }
+          if (sg_nc > 0 && (sg_which != which || sg_n != n || sg_nc == kSegChunks)) {
+            issue_segment();
+            if (!ok) break;
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          ++task;
+          if (sg_nc == 0) {
+            sg_b = b;
+            sg_which = which;
+            sg_n = n;
+            sg_c = c;
+          }
+          ++sg_nc;
         }
+        if (ok) issue_segment();
         next = __shfl_sync(0xffffffffu, after, 0);
       }
       if (lane == 0 && ok) close_group();
@@ -1603,25 +1634,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
           break;
         const OvTask k = desc[slot];
         if (k.stop) break;
-        const int e0 = k.c * kChunk;
-        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kBulkSlot);
-        uint4 raw[kStatVecs];
+        RowStat* srow = stats + (((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks;
+        for (int j = 0; j < k.nc; ++j) {
+          const int cc = k.c + j;
+          const int e0 = cc * kChunk;
+          const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kSegBytes +
+                                                           (size_t)j * kBulkSlot);
+          uint4 raw[kStatVecs];
 #pragma unroll
-        for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
-        float sd;
-        const float m = chunk_stat<T>(raw, V - e0, k.cs, &sd);
-        const int am = k.greedy ? chunk_argmax<T>(raw, V - e0, m) : 0;
+          for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
+          float sd;
+          const float m = chunk_stat<T>(raw, V - e0, k.cs, &sd);
+          const int am = k.greedy ? chunk_argmax<T>(raw, V - e0, m) : 0;
+          if (lane == 0) {
+            RowStat r;
+            r.m = m;
+            r.pad = pack_index(am);
+            r.s = (double)sd;
+            srow[cc] = r;
+          }
+        }
         __syncwarp();
         if (lane == 0) {
-          RowStat r;
-          r.m = m;
-          r.pad = pack_index(am);
-          r.s = (double)sd;
-          stats[(((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks + k.c] = r;
           ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
           // the last task of a closed group publishes the group's count
           __threadfence_block();
-          if (atomicSub(&grp[k.grp].remaining, 1) == 1) {
+          if (atomicSub(&grp[k.grp].remaining, k.nc) == k.nc) {
             __threadfence();
             atomicAdd(req_done + grp[k.grp].b, (uint32_t)grp[k.grp].total);
             *reinterpret_cast<volatile int*>(&grp[k.grp].free) = 1;
@@ -1720,9 +1758,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
         const T* trow = target + ((int64_t)b * M + node) * V;
         const T* drow = draft + ((int64_t)b * M + node) * V;
         double* zs = zsum + (int64_t)b * n_chunks;
+        const int nseg = (n_chunks + kSegChunks - 1) / kSegChunks;
         if (tid == 0) {
-          for (int c = 0; c < n_chunks && ring_ok; ++c) {
-            const int64_t r = rtask + c;
+          for (int g = 0; g < nseg && ring_ok; ++g) {
+            const int64_t r = rtask + g;
             const int p = (int)(r % kOvPairs);
             if (r >= kOvPairs &&
                 !ptx::mbar_wait(ptx::smem_u32(&empty[p]), (uint32_t)(((r / kOvPairs) & 1) ^ 1), abort,
@@ -1730,34 +1769,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
               ring_ok = false;
               break;
             }
-            const int64_t e0 = (int64_t)c * kChunk;
+            const int64_t e0 = (int64_t)g * kSegChunks * kChunk;
             const int64_t left = (int64_t)V - e0;
-            const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
+            const int64_t want = (int64_t)kSegChunks * kChunk;
+            const uint32_t bytes = (uint32_t)((left < want ? left : want) * sizeof(T));
             const uint32_t fb = ptx::smem_u32(&full[p]);
             ptx::mbar_arrive_expect_tx(fb, 2 * bytes);
-            uint8_t* sp = ring + (size_t)p * 2 * kBulkSlot;
+            uint8_t* sp = ring + (size_t)p * 2 * kSegBytes;
             ptx::bulk_g2s(ptx::smem_u32(sp), trow + e0, bytes, fb);
-            ptx::bulk_g2s(ptx::smem_u32(sp + kBulkSlot), drow + e0, bytes, fb);
+            ptx::bulk_g2s(ptx::smem_u32(sp + kSegBytes), drow + e0, bytes, fb);
           }
         } else if (warp >= 1) {
-          for (int c = warp - 1; c < n_chunks; c += kOvConsumers) {
-            const int64_t r = rtask + c;
+          for (int g = warp - 1; g < nseg; g += kOvConsumers) {
+            const int64_t r = rtask + g;
             const int p = (int)(r % kOvPairs);
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&full[p]),
                                                         (uint32_t)((r / kOvPairs) & 1), abort, wait)))
               break;
-            const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)p * 2 * kBulkSlot);
-            const float ls = smem_chunk_mass<T>(sp, sp + kBulkSlot / 16, c * kChunk, V, sh.ctx,
-                                                sh.ctx.nrej);
-            const dfloat tot = df_warp_sum(df_make(ls));
-            __syncwarp();
-            if (lane == 0) {
-              zs[c] = df_to_d(tot);
-              ptx::mbar_arrive(ptx::smem_u32(&empty[p]));
+            const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)p * 2 * kSegBytes);
+            for (int j = 0; j < kSegChunks; ++j) {
+              const int c = g * kSegChunks + j;
+              if (c >= n_chunks) break;
+              const float ls = smem_chunk_mass<T>(sp + j * (kBulkSlot / 16),
+                                                  sp + (kSegBytes + j * kBulkSlot) / 16, c * kChunk,
+                                                  V, sh.ctx, sh.ctx.nrej);
+              const dfloat tot = df_warp_sum(df_make(ls));
+              if (lane == 0) zs[c] = df_to_d(tot);
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[p]));
           }
         }
-        rtask += n_chunks;
+        rtask += nseg;
         __syncthreads();
         if (*abort) {
           ring_ok = false;

@@ -1633,7 +1633,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
                                                     (uint32_t)((t / kOvSlots) & 1), abort, wait)))
           break;
         const OvTask k = desc[slot];
-        if (k.stop) break;
+        if (k.stop) {
+          // the slot goes back too: the ring may hold fewer slots than there
+          // are consumers, so later stop tasks reuse it
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
+          break;
+        }
         RowStat* srow = stats + (((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks;
         for (int j = 0; j < k.nc; ++j) {
           const int cc = k.c + j;

@@ -195,3 +195,18 @@ def test_greedy_mixed_batch_and_ties(impl):
     assert g["accepted_len"][0] == 0 and g["out_tokens"][0, 0] == 100
     greedy = lg["temperature"] == 0.0
     assert np.array_equal(g["out_tokens"][greedy], o["out_tokens"][greedy])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_request_shards_reproduce_the_whole_batch(impl):
+    """Request shards on several GPUs: each shard passes the global index of
+    its first request as b_base, so its uniforms, and hence its outputs,
+    are those of the same requests in one whole-batch call."""
+    wl = workload("chain_7b").scaled(B=10, V=16384)
+    lg = logits_inputs(wl, seed=12)
+    whole, _, _ = _run(wl, lg, seed=77, offset=3, impl=impl)
+    for lo, hi in [(0, 4), (4, 7), (7, 10)]:
+        part = {k: (v[lo:hi] if isinstance(v, np.ndarray) else v) for k, v in lg.items()}
+        g, _, _ = _run(wl.scaled(B=hi - lo), part, seed=77, offset=3, b_base=lo, impl=impl)
+        for key in ("out_tokens", "path", "accepted_len"):
+            assert np.array_equal(g[key], whole[key][lo:hi]), (key, lo)

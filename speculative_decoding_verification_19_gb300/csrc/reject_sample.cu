@@ -1394,6 +1394,27 @@ __device__ __forceinline__ float smem_chunk_mass(const uint4* st, const uint4* s
   return s;
 }
 
+// Wait until the CTA's issue count (shared memory, written by its issuing
+// thread) exceeds `need`; gives up like ptx::mbar_wait.
+__device__ __forceinline__ bool wait_issued(volatile long long* cnt, long long need,
+                                            volatile int* abort, uint64_t timeout_cycles) {
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (*cnt >= need) return true;
+    if ((it & 7u) == 7u) {
+      if (*abort) return false;
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if ((uint64_t)(now - t0) > timeout_cycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
 // ctl: [0] next task batch, [1] next request to decide, [2] CTAs finished,
 // [3] the call failed (a wait gave up)
 template <typename T>
@@ -1411,6 +1432,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
   __shared__ OvGroup grp[kOvGroups];
   __shared__ uint64_t full[kOvSlots], empty[kOvSlots];
   __shared__ int s_abort, s_req;
+  // copies issued into the ring so far (tasks for stream CTAs, chunk pairs
+  // for deciders): a reader waits for its copy to be issued before waiting
+  // on the slot's full barrier, so that it never waits more than one phase
+  // ahead of the barrier (there are more readers than slots)
+  __shared__ long long s_issued;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1432,8 +1458,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
       ptx::mbar_init(ptx::smem_u32(&empty[i]), 1);
     }
     s_abort = 0;
+    s_issued = 0;
     ptx::fence_mbar_init();
   }
+  volatile long long* issued = &s_issued;
   for (int g = tid; g < kOvGroups; g += kDecThreads) grp[g].free = 1;
   __syncthreads();
   pdl_trigger();
@@ -1544,6 +1572,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
               ptx::bulk_g2s(ptx::smem_u32(ring + (size_t)slot * kSegBytes),
                             (sg_which == 0 ? target : draft) + ((int64_t)sg_b * M + sg_n) * V + e0, bytes,
                             fb);
+              *issued = task + 1;
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1615,22 +1644,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
           if (ok) {
             desc[slot].stop = 1;
             ptx::mbar_arrive(ptx::smem_u32(&full[slot]));
+            *issued = task + 1;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         ++task;
       }
       // every copy issued lands before the CTA may exit
-      if (lane == 0)
-        for (int64_t u = task > kOvSlots ? task - kOvSlots : 0; u < task; ++u)
+      if (lane == 0) {
+        const long long n_iss = *issued;
+        for (long long u = n_iss > kOvSlots ? n_iss - kOvSlots : 0; u < n_iss; ++u)
           ptx::mbar_drain(ptx::smem_u32(&full[u % kOvSlots]), (uint32_t)((u / kOvSlots) & 1),
                           kDefaultWaitCycles);
+      }
     } else {
       // consumers: task t on warp 1 + t mod 15
       for (int64_t t = warp - 1;; t += kOvConsumers) {
         const int slot = (int)(t % kOvSlots);
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&full[slot]),
-                                                    (uint32_t)((t / kOvSlots) & 1), abort, wait)))
+        if (!__all_sync(0xffffffffu, wait_issued(issued, t + 1, abort, wait) &&
+                                         ptx::mbar_wait(ptx::smem_u32(&full[slot]),
+                                                        (uint32_t)((t / kOvSlots) & 1), abort, wait)))
           break;
         const OvTask k = desc[slot];
         if (k.stop) {
@@ -1784,13 +1817,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
             uint8_t* sp = ring + (size_t)p * 2 * kSegBytes;
             ptx::bulk_g2s(ptx::smem_u32(sp), trow + e0, bytes, fb);
             ptx::bulk_g2s(ptx::smem_u32(sp + kSegBytes), drow + e0, bytes, fb);
+            *issued = r + 1;
           }
         } else if (warp >= 1) {
           for (int g = warp - 1; g < nseg; g += kOvConsumers) {
             const int64_t r = rtask + g;
             const int p = (int)(r % kOvPairs);
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&full[p]),
-                                                        (uint32_t)((r / kOvPairs) & 1), abort, wait)))
+            if (!__all_sync(0xffffffffu, wait_issued(issued, r + 1, abort, wait) &&
+                                             ptx::mbar_wait(ptx::smem_u32(&full[p]),
+                                                            (uint32_t)((r / kOvPairs) & 1), abort,
+                                                            wait)))
               break;
             const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)p * 2 * kSegBytes);
             for (int j = 0; j < kSegChunks; ++j) {
@@ -1850,10 +1886,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
     }
     // the residual copies issued have all been waited for by their readers;
     // after a wait that gave up, drain what may still be in flight
-    if (tid == 0 && *abort)
-      for (int64_t r = rtask > kOvPairs ? rtask - kOvPairs : 0; r < rtask; ++r)
+    if (tid == 0 && *abort) {
+      const long long n_iss = *issued;
+      for (long long r = n_iss > kOvPairs ? n_iss - kOvPairs : 0; r < n_iss; ++r)
         ptx::mbar_drain(ptx::smem_u32(&full[r % kOvPairs]), (uint32_t)((r / kOvPairs) & 1),
                         kDefaultWaitCycles);
+    }
     if (tid == 0 && *abort) {
       *failed = 1u;
       raise_status(status, SPEC_ERR_TIMEOUT);

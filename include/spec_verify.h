@@ -71,7 +71,7 @@ typedef enum spec_dtype { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 /* Attention kernel selection (spec_dims.attn_impl). */
 typedef enum spec_attn_impl {
   SPEC_ATTN_AUTO = 0,          /* tensor cores when the shape allows, else CUDA cores */
-  SPEC_ATTN_CUDA_CORES = 1,    /* split-KV on CUDA cores: group*M <= 64, D 64/128, bf16/f32 */
+  SPEC_ATTN_CUDA_CORES = 1,    /* split-KV on CUDA cores: group*M <= 128, D 64/128, bf16/f32 */
   SPEC_ATTN_TENSOR_CORES = 2   /* tcgen05 + TMA: bf16, D = 128, group*M <= 128 */
 } spec_attn_impl;
 
@@ -90,7 +90,8 @@ typedef enum spec_reject_impl {
 
 typedef struct spec_dims {
   int32_t B;            /* requests in the batch */
-  int32_t M;            /* query rows per request: gamma+1, or tree nodes incl. root */
+  int32_t M;            /* query rows per request: gamma+1, or tree nodes incl. root;
+                           1..128 (SPEC_ERR_UNSUPPORTED above) */
   int32_t Hq;           /* query heads */
   int32_t Hkv;          /* KV heads; query head h reads KV head h / (Hq/Hkv) */
   int32_t D;            /* head size (64 or 128) */
@@ -301,7 +302,7 @@ spec_status spec_reject_sample_noalloc(const void* target_logits,
  */
 #define SPEC_CTRL_MAX_WINDOW 64
 #define SPEC_CTRL_HIST_BINS 10
-#define SPEC_STEP_MAX_POS 65
+#define SPEC_STEP_MAX_POS 129
 
 typedef struct spec_ctrl_config {
   int32_t window;          /* steps the acceptance rate is taken over (<= 64); 16 */

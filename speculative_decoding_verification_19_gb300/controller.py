@@ -14,7 +14,7 @@ from ._native import SpecError, lib
 
 MAX_WINDOW = 64
 HIST_BINS = 10
-MAX_POS = 65
+MAX_POS = 129  # SPEC_STEP_MAX_POS
 
 
 class CtrlConfig(ctypes.Structure):

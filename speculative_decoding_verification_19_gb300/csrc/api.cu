@@ -43,7 +43,7 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.tc_rq_off = take(16 * (size_t)d.B);
   L.tc_start_off = take(32 * ((size_t)kMaxAttnCtas + 1));
   L.tc_pair_off = take(sizeof(int32_t) * (size_t)d.B * (size_t)(d.Hkv > 0 ? d.Hkv : 0));
-  L.tc_anc_off = take(sizeof(uint64_t) * (size_t)d.B * d.M);
+  L.tc_anc_off = take(2 * sizeof(uint64_t) * (size_t)d.B * d.M);
   L.tc_sync_off = take(16);
   const int group = d.Hkv > 0 ? d.Hq / d.Hkv : 0;
   L.rows = group * d.M;
@@ -59,9 +59,7 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_off = take(L.rs_bytes);
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
-  L.rsf_ctl_off = take(16);
-  L.rsf_req_off = take(sizeof(uint32_t) * (size_t)d.B);
-  L.rsf_rec_off = take(32 * (size_t)d.B * d.M);
+  off = rsf_layout(d, off, &L);
   L.total = off;
   return L;
 }
@@ -71,7 +69,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 spec_status check_common(const spec_dims* d) {
   if (d == nullptr) return SPEC_ERR_INVALID_ARG;
   if (d->B < 1 || d->M < 1) return SPEC_ERR_INVALID_ARG;
-  if (d->M > 64) return SPEC_ERR_UNSUPPORTED;
+  if (d->M > kMaxNodes) return SPEC_ERR_UNSUPPORTED;
   if (d->block != kBlock) return SPEC_ERR_UNSUPPORTED;
   if ((d->kv_dtype != SPEC_BF16 && d->kv_dtype != SPEC_F32) ||
       (d->logits_dtype != SPEC_BF16 && d->logits_dtype != SPEC_F32))
@@ -152,7 +150,7 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
                      (int64_t)dims->B * dims->Hkv *
                              ceil_div64((int64_t)dims->max_blocks * kBlock, 64) <
                          ((int64_t)1 << 31);
-  const bool simt_ok = R <= 64;
+  const bool simt_ok = R <= 128;
   bool use_tc;
   if (dims->attn_impl == SPEC_ATTN_TENSOR_CORES) {
     if (!tc_ok) return SPEC_ERR_UNSUPPORTED;

@@ -108,10 +108,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
 constexpr int kTileKeys = 32;
 constexpr int kSimtThreads = 128;
 constexpr int kSimtWarps = kSimtThreads / kWarp;
+constexpr int kMaxRows = 128;  // new rows per request (tree nodes)
 
 size_t attn_simt_smem_bytes(int R, int D) {
   return sizeof(float) * ((size_t)R * D + kTileKeys * (D + 4) + kTileKeys * D + (size_t)R * kTileKeys) +
-         sizeof(unsigned long long) * 64;
+         sizeof(unsigned long long) * 2 * kMaxRows;
 }
 
 template <typename T, int D, int RPW>
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_split_kernel(
   float* ks = qs + R * D;
   float* vs = ks + kTileKeys * (D + 4);
   float* ps = vs + kTileKeys * D;
+  // [row][2]: bits 0..63 and 64..127 of each row's mask
   unsigned long long* anc = reinterpret_cast<unsigned long long*>(ps + R * kTileKeys);
 
   // queries of the rows that read KV head h: row r = i*group + g
@@ -147,19 +149,22 @@ __global__ void __launch_bounds__(kSimtThreads) attn_split_kernel(
     qs[e] = to_f32(q[(((int64_t)b * d.M + i) * d.Hq + hq) * D + dd]) * qscale;
   }
   // ancestor-or-self masks of the new rows
-  if (tid < d.M) {
-    unsigned long long m = 0;
+  for (int i = tid; i < d.M; i += kSimtThreads) {
+    unsigned long long lo = 0, hi = 0;
     if (parent == nullptr) {
-      m = (tid == 63) ? ~0ull : ((1ull << (tid + 1)) - 1);
+      lo = i >= 63 ? ~0ull : ((1ull << (i + 1)) - 1);
+      hi = i >= 127 ? ~0ull : (i >= 64 ? ((1ull << (i - 63)) - 1) : 0ull);
     } else {
+      // the append kernel has checked the topology (parent[n] < n), so
+      // the walk reaches the root
       const int32_t* par = parent + (int64_t)b * d.M;
-      int n = tid;
-      for (int step = 0; step <= 64 && n >= 0; ++step) {
-        m |= 1ull << n;
-        n = par[n];
+      for (int n = i, step = 0; step <= kMaxRows && n >= 0; ++step, n = par[n]) {
+        if (n < 64) lo |= 1ull << n;
+        else hi |= 1ull << (n - 64);
       }
     }
-    anc[tid] = m;
+    anc[2 * i] = lo;
+    anc[2 * i + 1] = hi;
   }
 
   float o[RPW][DPL];
@@ -224,7 +229,10 @@ __global__ void __launch_bounds__(kSimtThreads) attn_split_kernel(
       if (r >= R) break;  // warp-uniform
       const int i = r / group;
       bool vis = t < k1;
-      if (vis && t >= ctx) vis = (anc[i] >> (t - ctx)) & 1ull;
+      if (vis && t >= ctx) {
+        const int k = t - ctx;  // new position, < M
+        vis = (anc[2 * i + (k >> 6)] >> (k & 63)) & 1ull;
+      }
       const float sj = vis ? sc[j] : -INFINITY;
       const float mnew = fmaxf(mrow[j], warp_max(sj));
       float p = 0.f, corr = 1.f;
@@ -381,12 +389,14 @@ static cudaError_t launch_simt(const AttnArgs& a, const WsLayout& lay, cudaStrea
     if (rpw <= 2) SPECV_SIMT(128, 2);
     else if (rpw <= 4) SPECV_SIMT(128, 4);
     else if (rpw <= 8) SPECV_SIMT(128, 8);
-    else SPECV_SIMT(128, 16);
+    else if (rpw <= 16) SPECV_SIMT(128, 16);
+    else SPECV_SIMT(128, 32);
   } else {
     if (rpw <= 2) SPECV_SIMT(64, 2);
     else if (rpw <= 4) SPECV_SIMT(64, 4);
     else if (rpw <= 8) SPECV_SIMT(64, 8);
-    else SPECV_SIMT(64, 16);
+    else if (rpw <= 16) SPECV_SIMT(64, 16);
+    else SPECV_SIMT(64, 32);
   }
 #undef SPECV_SIMT
   ++*launches;

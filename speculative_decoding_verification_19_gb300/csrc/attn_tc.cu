@@ -154,24 +154,36 @@ struct Cursor {
   }
 };
 
+// Bits [s, s + 64) of the 128-bit mask (lo, hi) as one word, bit j holding
+// mask bit s + j; bits outside [0, 128) read as 0 (s may be negative).
+__device__ __forceinline__ unsigned long long mask_window(unsigned long long lo,
+                                                          unsigned long long hi, int s) {
+  if (s <= -64 || s >= 128) return 0ull;
+  if (s < 0) return lo << -s;
+  if (s == 0) return lo;
+  if (s < 64) return (lo >> s) | (hi << (64 - s));
+  return hi >> (s - 64);
+}
+
 // Keys of a tile visible to a row, bit j for tile column j: below the
 // tile's valid keys and the request's length L, and either in the cached
 // prefix (position < ctx) or a new position that is an ancestor-or-self of
-// the row's node (bit pos - ctx of anc).
+// the row's node (bit pos - ctx of the 128-bit mask anc_lo, anc_hi).
 __device__ __forceinline__ unsigned long long tile_visibility(int kpos0, int nkeys, int ctx, int L,
-                                                              unsigned long long anc, bool real) {
+                                                              unsigned long long anc_lo,
+                                                              unsigned long long anc_hi, bool real) {
   if (!real) return 0ull;
   const int lim = min(L - kpos0, nkeys);  // nkeys is 16..64
   unsigned long long v = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1));
   const int c0 = ctx - kpos0;  // tile columns in the cached prefix
-  unsigned long long vm;
-  if (c0 >= 64)
-    vm = ~0ull;
-  else if (c0 > 0)
-    vm = ((1ull << c0) - 1) | (anc << c0);
-  else
-    vm = -c0 >= 64 ? 0ull : (anc >> -c0);
-  return v & vm;
+  const unsigned long long pre = c0 >= 64 ? ~0ull : (c0 > 0 ? ((1ull << c0) - 1) : 0ull);
+  return v & (pre | mask_window(anc_lo, anc_hi, -c0));
+}
+
+// Ancestor-or-self mask of row i of a chain: bits 0..i.
+__device__ __forceinline__ void chain_mask(int i, unsigned long long* lo, unsigned long long* hi) {
+  *lo = i >= 63 ? ~0ull : ((1ull << (i + 1)) - 1);
+  *hi = i >= 127 ? ~0ull : (i >= 64 ? ((1ull << (i - 63)) - 1) : 0ull);
 }
 
 __device__ __forceinline__ int tile_pages(int L, int tile) {
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ k_cache,
     __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int4* rq, const int4* starts, const unsigned long long* anc_ws, int* pairs, spec_dims d,
+    const int4* rq, const int4* starts, const ulonglong2* anc_ws, int* pairs, spec_dims d,
     float qscale2, float* part, __nv_bfloat16* __restrict__ out,
     float* __restrict__ lse, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
@@ -577,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       cu.start(st0, st1, rq, B);
       int64_t t = 0;
       float m_used = -INFINITY, l = 0.f;
-      unsigned long long anc = 0, anc_n = 0;
+      ulonglong2 anc = make_ulonglong2(0ull, 0ull), anc_n = anc;
       int anc_b = -1, anc_nb = -1;  // requests whose masks anc and anc_n hold
       int ctx = 0, L = 0, tile0 = 0;
       int n_whole = 0;  // pair ends with output so far (barrier phase)
@@ -593,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           m_used = -INFINITY;
           l = 0.f;
           if (anc_ws == nullptr) {
-            anc = (i >= 63) ? ~0ull : ((1ull << (i + 1)) - 1);
+            chain_mask(i, &anc.x, &anc.y);
           } else if (real && cu.b != anc_b) {
             // tree masks come from the prep kernel; the next request's mask
             // is loaded one request ahead
@@ -645,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         } else {
           // visibility of the tile's keys as a bitmask, then the same maximum
           // as the plain path over the visible ones
-          const unsigned long long vis = tile_visibility(kpos0, nkeys, ctx, L, anc, real);
+          const unsigned long long vis = tile_visibility(kpos0, nkeys, ctx, L, anc.x, anc.y, real);
           vh = (uint32_t)(vis >> jbase);
           const uint32_t vo = (uint32_t)(vis >> (jbase ^ 32));
           float a0 = -INFINITY, a1 = -INFINITY;
@@ -918,7 +930,7 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
     const int32_t* block_table, const int32_t* ctx_lens,
     const int32_t* __restrict__ parent, spec_dims d, int G, int32_t* __restrict__ ntiles,
     int64_t* __restrict__ pre, int4* __restrict__ rq, int4* __restrict__ starts,
-    int* __restrict__ pairs, unsigned long long* __restrict__ anc_ws,
+    int* __restrict__ pairs, ulonglong2* __restrict__ anc_ws,
     uint32_t* __restrict__ arrivals, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
     uint32_t* __restrict__ status) {
   __shared__ int s_last;
@@ -979,9 +991,12 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(
     // so every walk ends at the root within M steps)
     const int32_t* par = parent + (int64_t)b * M;
     for (int n = tid; n < M; n += blockDim.x) {
-      unsigned long long a = 0;
-      for (int k = n; k >= 0; k = par[k]) a |= 1ull << k;
-      anc_ws[(int64_t)b * M + n] = a;
+      unsigned long long lo = 0, hi = 0;  // bits 0..63, 64..127
+      for (int k = n; k >= 0; k = par[k]) {
+        if (k < 64) lo |= 1ull << k;
+        else hi |= 1ull << (k - 64);
+      }
+      anc_ws[(int64_t)b * M + n] = make_ulonglong2(lo, hi);
     }
   }
   if (tid == 0) {
@@ -1139,7 +1154,7 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
   int4* rq = reinterpret_cast<int4*>(ws + lay.tc_rq_off);
   int4* starts = reinterpret_cast<int4*>(ws + lay.tc_start_off);
   int* pairs = reinterpret_cast<int*>(ws + lay.tc_pair_off);
-  unsigned long long* anc = reinterpret_cast<unsigned long long*>(ws + lay.tc_anc_off);
+  ulonglong2* anc = reinterpret_cast<ulonglong2*>(ws + lay.tc_anc_off);
   uint32_t* arrivals = reinterpret_cast<uint32_t*>(ws + lay.tc_sync_off);
   float* part = reinterpret_cast<float*>(ws + lay.attn_off);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
@@ -1179,7 +1194,7 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
                            static_cast<__nv_bfloat16*>(a.k_cache),
                            static_cast<__nv_bfloat16*>(a.v_cache), a.block_table,
                            (const int4*)rq, (const int4*)starts,
-                           a.parent != nullptr ? (const unsigned long long*)anc : nullptr, pairs, d,
+                           a.parent != nullptr ? (const ulonglong2*)anc : nullptr, pairs, d,
                            qscale2, part, static_cast<__nv_bfloat16*>(a.out), a.lse, status);
     if (e != cudaSuccess) return e;
   }

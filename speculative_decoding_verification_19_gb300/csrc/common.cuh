@@ -11,6 +11,7 @@
 namespace specv {
 
 constexpr int kBlock = 16;          // tokens per KV block
+constexpr int kMaxNodes = 128;      // new rows (draft-tree nodes incl. the root) per request
 constexpr int kWarp = 32;
 
 // ---------------------------------------------------------------------------
@@ -144,7 +145,7 @@ struct WsLayout {
   size_t tc_start_off;    // [kMaxAttnCtas+1][2] int4 per CTA: first tile, its (request, head,
                           // tile), the request's record and the end tile
   size_t tc_pair_off;     // [B*Hkv] int32 per (request, KV head): tiles run by the later CTAs
-  size_t tc_anc_off;      // [B*M] u64 ancestor-or-self mask of every tree row
+  size_t tc_anc_off;      // [B*M] 128-bit ancestor-or-self mask of every tree row (2 u64)
   size_t tc_sync_off;     // uint32 arrival count of the request-check kernel
   size_t attn_off;        // split-KV partials of either attention path (f32)
   size_t attn_bytes;
@@ -157,9 +158,14 @@ struct WsLayout {
   size_t rs_zsum_off;     // [B, n_chunks] f64: residual mass of each statistics chunk
   int rs_chunk;           // logits per statistics chunk
   int rs_chunks;          // statistics chunks per row
-  size_t rsf_ctl_off;     // fused reject kernel: item counter, CTAs done, epoch tag (u32 x 4)
-  size_t rsf_req_off;     // [B] u32 items finished per request
-  size_t rsf_rec_off;     // [B, M] 32-byte record per (request, node)
+  // the one-kernel reject path (laid out by rsf_layout)
+  size_t rsf_ctl_off;     // 64 u32 control words
+  size_t rsf_norm_off;    // [B, 2M] 16-byte row normalisers
+  size_t rsf_rowcnt_off;  // [B, 2M] u32 statistics chunks finished per row
+  size_t rsf_req_off;     // [B] u32 rows finished per request
+  size_t rsf_list_off;    // [B] u32 request of each residual entry
+  size_t rsf_ready_off;   // [B] u32 the entry is written
+  size_t rsf_rescnt_off;  // [B] u32 residual units finished per request
   size_t total;
 };
 

@@ -201,7 +201,7 @@ spec_status spec_ctrl_metrics(const spec_ctrl_config* cfg, const spec_ctrl_reque
 
 spec_status spec_step_stats(const int32_t* accepted_len, const int32_t* path, const int32_t* parent,
                             int32_t B, int32_t M, spec_step_stats_out* out) {
-  if (accepted_len == nullptr || out == nullptr || B < 0 || M < 1 || M > 64)
+  if (accepted_len == nullptr || out == nullptr || B < 0 || M < 1 || M > SPEC_STEP_MAX_POS - 1)
     return SPEC_ERR_INVALID_ARG;
   memset(out, 0, sizeof(*out));
   double twe = 0;
@@ -222,17 +222,17 @@ spec_status spec_step_stats(const int32_t* accepted_len, const int32_t* path, co
     if (parent != nullptr && path != nullptr) {
       const int32_t* par = parent + (int64_t)b * M;
       // leaves of the drafted tree, and those below the first accepted node
-      unsigned long long has_kid = 0;
+      bool has_kid[SPEC_STEP_MAX_POS] = {};
       for (int c = 1; c < M; ++c)
-        if (par[c] >= 0 && par[c] < 64) has_kid |= 1ull << par[c];
+        if (par[c] >= 0 && par[c] < M) has_kid[par[c]] = true;
       int leaves = 0, hit = 0;
       const int first = a >= 1 ? path[(int64_t)b * M + 1] : -1;
       for (int c = 1; c < M; ++c) {
-        if ((has_kid >> c) & 1ull) continue;
+        if (has_kid[c]) continue;
         ++leaves;
         if (first < 0) continue;
         int x = c;
-        for (int guard = 0; guard < M && x > 0; ++guard) {
+        for (int guard = 0; guard < M && x > 0 && x < M; ++guard) {
           if (x == first) {
             ++hit;
             break;

@@ -42,7 +42,7 @@ namespace specv {
 constexpr int kRsThreads = 256;   // CTA size of the statistics kernel for unaligned rows
 constexpr int kDecThreads = 512;  // decide CTA size
 constexpr int kDecWarps = kDecThreads / kWarp;
-constexpr int kMaxM = 64;
+constexpr int kMaxM = kMaxNodes;
 constexpr int kMaxSweeps = 256;
 
 // Statistics chunk: one warp task, 32 lanes x 8 vectors (2048 bf16 / 1024 fp32 logits).
@@ -63,8 +63,11 @@ __device__ __forceinline__ bool row_needed(const int32_t* parent, int M, int b, 
   if (parent == nullptr) return n < M - 1;
   const int lane = threadIdx.x % kWarp;
   const int32_t* par = parent + (int64_t)b * M;
-  const int k1 = n + 1 + lane, k2 = n + 1 + kWarp + lane;
-  const bool f = (k1 < M && par[k1] == n) || (k2 < M && par[k2] == n);
+  bool f = false;
+  for (int k0 = n + 1; k0 < M; k0 += kWarp) {  // children have larger indices
+    const int k = k0 + lane;
+    f |= k < M && par[k] == n;
+  }
   return __any_sync(0xffffffffu, f);
 }
 
@@ -1318,598 +1321,722 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// One kernel, two roles: the logit stream on most SMs, the decisions on the
-// others, at the same time.
+// One kernel for a chain: statistics, decisions and draws, all warps alike.
 //
-// Stream CTAs (blockIdx < n_stream) claim batches of statistics tasks from a
-// global counter, in request-major order (request b's rows, chunks fastest),
-// copy each task's 4 KB chunk into a ring of shared-memory slots with 1-D
-// bulk copies (one issuing lane), and reduce it on 15 consumer warps, as
-// rs_rowstats_bulk_kernel does; after each chunk's statistics are written
-// the count of finished tasks of its request goes up (a release).  They
-// never wait on the deciders, so the stream runs at the rate of HBM.
+// Every warp streams statistics chunks through a private ring of 4 KB
+// shared-memory slots filled by 1-D bulk copies (as rs_rowstats_bulk_kernel
+// does), claiming batches of chunks from a global counter in request-major
+// order, so that requests are finished one after another while the stream
+// goes on.  What the finished chunks make ready is done by the warp that
+// makes it ready, between batches, while its next copies are in flight:
+//   * the chunks that complete a row: the row's normaliser (max m, sum S in
+//     fp64, and its first largest logit) from the row's chunk statistics;
+//   * the row that completes a request: the request's decisions (the accept
+//     tests of the chain, the number accepted) and, when every draft was
+//     accepted, the bonus draw from p; a rejection posts the request's
+//     residual chunks (one unit per statistics chunk) to a global list;
+//   * a residual unit, claimed from that list by any warp: the mass of
+//     max(0, p - q) over one chunk of the node's rows (re-read while still in
+//     L2); the unit that completes a request picks the chunk from the masses
+//     and the token inside it.
+// Only the decisions of the last requests, and their residual units (spread
+// over every warp), come after the stream ends.
 //
-// Decider CTAs take requests in order from a second counter, wait until the
-// request's count is complete (acquire; the stream reaches requests in order,
-// so this is soon), and run the decisions of rs_decide_kernel; a draw from a
-// residual is finished in the same CTA: the residual's mass over every
-// statistics chunk of the node's two rows (re-read while still in L2, all
-// warps, several chunks in flight), the chunk picked by the masses, and the
-// element found inside it.  Only the last requests' decisions come after the
-// stream ends.
+// Global control words ctl[] (two 128-byte lines: the batch counter, hit
+// by every claim, apart from the words idle warps poll):
+//   [0] next batch of statistics chunks  [1] residual entries allocated
+//   [2] CTAs finished
+//   [32] residual units published        [33] residual units claimed
+//   [34] requests finished               [35] the call failed (a wait gave up)
+// Every counter is back at zero when the call ends (the last CTA out resets
+// ctl and the entries' flags; each per-row and per-request counter is reset
+// by the warp that saw it complete), so the next call starts clean.  After a
+// wait gave up (SPEC_ERR_TIMEOUT) they are not: the workspace is initialised
+// again before the next call.
 // ---------------------------------------------------------------------------
-constexpr int kOvWarps = 16;      // per CTA: stream = producer warp + 15 consumers
-constexpr int kOvConsumers = kOvWarps - 1;
-// A stream task is a segment of up to four consecutive statistics chunks of
-// one row, copied by one 1-D bulk copy (16 KB): the copies one thread can
-// issue per microsecond, not the bytes, bounded 4 KB copies.
-constexpr int kSegChunks = 4;
-constexpr int kSegBytes = kSegChunks * kBulkSlot;
-constexpr int kOvSlots = 11;      // 16 KB ring slots (a decider pairs them: 5 of 32 KB)
-constexpr int kOvPairs = kOvSlots / 2;
-constexpr int kOvBatch = 32;      // tasks per claim
-constexpr int kOvGroups = 16;     // completion groups in flight per stream CTA
-constexpr int kOvMaxMeta = 2048;  // requests whose temperature and tree masks sit in shared memory
-constexpr int kOvMaxDeciders = 24;
-constexpr size_t kOvRingBytes = (size_t)kOvSlots * kSegBytes;
-constexpr size_t kOvSmem = kOvRingBytes + kOvMaxMeta * (sizeof(float) + sizeof(uint64_t)) + 1024;
-static_assert(kOvWarps * kWarp == kDecThreads, "a decider CTA is a decide CTA");
-constexpr int kGroupOpen = 1 << 30;  // a group's count before its producer closes it
+constexpr int kFWarps = 16;   // warps per CTA (one CTA per SM)
+constexpr int kFRing = 3;     // 4 KB slots per warp
+constexpr int kFBatch = 4;    // statistics chunks per claim
+constexpr size_t kFSmem = (size_t)kFWarps * kFRing * kBulkSlot + 1024;
+constexpr int kFCtl = 64;
+constexpr int kCBatch = 0, kCEntries = 1, kCCtas = 2;
+constexpr int kCPub = 32, kCClaim = 33, kCFin = 34, kCFail = 35;
 
-struct OvTask {
-  int b, which, n, c;  // request, target (0) or draft (1) row, node, first chunk
-  int nc;              // chunks in the segment
-  float cs;
-  int greedy, stop, grp;
-  int pad[3];
+// Normaliser of one logits row: its maximum m, S = sum exp2((z - m) cs) and
+// the index of its first largest logit.
+struct RowNorm {
+  float m;
+  int amax;
+  double S;
 };
 
-// Consecutive statistics tasks of one request on one stream CTA: the count
-// of finished tasks is published for the whole group at once (one fence and
-// one atomic), not per task.
-struct OvGroup {
-  int b, total;
-  int remaining;  // kGroupOpen - tasks finished - (kGroupOpen - total) once closed
-  int free;
+struct FusedWs {
+  RowStat* stats;
+  RowNorm* norms;       // [B][2M]: target row n at n, draft row n at M + n
+  uint32_t* row_cnt;    // [B][2M]: statistics chunks finished per row
+  uint32_t* req_rows;   // [B]: rows finished per request
+  uint32_t* res_list;   // [B]: request of each residual entry
+  uint32_t* res_ready;  // [B]: the entry is written
+  uint32_t* res_cnt;    // [B]: residual units finished per request
+  DrawState* draws;     // [B]: the residual law of each posted request
+  double* zsum;         // [B][n_chunks]: residual mass per chunk
+  uint32_t* ctl;        // [kFCtl]
+  uint32_t* status;
 };
 
-// Weights of the residual law over one chunk held in shared memory (target
-// and draft chunks side by side), by one warp: lane l takes vectors v * 32 + l.
-template <typename T>
-__device__ __forceinline__ float smem_chunk_mass(const uint4* st, const uint4* sd, int e0, int V,
-                                                 const DecideCtx& c, int nrej) {
-  constexpr int EPV = 16 / sizeof(T);
-  const int lane = threadIdx.x % kWarp;
-  float s = 0.f;
-#pragma unroll
-  for (int v = 0; v < kStatVecs; ++v) {
-    const int e = e0 + (v * kWarp + lane) * EPV;
-    if (e >= V) continue;
-    float zt[EPV], zd[EPV];
-    unpack16(st[v * kWarp + lane], zt);
-    unpack16(sd[v * kWarp + lane], zd);
-#pragma unroll
-    for (int i = 0; i < EPV; ++i) s += (e + i < V) ? weight_of(zt[i], zd[i], c, nrej) : 0.f;
-  }
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// A chunk statistic written by another SM during this kernel, read through L2.
+__device__ __forceinline__ RowStat ld_stat(const RowStat* p) {
+  const uint4 r = __ldcg(reinterpret_cast<const uint4*>(p));
+  RowStat s;
+  s.m = __uint_as_float(r.x);
+  s.pad = __uint_as_float(r.y);
+  s.s = __hiloint2double((int)r.w, (int)r.z);
   return s;
 }
 
-// Wait until the CTA's issue count (shared memory, written by its issuing
-// thread) exceeds `need`; gives up like ptx::mbar_wait.
-__device__ __forceinline__ bool wait_issued(volatile long long* cnt, long long need,
-                                            volatile int* abort, uint64_t timeout_cycles) {
-  long long t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (*cnt >= need) return true;
-    if ((it & 7u) == 7u) {
-      if (*abort) return false;
-      const long long now = clock64();
-      if (t0 == 0) {
-        t0 = now;
-      } else if ((uint64_t)(now - t0) > timeout_cycles) {
-        *abort = 1;
-        return false;
-      }
+__device__ __forceinline__ RowNorm ld_norm(const RowNorm* p) {
+  const uint4 r = __ldcg(reinterpret_cast<const uint4*>(p));
+  RowNorm n;
+  n.m = __uint_as_float(r.x);
+  n.amax = (int)r.y;
+  n.S = __hiloint2double((int)r.w, (int)r.z);
+  return n;
+}
+
+// The normaliser of one row from its chunk statistics (one warp), formed as
+// rs_decide_kernel forms it: the fp32 maximum, the fp64 sum of the rescaled
+// chunk sums, and the first chunk holding the maximum for the argmax.
+__device__ __noinline__ void fused_row_norm(const RowStat* st, int n_chunks, int chunk, float cs,
+                                            RowNorm* out) {
+  const int lane = threadIdx.x % kWarp;
+  constexpr int kItems = 16;  // n_chunks <= 512
+  float im[kItems];
+  double is[kItems];
+  int ia[kItems];
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    const int c = lane + j * kWarp;
+    if (c < n_chunks) {
+      const RowStat x = ld_stat(st + c);
+      im[j] = x.m;
+      is[j] = x.s;
+      ia[j] = unpack_index(x.pad);
+    } else {
+      im[j] = -INFINITY;
+      is[j] = 0.0;
+      ia[j] = 0;
     }
-    __nanosleep(32);
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) m = fmaxf(m, im[j]);
+  m = warp_max(m);
+  double s = 0.0;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j)
+    if (im[j] != -INFINITY) s += is[j] * (double)fast_exp2((im[j] - m) * cs);
+  s = warp_sum(s);
+  int c_first = 0x7fffffff, a_first = 0;
+#pragma unroll
+  for (int j = kItems - 1; j >= 0; --j) {  // this lane's first chunk holding m
+    const int c = lane + j * kWarp;
+    if (c < n_chunks && im[j] == m) {
+      c_first = c;
+      a_first = ia[j];
+    }
+  }
+  const int cmin = __reduce_min_sync(0xffffffffu, c_first);
+  const unsigned own = __ballot_sync(0xffffffffu, c_first == cmin);
+  const int am = __shfl_sync(0xffffffffu, a_first, __ffs(own) - 1);
+  if (lane == 0) {
+    RowNorm r;
+    r.m = m;
+    r.amax = cmin < n_chunks ? cmin * chunk + am : 0;
+    r.S = s;
+    *out = r;
   }
 }
 
-// ctl: [0] next task batch, [1] next request to decide, [2] CTAs finished,
-// [3] the call failed (a wait gave up)
+// Marks request b finished (its outputs are written).
+__device__ __forceinline__ void fused_finish(uint32_t* ctl) {
+  if (threadIdx.x % kWarp == 0) {
+    __threadfence();
+    atomicAdd(ctl + kCFin, 1u);
+  }
+}
+
+// The decisions of chain request b, by one warp, once every row's normaliser
+// is written: validation, the accept tests of every draft at once (the same
+// arithmetic as rs_decide_kernel's chain path), the outputs, and the draw
+// (bonus from p here; a residual is posted as units).
 template <typename T>
-__global__ void __launch_bounds__(kDecThreads, 1) rs_overlap_kernel(
+__device__ __noinline__ void fused_decide(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
-    const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
-    uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
+    const float* __restrict__ temperature, uint64_t seed, uint64_t offset, uint64_t b_base,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ path, int32_t* __restrict__ accepted_len,
+    float* __restrict__ probe, const spec_dims& d, int n_chunks, int chunk, const FusedWs& w,
+    int b) {
+  const int lane = threadIdx.x % kWarp;
+  const int M = d.M, V = d.V;
+  const float temp = temperature[b];
+  const bool greedy = temp == 0.f;
+  const float cs = stat_scale(temp);
+  const RowNorm* nb = w.norms + (int64_t)b * 2 * M;
+  int32_t* ot = out_tokens + (int64_t)b * M;
+  int32_t* pt = path + (int64_t)b * M;
+  float* pr = probe != nullptr ? probe + (int64_t)b * M * 4 : nullptr;
+
+  // validation: the temperature, the drafted tokens, every row's normaliser
+  bool bad_arg = !temperature_valid(temp), bad_tok = false, bad_row = false;
+  for (int n = lane; n < M; n += kWarp) {
+    if (n >= 1) {
+      const int32_t x = tokens[(int64_t)b * M + n];
+      bad_tok |= (x < 0 || x >= V);
+    }
+    const RowNorm t = ld_norm(nb + n);
+    bad_row |= !(t.m > -INFINITY && t.m < INFINITY && t.S > 0.0 && t.S < INFINITY);
+    if (n < M - 1) {
+      const RowNorm q = ld_norm(nb + M + n);
+      bad_row |= !(q.m > -INFINITY && q.m < INFINITY && q.S > 0.0 && q.S < INFINITY);
+    }
+  }
+  bad_arg = __any_sync(0xffffffffu, bad_arg);
+  bad_tok = __any_sync(0xffffffffu, bad_tok);
+  bad_row = __any_sync(0xffffffffu, bad_row);
+  if (bad_arg || bad_tok || bad_row) {
+    for (int i = lane; i < M; i += kWarp) {
+      ot[i] = -1;
+      pt[i] = -1;
+    }
+    if (pr != nullptr)
+      for (int i = lane; i < 4 * M; i += kWarp) pr[i] = -1.f;
+    if (lane == 0) {
+      accepted_len[b] = -1;
+      raise_status(w.status, bad_arg ? SPEC_ERR_INVALID_ARG
+                             : bad_tok ? SPEC_ERR_DEVICE_BOUNDS
+                                       : SPEC_ERR_NONFINITE);
+    }
+    fused_finish(w.ctl);
+    return;
+  }
+
+  // the accept tests: lane n - 1 (mod 32) tests draft n against row n - 1
+  const uint64_t bglob = b_base + (uint64_t)b;
+  const double cs64 = (double)cs;
+  int fr = M;  // first rejected draft, M if none
+  for (int n0 = 1; n0 < M && fr == M; n0 += kWarp) {
+    const int n = n0 + lane;
+    bool rej = false;
+    float pp = -1.f, qq = -1.f;
+    if (n < M) {
+      const int p = n - 1;
+      const int32_t x = tokens[(int64_t)b * M + n];
+      const int64_t o = ((int64_t)b * M + p) * V + x;
+      const float zt = to_f32(target[o]), zd = to_f32(draft[o]);
+      const RowNorm t = ld_norm(nb + p), q = ld_norm(nb + M + p);
+      if (greedy) {
+        rej = x != t.amax;
+        pp = rej ? 0.f : 1.f;
+        qq = x == q.amax ? 1.f : 0.f;
+      } else {
+        const Philox4 r = philox4x64_10((uint64_t)n + 1, bglob, offset, 0, seed, 0);
+        const float uacc = (float)u24(r.w[0]);
+        const double et = ((double)zt - (double)t.m) * cs64;  // log2 unnormalised p(x)
+        const double ed = ((double)zd - (double)q.m) * cs64;  // log2 unnormalised q(x)
+        const float st_f = (float)t.S, sd_f = (float)q.S;
+        bool acc;
+        if (ed == -INFINITY) {
+          acc = et != -INFINITY;
+        } else if (et == -INFINITY) {
+          acc = false;
+        } else {
+          const double e = et - ed;
+          const double ei = rint(e);
+          const float ratio =
+              ldexpf(fast_exp2((float)(e - ei)), (int)fmax(fmin(ei, 300.0), -300.0)) * (sd_f / st_f);
+          acc = uacc < ratio;
+        }
+        rej = !acc;
+        pp = exp2f((float)et) / st_f;
+        qq = exp2f((float)ed) / sd_f;
+      }
+    }
+    const unsigned rb = __ballot_sync(0xffffffffu, rej);
+    const int first = rb ? n0 + __ffs(rb) - 1 : M;
+    // probes of the tested drafts: up to and including the first rejected
+    if (pr != nullptr && n < M) {
+      const bool tested = n <= first;
+      pr[n * 4 + 0] = tested ? pp : -1.f;
+      pr[n * 4 + 1] = tested ? qq : -1.f;
+      pr[n * 4 + 2] = -1.f;
+      pr[n * 4 + 3] = -1.f;
+    }
+    if (first < M) fr = first;
+  }
+  if (pr != nullptr) {
+    for (int n = fr + 1 + lane; n < M; n += kWarp) {  // past the first rejection: untested
+      pr[n * 4 + 0] = -1.f;
+      pr[n * 4 + 1] = -1.f;
+      pr[n * 4 + 2] = -1.f;
+      pr[n * 4 + 3] = -1.f;
+    }
+    if (lane == 0)
+      for (int i = 0; i < 4; ++i) pr[i] = -1.f;  // the root is never tested
+  }
+  const int a = fr < M ? fr - 1 : M - 1;  // accepted drafts = the node that draws
+  for (int n = lane; n < M; n += kWarp) {
+    pt[n] = n <= a ? n : -1;
+    if (n < a) ot[n] = tokens[(int64_t)b * M + n + 1];
+    else if (n > a) ot[n] = -1;
+  }
+  if (lane == 0) accepted_len[b] = a;
+
+  if (greedy) {
+    // the token at node a is its target row's first largest logit
+    if (lane == 0) {
+      ot[a] = ld_norm(nb + a).amax;
+      if (pr != nullptr) {
+        pr[a * 4 + 2] = 1.f;
+        pr[a * 4 + 3] = 1.f;
+      }
+    }
+    fused_finish(w.ctl);
+    return;
+  }
+  const Philox4 r = philox4x64_10((uint64_t)a + 1, bglob, offset, 0, seed, 0);
+  const double u = (double)u24(r.w[1]);
+  const RowNorm ta = ld_norm(nb + a);
+  DecideCtx c;
+  c.mT = ta.m;
+  c.invST = (float)(1.0 / ta.S);
+  c.cs = cs;
+  if (fr < M) {
+    // the residual max(0, p_a - q_a): post its chunks
+    const RowNorm da = ld_norm(nb + M + a);
+    c.mD = da.m;
+    c.invSD = (float)(1.0 / da.S);
+    c.nrej = 1;
+    if (lane == 0) {
+      DrawState& ds = w.draws[b];
+      ds.c.mT = c.mT;
+      ds.c.mD = c.mD;
+      ds.c.invST = c.invST;
+      ds.c.invSD = c.invSD;
+      ds.c.cs = c.cs;
+      ds.c.nrej = 1;
+      ds.u = u;
+      ds.node = a;
+      ds.a = a;
+      ds.pending = 1;
+      const uint32_t e = atomicAdd(w.ctl + kCEntries, 1u);
+      w.res_list[e] = (uint32_t)b;
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(w.res_ready + e), "r"(1u) : "memory");
+      atomicAdd(w.ctl + kCPub, (uint32_t)n_chunks);
+    }
+    return;
+  }
+  // every draft accepted: the bonus token from p of the last node
+  c.mD = 0.f;
+  c.invSD = 0.f;
+  c.nrej = 0;
+  const T* trow = target + ((int64_t)b * M + a) * V;
+  const RowStat* tst = w.stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
+  float wt;
+  double z;
+  const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &wt, &z);
+  if (lane == 0) {
+    ot[a] = tk;
+    if (pr != nullptr) {
+      pr[a * 4 + 2] = 1.0f;
+      pr[a * 4 + 3] = (float)((double)wt / z);
+    }
+  }
+  fused_finish(w.ctl);
+}
+
+// One residual unit (entry e, statistics chunk c), by one warp: the chunk's
+// residual mass; the unit that completes its request draws the token.
+template <typename T>
+__device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
+                                                 const T* __restrict__ draft,
+                                                 int32_t* __restrict__ out_tokens,
+                                                 float* __restrict__ probe, const spec_dims& d,
+                                                 int n_chunks, int chunk, const FusedWs& w,
+                                                 uint32_t e, int c, volatile int* abort,
+                                                 uint64_t wait) {
+  const int lane = threadIdx.x % kWarp;
+  const int M = d.M, V = d.V;
+  // the entry is allocated; its writer publishes it right away (bounded)
+  if (lane == 0) {
+    long long t0 = 0;
+    for (uint32_t it = 0; ld_acquire_u32(w.res_ready + e) == 0u; ++it) {
+      if ((it & 15u) == 15u) {
+        if (*abort || ld_relaxed_u32(w.ctl + kCFail) != 0u) {
+          *abort = 1;
+          break;
+        }
+        const long long now = clock64();
+        if (t0 == 0) {
+          t0 = now;
+        } else if ((uint64_t)(now - t0) > wait) {
+          *abort = 1;
+          break;
+        }
+      }
+      __nanosleep(64);
+    }
+  }
+  if (__shfl_sync(0xffffffffu, (int)*abort, 0)) return false;
+  const int b = (int)__ldcg(w.res_list + e);
+  const DrawState* ds = w.draws + b;
+  DecideCtx ctx;
+  ctx.mT = __ldcg(&ds->c.mT);
+  ctx.mD = __ldcg(&ds->c.mD);
+  ctx.invST = __ldcg(&ds->c.invST);
+  ctx.invSD = __ldcg(&ds->c.invSD);
+  ctx.cs = __ldcg(&ds->c.cs);
+  ctx.nrej = 1;
+  const int node = __ldcg(&ds->node);
+  const T* trow = target + ((int64_t)b * M + node) * V;
+  const T* drow = draft + ((int64_t)b * M + node) * V;
+  uint4 raw_t[kStatVecs], raw_d[kStatVecs];
+  const float ls = lane_weights<T>(trow, drow, (int64_t)c * chunk, V, ctx, 1, raw_t, raw_d);
+  const dfloat tot = df_warp_sum(df_make(ls));
+  double* zs = w.zsum + (int64_t)b * n_chunks;
+  uint32_t done = 0;
+  if (lane == 0) {
+    zs[c] = df_to_d(tot);
+    __threadfence();
+    done = atomicAdd(w.res_cnt + b, 1u) + 1u;
+  }
+  done = __shfl_sync(0xffffffffu, done, 0);
+  if (done != (uint32_t)n_chunks) return true;
+  // the last unit of request b: the draw
+  __threadfence();
+  const int a_acc = __ldcg(&ds->a);
+  const double u = __ldcg(&ds->u);
+  double Z = 0.0;
+  for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
+  Z = warp_sum(Z);
+  float wt;
+  int tk;
+  double zrep;
+  if (Z > 0.0) {
+    double pre;
+    const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
+    const double trel = u * Z - pre;
+    const float th = (float)trel;
+    tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, ctx, 1,
+                            dfloat{th, (float)(trel - (double)th)}, &wt);
+    zrep = Z;
+  } else {
+    // a residual of zero mass: the draw from p of the node
+    DecideCtx cp = ctx;
+    cp.nrej = 0;
+    const RowStat* tst = w.stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
+    double z;
+    tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, cp, u, &wt, &z);
+    zrep = z;
+    Z = 1.0;
+  }
+  if (lane == 0) {
+    out_tokens[(int64_t)b * M + a_acc] = tk;
+    if (probe != nullptr) {
+      probe[((int64_t)b * M + node) * 4 + 2] = (float)Z;
+      probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)wt / zrep);
+    }
+    w.res_cnt[b] = 0u;  // ready for the next call
+  }
+  fused_finish(w.ctl);
+  return true;
+}
+
+
+template <typename T>
+__global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
+    const float* __restrict__ temperature, uint64_t seed, uint64_t offset, uint64_t b_base,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, RowStat* stats, DrawState* draws, double* zsum, uint32_t* ctl, uint32_t* req_done,
-    int n_stream, uint32_t* status) {
+    int chunk, FusedWs w) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kChunk = kWarp * kStatVecs * EPV;
-  __shared__ DecideSmem sh;
-  __shared__ OvTask desc[kOvSlots];
-  __shared__ OvGroup grp[kOvGroups];
-  __shared__ uint64_t full[kOvSlots], empty[kOvSlots];
-  __shared__ int s_abort, s_req;
-  // copies issued into the ring so far (tasks for stream CTAs, chunk pairs
-  // for deciders): a reader waits for its copy to be issued before waiting
-  // on the slot's full barrier, so that it never waits more than one phase
-  // ahead of the barrier (there are more readers than slots)
-  __shared__ long long s_issued;
+  __shared__ uint64_t full[kFWarps][kFRing];
+  __shared__ long long s_task[kFWarps][kFRing];
+  __shared__ int s_abort, s_last;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* s_temp = reinterpret_cast<float*>(ring + kOvRingBytes);
-  unsigned long long* s_kids = reinterpret_cast<unsigned long long*>(s_temp + kOvMaxMeta);
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int B = d.B, M = d.M, V = d.V;
   const uint64_t wait = wait_limit_cycles(d);
-  volatile int* abort = &s_abort;
-  const int rows = parent == nullptr ? 2 * M - 1 : 2 * M;  // rows numbered per request
-  const int64_t per_req = (int64_t)rows * n_chunks;
-  const int64_t ntask = per_req * B;
-  volatile uint32_t* failed = ctl + 3;
-  const bool meta_in_smem = B <= kOvMaxMeta;
-
   if (tid == 0) {
-    for (int i = 0; i < kOvSlots; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&empty[i]), 1);
-    }
+    for (int i = 0; i < kFWarps; ++i)
+      for (int j = 0; j < kFRing; ++j) ptx::mbar_init(ptx::smem_u32(&full[i][j]), 1);
     s_abort = 0;
-    s_issued = 0;
     ptx::fence_mbar_init();
   }
-  volatile long long* issued = &s_issued;
-  for (int g = tid; g < kOvGroups; g += kDecThreads) grp[g].free = 1;
   __syncthreads();
   pdl_trigger();
   pdl_wait();  // the logits may come from the previous kernel
+  volatile int* abort = &s_abort;
+  uint32_t* ctl = w.ctl;
+  const int rows = 2 * M - 1;  // target rows 0..M-1, then draft rows 0..M-2
+  const int64_t per_req = (int64_t)rows * n_chunks;
+  const int64_t ntask = per_req * B;
+  const int64_t nbatch = (ntask + kFBatch - 1) / kFBatch;
+  uint8_t* myring = ring + (size_t)warp * kFRing * kBulkSlot;
+  uint64_t* mybars = full[warp];
+  long long* mytask = s_task[warp];
+  // Warps 0..3 of each CTA take residual units between their batches; after
+  // the stream, warp 0 stays to take them until every request is finished,
+  // the others leave once they hold none.
+  const bool poll = warp < 4;
+  const bool poller = warp == 0;
 
-  if ((int)blockIdx.x < n_stream) {
-    // ================================================================ stream
-    // the requests' temperatures and tree masks, once, before any copy is
-    // queued (a plain load behind queued bulk copies waits for all of them)
-    if (meta_in_smem) {
-      for (int i = tid; i < B; i += kDecThreads) s_temp[i] = temperature[i];
-      if (parent != nullptr)
-        for (int i = warp; i < B; i += kOvWarps) {
-          const int32_t* pr = parent + (int64_t)i * M;
-          unsigned lo = 0, hi = 0;
-          for (int k = 1 + lane; k < M; k += kWarp) {
-            const int pn = pr[k];
-            if (pn >= 0 && pn < 32) lo |= 1u << pn;
-            else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
-          }
-          lo = __reduce_or_sync(0xffffffffu, lo);
-          hi = __reduce_or_sync(0xffffffffu, hi);
-          if (lane == 0) s_kids[i] = ((unsigned long long)hi << 32) | lo;
-        }
+  // the stream: tasks [it, it_end) of the current batch are still to be
+  // issued; `next` is the batch claimed after it (claimed one batch early,
+  // so the atomic's latency hides behind the copies)
+  int64_t it = 0, it_end = 0;
+  uint32_t next = 0;  // lane 0: the claim's result, read one batch later
+  if (lane == 0) next = atomicAdd(ctl + kCBatch, 1u);
+  bool stream_done = false;
+  int64_t issued = 0, consumed = 0;
+  auto issue_one = [&]() -> bool {  // whole warp; false once the stream has no task left
+    if (it == it_end) {
+      const uint32_t nb = __shfl_sync(0xffffffffu, next, 0);
+      if ((int64_t)nb >= nbatch) return false;
+      it = (int64_t)nb * kFBatch;
+      it_end = it + kFBatch < ntask ? it + kFBatch : ntask;
+      if (lane == 0) next = atomicAdd(ctl + kCBatch, 1u);
     }
-    __syncthreads();
-    if (warp == 0) {
-      // producer: the whole warp walks the tasks, lane 0 issues the copies
-      int64_t task = 0;  // tasks issued by this CTA
-      int ngrp = 0;      // groups opened by this CTA
-      int g_open = -1, g_count = 0;
-      bool ok = true;
-      int cur_b = -1;
-      unsigned long long kids = 0;  // nodes of request cur_b that have children
-      float cur_cs = 1.f;
-      int cur_greedy = 0;
-      auto close_group = [&]() {  // lane 0
-        if (g_open >= 0) {
-          grp[g_open].total = g_count;
-          __threadfence_block();
-          if (atomicSub(&grp[g_open].remaining, kGroupOpen - g_count) == kGroupOpen - g_count) {
-            // every task already finished: publish here
-            __threadfence();
-            atomicAdd(req_done + grp[g_open].b, (uint32_t)g_count);
-            *reinterpret_cast<volatile int*>(&grp[g_open].free) = 1;
-          }
-          g_open = -1;
-        }
-      };
-      uint32_t next = 0;
-      if (lane == 0) next = atomicAdd(ctl + 0, 1u);
-      next = __shfl_sync(0xffffffffu, next, 0);
-      while (ok) {
-        const int64_t t0 = (int64_t)next * kOvBatch;
-        if (t0 >= ntask) break;
-        // claim the next batch now: its index is needed only after this one
-        uint32_t after = 0;
-        if (lane == 0) after = atomicAdd(ctl + 0, 1u);
-        const int64_t t1 = t0 + kOvBatch < ntask ? t0 + kOvBatch : ntask;
-        bool sg_c_first_of_batch = true;  // the batch's first segment opens a group
-        // the batch's first task decoded once, then walked (chunks fastest)
-        int b = (int)(t0 / per_req);
-        const int rem0 = (int)(t0 - (int64_t)b * per_req);
-        int row = rem0 / n_chunks, c = rem0 - row * n_chunks;
-        // segments: consecutive chunks of one row, up to kSegChunks
-        int sg_b = -1, sg_which = 0, sg_n = 0, sg_c = 0, sg_nc = 0;
-        auto issue_segment = [&]() {  // whole warp; lane 0 issues
-          if (sg_nc == 0) return;
-          const int slot = (int)(task % kOvSlots);
-          if (lane == 0) {
-            // a new group at the batch's first segment and at every new request
-            if (g_open < 0 || grp[g_open].b != sg_b || sg_c_first_of_batch) {
-              close_group();
-              const int g = ngrp % kOvGroups;
-              long long w0 = 0;
-              while (!*reinterpret_cast<volatile int*>(&grp[g].free)) {  // bounded
-                const long long now = clock64();
-                if (w0 == 0) w0 = now;
-                else if ((uint64_t)(now - w0) > wait || *abort) {
-                  *abort = 1;
-                  ok = false;
-                  break;
-                }
-              }
-              if (ok) {
-                grp[g].free = 0;
-                grp[g].b = sg_b;
-                grp[g].total = 0;
-                grp[g].remaining = kGroupOpen;
-                g_open = g;
-                g_count = 0;
-                ++ngrp;
-              }
-            }
-            if (ok && task >= kOvSlots &&
-                !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
-                                abort, wait))
-              ok = false;
-            if (ok) {
-              g_count += sg_nc;
-              desc[slot] = OvTask{sg_b, sg_which, sg_n, sg_c, sg_nc, cur_cs, cur_greedy, 0, g_open, {0, 0, 0}};
-              const int64_t e0 = (int64_t)sg_c * kChunk;
-              const int64_t left = (int64_t)V - e0;
-              const int64_t want = (int64_t)sg_nc * kChunk;
-              const uint32_t bytes = (uint32_t)((left < want ? left : want) * sizeof(T));
-              const uint32_t fb = ptx::smem_u32(&full[slot]);
-              ptx::mbar_arrive_expect_tx(fb, bytes);
-              ptx::bulk_g2s(ptx::smem_u32(ring + (size_t)slot * kSegBytes),
-                            (sg_which == 0 ? target : draft) + ((int64_t)sg_b * M + sg_n) * V + e0, bytes,
-                            fb);
-              *issued = task + 1;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          ++task;
-          sg_nc = 0;
-          sg_c_first_of_batch = false;
-        };
-        for (int64_t t = t0; t < t1 && ok; ++t) {
-          if (t > t0 && ++c == n_chunks) {
-            c = 0;
-            if (++row == rows) {
-              row = 0;
-              ++b;
-            }
-          }
-          const int which = row < M ? 0 : 1, n = row < M ? row : row - M;
-          if (b != cur_b) {
-            issue_segment();
-            if (!ok) break;
-            cur_b = b;
-            float temp;
-            if (meta_in_smem) {
-              temp = s_temp[b];
-              kids = parent != nullptr ? s_kids[b] : 0;
-            } else {
-              temp = temperature[b];
-              kids = 0;
-              if (parent != nullptr) {
-                const int32_t* pr = parent + (int64_t)b * M;
-                unsigned lo = 0, hi = 0;
-                for (int k = 1 + lane; k < M; k += kWarp) {
-                  const int pn = pr[k];
-                  if (pn >= 0 && pn < 32) lo |= 1u << pn;
-                  else if (pn >= 32 && pn < 64) hi |= 1u << (pn - 32);
-                }
-                lo = __reduce_or_sync(0xffffffffu, lo);
-                hi = __reduce_or_sync(0xffffffffu, hi);
-                kids = ((unsigned long long)hi << 32) | lo;
-              }
-            }
-            cur_cs = stat_scale(temp);
-            cur_greedy = temp == 0.f;
-          }
-          if (which == 1 && parent != nullptr && !((kids >> n) & 1ull)) continue;  // a leaf's draft row
-          if (sg_nc > 0 && (sg_which != which || sg_n != n || sg_nc == kSegChunks)) {
-            issue_segment();
-            if (!ok) break;
-          }
-          if (sg_nc == 0) {
-            sg_b = b;
-            sg_which = which;
-            sg_n = n;
-            sg_c = c;
-          }
-          ++sg_nc;
-        }
-        if (ok) issue_segment();
-        next = __shfl_sync(0xffffffffu, after, 0);
+    const int64_t t = it++;
+    const int slot = (int)(issued % kFRing);
+    if (lane == 0) {
+      const int b = (int)(t / per_req);
+      const int rem = (int)(t - (int64_t)b * per_req);
+      const int row = rem / n_chunks, c = rem - row * n_chunks;
+      const T* src = row < M ? target + ((int64_t)b * M + row) * V
+                             : draft + ((int64_t)b * M + (row - M)) * V;
+      const int64_t e0 = (int64_t)c * kChunk;
+      const int64_t left = (int64_t)V - e0;
+      const uint32_t bytes = (uint32_t)((left < kChunk ? left : kChunk) * sizeof(T));
+      mytask[slot] = t;
+      const uint32_t bar = ptx::smem_u32(&mybars[slot]);
+      ptx::mbar_arrive_expect_tx(bar, bytes);
+      ptx::bulk_g2s(ptx::smem_u32(myring + (size_t)slot * kBulkSlot), src + e0, bytes, bar);
+    }
+    ++issued;
+    return true;
+  };
+
+  // finished chunks of one row not yet counted (published at each row
+  // change and at the end of each batch)
+  int acc_key = -1, acc_b = 0;
+  uint32_t acc_n = 0;
+  float acc_cs = 1.f;
+  auto flush_row = [&]() -> bool {  // whole warp; false if a wait gave up
+    if (acc_n == 0) return true;
+    uint32_t old = 0;
+    if (lane == 0) {
+      __threadfence();  // this warp's statistics before the count
+      old = atomicAdd(w.row_cnt + acc_key, acc_n);
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    const uint32_t n = acc_n;
+    acc_n = 0;
+    if (old + n != (uint32_t)n_chunks) return true;
+    // this warp finished the row: its normaliser
+    __threadfence();
+    const int b = acc_b, row = acc_key - b * 2 * M;
+    const int which = row < M ? 0 : 1, node = row < M ? row : row - M;
+    fused_row_norm(w.stats + (((int64_t)b * 2 + which) * M + node) * n_chunks, n_chunks, chunk,
+                   acc_cs, w.norms + acc_key);
+    uint32_t r = 0;
+    if (lane == 0) {
+      w.row_cnt[acc_key] = 0u;  // ready for the next call
+      __threadfence();
+      r = atomicAdd(w.req_rows + b, 1u) + 1u;
+    }
+    r = __shfl_sync(0xffffffffu, r, 0);
+    if (r != (uint32_t)rows) return true;
+    // ... and the request: its decisions
+    __threadfence();
+    if (lane == 0) w.req_rows[b] = 0u;
+    fused_decide<T>(target, draft, tokens, temperature, seed, offset, b_base, out_tokens, path,
+                    accepted_len, probe, d, n_chunks, chunk, w, b);
+    return true;
+  };
+
+  int64_t reserved = -1;  // a residual unit this warp claimed and has not done
+  int cur_b = -1;
+  float cs = 1.f;
+  bool greedy = false;
+  long long idle0 = 0;
+  int backoff = 64;
+  for (;;) {
+    if (*abort) break;
+    while (!stream_done && issued - consumed < kFRing)
+      if (!issue_one()) stream_done = true;
+    // the control words, loaded now and looked at after the batch
+    uint4 cw = make_uint4(0, 0, 0, 0);
+    if (lane == 0 && poll)
+      asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                   : "l"(ctl + kCPub)
+                   : "memory");
+    bool ok = true;
+    const bool had_work = consumed < issued;
+    for (int k = 0; k < kFBatch && consumed < issued; ++k) {
+      const int slot = (int)(consumed % kFRing);
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&mybars[slot]),
+                                                   (uint32_t)((consumed / kFRing) & 1), abort,
+                                                   wait))) {
+        ok = false;
+        break;
       }
-      if (lane == 0 && ok) close_group();
-      // one stop task per consumer warp
-      for (int w = 0; w < kOvConsumers && ok; ++w) {
-        const int slot = (int)(task % kOvSlots);
-        if (lane == 0) {
-          if (task >= kOvSlots &&
-              !ptx::mbar_wait(ptx::smem_u32(&empty[slot]), (uint32_t)(((task / kOvSlots) & 1) ^ 1),
-                              abort, wait))
-            ok = false;
-          if (ok) {
-            desc[slot].stop = 1;
-            ptx::mbar_arrive(ptx::smem_u32(&full[slot]));
-            *issued = task + 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        ++task;
+      const int64_t t = mytask[slot];
+      const int b = (int)(t / per_req);
+      const int rem = (int)(t - (int64_t)b * per_req);
+      const int row = rem / n_chunks, c = rem - row * n_chunks;
+      if (b != cur_b) {
+        cur_b = b;
+        const float temp = temperature[b];
+        cs = stat_scale(temp);
+        greedy = temp == 0.f;
       }
-      // every copy issued lands before the CTA may exit
-      if (lane == 0) {
-        const long long n_iss = *issued;
-        for (long long u = n_iss > kOvSlots ? n_iss - kOvSlots : 0; u < n_iss; ++u)
-          ptx::mbar_drain(ptx::smem_u32(&full[u % kOvSlots]), (uint32_t)((u / kOvSlots) & 1),
-                          kDefaultWaitCycles);
-      }
-    } else {
-      // consumers: task t on warp 1 + t mod 15
-      for (int64_t t = warp - 1;; t += kOvConsumers) {
-        const int slot = (int)(t % kOvSlots);
-        if (!__all_sync(0xffffffffu, wait_issued(issued, t + 1, abort, wait) &&
-                                         ptx::mbar_wait(ptx::smem_u32(&full[slot]),
-                                                        (uint32_t)((t / kOvSlots) & 1), abort, wait)))
-          break;
-        const OvTask k = desc[slot];
-        if (k.stop) {
-          // the slot goes back too: the ring may hold fewer slots than there
-          // are consumers, so later stop tasks reuse it
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
-          break;
-        }
-        RowStat* srow = stats + (((int64_t)k.b * 2 + k.which) * M + k.n) * n_chunks;
-        for (int j = 0; j < k.nc; ++j) {
-          const int cc = k.c + j;
-          const int e0 = cc * kChunk;
-          const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kSegBytes +
-                                                           (size_t)j * kBulkSlot);
-          uint4 raw[kStatVecs];
+      const int e0 = c * kChunk;
+      const int nvalid = V - e0;
+      const uint4* sv = reinterpret_cast<const uint4*>(myring + (size_t)slot * kBulkSlot);
+      uint4 raw[kStatVecs];
 #pragma unroll
-          for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
-          float sd;
-          const float m = chunk_stat<T>(raw, V - e0, k.cs, &sd);
-          const int am = k.greedy ? chunk_argmax<T>(raw, V - e0, m) : 0;
-          if (lane == 0) {
-            RowStat r;
-            r.m = m;
-            r.pad = pack_index(am);
-            r.s = (double)sd;
-            srow[cc] = r;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(ptx::smem_u32(&empty[slot]));
-          // the last task of a closed group publishes the group's count
-          __threadfence_block();
-          if (atomicSub(&grp[k.grp].remaining, k.nc) == k.nc) {
-            __threadfence();
-            atomicAdd(req_done + grp[k.grp].b, (uint32_t)grp[k.grp].total);
-            *reinterpret_cast<volatile int*>(&grp[k.grp].free) = 1;
-          }
-        }
+      for (int v = 0; v < kStatVecs; ++v) raw[v] = sv[v * kWarp + lane];
+      float sd;
+      const float m = chunk_stat<T>(raw, nvalid, cs, &sd);
+      const int am = greedy ? chunk_argmax<T>(raw, nvalid, m) : 0;
+      const int which = row < M ? 0 : 1, node = row < M ? row : row - M;
+      if (lane == 0) {
+        RowStat r;
+        r.m = m;
+        r.pad = pack_index(am);
+        r.s = (double)sd;
+        w.stats[(((int64_t)b * 2 + which) * M + node) * n_chunks + c] = r;
       }
-    }
-    __syncthreads();
-    if (tid == 0 && *abort) {
-      *failed = 1u;
-      raise_status(status, SPEC_ERR_TIMEOUT);
-    }
-  } else {
-    // =============================================================== deciders
-    int64_t rtask = 0;  // chunk pairs this CTA has copied for residual passes
-    bool ring_ok = true;
-    for (;;) {
-      if (tid == 0) s_req = (int)atomicAdd(ctl + 1, 1u);
-      __syncthreads();
-      const int b = s_req;
-      __syncthreads();
-      if (b >= B) break;
-      // tasks of request b: its target rows and the draft rows it reads
-      int nrows = parent == nullptr ? 2 * M - 1 : M;
-      if (parent != nullptr) {
-        // nodes named as a parent read their draft rows (warps 0 and 1
-        // cover nodes 1..63; each sets the bits of the parents it sees)
-        unsigned lo = 0, hi = 0;
-        if (tid >= 1 && tid < M) {
-          const int pn = parent[(int64_t)b * M + tid];
-          if (pn >= 0 && pn < 32) lo = 1u << pn;
-          else if (pn >= 32 && pn < 64) hi = 1u << (pn - 32);
+      ++consumed;
+      __syncwarp();
+      // the slot's reads are done before the async proxy refills it
+      ptx::fence_proxy_async_smem();
+      if (!stream_done && !issue_one()) stream_done = true;
+      const int key = b * 2 * M + row;
+      if (key != acc_key) {
+        if (!flush_row()) {
+          ok = false;
+          break;
         }
-        if (warp < 2) {
-          lo = __reduce_or_sync(0xffffffffu, lo);
-          hi = __reduce_or_sync(0xffffffffu, hi);
-          if (lane == 0) {
-            sh.chain_rej[2 * warp] = (int)lo;
-            sh.chain_rej[2 * warp + 1] = (int)hi;
-          }
-        }
-        __syncthreads();
-        const unsigned long long kd =
-            ((unsigned long long)((unsigned)sh.chain_rej[1] | (unsigned)sh.chain_rej[3]) << 32) |
-            ((unsigned)sh.chain_rej[0] | (unsigned)sh.chain_rej[2]);
-        nrows += __popcll(kd);
-        __syncthreads();
+        acc_key = key;
+        acc_b = b;
+        acc_cs = cs;
       }
-      const uint32_t target_count = (uint32_t)((int64_t)nrows * n_chunks);
-      // wait for the stream to finish request b (bounded; a failed call stops it)
-      if (tid == 0) {
-        long long t0 = 0;
-        bool lost = false;
-        for (uint32_t it = 0;; ++it) {
-          uint32_t v;
-          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(req_done + b) : "memory");
-          if (v >= target_count) break;
-          if (*failed) {
-            lost = true;
-            break;
-          }
-          if ((it & 15u) == 15u) {
-            const long long now = clock64();
-            if (t0 == 0) {
-              t0 = now;
-            } else if ((uint64_t)(now - t0) > wait) {
-              lost = true;
-              *failed = 1u;
-              raise_status(status, SPEC_ERR_TIMEOUT);
-              break;
-            }
-          }
-          __nanosleep(64);
-        }
-        s_abort = lost || !ring_ok;
-      }
-      __syncthreads();
-      const bool lost = s_abort != 0;
-      __syncthreads();
-      decide_request<T, true>(target, draft, tokens, parent, temperature, seed, offset, b_base,
-                              out_tokens, path, accepted_len, probe, d, n_chunks, chunk, stats,
-                              draws, status, b, lost, sh);
-      __syncthreads();
-      // A draw from a residual, finished here: the residual's mass over each
-      // statistics chunk of the node's two rows (bulk copies of the chunk
-      // pairs into the ring, thread 0 issuing, warps 1..15 reducing), then
-      // the chunk and the element, as rs_residual_sums_kernel and
-      // rs_residual_draw_kernel do.
-      const DrawState* dsb = draws + b;
-      if (!lost && dsb->pending) {
-        const int node = dsb->node, a_acc = dsb->a;
-        const double u = dsb->u;
-        for (int i = tid; i < (int)(sizeof(DecideCtx) / 4); i += kDecThreads)
-          reinterpret_cast<uint32_t*>(&sh.ctx)[i] = reinterpret_cast<const uint32_t*>(&dsb->c)[i];
-        __syncthreads();
-        const T* trow = target + ((int64_t)b * M + node) * V;
-        const T* drow = draft + ((int64_t)b * M + node) * V;
-        double* zs = zsum + (int64_t)b * n_chunks;
-        const int nseg = (n_chunks + kSegChunks - 1) / kSegChunks;
-        if (tid == 0) {
-          for (int g = 0; g < nseg && ring_ok; ++g) {
-            const int64_t r = rtask + g;
-            const int p = (int)(r % kOvPairs);
-            if (r >= kOvPairs &&
-                !ptx::mbar_wait(ptx::smem_u32(&empty[p]), (uint32_t)(((r / kOvPairs) & 1) ^ 1), abort,
-                                wait)) {
-              ring_ok = false;
-              break;
-            }
-            const int64_t e0 = (int64_t)g * kSegChunks * kChunk;
-            const int64_t left = (int64_t)V - e0;
-            const int64_t want = (int64_t)kSegChunks * kChunk;
-            const uint32_t bytes = (uint32_t)((left < want ? left : want) * sizeof(T));
-            const uint32_t fb = ptx::smem_u32(&full[p]);
-            ptx::mbar_arrive_expect_tx(fb, 2 * bytes);
-            uint8_t* sp = ring + (size_t)p * 2 * kSegBytes;
-            ptx::bulk_g2s(ptx::smem_u32(sp), trow + e0, bytes, fb);
-            ptx::bulk_g2s(ptx::smem_u32(sp + kSegBytes), drow + e0, bytes, fb);
-            *issued = r + 1;
-          }
-        } else if (warp >= 1) {
-          for (int g = warp - 1; g < nseg; g += kOvConsumers) {
-            const int64_t r = rtask + g;
-            const int p = (int)(r % kOvPairs);
-            if (!__all_sync(0xffffffffu, wait_issued(issued, r + 1, abort, wait) &&
-                                             ptx::mbar_wait(ptx::smem_u32(&full[p]),
-                                                            (uint32_t)((r / kOvPairs) & 1), abort,
-                                                            wait)))
-              break;
-            const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)p * 2 * kSegBytes);
-            for (int j = 0; j < kSegChunks; ++j) {
-              const int c = g * kSegChunks + j;
-              if (c >= n_chunks) break;
-              const float ls = smem_chunk_mass<T>(sp + j * (kBulkSlot / 16),
-                                                  sp + (kSegBytes + j * kBulkSlot) / 16, c * kChunk,
-                                                  V, sh.ctx, sh.ctx.nrej);
-              const dfloat tot = df_warp_sum(df_make(ls));
-              if (lane == 0) zs[c] = df_to_d(tot);
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[p]));
-          }
-        }
-        rtask += nseg;
-        __syncthreads();
-        if (*abort) {
-          ring_ok = false;
-        } else if (warp == 0) {
-          double Z = 0.0;
-          for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
-          Z = warp_sum(Z);
-          if (Z > 0.0) {
-            double pre;
-            const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
-            const double trel = u * Z - pre;
-            const float th = (float)trel;
-            float w;
-            const int tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, sh.ctx,
-                                              sh.ctx.nrej, dfloat{th, (float)(trel - (double)th)}, &w);
-            if (lane == 0) {
-              out_tokens[(int64_t)b * M + a_acc] = tk;
-              if (probe != nullptr) {
-                probe[((int64_t)b * M + node) * 4 + 2] = (float)Z;
-                probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / Z);
-              }
-            }
-          } else {
-            // a residual of zero mass: the draw from p of the node
-            const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + node) * n_chunks;
-            float w;
-            double z;
-            const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, sh.ctx, u, &w, &z);
-            if (lane == 0) {
-              out_tokens[(int64_t)b * M + a_acc] = tk;
-              if (probe != nullptr) {
-                probe[((int64_t)b * M + node) * 4 + 2] = 1.0f;
-                probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / z);
-              }
-            }
-          }
-        }
-      }
-      if (tid == 0) req_done[b] = 0u;  // ready for the next call
-      __syncthreads();
+      ++acc_n;
     }
-    // the residual copies issued have all been waited for by their readers;
-    // after a wait that gave up, drain what may still be in flight
-    if (tid == 0 && *abort) {
-      const long long n_iss = *issued;
-      for (long long r = n_iss > kOvPairs ? n_iss - kOvPairs : 0; r < n_iss; ++r)
-        ptx::mbar_drain(ptx::smem_u32(&full[r % kOvPairs]), (uint32_t)((r / kOvPairs) & 1),
-                        kDefaultWaitCycles);
+    if (ok && !flush_row()) ok = false;
+    if (!ok) break;
+    // residual units: claim one when some are published and unclaimed, do
+    // the one held once it is published
+    const uint32_t pub = __shfl_sync(0xffffffffu, cw.x, 0);
+    const uint32_t clm = __shfl_sync(0xffffffffu, cw.y, 0);
+    const uint32_t fin = __shfl_sync(0xffffffffu, cw.z, 0);
+    const uint32_t fail = __shfl_sync(0xffffffffu, cw.w, 0);
+    if (poll && fail != 0u) {
+      *abort = 1;
+      break;
     }
-    if (tid == 0 && *abort) {
-      *failed = 1u;
-      raise_status(status, SPEC_ERR_TIMEOUT);
+    bool progressed = had_work;
+    if (poll && reserved < 0 && pub > clm) {
+      uint32_t u = 0;
+      if (lane == 0) u = atomicAdd(ctl + kCClaim, 1u);
+      reserved = (int64_t)__shfl_sync(0xffffffffu, u, 0);
+    }
+    if (reserved >= 0 && (uint64_t)reserved < (uint64_t)pub) {
+      const uint32_t e = (uint32_t)(reserved / n_chunks);
+      const int c = (int)(reserved - (int64_t)e * n_chunks);
+      reserved = -1;
+      if (!fused_residual_unit<T>(target, draft, out_tokens, probe, d, n_chunks, chunk, w, e, c,
+                                  abort, wait))
+        break;
+      progressed = true;
+    }
+    if (stream_done && consumed == issued) {
+      // the stream is over for this warp: stay for residual units (the
+      // poller, or a warp holding an unpublished claim) until every request
+      // is finished
+      if (poll && fin >= (uint32_t)B) break;
+      if (!poller && reserved < 0) break;
+      if (!progressed) {
+        const long long now = clock64();
+        if (idle0 == 0) {
+          idle0 = now;
+        } else if ((uint64_t)(now - idle0) > wait) {
+          *abort = 1;
+          break;
+        }
+        __nanosleep(backoff);
+        backoff = backoff < 1024 ? 2 * backoff : 1024;
+      } else {
+        idle0 = 0;
+        backoff = 64;
+      }
     }
   }
-
-  // the last CTA out puts the counters back for the next call
+  // a wait that gave up fails the call for every CTA at once
+  if (lane == 0 && *abort) atomicExch(ctl + kCFail, 1u);
+  // copies issued but not consumed (only after a wait gave up) land before
+  // the CTA exits; these waits ignore the abort flag and keep their own limit
+  if (lane == 0)
+    for (int64_t u = consumed; u < issued; ++u)
+      ptx::mbar_drain(ptx::smem_u32(&mybars[u % kFRing]), (uint32_t)((u / kFRing) & 1),
+                      kDefaultWaitCycles);
   __syncthreads();
+  if (tid == 0 && *abort) raise_status(w.status, SPEC_ERR_TIMEOUT);
+  // the last CTA out: a failed call fails every request; the counters go
+  // back to zero for the next call
   if (tid == 0) {
     __threadfence();
-    if (atomicAdd(ctl + 2, 1u) == gridDim.x - 1) {
-      *reinterpret_cast<volatile uint32_t*>(ctl + 0) = 0u;
-      *reinterpret_cast<volatile uint32_t*>(ctl + 1) = 0u;
-      *reinterpret_cast<volatile uint32_t*>(ctl + 3) = 0u;
-      *reinterpret_cast<volatile uint32_t*>(ctl + 2) = 0u;
+    s_last = atomicAdd(ctl + kCCtas, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    const uint32_t ne = ld_relaxed_u32(ctl + kCEntries);
+    const bool failed = ld_relaxed_u32(ctl + kCFail) != 0u;
+    for (uint32_t e = tid; e < ne && e < (uint32_t)B; e += blockDim.x) w.res_ready[e] = 0u;
+    if (failed)
+      for (int b = tid; b < B; b += blockDim.x) accepted_len[b] = -1;
+    __syncthreads();
+    if (tid == 0) {
+      ctl[kCBatch] = 0u;
+      ctl[kCEntries] = 0u;
+      ctl[kCPub] = 0u;
+      ctl[kCClaim] = 0u;
+      ctl[kCFin] = 0u;
+      ctl[kCFail] = 0u;
+      __threadfence();
+      ctl[kCCtas] = 0u;
     }
   }
 }
+
 
 // ---------------------------------------------------------------------------
 // host launcher
@@ -1979,48 +2106,70 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
 }
 
 template <typename T>
-static cudaError_t launch_overlap_t(const RsArgs& a, const WsLayout& lay, cudaStream_t st,
-                                    int* launches) {
+static cudaError_t launch_fused_t(const RsArgs& a, const WsLayout& lay, cudaStream_t st,
+                                  int* launches) {
   const spec_dims& d = a.d;
   char* ws = static_cast<char*>(a.ws);
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // deciders: enough to keep up with the stream's requests, at most one per
-  // request; every other SM streams
-  const int n_dec = d.B < kOvMaxDeciders ? d.B : kOvMaxDeciders;
-  const int n_stream = sms - n_dec > 1 ? sms - n_dec : 1;
-  e = cudaFuncSetAttribute(rs_overlap_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kOvSmem);
+  e = cudaFuncSetAttribute(rs_fused_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kFSmem);
   if (e != cudaSuccess) return e;
-  PdlLaunch L(dim3(n_stream + n_dec), dim3(kDecThreads), kOvSmem, st);
-  e = cudaLaunchKernelEx(&L.cfg, rs_overlap_kernel<T>, static_cast<const T*>(a.target),
-                         static_cast<const T*>(a.draft), a.tokens, a.parent, a.temperature, a.seed,
-                         a.offset, a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d,
-                         lay.rs_chunks, lay.rs_chunk, reinterpret_cast<RowStat*>(ws + lay.rs_off),
-                         reinterpret_cast<DrawState*>(ws + lay.rs_draw_off),
-                         reinterpret_cast<double*>(ws + lay.rs_zsum_off),
-                         reinterpret_cast<uint32_t*>(ws + lay.rsf_ctl_off),
-                         reinterpret_cast<uint32_t*>(ws + lay.rsf_req_off), n_stream,
-                         reinterpret_cast<uint32_t*>(ws + lay.status_off));
+  FusedWs w;
+  w.stats = reinterpret_cast<RowStat*>(ws + lay.rs_off);
+  w.norms = reinterpret_cast<RowNorm*>(ws + lay.rsf_norm_off);
+  w.row_cnt = reinterpret_cast<uint32_t*>(ws + lay.rsf_rowcnt_off);
+  w.req_rows = reinterpret_cast<uint32_t*>(ws + lay.rsf_req_off);
+  w.res_list = reinterpret_cast<uint32_t*>(ws + lay.rsf_list_off);
+  w.res_ready = reinterpret_cast<uint32_t*>(ws + lay.rsf_ready_off);
+  w.res_cnt = reinterpret_cast<uint32_t*>(ws + lay.rsf_rescnt_off);
+  w.draws = reinterpret_cast<DrawState*>(ws + lay.rs_draw_off);
+  w.zsum = reinterpret_cast<double*>(ws + lay.rs_zsum_off);
+  w.ctl = reinterpret_cast<uint32_t*>(ws + lay.rsf_ctl_off);
+  w.status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
+  PdlLaunch L(dim3(sms), dim3(kFWarps * kWarp), kFSmem, st);
+  e = cudaLaunchKernelEx(&L.cfg, rs_fused_kernel<T>, static_cast<const T*>(a.target),
+                         static_cast<const T*>(a.draft), a.tokens, a.temperature, a.seed, a.offset,
+                         a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d, lay.rs_chunks,
+                         lay.rs_chunk, w);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaGetLastError();
 }
 
-bool rso_supported(const spec_dims& d, bool aligned) { return aligned && d.M <= kMaxM; }
+size_t rsf_layout(const spec_dims& d, size_t off, WsLayout* L) {
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = (off + bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t rows = (size_t)d.B * 2 * d.M;
+  L->rsf_ctl_off = take(sizeof(uint32_t) * kFCtl);
+  L->rsf_norm_off = take(sizeof(RowNorm) * rows);
+  L->rsf_rowcnt_off = take(sizeof(uint32_t) * rows);
+  L->rsf_req_off = take(sizeof(uint32_t) * (size_t)d.B);
+  L->rsf_list_off = take(sizeof(uint32_t) * (size_t)d.B);
+  L->rsf_ready_off = take(sizeof(uint32_t) * (size_t)d.B);
+  L->rsf_rescnt_off = take(sizeof(uint32_t) * (size_t)d.B);
+  return off;
+}
+
+bool rso_supported(const spec_dims& d, bool aligned, bool chain) {
+  return aligned && chain && d.M <= kMaxM;
+}
 
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches) {
   const int esz = a.d.logits_dtype == SPEC_BF16 ? 2 : 4;
   const bool aligned = ((size_t)a.d.V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0;
-  const bool fused_ok = rso_supported(a.d, aligned);
+  const bool fused_ok = rso_supported(a.d, aligned, a.parent == nullptr);
   if (a.d.reject_impl == SPEC_REJECT_FUSED || (a.d.reject_impl == SPEC_REJECT_AUTO && fused_ok)) {
     if (!fused_ok) return cudaErrorNotSupported;
-    return a.d.logits_dtype == SPEC_BF16 ? launch_overlap_t<__nv_bfloat16>(a, lay, st, launches)
-                                         : launch_overlap_t<float>(a, lay, st, launches);
+    return a.d.logits_dtype == SPEC_BF16 ? launch_fused_t<__nv_bfloat16>(a, lay, st, launches)
+                                         : launch_fused_t<float>(a, lay, st, launches);
   }
   if (a.d.logits_dtype == SPEC_BF16)
     return aligned ? launch_rs_t<__nv_bfloat16, true>(a, lay, st, launches)

@@ -13,7 +13,7 @@ struct RowStat {
   double s;
 };
 
-constexpr int kRsMaxM = 64;
+constexpr int kRsMaxM = kMaxNodes;
 
 // Law at the node where a request draws: row maxima and normalisers of the
 // node's target / draft rows, and the masses of the residuals taken so far.
@@ -56,8 +56,11 @@ int rs_max_vocab(int logits_dtype);
 // Returns cudaErrorNotSupported when the fused path is asked for and the
 // shape does not allow it.
 cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int* launches);
-// The fused kernel (statistics stream and decisions in one launch) takes
-// 16-byte aligned rows.
-bool rso_supported(const spec_dims& d, bool aligned);
+// The one-kernel path (statistics, decisions and draws in one launch) takes
+// chains with 16-byte aligned rows.
+bool rso_supported(const spec_dims& d, bool aligned, bool chain);
+// Lays out the one-kernel path's scratch from byte offset `off` (256-byte
+// aligned) and returns the end.
+size_t rsf_layout(const spec_dims& d, size_t off, WsLayout* L);
 
 }  // namespace specv

@@ -125,12 +125,13 @@ extern "C" spec_status spec_reject_sample_noalloc(
   const bool aligned = ((size_t)dims->V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(target_logits) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(draft_logits) % 16) == 0;
-  const bool fused = dims->reject_impl != SPEC_REJECT_STAGED && rso_supported(*dims, aligned);
+  const bool fused = dims->reject_impl != SPEC_REJECT_STAGED &&
+                     rso_supported(*dims, aligned, parent == nullptr);
   if (dims->reject_impl == SPEC_REJECT_FUSED && !fused) return SPEC_ERR_UNSUPPORTED;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   // status, the chunk statistics, the draw states, the residual chunk
-  // masses; for the fused kernel also its four counters and the finished
-  // tasks of each request
+  // masses; for the one-kernel path also its control words, row
+  // normalisers and counters
   WsLayout lay;
   memset(&lay, 0, sizeof(lay));
   lay.status_off = 0;
@@ -141,11 +142,7 @@ extern "C" spec_status spec_reject_sample_noalloc(
   lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
   lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
   lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
-  if (fused) {
-    lay.rsf_ctl_off = up(lay.total);
-    lay.rsf_req_off = up(lay.rsf_ctl_off + 16);
-    lay.total = lay.rsf_req_off + sizeof(uint32_t) * (size_t)dims->B;
-  }
+  if (fused) lay.total = rsf_layout(*dims, up(lay.total), &lay);
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;

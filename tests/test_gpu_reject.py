@@ -22,12 +22,19 @@ from synth import bf16_round, logits_inputs, workload  # noqa: E402
 
 
 IMPLS = [sv.REJECT_FUSED, sv.REJECT_STAGED]
+# trees run on the staged kernels; the one-kernel path takes chains only
+TREE_IMPLS = [sv.REJECT_AUTO, sv.REJECT_STAGED]
 
 
 def _run(wl, lg, seed, offset, b_base=0, impl=sv.REJECT_AUTO):
     B, M, V = lg["target"].shape
     dims = dims_for(wl, B, V=V)
     dims.reject_impl = impl
+    if impl == sv.REJECT_FUSED and lg["parent"] is not None:
+        with pytest.raises(sv.SpecError) as err:
+            gpu_reject(wl, lg, seed, offset, b_base=b_base, dims=dims)
+        assert err.value.code == 3  # SPEC_ERR_UNSUPPORTED: nothing launched
+        dims.reject_impl = sv.REJECT_AUTO
     g = gpu_reject(wl, lg, seed, offset, b_base=b_base, dims=dims)
     o = oracle_reject_sample(lg["target"], lg["draft"], lg["tokens"],
                              lg["parent"], lg["temperature"], seed, offset,
@@ -79,7 +86,7 @@ def test_maximum_sizes(B, gamma, V, dtype):
         assert g["status"] == 0
 
 
-@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("impl", TREE_IMPLS)
 @pytest.mark.parametrize("V", [64, 32000])
 def test_trees(V, impl):
     wl = workload("tree_64").scaled(B=6, V=V)
@@ -88,7 +95,7 @@ def test_trees(V, impl):
         _run(wl, lg, seed=7, offset=offset, impl=impl)
 
 
-@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("impl", TREE_IMPLS)
 def test_small_trees_many_rejections(impl):
     # wide fan-out, noisy draft: several rejections per node
     wl = workload("tree_64").scaled(B=8, V=48, gamma=2, tree_width=8,

@@ -83,7 +83,8 @@ def test_refuses_sizes_beyond_its_scratch():
     with pytest.raises(sv.SpecError) as e:
         sv.spec_reject_sample_noalloc(t, t, i, None, f, 1, 0, i, i.clone(), a, None, dims)
     assert e.value.code == 3
-    # the fused kernel's records: 40000 requests x 5 nodes x 32 bytes
+    # the one-kernel path's scratch: 40000 requests' chunk statistics, row
+    # normalisers and counters (over 6 MB)
     B = 40000
     dims = sv.make_dims(B=B, M=M, V=64, reject_impl=sv.REJECT_FUSED)
     t = torch.zeros(B, M, 64, dtype=torch.bfloat16, device="cuda")

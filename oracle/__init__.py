@@ -38,6 +38,9 @@ from .reject_sample import (  # noqa: F401
     softmax_rows,
     greedy_rows,
     row_law,
+    filter_law,
+    filter_order,
+    FILTER_NEAR,
     NONFINITE,
     INVALID_ARG,
     BAD_TOKEN,

@@ -43,6 +43,17 @@ What the pages fix, and the readings taken where they are silent:
   every draw -- after a rejection or at the end -- is that token, whatever
   the uniforms.  Page 2 §5.1 asks for the same sampling rule on both sides,
   so the draft row's law at T = 0 is its own point mass.
+* Filtered sampling (page 2 §5.1: a target that samples from its nucleus,
+  top-p, and a draft that samples differently make the two laws drift
+  apart, so both sides use one rule).  Reading taken: a request may carry a
+  top-k count and a top-p mass; each row's law (target and draft alike) is
+  restricted to a prefix of its tokens ordered by logit, largest first, the
+  smaller index first among equal logits -- the first k of them (top-k), then
+  the shortest prefix of those whose mass reaches top_p times their total
+  (top-p) -- and renormalised; the verify walk then runs on the restricted
+  laws, so its output follows the restricted target law.  k = 0 and
+  top_p = 1 leave a row as it is; at T = 0 the filters change nothing (the
+  point mass is the first token of the order).
 """
 from __future__ import annotations
 
@@ -54,6 +65,7 @@ INVALID_ARG = 1   # request failed: bad temperature or topology
 NONFINITE = 5     # request failed: a row it needs has no distribution
 BAD_TOKEN = 6     # request failed: a drafted token outside [0, V)
 NEAR = 1e-6       # decisions closer than this to their threshold are flagged
+FILTER_NEAR = 1e-5  # top-p cuts whose mass is this close (relative) to the target are flagged
 
 
 def softmax_rows(logits: np.ndarray, T: float) -> np.ndarray:
@@ -77,6 +89,43 @@ def row_law(logits: np.ndarray, T: float) -> np.ndarray:
     """The law of a row at temperature T: softmax(z / T), or the point mass
     on the largest logit at T = 0."""
     return greedy_rows(logits) if T == 0.0 else softmax_rows(logits, T)
+
+
+def filter_order(logits: np.ndarray) -> np.ndarray:
+    """Token indices by logit, largest first; the smaller index first among
+    equal logits."""
+    z = np.asarray(logits, dtype=np.float64)
+    return np.lexsort((np.arange(z.shape[-1]), -z))
+
+
+def filter_law(law: np.ndarray, logits: np.ndarray, top_k: int = 0, top_p: float = 1.0):
+    """A row's law restricted by top-k and then top-p, renormalised.
+
+    Keeps the first n tokens of filter_order(logits): n = top_k (all when
+    top_k is 0 or at least V), then the smallest n' <= n whose running mass
+    in that order reaches top_p times the mass of the first n (all n when
+    top_p is 1).  Returns (restricted law, margin): margin is the relative
+    distance of the top-p target from the running masses on either side of
+    the cut (inf without a top-p cut).
+    """
+    law = np.asarray(law, dtype=np.float64)
+    V = law.shape[-1]
+    order = filter_order(logits)
+    n = V if top_k <= 0 else min(int(top_k), V)
+    margin = np.inf
+    if top_p < 1.0:
+        c = np.cumsum(law[order[:n]])
+        target = float(top_p) * c[-1]
+        cut = int(np.searchsorted(c, target, side="left")) + 1
+        cut = min(cut, n)
+        above = c[cut - 1] - target
+        below = target - (c[cut - 2] if cut >= 2 else 0.0)
+        margin = min(abs(above), abs(below)) / target
+        n = cut
+    out = np.zeros_like(law)
+    keep = order[:n]
+    out[keep] = law[keep]
+    return out / out.sum(), margin
 
 
 def row_has_distribution(row: np.ndarray) -> bool:
@@ -204,7 +253,7 @@ def verify_request(p_row, q_row, tokens, children, chooser):
 
 
 def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
-                         offset, b_base=0):
+                         offset, b_base=0, top_k=None, top_p=None):
     """Verify decisions for a batch.
 
     target, draft : [B, M, V] logits (row n = distribution over n's children)
@@ -212,6 +261,9 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
     parent        : [B, M] parent indices (parent[b, 0] = -1) or None (chain)
     temperature   : [B] fp32 values: positive normal finite, or 0 (greedy)
     seed, offset  : Philox key word and counter word 2; b_base + b is word 1
+    top_k, top_p  : [B] int32 / fp32 per-request filters, or None (top_k 0
+                    and top_p 1 filter nothing); top_k >= 0 and
+                    0 < top_p <= 1, else the request fails (INVALID_ARG)
 
     Returns dict of numpy arrays:
       out_tokens [B, M] int32 (emitted tokens, then -1)
@@ -225,6 +277,9 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
       smp_margin [B] float64: the same for the final draw only
       band       [B, 2] int32: token index range a draw within 1e-6 of u
                  could have selected (the final draw)
+      flt_margin [B] float64: smallest relative margin of a top-p cut over
+                 the rows the walk used (inf without one); below FILTER_NEAR
+                 the kept set is near its threshold
       status     [B] int32: 0, INVALID_ARG, NONFINITE or BAD_TOKEN
     Failed requests (status != 0) keep accepted_len -1 and -1 rows.
     """
@@ -239,14 +294,18 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
     acc_margin = np.full(B, np.inf, dtype=np.float64)
     smp_margin = np.full(B, np.inf, dtype=np.float64)
     band = np.full((B, 2), -1, dtype=np.int32)
+    flt_margin = np.full(B, np.inf, dtype=np.float64)
     status = np.zeros(B, dtype=np.int32)
     for b in range(B):
         par = None if parent is None else np.asarray(parent[b])
         kids = children_lists(par, M)
         T = float(np.float32(temperature[b]))
+        k = 0 if top_k is None else int(top_k[b])
+        tp = 1.0 if top_p is None else float(np.float32(top_p[b]))
         # temperature must be 0 (greedy) or a positive, normal, finite fp32 value
         t_ok = T == 0.0 or (T >= float(np.finfo(np.float32).tiny) and np.isfinite(T))
-        if not t_ok or (par is not None and not valid_topology(par)):
+        f_ok = k >= 0 and tp > 0.0 and tp <= 1.0     # NaN fails both comparisons
+        if not t_ok or not f_ok or (par is not None and not valid_topology(par)):
             status[b] = INVALID_ARG
             continue
         if np.any((tokens[b, 1:] < 0) | (tokens[b, 1:] >= V)):
@@ -259,10 +318,19 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
             continue
         u_acc, u_smp = uniforms_for(seed, offset, b_base + b, M)
         chooser = UniformChooser(u_acc, u_smp, exact=(T == 0.0))
-        res = verify_request(
-            lambda n: row_law(target[b, n], T),
-            lambda n: row_law(draft[b, n], T),
-            tokens[b], kids, chooser)
+        fm = [np.inf]
+
+        def law(rows, n, b=b, T=T, k=k, tp=tp, fm=fm):
+            base = row_law(rows[b, n], T)
+            if T == 0.0 or (k == 0 and tp >= 1.0):
+                return base
+            out, m = filter_law(base, rows[b, n], k, tp)
+            fm[0] = min(fm[0], m)
+            return out
+
+        res = verify_request(lambda n: law(target, n), lambda n: law(draft, n),
+                             tokens[b], kids, chooser)
+        flt_margin[b] = fm[0]
         a = len(res["path"]) - 1
         acc[b] = a
         path_out[b, :a + 1] = res["path"]
@@ -278,4 +346,5 @@ def oracle_reject_sample(target, draft, tokens, parent, temperature, seed,
         band[b] = chooser.band
     return dict(out_tokens=out_tokens, path=path_out, accepted_len=acc,
                 probe=probe, margin=margin, acc_margin=acc_margin,
-                smp_margin=smp_margin, band=band, status=status)
+                smp_margin=smp_margin, band=band, flt_margin=flt_margin,
+                status=status)

@@ -163,8 +163,7 @@ struct WsLayout {
   size_t rsf_norm_off;    // [B, 2M] 16-byte row normalisers
   size_t rsf_rowcnt_off;  // [B, 2M] u32 statistics chunks finished per row
   size_t rsf_req_off;     // [B] u32 rows finished per request
-  size_t rsf_list_off;    // [B] u32 request of each residual entry
-  size_t rsf_ready_off;   // [B] u32 the entry is written
+  size_t rsf_list_off;    // [B] 48-byte residual entries in the order posted
   size_t rsf_rescnt_off;  // [B] u32 residual units finished per request
   size_t total;
 };

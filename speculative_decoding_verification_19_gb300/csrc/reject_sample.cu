@@ -1335,12 +1335,16 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 //     tests of the chain, the number accepted) and, when every draft was
 //     accepted, the bonus draw from p; a rejection posts the request's
 //     residual chunks (one unit per statistics chunk) to a global list;
-//   * a residual unit, claimed from that list by any warp: the mass of
-//     max(0, p - q) over one chunk of the node's rows (re-read while still in
-//     L2); the unit that completes a request picks the chunk from the masses
-//     and the token inside it.
+//   * a residual unit, claimed from that list by a warp between batches
+//     (warps 0..3 of each CTA) or once its stream is over (every warp): the
+//     masses of max(0, p - q) over four statistics chunks of the node's rows
+//     (re-read while still in L2); the unit that completes a request picks
+//     the chunk from the masses and the token inside it.
 // Only the decisions of the last requests, and their residual units (spread
-// over every warp), come after the stream ends.
+// over every warp), come after the stream ends.  A warp's count of finished
+// chunks is added to its row's counter at the end of each batch and the
+// returned count looked at one batch later, so that the stream never waits
+// for the atomic.
 //
 // Global control words ctl[] (two 128-byte lines: the batch counter, hit
 // by every claim, apart from the words idle warps poll):
@@ -1357,6 +1361,7 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 constexpr int kFWarps = 16;   // warps per CTA (one CTA per SM)
 constexpr int kFRing = 3;     // 4 KB slots per warp
 constexpr int kFBatch = 4;    // statistics chunks per claim
+constexpr int kFUnit = 4;     // statistics chunks per residual unit
 constexpr size_t kFSmem = (size_t)kFWarps * kFRing * kBulkSlot + 1024;
 constexpr int kFCtl = 64;
 constexpr int kCBatch = 0, kCEntries = 1, kCCtas = 2;
@@ -1370,15 +1375,24 @@ struct RowNorm {
   double S;
 };
 
+// A posted residual draw: the request, its node and law, and the uniform;
+// `ready` is written last (release) and read first (acquire).
+struct ResEntry {
+  int b, node, a, pad0;
+  float mT, mD, invST, invSD;
+  float cs;
+  uint32_t ready;
+  double u;
+};
+static_assert(sizeof(ResEntry) == 48, "three 16-byte loads");
+
 struct FusedWs {
   RowStat* stats;
   RowNorm* norms;       // [B][2M]: target row n at n, draft row n at M + n
   uint32_t* row_cnt;    // [B][2M]: statistics chunks finished per row
   uint32_t* req_rows;   // [B]: rows finished per request
-  uint32_t* res_list;   // [B]: request of each residual entry
-  uint32_t* res_ready;  // [B]: the entry is written
+  ResEntry* entries;    // [B]: residual draws in the order posted
   uint32_t* res_cnt;    // [B]: residual units finished per request
-  DrawState* draws;     // [B]: the residual law of each posted request
   double* zsum;         // [B][n_chunks]: residual mass per chunk
   uint32_t* ctl;        // [kFCtl]
   uint32_t* status;
@@ -1627,22 +1641,20 @@ __device__ __noinline__ void fused_decide(
     c.invSD = (float)(1.0 / da.S);
     c.nrej = 1;
     if (lane == 0) {
-      DrawState& ds = w.draws[b];
-      ds.c.mT = c.mT;
-      ds.c.mD = c.mD;
-      ds.c.invST = c.invST;
-      ds.c.invSD = c.invSD;
-      ds.c.cs = c.cs;
-      ds.c.nrej = 1;
-      ds.u = u;
-      ds.node = a;
-      ds.a = a;
-      ds.pending = 1;
       const uint32_t e = atomicAdd(w.ctl + kCEntries, 1u);
-      w.res_list[e] = (uint32_t)b;
+      ResEntry* r = w.entries + e;
+      r->b = b;
+      r->node = a;
+      r->a = a;
+      r->mT = c.mT;
+      r->mD = c.mD;
+      r->invST = c.invST;
+      r->invSD = c.invSD;
+      r->cs = c.cs;
+      r->u = u;
       __threadfence();
-      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(w.res_ready + e), "r"(1u) : "memory");
-      atomicAdd(w.ctl + kCPub, (uint32_t)n_chunks);
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&r->ready), "r"(1u) : "memory");
+      atomicAdd(w.ctl + kCPub, (uint32_t)((n_chunks + kFUnit - 1) / kFUnit));
     }
     return;
   }
@@ -1665,22 +1677,24 @@ __device__ __noinline__ void fused_decide(
   fused_finish(w.ctl);
 }
 
-// One residual unit (entry e, statistics chunk c), by one warp: the chunk's
-// residual mass; the unit that completes its request draws the token.
+// One residual unit (entry e, chunk group g: statistics chunks
+// [kFUnit g, kFUnit g + kFUnit)), by one warp: each chunk's residual mass;
+// the unit that completes its request draws the token.
 template <typename T>
 __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
                                                  const T* __restrict__ draft,
                                                  int32_t* __restrict__ out_tokens,
                                                  float* __restrict__ probe, const spec_dims& d,
                                                  int n_chunks, int chunk, const FusedWs& w,
-                                                 uint32_t e, int c, volatile int* abort,
+                                                 uint32_t e, int g, volatile int* abort,
                                                  uint64_t wait) {
   const int lane = threadIdx.x % kWarp;
   const int M = d.M, V = d.V;
+  ResEntry* ent = w.entries + e;
   // the entry is allocated; its writer publishes it right away (bounded)
   if (lane == 0) {
     long long t0 = 0;
-    for (uint32_t it = 0; ld_acquire_u32(w.res_ready + e) == 0u; ++it) {
+    for (uint32_t it = 0; ld_acquire_u32(&ent->ready) == 0u; ++it) {
       if ((it & 15u) == 15u) {
         if (*abort || ld_relaxed_u32(w.ctl + kCFail) != 0u) {
           *abort = 1;
@@ -1698,34 +1712,38 @@ __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
     }
   }
   if (__shfl_sync(0xffffffffu, (int)*abort, 0)) return false;
-  const int b = (int)__ldcg(w.res_list + e);
-  const DrawState* ds = w.draws + b;
+  const uint4 r0 = __ldcg(reinterpret_cast<const uint4*>(ent));
+  const uint4 r1 = __ldcg(reinterpret_cast<const uint4*>(ent) + 1);
+  const uint4 r2 = __ldcg(reinterpret_cast<const uint4*>(ent) + 2);
+  const int b = (int)r0.x, node = (int)r0.y, a_acc = (int)r0.z;
   DecideCtx ctx;
-  ctx.mT = __ldcg(&ds->c.mT);
-  ctx.mD = __ldcg(&ds->c.mD);
-  ctx.invST = __ldcg(&ds->c.invST);
-  ctx.invSD = __ldcg(&ds->c.invSD);
-  ctx.cs = __ldcg(&ds->c.cs);
+  ctx.mT = __uint_as_float(r1.x);
+  ctx.mD = __uint_as_float(r1.y);
+  ctx.invST = __uint_as_float(r1.z);
+  ctx.invSD = __uint_as_float(r1.w);
+  ctx.cs = __uint_as_float(r2.x);
   ctx.nrej = 1;
-  const int node = __ldcg(&ds->node);
+  const double u = __hiloint2double((int)r2.w, (int)r2.z);
   const T* trow = target + ((int64_t)b * M + node) * V;
   const T* drow = draft + ((int64_t)b * M + node) * V;
-  uint4 raw_t[kStatVecs], raw_d[kStatVecs];
-  const float ls = lane_weights<T>(trow, drow, (int64_t)c * chunk, V, ctx, 1, raw_t, raw_d);
-  const dfloat tot = df_warp_sum(df_make(ls));
   double* zs = w.zsum + (int64_t)b * n_chunks;
+  const int c1 = min(n_chunks, (g + 1) * kFUnit);
+  for (int c = g * kFUnit; c < c1; ++c) {
+    uint4 raw_t[kStatVecs], raw_d[kStatVecs];
+    const float ls = lane_weights<T>(trow, drow, (int64_t)c * chunk, V, ctx, 1, raw_t, raw_d);
+    const dfloat tot = df_warp_sum(df_make(ls));
+    if (lane == 0) zs[c] = df_to_d(tot);
+  }
+  const uint32_t n_units = (uint32_t)((n_chunks + kFUnit - 1) / kFUnit);
   uint32_t done = 0;
   if (lane == 0) {
-    zs[c] = df_to_d(tot);
     __threadfence();
     done = atomicAdd(w.res_cnt + b, 1u) + 1u;
   }
   done = __shfl_sync(0xffffffffu, done, 0);
-  if (done != (uint32_t)n_chunks) return true;
+  if (done != n_units) return true;
   // the last unit of request b: the draw
   __threadfence();
-  const int a_acc = __ldcg(&ds->a);
-  const double u = __ldcg(&ds->u);
   double Z = 0.0;
   for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
   Z = warp_sum(Z);
@@ -1762,7 +1780,6 @@ __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
   return true;
 }
 
-
 template <typename T>
 __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
     const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
@@ -1775,6 +1792,10 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
   __shared__ uint64_t full[kFWarps][kFRing];
   __shared__ long long s_task[kFWarps][kFRing];
   __shared__ int s_abort, s_last;
+  // the control words [kCPub..kCFail] as last read by a warp of this CTA, and
+  // when: idle warps read them here instead of from L2
+  __shared__ uint32_t s_cw[4];
+  __shared__ long long s_cw_time;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1785,31 +1806,41 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
     for (int i = 0; i < kFWarps; ++i)
       for (int j = 0; j < kFRing; ++j) ptx::mbar_init(ptx::smem_u32(&full[i][j]), 1);
     s_abort = 0;
+    s_cw[0] = s_cw[1] = s_cw[2] = s_cw[3] = 0u;
+    s_cw_time = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
   pdl_trigger();
   pdl_wait();  // the logits may come from the previous kernel
   volatile int* abort = &s_abort;
+  volatile uint32_t* cws = s_cw;
+  volatile long long* cw_time = &s_cw_time;
   uint32_t* ctl = w.ctl;
   const int rows = 2 * M - 1;  // target rows 0..M-1, then draft rows 0..M-2
   const int64_t per_req = (int64_t)rows * n_chunks;
   const int64_t ntask = per_req * B;
   const int64_t nbatch = (ntask + kFBatch - 1) / kFBatch;
+  const uint32_t n_units = (uint32_t)((n_chunks + kFUnit - 1) / kFUnit);
   uint8_t* myring = ring + (size_t)warp * kFRing * kBulkSlot;
   uint64_t* mybars = full[warp];
   long long* mytask = s_task[warp];
-  // Warps 0..3 of each CTA take residual units between their batches; after
-  // the stream, warp 0 stays to take them until every request is finished,
-  // the others leave once they hold none.
+  // warps 0..3 of each CTA take residual units between their batches
   const bool poll = warp < 4;
-  const bool poller = warp == 0;
+
+  // the control words, from L2 (lane 0), kept in shared memory for the CTA
+  auto load_cw = [&](uint4& cw) {
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                 : "l"(ctl + kCPub)
+                 : "memory");
+  };
 
   // the stream: tasks [it, it_end) of the current batch are still to be
-  // issued; `next` is the batch claimed after it (claimed one batch early,
-  // so the atomic's latency hides behind the copies)
+  // issued; lane 0's `next` is the batch claimed after it (claimed one batch
+  // early, so that the atomic's latency hides behind the copies)
   int64_t it = 0, it_end = 0;
-  uint32_t next = 0;  // lane 0: the claim's result, read one batch later
+  uint32_t next = 0;
   if (lane == 0) next = atomicAdd(ctl + kCBatch, 1u);
   bool stream_done = false;
   int64_t issued = 0, consumed = 0;
@@ -1841,63 +1872,93 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
     return true;
   };
 
-  // finished chunks of one row not yet counted (published at each row
-  // change and at the end of each batch)
+  // Finished chunks of one row not yet counted (acc_*), and the count added
+  // last whose returned value is still to be looked at (pend_*: lane 0's
+  // atomic result, read one batch later).
   int acc_key = -1, acc_b = 0;
   uint32_t acc_n = 0;
   float acc_cs = 1.f;
-  auto flush_row = [&]() -> bool {  // whole warp; false if a wait gave up
-    if (acc_n == 0) return true;
-    uint32_t old = 0;
-    if (lane == 0) {
-      __threadfence();  // this warp's statistics before the count
-      old = atomicAdd(w.row_cnt + acc_key, acc_n);
-    }
-    old = __shfl_sync(0xffffffffu, old, 0);
-    const uint32_t n = acc_n;
-    acc_n = 0;
-    if (old + n != (uint32_t)n_chunks) return true;
-    // this warp finished the row: its normaliser
+  int pend_key = -1, pend_b = 0;
+  uint32_t pend_n = 0, pend_old = 0;
+  float pend_cs = 1.f;
+  // Looks at the pending count: the warp whose chunks complete a row forms
+  // its normaliser; the row that completes a request has it decided.
+  auto resolve = [&]() {  // whole warp
+    if (pend_n == 0) return;
+    const uint32_t old = __shfl_sync(0xffffffffu, pend_old, 0);
+    const uint32_t n = pend_n;
+    pend_n = 0;
+    if (old + n != (uint32_t)n_chunks) return;
     __threadfence();
-    const int b = acc_b, row = acc_key - b * 2 * M;
+    const int b = pend_b, row = pend_key - b * 2 * M;
     const int which = row < M ? 0 : 1, node = row < M ? row : row - M;
     fused_row_norm(w.stats + (((int64_t)b * 2 + which) * M + node) * n_chunks, n_chunks, chunk,
-                   acc_cs, w.norms + acc_key);
+                   pend_cs, w.norms + pend_key);
     uint32_t r = 0;
     if (lane == 0) {
-      w.row_cnt[acc_key] = 0u;  // ready for the next call
+      w.row_cnt[pend_key] = 0u;  // ready for the next call
       __threadfence();
       r = atomicAdd(w.req_rows + b, 1u) + 1u;
     }
     r = __shfl_sync(0xffffffffu, r, 0);
-    if (r != (uint32_t)rows) return true;
-    // ... and the request: its decisions
+    if (r != (uint32_t)rows) return;
     __threadfence();
     if (lane == 0) w.req_rows[b] = 0u;
     fused_decide<T>(target, draft, tokens, temperature, seed, offset, b_base, out_tokens, path,
                     accepted_len, probe, d, n_chunks, chunk, w, b);
-    return true;
+  };
+  // Adds the accumulated count to its row (after this warp's statistics are
+  // visible); the previous pending count is looked at first.
+  auto flush = [&]() {  // whole warp
+    if (acc_n == 0) return;
+    resolve();
+    if (lane == 0) {
+      __threadfence();
+      pend_old = atomicAdd(w.row_cnt + acc_key, acc_n);
+    }
+    pend_key = acc_key;
+    pend_b = acc_b;
+    pend_n = acc_n;
+    pend_cs = acc_cs;
+    acc_n = 0;
   };
 
   int64_t reserved = -1;  // a residual unit this warp claimed and has not done
+  // Claims a unit when some are published and unclaimed, and does the one
+  // held once it is published.  Returns false if a wait gave up.
+  auto take_units = [&](uint32_t pub, uint32_t clm, bool* progressed) -> bool {
+    if (reserved < 0 && pub > clm) {
+      uint32_t u = 0;
+      if (lane == 0) u = atomicAdd(ctl + kCClaim, 1u);
+      reserved = (int64_t)__shfl_sync(0xffffffffu, u, 0);
+    }
+    if (reserved >= 0 && (uint64_t)reserved < (uint64_t)pub) {
+      const uint32_t e = (uint32_t)(reserved / n_units);
+      const int g = (int)(reserved - (int64_t)e * n_units);
+      reserved = -1;
+      *progressed = true;
+      return fused_residual_unit<T>(target, draft, out_tokens, probe, d, n_chunks, chunk, w, e, g,
+                                    abort, wait);
+    }
+    return true;
+  };
+
+  // ---- the stream ---------------------------------------------------------
   int cur_b = -1;
   float cs = 1.f;
   bool greedy = false;
-  long long idle0 = 0;
-  int backoff = 64;
-  for (;;) {
-    if (*abort) break;
+  bool ok = true;
+  while (ok) {
+    if (*abort) {
+      ok = false;
+      break;
+    }
     while (!stream_done && issued - consumed < kFRing)
       if (!issue_one()) stream_done = true;
+    if (consumed == issued) break;  // nothing left to stream for this warp
     // the control words, loaded now and looked at after the batch
     uint4 cw = make_uint4(0, 0, 0, 0);
-    if (lane == 0 && poll)
-      asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                   : "l"(ctl + kCPub)
-                   : "memory");
-    bool ok = true;
-    const bool had_work = consumed < issued;
+    if (lane == 0 && poll) load_cw(cw);
     for (int k = 0; k < kFBatch && consumed < issued; ++k) {
       const int slot = (int)(consumed % kFRing);
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&mybars[slot]),
@@ -1940,64 +2001,78 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
       if (!stream_done && !issue_one()) stream_done = true;
       const int key = b * 2 * M + row;
       if (key != acc_key) {
-        if (!flush_row()) {
-          ok = false;
-          break;
-        }
+        flush();
         acc_key = key;
         acc_b = b;
         acc_cs = cs;
       }
       ++acc_n;
     }
-    if (ok && !flush_row()) ok = false;
     if (!ok) break;
-    // residual units: claim one when some are published and unclaimed, do
-    // the one held once it is published
+    flush();
+    if (poll) {
+      const uint32_t pub = __shfl_sync(0xffffffffu, cw.x, 0);
+      const uint32_t clm = __shfl_sync(0xffffffffu, cw.y, 0);
+      const uint32_t fail = __shfl_sync(0xffffffffu, cw.w, 0);
+      if (fail != 0u) {
+        *abort = 1;
+        ok = false;
+        break;
+      }
+      bool prog = false;
+      if (!take_units(pub, clm, &prog)) ok = false;
+    }
+  }
+  // the stream is over for this warp: its last count is looked at
+  if (ok && !*abort) {
+    flush();
+    resolve();
+  }
+
+  // ---- after the stream: residual units until every request is finished --
+  long long idle0 = 0;
+  int backoff = 32;
+  while (ok && !*abort) {
+    uint4 cw;
+    const long long now = clock64();
+    if (warp == 0 || now - *cw_time > 2000) {
+      // this CTA's copy is old: read the words from L2
+      if (lane == 0) {
+        load_cw(cw);
+        cws[0] = cw.x;
+        cws[1] = cw.y;
+        cws[2] = cw.z;
+        cws[3] = cw.w;
+        *cw_time = now;
+      }
+    } else if (lane == 0) {
+      cw = make_uint4(cws[0], cws[1], cws[2], cws[3]);
+    }
     const uint32_t pub = __shfl_sync(0xffffffffu, cw.x, 0);
     const uint32_t clm = __shfl_sync(0xffffffffu, cw.y, 0);
     const uint32_t fin = __shfl_sync(0xffffffffu, cw.z, 0);
     const uint32_t fail = __shfl_sync(0xffffffffu, cw.w, 0);
-    if (poll && fail != 0u) {
+    if (fail != 0u) {
       *abort = 1;
       break;
     }
-    bool progressed = had_work;
-    if (poll && reserved < 0 && pub > clm) {
-      uint32_t u = 0;
-      if (lane == 0) u = atomicAdd(ctl + kCClaim, 1u);
-      reserved = (int64_t)__shfl_sync(0xffffffffu, u, 0);
+    if (fin >= (uint32_t)B) break;
+    bool prog = false;
+    if (!take_units(pub, clm, &prog)) break;
+    if (prog) {
+      idle0 = 0;
+      backoff = 32;
+      continue;
     }
-    if (reserved >= 0 && (uint64_t)reserved < (uint64_t)pub) {
-      const uint32_t e = (uint32_t)(reserved / n_chunks);
-      const int c = (int)(reserved - (int64_t)e * n_chunks);
-      reserved = -1;
-      if (!fused_residual_unit<T>(target, draft, out_tokens, probe, d, n_chunks, chunk, w, e, c,
-                                  abort, wait))
-        break;
-      progressed = true;
+    const long long t = clock64();
+    if (idle0 == 0) {
+      idle0 = t;
+    } else if ((uint64_t)(t - idle0) > wait) {
+      *abort = 1;
+      break;
     }
-    if (stream_done && consumed == issued) {
-      // the stream is over for this warp: stay for residual units (the
-      // poller, or a warp holding an unpublished claim) until every request
-      // is finished
-      if (poll && fin >= (uint32_t)B) break;
-      if (!poller && reserved < 0) break;
-      if (!progressed) {
-        const long long now = clock64();
-        if (idle0 == 0) {
-          idle0 = now;
-        } else if ((uint64_t)(now - idle0) > wait) {
-          *abort = 1;
-          break;
-        }
-        __nanosleep(backoff);
-        backoff = backoff < 1024 ? 2 * backoff : 1024;
-      } else {
-        idle0 = 0;
-        backoff = 64;
-      }
-    }
+    __nanosleep(backoff);
+    backoff = backoff < 512 ? 2 * backoff : 512;
   }
   // a wait that gave up fails the call for every CTA at once
   if (lane == 0 && *abort) atomicExch(ctl + kCFail, 1u);
@@ -2020,7 +2095,7 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
     __threadfence();
     const uint32_t ne = ld_relaxed_u32(ctl + kCEntries);
     const bool failed = ld_relaxed_u32(ctl + kCFail) != 0u;
-    for (uint32_t e = tid; e < ne && e < (uint32_t)B; e += blockDim.x) w.res_ready[e] = 0u;
+    for (uint32_t e = tid; e < ne && e < (uint32_t)B; e += blockDim.x) w.entries[e].ready = 0u;
     if (failed)
       for (int b = tid; b < B; b += blockDim.x) accepted_len[b] = -1;
     __syncthreads();
@@ -2036,7 +2111,6 @@ __global__ void __launch_bounds__(kFWarps * kWarp, 1) rs_fused_kernel(
     }
   }
 }
-
 
 // ---------------------------------------------------------------------------
 // host launcher
@@ -2122,10 +2196,8 @@ static cudaError_t launch_fused_t(const RsArgs& a, const WsLayout& lay, cudaStre
   w.norms = reinterpret_cast<RowNorm*>(ws + lay.rsf_norm_off);
   w.row_cnt = reinterpret_cast<uint32_t*>(ws + lay.rsf_rowcnt_off);
   w.req_rows = reinterpret_cast<uint32_t*>(ws + lay.rsf_req_off);
-  w.res_list = reinterpret_cast<uint32_t*>(ws + lay.rsf_list_off);
-  w.res_ready = reinterpret_cast<uint32_t*>(ws + lay.rsf_ready_off);
+  w.entries = reinterpret_cast<ResEntry*>(ws + lay.rsf_list_off);
   w.res_cnt = reinterpret_cast<uint32_t*>(ws + lay.rsf_rescnt_off);
-  w.draws = reinterpret_cast<DrawState*>(ws + lay.rs_draw_off);
   w.zsum = reinterpret_cast<double*>(ws + lay.rs_zsum_off);
   w.ctl = reinterpret_cast<uint32_t*>(ws + lay.rsf_ctl_off);
   w.status = reinterpret_cast<uint32_t*>(ws + lay.status_off);
@@ -2150,8 +2222,7 @@ size_t rsf_layout(const spec_dims& d, size_t off, WsLayout* L) {
   L->rsf_norm_off = take(sizeof(RowNorm) * rows);
   L->rsf_rowcnt_off = take(sizeof(uint32_t) * rows);
   L->rsf_req_off = take(sizeof(uint32_t) * (size_t)d.B);
-  L->rsf_list_off = take(sizeof(uint32_t) * (size_t)d.B);
-  L->rsf_ready_off = take(sizeof(uint32_t) * (size_t)d.B);
+  L->rsf_list_off = take(sizeof(ResEntry) * (size_t)d.B);
   L->rsf_rescnt_off = take(sizeof(uint32_t) * (size_t)d.B);
   return off;
 }

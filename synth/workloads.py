@@ -12,8 +12,9 @@ suite is named, so the inputs here are synthetic stand-ins with those shapes:
   (fp32 for the tiny workload);
 * a paged KV cache [num_blocks, Hkv, block, D] whose block tables are a seeded
   random permutation of the physical blocks;
-* for the tree workload, a random ancestor-closed 64-node subtree of the full
-  depth-4 width-4 tree, numbered in BFS order.
+* for the tree workloads, a random ancestor-closed subtree (64 nodes of the
+  full depth-4 width-4 tree; 128 nodes of the depth-4 width-8 tree), numbered
+  in BFS order.
 
 Draft tokens are drawn with the Gumbel-max trick (argmax of d/T plus
 independent standard Gumbel noise), which samples softmax(d/T) exactly without
@@ -63,7 +64,7 @@ class Workload:
         return Workload(**d)
 
 
-# The five synthetic workloads, named by what they are.
+# The synthetic workloads, named by what they are.
 WORKLOADS = {
     "tiny_chain": Workload(
         name="tiny_chain", B=1, gamma=4, V=32, sigma=2.0, noise=0.5, T=1.0,
@@ -78,6 +79,13 @@ WORKLOADS = {
         name="tree_64", B=16, gamma=4, V=32000, sigma=3.0, noise=1.0, T=1.0,
         Hq=32, Hkv=32, D=128, ctx=("fixed", 4096), tree_width=4,
         tree_nodes=64),
+    # a wide tree past 64 nodes (page "推测解码的工程真相 2026", tree-attention
+    # section: widths 6 and 8, batch x width kept at 256): 128 nodes grown in
+    # the full depth-4 width-8 tree, 32 requests x width 8 = 256
+    "tree_wide_128": Workload(
+        name="tree_wide_128", B=32, gamma=4, V=32000, sigma=3.0, noise=1.0, T=1.0,
+        Hq=32, Hkv=32, D=128, ctx=("fixed", 4096), tree_width=8,
+        tree_nodes=128),
     "stress_gqa_152k": Workload(
         name="stress_gqa_152k", B=128, gamma=4, V=152064, sigma=3.0,
         noise=1.5, T=1.0, Hq=64, Hkv=8, D=128, ctx=("uniform", 4096, 32768)),

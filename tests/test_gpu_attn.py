@@ -96,6 +96,27 @@ def test_tree_rows_up_to_128():
     _check(wl, kv, parent, impls=[sv.ATTN_TENSOR_CORES])
 
 
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f32")])
+def test_wide_tree_128_nodes(D, dtype):
+    # 128 nodes: ancestor masks past 64 bits, on each kernel that takes the
+    # shape (128 rows per KV head)
+    wl = workload("tree_wide_128").scaled(D=D, dtype=dtype, Hq=2, Hkv=2)
+    kv = kv_inputs_host(wl, seed=15, B=2, ctx=np.array([0, 1500]))
+    parent = logits_inputs(wl.scaled(V=16), seed=15, B=2)["parent"]
+    assert parent.shape == (2, 128) and (parent >= 64).any()
+    _check(wl, kv, parent)
+
+
+def test_more_rows_than_a_kernel_takes():
+    # 128 nodes x 2 query heads per KV head = 256 rows: refused before launch
+    wl = workload("tree_wide_128").scaled(Hq=4, Hkv=2)
+    kv = kv_inputs_host(wl, seed=16, B=1, ctx=np.array([100]))
+    parent = logits_inputs(wl.scaled(V=16), seed=16, B=1)["parent"]
+    with pytest.raises(sv.SpecError) as e:
+        gpu_attn(wl, kv, parent)
+    assert e.value.code == 3  # SPEC_ERR_UNSUPPORTED
+
+
 def test_small_head_dim_tree():
     wl = workload("tree_64").scaled(D=64, Hq=4, Hkv=2, tree_nodes=21, gamma=3)
     kv = kv_inputs_host(wl, seed=5, B=3, ctx=np.array([0, 40, 129]))

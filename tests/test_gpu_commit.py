@@ -30,9 +30,10 @@ def _commit(wl, kv, path, acc, alias=False):
             new.cpu().numpy(), sv.device_status(ws))
 
 
-@pytest.mark.parametrize("alias", [False, True])
-def test_tree_compaction(alias):
-    wl = workload("tree_64").scaled(V=2000)
+@pytest.mark.parametrize("name,alias", [("tree_64", False), ("tree_64", True),
+                                        ("tree_wide_128", False)])
+def test_tree_compaction(name, alias):
+    wl = workload(name).scaled(V=2000)
     B = 6
     lg = logits_inputs(wl, seed=8, B=B)
     kv = kv_inputs_host(wl.scaled(Hq=4, Hkv=4), seed=8, B=B,

@@ -96,6 +96,18 @@ def test_trees(V, impl):
 
 
 @pytest.mark.parametrize("impl", TREE_IMPLS)
+def test_wide_tree_128_nodes(impl):
+    # 128 nodes of a width-8 tree: child lists and draft-row selection past
+    # node 64, up to 7 residual updates at one node
+    wl = workload("tree_wide_128").scaled(B=6)
+    lg = logits_inputs(wl, seed=14)
+    assert (lg["parent"] >= 64).any()
+    for offset in range(3):
+        g, o, _ = _run(wl, lg, seed=13, offset=offset, impl=impl)
+        assert g["status"] == 0
+
+
+@pytest.mark.parametrize("impl", TREE_IMPLS)
 def test_small_trees_many_rejections(impl):
     # wide fan-out, noisy draft: several rejections per node
     wl = workload("tree_64").scaled(B=8, V=48, gamma=2, tree_width=8,

@@ -41,6 +41,13 @@ def test_workload_shapes():
     t = workload("tree_64").scaled(V=64)
     d = logits_inputs(t, 0, B=2)
     assert d["parent"].shape == (2, 64)
+    w = workload("tree_wide_128").scaled(V=64)
+    d = logits_inputs(w, 0, B=2)
+    par = d["parent"]
+    assert par.shape == (2, 128) and np.all(par[:, 0] == -1)
+    assert np.all(par[:, 1:] < np.arange(1, 128)) and np.all(par[:, 1:] >= 0)
+    assert max(np.bincount(p[1:]).max() for p in par) <= 8
+    assert w.B * w.tree_width <= 256
     lay = kv_layout(WORKLOADS["chain_gqa_128k"], 0)
     need = (lay["ctx_lens"] + 9 + 15) // 16
     assert np.all((lay["block_table"] >= 0).sum(1) == need)

@@ -191,7 +191,12 @@ spec_status spec_verify_attn(const void* q, const void* k_new,
  *                                          (rows of leaves are not read)
  *   tokens        [B, M] int32   drafted token of node n (tokens[b][0] unused)
  *   parent        [B, M] int32 or NULL (chain)
- *   temperature   [B] float      > 0 and finite
+ *   temperature   [B] float      a positive normal finite value, or 0:
+ *                                greedy (page 1 §4.3, first point) -- each
+ *                                row's law is the point mass on its largest
+ *                                logit (smallest index among equal ones), so
+ *                                a draft is accepted iff it is that token
+ *                                and every draw returns it
  *   out_tokens    [B, M] int32   emitted tokens: the a accepted drafts, then
  *                                the drawn token; -1 after that
  *   path          [B, M] int32   accepted node indices, starting with 0; -1 after
@@ -216,6 +221,42 @@ spec_status spec_reject_sample(const void* target_logits,
                                int32_t* accepted_len, float* probe,
                                const spec_dims* dims, void* ws,
                                size_t ws_bytes, void* stream);
+
+/*
+ * spec_reject_sample_filtered -- spec_reject_sample with top-k / top-p
+ * restricted laws.
+ *
+ * Page 2 §5.1: target and draft must sample by one rule (its example: a
+ * nucleus-sampling target against a differently sampling draft).  For a
+ * request with top_k[b] = k and top_p[b] = t, the law of every row it uses,
+ * target and draft alike, is restricted to a prefix of the row's tokens in
+ * the order of their logits, largest first, the smaller index first among
+ * equal logits: the first k tokens (k = 0: all), then the shortest prefix of
+ * those whose mass reaches t times their mass (t = 1: all of them); the
+ * restricted law is renormalised and the walk above runs on it, so the
+ * emitted tokens follow the restricted target law.  At temperature 0 the
+ * filters change nothing.
+ *
+ *   top_k  [B] int32 or NULL   >= 0 (0: no top-k)
+ *   top_p  [B] float or NULL   in (0, 1] (1: no top-p)
+ * Other arguments as in spec_reject_sample.  A request with k < 0 or t
+ * outside (0, 1] fails (SPEC_ERR_INVALID_ARG, accepted_len = -1).  The probe
+ * reports the restricted laws.  Filters run on the staged kernels: with
+ * dims->reject_impl = SPEC_REJECT_FUSED and a filter given the call returns
+ * SPEC_ERR_UNSUPPORTED and launches nothing.  Each needed row of a filtered
+ * request costs a few extra passes over the row (its kept prefix is found by
+ * a radix select over the logits' order keys).
+ */
+spec_status spec_reject_sample_filtered(const void* target_logits,
+                                        const void* draft_logits,
+                                        const int32_t* tokens, const int32_t* parent,
+                                        const float* temperature,
+                                        const int32_t* top_k, const float* top_p,
+                                        uint64_t seed, uint64_t offset, uint64_t b_base,
+                                        int32_t* out_tokens, int32_t* path,
+                                        int32_t* accepted_len, float* probe,
+                                        const spec_dims* dims, void* ws,
+                                        size_t ws_bytes, void* stream);
 
 /*
  * kv_commit -- roll back / compact the cache to the accepted path.

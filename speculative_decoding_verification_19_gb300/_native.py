@@ -28,7 +28,8 @@ REJECT_AUTO, REJECT_STAGED, REJECT_FUSED = 0, 1, 2
 # every symbol the header declares
 EXPORTS = (
     "spec_workspace_size", "spec_workspace_init", "spec_get_device_status",
-    "spec_verify_attn", "spec_reject_sample", "kv_commit", "spec_philox_block",
+    "spec_verify_attn", "spec_reject_sample", "spec_reject_sample_filtered", "kv_commit",
+    "spec_philox_block",
     "spec_status_string", "spec_last_launch_count", "spec_reject_sample_noalloc",
     "spec_ctrl_default_config", "spec_ctrl_init", "spec_ctrl_update", "spec_ctrl_metrics",
     "spec_step_stats",
@@ -79,6 +80,9 @@ def lib() -> ctypes.CDLL:
     L.spec_reject_sample.argtypes = [vp, vp, vp, vp, vp, u64, u64, u64, vp, vp, vp,
                                      vp, pd, vp, sz, vp]
     L.spec_reject_sample.restype = i32
+    L.spec_reject_sample_filtered.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u64, u64, vp,
+                                              vp, vp, vp, pd, vp, sz, vp]
+    L.spec_reject_sample_filtered.restype = i32
     L.spec_reject_sample_noalloc.argtypes = [vp, vp, vp, vp, vp, u64, u64, u64, vp, vp,
                                              vp, vp, pd, vp]
     L.spec_reject_sample_noalloc.restype = i32
@@ -168,13 +172,25 @@ def spec_verify_attn(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens,
 
 def spec_reject_sample(target_logits, draft_logits, tokens, parent, temperature,
                        seed, offset, out_tokens, path, accepted_len, probe,
-                       dims: SpecDims, ws, b_base=0, stream=None) -> int:
-    code = lib().spec_reject_sample(
-        _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent),
-        _ptr(temperature), int(seed) % (1 << 64), int(offset) % (1 << 64),
-        int(b_base) % (1 << 64), _ptr(out_tokens), _ptr(path), _ptr(accepted_len),
-        _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(stream))
-    _check("spec_reject_sample", code)
+                       dims: SpecDims, ws, b_base=0, stream=None, top_k=None,
+                       top_p=None) -> int:
+    """spec_reject_sample; with top_k and / or top_p ([B] int32 / float32
+    device tensors) spec_reject_sample_filtered."""
+    if top_k is None and top_p is None:
+        code = lib().spec_reject_sample(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent),
+            _ptr(temperature), int(seed) % (1 << 64), int(offset) % (1 << 64),
+            int(b_base) % (1 << 64), _ptr(out_tokens), _ptr(path), _ptr(accepted_len),
+            _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(stream))
+        _check("spec_reject_sample", code)
+    else:
+        code = lib().spec_reject_sample_filtered(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent),
+            _ptr(temperature), _ptr(top_k), _ptr(top_p), int(seed) % (1 << 64),
+            int(offset) % (1 << 64), int(b_base) % (1 << 64), _ptr(out_tokens), _ptr(path),
+            _ptr(accepted_len), _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(),
+            _stream(stream))
+        _check("spec_reject_sample_filtered", code)
     return lib().spec_last_launch_count()
 
 

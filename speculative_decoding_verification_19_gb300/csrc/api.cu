@@ -59,6 +59,7 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_off = take(L.rs_bytes);
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
+  L.rs_filt_off = take(sizeof(FilterInfo) * (size_t)d.B * 2 * d.M);
   off = rsf_layout(d, off, &L);
   L.total = off;
   return L;
@@ -186,12 +187,13 @@ spec_status spec_verify_attn(const void* q, const void* k_new, const void* v_new
   return from_cuda(e);
 }
 
-spec_status spec_reject_sample(const void* target_logits, const void* draft_logits,
-                               const int32_t* tokens, const int32_t* parent,
-                               const float* temperature, uint64_t seed, uint64_t offset,
-                               uint64_t b_base, int32_t* out_tokens, int32_t* path,
-                               int32_t* accepted_len, float* probe, const spec_dims* dims,
-                               void* ws, size_t ws_bytes, void* stream) {
+static spec_status reject_common(const void* target_logits, const void* draft_logits,
+                                 const int32_t* tokens, const int32_t* parent,
+                                 const float* temperature, const int32_t* top_k,
+                                 const float* top_p, uint64_t seed, uint64_t offset,
+                                 uint64_t b_base, int32_t* out_tokens, int32_t* path,
+                                 int32_t* accepted_len, float* probe, const spec_dims* dims,
+                                 void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
   spec_status s = check_common(dims);
   if (s != SPEC_OK) return s;
@@ -205,6 +207,8 @@ spec_status spec_reject_sample(const void* target_logits, const void* draft_logi
   if (!target_logits || !draft_logits || !tokens || !temperature || !out_tokens || !path ||
       !accepted_len)
     return SPEC_ERR_INVALID_ARG;
+  if ((top_k != nullptr || top_p != nullptr) && dims->reject_impl == SPEC_REJECT_FUSED)
+    return SPEC_ERR_UNSUPPORTED;  // the one-kernel path has no filters
   const WsLayout lay = workspace_layout(*dims);
   RsArgs a;
   a.target = target_logits;
@@ -212,6 +216,8 @@ spec_status spec_reject_sample(const void* target_logits, const void* draft_logi
   a.tokens = tokens;
   a.parent = parent;
   a.temperature = temperature;
+  a.top_k = top_k;
+  a.top_p = top_p;
   a.seed = seed;
   a.offset = offset;
   a.b_base = b_base;
@@ -226,6 +232,30 @@ spec_status spec_reject_sample(const void* target_logits, const void* draft_logi
   g_launches = launches;
   if (e == cudaErrorNotSupported) return SPEC_ERR_UNSUPPORTED;
   return from_cuda(e);
+}
+
+spec_status spec_reject_sample(const void* target_logits, const void* draft_logits,
+                               const int32_t* tokens, const int32_t* parent,
+                               const float* temperature, uint64_t seed, uint64_t offset,
+                               uint64_t b_base, int32_t* out_tokens, int32_t* path,
+                               int32_t* accepted_len, float* probe, const spec_dims* dims,
+                               void* ws, size_t ws_bytes, void* stream) {
+  return reject_common(target_logits, draft_logits, tokens, parent, temperature, nullptr,
+                       nullptr, seed, offset, b_base, out_tokens, path, accepted_len, probe, dims,
+                       ws, ws_bytes, stream);
+}
+
+spec_status spec_reject_sample_filtered(const void* target_logits, const void* draft_logits,
+                                        const int32_t* tokens, const int32_t* parent,
+                                        const float* temperature, const int32_t* top_k,
+                                        const float* top_p, uint64_t seed, uint64_t offset,
+                                        uint64_t b_base, int32_t* out_tokens, int32_t* path,
+                                        int32_t* accepted_len, float* probe,
+                                        const spec_dims* dims, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  return reject_common(target_logits, draft_logits, tokens, parent, temperature, top_k, top_p,
+                       seed, offset, b_base, out_tokens, path, accepted_len, probe, dims, ws,
+                       ws_bytes, stream);
 }
 
 spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,

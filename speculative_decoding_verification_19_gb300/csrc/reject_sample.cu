@@ -367,6 +367,354 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
 }
 
 // ---------------------------------------------------------------------------
+// Filtered laws (top-k, top-p): the kept prefix of each row
+// ---------------------------------------------------------------------------
+// Page 2 §5.1: target and draft must sample by one rule (a nucleus-sampling
+// target against a differently sampling draft is its example).  A request
+// with a top-k count and / or a top-p mass restricts the law of every row it
+// uses -- target and draft alike -- to a prefix of the row's tokens ordered
+// by logit, largest first, the smaller index first among equal logits: the
+// first k, then the shortest prefix of those whose mass reaches top_p times
+// their mass.  The prefix is held as (v, idx): a token is kept iff its logit
+// is above v, or equal to v with an index at most idx.
+//
+// One CTA per row, after the statistics pass (the row maximum m comes from
+// the chunk statistics).  The k-th token and the top-p cut are found by a
+// most-significant-digit-first radix select over 8-bit digits of an
+// order-preserving key of the logit (two digits settle a bf16 value, four an
+// fp32 one), each digit one pass over the row building a 256-bin histogram
+// of counts and of masses exp2((z - m) cs) in shared memory; the tokens equal
+// to the cut's value are then taken in index order (one more pass, in tiles,
+// with a block-wide prefix count).  Kept mass K = sum over kept tokens of
+// exp2((z - m) cs), so that the restricted law is exp2((z - m) cs) / K.
+constexpr int kFiltThreads = 512;
+constexpr int kFiltWarps = kFiltThreads / kWarp;
+
+// Order key of a logit: larger logits get smaller keys (ascending key = the
+// filter's order of values).
+__device__ __forceinline__ uint32_t desc_key(float z) {
+  const uint32_t b = __float_as_uint(z);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b ^ 0x80000000u);
+  return ~ord;
+}
+
+struct FilterSmem {
+  uint32_t cnt[256];
+  unsigned long long mass[256];  // fixed point: 2^40 per unit of exp2((z - m) cs)
+  double red[kFiltWarps];
+  int wsum[kFiltWarps];
+  uint32_t prefix;   // key digits fixed so far
+  uint32_t rem;      // tokens still to take inside the prefix (count select)
+  double rem_mass;   // mass still to take inside the prefix (mass select)
+  double above;      // mass of the tokens before the prefix
+  uint32_t group_n;  // tokens of the final group (inside the kept-k set)
+  int found_idx;
+  float found_val;
+  int running;
+};
+constexpr double kMassScale = 1099511627776.0;  // 2^40
+
+// Whether token e (logit z, key `key`) is in the kept-k set: key group below
+// kkey's, or equal with an index at most kidx (kkey = 0xffffffff, kidx =
+// INT_MAX keep everything).
+__device__ __forceinline__ bool in_kept(uint32_t key, int64_t e, uint32_t kkey, uint32_t kshift,
+                                        int kidx) {
+  const uint32_t kg = key >> kshift, kk = kkey >> kshift;
+  return kg < kk || (kg == kk && e <= (int64_t)kidx);
+}
+
+// One radix digit: the histogram of digit `d` (counts, and with kMass the
+// masses) over the tokens whose higher digits equal `prefix` and that lie in
+// the kept-k set.  Lanes of a warp that fall in one bin are combined first
+// (one shared-memory atomic per bin and warp instruction): the masses as 2^40
+// fixed point, summed over the group in two 20-bit halves.
+template <typename T, bool kAligned, bool kMass>
+__device__ void filter_hist(const T* row, int V, float m, float cs, int d, uint32_t prefix,
+                            uint32_t kkey, uint32_t kshift, int kidx, FilterSmem& sh) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  for (int i = tid; i < 256; i += kFiltThreads) {
+    sh.cnt[i] = 0u;
+    sh.mass[i] = 0ull;
+  }
+  __syncthreads();
+  const int sh_d = 8 * d;
+  // warp-uniform trip count: every lane takes part in the match / reduce
+  for (int64_t e0 = (int64_t)warp * kWarp * EPV; e0 < V; e0 += (int64_t)kFiltThreads * EPV) {
+    const int64_t e = e0 + (int64_t)lane * EPV;
+    float z[EPV];
+    if (e < V) {
+      load_vec<T, kAligned>(row, e, V, z);
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) z[i] = -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      const uint32_t key = desc_key(z[i]);
+      const bool in = e + i < V && (d == 3 || (key >> (sh_d + 8)) == (prefix >> (sh_d + 8))) &&
+                      in_kept(key, e + i, kkey, kshift, kidx);
+      const uint32_t bin = in ? (key >> sh_d) & 255u : 256u + lane;  // out: a group of one
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      const bool leader = lane == __ffs(peers) - 1;
+      if (kMass) {
+        const unsigned long long fx =
+            in ? (unsigned long long)((double)fast_exp2((z[i] - m) * cs) * kMassScale) : 0ull;
+        const unsigned hs = __reduce_add_sync(peers, (unsigned)(fx >> 20));
+        const unsigned ls = __reduce_add_sync(peers, (unsigned)(fx & 0xfffffu));
+        if (in && leader) atomicAdd(&sh.mass[bin], ((unsigned long long)hs << 20) + ls);
+      }
+      if (in && leader) atomicAdd(&sh.cnt[bin], (uint32_t)__popc(peers));
+    }
+  }
+  __syncthreads();
+}
+
+// Exact (fp64) mass of the kept set: tokens with key group below gkey, or
+// equal with an index at most gidx, within the kept-k set.
+template <typename T, bool kAligned>
+__device__ double filter_kept_mass(const T* row, int V, float m, float cs, uint32_t gkey,
+                                   uint32_t gshift, int gidx, uint32_t kkey, uint32_t kshift,
+                                   int kidx, FilterSmem& sh) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int tid = threadIdx.x;
+  double acc = 0.0;
+  for (int64_t e = (int64_t)tid * EPV; e < V; e += (int64_t)kFiltThreads * EPV) {
+    float z[EPV];
+    load_vec<T, kAligned>(row, e, V, z);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      const uint32_t key = desc_key(z[i]);
+      const bool keep = e + i < V && in_kept(key, e + i, gkey, gshift, gidx) &&
+                        in_kept(key, e + i, kkey, kshift, kidx);
+      if (keep) s += fast_exp2((z[i] - m) * cs);
+    }
+    acc += (double)s;
+  }
+  acc = warp_sum(acc);
+  __syncthreads();
+  if (tid % kWarp == 0) sh.red[tid / kWarp] = acc;
+  __syncthreads();
+  double t = 0.0;
+  for (int w = 0; w < kFiltWarps; ++w) t += sh.red[w];
+  __syncthreads();
+  return t;
+}
+
+// The j-th (1-based) token in index order whose key group (key >> gshift)
+// equals gkey: its index and logit, into sh.found_idx / sh.found_val.
+template <typename T, bool kAligned>
+__device__ void filter_nth(const T* row, int V, uint32_t gkey, uint32_t gshift, int j,
+                           FilterSmem& sh) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int kVecs = 4;  // vectors per thread per tile, consecutive
+  constexpr int kPer = kVecs * EPV;
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  if (tid == 0) {
+    sh.running = 0;
+    sh.found_idx = -1;
+    sh.found_val = -INFINITY;
+  }
+  __syncthreads();
+  for (int64_t t0 = 0; t0 < V; t0 += (int64_t)kFiltThreads * kPer) {
+    const int64_t e0 = t0 + (int64_t)tid * kPer;
+    float z[kVecs][EPV];
+#pragma unroll
+    for (int v = 0; v < kVecs; ++v) {
+      if (e0 + v * EPV < V) {
+        load_vec<T, kAligned>(row, e0 + v * EPV, V, z[v]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) z[v][i] = -INFINITY;
+      }
+    }
+    int c = 0;
+#pragma unroll
+    for (int v = 0; v < kVecs; ++v)
+#pragma unroll
+      for (int i = 0; i < EPV; ++i)
+        c += (e0 + v * EPV + i < V && (desc_key(z[v][i]) >> gshift) == gkey) ? 1 : 0;
+    // block-wide exclusive prefix of the counts, in thread (= index) order
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == kWarp - 1) sh.wsum[warp] = incl;
+    __syncthreads();
+    int base = sh.running, total = 0;
+    for (int w = 0; w < kFiltWarps; ++w) {
+      if (w < warp) base += sh.wsum[w];
+      total += sh.wsum[w];
+    }
+    const int excl = base + incl - c;
+    if (c > 0 && excl < j && j <= excl + c) {
+      int need = j - excl;
+#pragma unroll
+      for (int v = 0; v < kVecs; ++v)
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) {
+          const int64_t e = e0 + v * EPV + i;
+          if (need > 0 && e < V && (desc_key(z[v][i]) >> gshift) == gkey) {
+            if (--need == 0) {
+              sh.found_idx = (int)e;
+              sh.found_val = z[v][i];
+            }
+          }
+        }
+    }
+    __syncthreads();
+    const bool done = sh.running + total >= j;
+    __syncthreads();
+    if (tid == 0) sh.running += total;
+    if (done) break;
+    __syncthreads();
+  }
+  __syncthreads();
+}
+
+template <typename T, bool kAligned>
+__global__ void __launch_bounds__(kFiltThreads) rs_filter_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ parent,
+    const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
+    const float* __restrict__ top_p, spec_dims d, int n_chunks, const RowStat* stats,
+    FilterInfo* __restrict__ finfo) {
+  __shared__ FilterSmem sh;
+  const int M = d.M, V = d.V;
+  const int which = blockIdx.x / M, n = blockIdx.x % M, b = blockIdx.y;
+  const int tid = threadIdx.x;
+  FilterInfo* out = finfo + ((int64_t)b * 2 + which) * M + n;
+  pdl_trigger();
+  pdl_wait();  // the statistics come from the previous kernel
+  const float temp = temperature[b];
+  const int k = top_k != nullptr ? top_k[b] : 0;
+  const float tp = top_p != nullptr ? top_p[b] : 1.0f;
+  const bool use_k = k > 0 && k < V;
+  const bool use_p = tp < 1.0f;
+  bool needed = which == 0 || row_needed(parent, M, b, which, n);
+  needed = __syncthreads_or(needed);
+  const bool valid = temperature_ok(temp) && k >= 0 && tp > 0.0f && tp <= 1.0f;
+  if (!needed || !valid || !(use_k || use_p)) {
+    if (tid == 0) *out = FilterInfo{-INFINITY, 0x7fffffff, 0.0};  // nothing filtered
+    return;
+  }
+  const T* row = (which == 0 ? target : draft) + ((int64_t)b * M + n) * V;
+  const float cs = stat_scale(temp);
+  // the row maximum from its chunk statistics
+  const RowStat* st = stats + (((int64_t)b * 2 + which) * M + n) * n_chunks;
+  float mx = -INFINITY;
+  for (int c = tid; c < n_chunks; c += kFiltThreads) mx = fmaxf(mx, st[c].m);
+  mx = warp_max(mx);
+  if (tid % kWarp == 0) sh.red[tid / kWarp] = (double)mx;
+  __syncthreads();
+  float m = -INFINITY;
+  for (int w = 0; w < kFiltWarps; ++w) m = fmaxf(m, (float)sh.red[w]);
+  __syncthreads();
+  if (!(m > -INFINITY && m < INFINITY)) {  // no distribution: the request fails later
+    if (tid == 0) *out = FilterInfo{-INFINITY, 0x7fffffff, 0.0};
+    return;
+  }
+  const int last_d = sizeof(T) == 2 ? 2 : 0;  // a bf16 value is settled by two digits
+  const uint32_t gshift = 8u * last_d;
+
+  // ---- top-k: the k-th token of the order ---------------------------------
+  uint32_t kkey = 0xffffffffu, kshift = 0;
+  int kidx = 0x7fffffff;
+  if (use_k) {
+    if (tid == 0) {
+      sh.prefix = 0u;
+      sh.rem = (uint32_t)k;
+    }
+    __syncthreads();
+    for (int dg = 3; dg >= last_d; --dg) {
+      filter_hist<T, kAligned, false>(row, V, m, cs, dg, sh.prefix, 0xffffffffu, 0, 0x7fffffff,
+                                      sh);
+      if (tid == 0) {
+        uint32_t cum = 0;
+        int bin = 255;
+        for (int i = 0; i < 256; ++i) {
+          if (cum + sh.cnt[i] >= sh.rem) {
+            bin = i;
+            break;
+          }
+          cum += sh.cnt[i];
+        }
+        sh.rem -= cum;
+        sh.prefix |= (uint32_t)bin << (8 * dg);
+      }
+      __syncthreads();
+    }
+    const uint32_t pk = sh.prefix;
+    filter_nth<T, kAligned>(row, V, pk >> gshift, gshift, (int)sh.rem, sh);
+    kkey = pk;
+    kshift = gshift;
+    kidx = sh.found_idx;
+    if (!use_p) {
+      const float vk = sh.found_val;
+      const double K = filter_kept_mass<T, kAligned>(row, V, m, cs, kkey, kshift, kidx,
+                                                     0xffffffffu, 0, 0x7fffffff, sh);
+      if (tid == 0) *out = FilterInfo{vk, kidx, K};
+      return;
+    }
+  }
+
+  // ---- top-p: the shortest prefix of the kept-k set reaching top_p of its mass
+  if (tid == 0) {
+    sh.prefix = 0u;
+    sh.above = 0.0;
+  }
+  __syncthreads();
+  for (int dg = 3; dg >= last_d; --dg) {
+    filter_hist<T, kAligned, true>(row, V, m, cs, dg, sh.prefix, kkey, kshift, kidx, sh);
+    if (tid == 0) {
+      if (dg == 3) {  // the first digit sees the whole kept-k set
+        double tot = 0.0;
+        for (int i = 0; i < 256; ++i) tot += (double)sh.mass[i] / kMassScale;
+        sh.rem_mass = (double)tp * tot;
+      }
+      // the first bin whose running mass reaches what is left to take
+      double cum = 0.0;
+      int bin = -1, last_nz = 0;
+      for (int i = 0; i < 256; ++i) {
+        if (sh.cnt[i] == 0u) continue;
+        last_nz = i;
+        const double mi = (double)sh.mass[i] / kMassScale;
+        if (cum + mi >= sh.rem_mass) {
+          bin = i;
+          break;
+        }
+        cum += mi;
+      }
+      if (bin < 0) {  // rounding at the very end: the last non-empty bin
+        bin = last_nz;
+        cum -= (double)sh.mass[bin] / kMassScale;
+      }
+      sh.rem_mass -= cum;
+      sh.above += cum;
+      sh.prefix |= (uint32_t)bin << (8 * dg);
+      if (dg == last_d) sh.group_n = sh.cnt[bin];
+    }
+    __syncthreads();
+  }
+  // The group of equal logits holding the cut: the smallest count j of its
+  // tokens (in index order) whose mass reaches what is left.
+  const uint32_t gp = sh.prefix >> gshift;
+  filter_nth<T, kAligned>(row, V, gp, gshift, 1, sh);  // its value
+  const float vp = sh.found_val;
+  const double e = (double)fast_exp2((vp - m) * cs);
+  const double jd = e > 0.0 ? ceil(sh.rem_mass / e) : 1.0;
+  const int jp = jd < 1.0 ? 1 : (jd > (double)sh.group_n ? (int)sh.group_n : (int)jd);
+  __syncthreads();
+  if (jp > 1) filter_nth<T, kAligned>(row, V, gp, gshift, jp, sh);
+  const int pidx = sh.found_idx;
+  const double K = filter_kept_mass<T, kAligned>(row, V, m, cs, sh.prefix, gshift, pidx, kkey,
+                                                 kshift, kidx, sh);
+  if (tid == 0) *out = FilterInfo{vp, pidx, K};
+}
+
+// ---------------------------------------------------------------------------
 // pass 2: decisions (and bonus draws); passes 3-4: residual draws
 // ---------------------------------------------------------------------------
 // Weights of the EPV elements starting at e (elements at or past `lim`
@@ -392,7 +740,7 @@ __device__ __forceinline__ float vec_weights(const T* trow, const T* drow, int64
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < EPV; ++i) {
-    w[i] = (e + i < lim) ? weight_of(zt[i], zd[i], c, nrej) : 0.f;
+    w[i] = (e + i < lim) ? weight_of(zt[i], zd[i], e + i, c, nrej) : 0.f;
     s += w[i];
   }
   return s;
@@ -566,7 +914,7 @@ __device__ __forceinline__ float lane_weights(const T* trow, const T* drow, int6
     unpack16(raw_t[v], zt);
     unpack16(raw_d[v], zd);
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) s += weight_of(zt[i], zd[i], c, nrej);
+    for (int i = 0; i < EPV; ++i) s += weight_of(zt[i], zd[i], e + v * EPV + i, c, nrej);
   }
   return s;
 }
@@ -617,7 +965,7 @@ __device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
       zd = __uint_as_float(wd);
     }
     const bool in = seg + lane * EW + i < V;
-    w[i] = in ? weight_of(zt, zd, c, nrej) : 0.f;
+    w[i] = in ? weight_of(zt, zd, seg + lane * EW + i, c, nrej) : 0.f;
     ls += w[i];
   }
   const dfloat cum = df_warp_scan(df_make(ls));
@@ -744,6 +1092,10 @@ struct DecideSmem {
   int chain_rej[kMaxM];  // chain: the accept test of node n failed
   float chain_p[kMaxM], chain_q[kMaxM];
   int rowA[2][kMaxM];    // greedy: each row's largest logit (smallest index)
+  // filtered laws: each row's kept prefix (v, idx) and kept mass K
+  float fv[2][kMaxM];
+  int fi[2][kMaxM];
+  double fK[2][kMaxM];
 };
 
 // The decisions of request b from its rows' chunk statistics, by one CTA of
@@ -759,7 +1111,7 @@ __device__ void decide_request(
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, const spec_dims& d, int n_chunks,
     int chunk, const RowStat* stats, DrawState* draws, uint32_t* status, int b, bool stats_lost,
-    DecideSmem& sh) {
+    const int32_t* top_k, const float* top_p, const FilterInfo* finfo, DecideSmem& sh) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kSweep = kDecThreads * EPV;
   const int tid = threadIdx.x;
@@ -779,6 +1131,14 @@ __device__ void decide_request(
   const float temp = temperature[b];
   const bool greedy = temp == 0.f;
   int bad_arg = !temperature_valid(temp);
+  if (top_k != nullptr) bad_arg |= top_k[b] < 0;
+  if (top_p != nullptr) {
+    const float tp = top_p[b];
+    bad_arg |= !(tp > 0.0f && tp <= 1.0f);
+  }
+  // the filter kernel marks a filtered row with its kept mass K > 0 (every
+  // row of a request is filtered alike; target row 0 is always read)
+  const bool filtered = finfo != nullptr && !greedy && finfo[(int64_t)b * 2 * M].K > 0.0;
   int bad_tok = 0;
   if (tid < M) {
     const int32_t x = tokens[(int64_t)b * M + tid];
@@ -806,6 +1166,13 @@ __device__ void decide_request(
       sh.first_child[p] = n;
     }
   }
+  if (filtered)
+    for (int r = tid; r < 2 * M; r += kDecThreads) {
+      const FilterInfo f = finfo[(int64_t)b * 2 * M + r];
+      sh.fv[r / M][r % M] = f.v;
+      sh.fi[r / M][r % M] = f.idx;
+      sh.fK[r / M][r % M] = f.K;
+    }
   __syncthreads();
   const float cs = stat_scale(temp);
 
@@ -875,7 +1242,7 @@ __device__ void decide_request(
     const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
     sh.uacc[tid] = (double)u24(r.w[0]);
     sh.usmp[tid] = (double)u24(r.w[1]);
-    if (tid >= 1 && parent == nullptr) {
+    if (tid >= 1 && parent == nullptr && !filtered) {
       // chain: every draft's test at once.  The exponent of p(x)/q(x) is
       // formed in fp64 and split into integer and fraction, so that one fp32
       // exp2 gives the ratio to about 3e-7 relative.
@@ -901,9 +1268,20 @@ __device__ void decide_request(
         sh.chain_q[tid] = exp2f((float)ed) / sd_f;
       }
     } else if (tid >= 1) {
-      const int p = parent[(int64_t)b * M + tid];
-      sh.px[tid] = exp2(((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64) / sh.rowS[0][p];
-      sh.qx[tid] = exp2(((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64) / sh.rowS[1][p];
+      const int p = parent ? parent[(int64_t)b * M + tid] : tid - 1;
+      if (filtered) {
+        // the restricted laws: zero outside the kept prefix, over the kept mass
+        const int x = sh.tok[tid];
+        const bool kt = kept_at(sh.gzt[tid], x, sh.fv[0][p], sh.fi[0][p]);
+        const bool kd = kept_at(sh.gzd[tid], x, sh.fv[1][p], sh.fi[1][p]);
+        sh.px[tid] = kt ? exp2(((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64) / sh.fK[0][p]
+                        : 0.0;
+        sh.qx[tid] = kd ? exp2(((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64) / sh.fK[1][p]
+                        : 0.0;
+      } else {
+        sh.px[tid] = exp2(((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64) / sh.rowS[0][p];
+        sh.qx[tid] = exp2(((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64) / sh.rowS[1][p];
+      }
     }
   }
   __syncthreads();
@@ -955,7 +1333,7 @@ __device__ void decide_request(
     return;
   }
 
-  if (parent == nullptr) {
+  if (parent == nullptr && !filtered) {
     // ---- a chain: the walk stops at the first rejected draft ---------------
     if (tid == 0) {
       int fr = M;
@@ -979,6 +1357,7 @@ __device__ void decide_request(
     }
     if (tid == 0) {
       accepted_len[b] = a;
+      ctx_no_filter(sh.ctx);
       sh.ctx.mT = sh.rowM[0][a];
       sh.ctx.invST = (float)(1.0 / sh.rowS[0][a]);
       sh.ctx.cs = cs;
@@ -1048,13 +1427,22 @@ __device__ void decide_request(
     const T* trow = target + ((int64_t)b * M + node) * V;
     const T* drow = draft + ((int64_t)b * M + node) * V;
     if (tid == 0) {
+      ctx_no_filter(sh.ctx);
       sh.ctx.mT = sh.rowM[0][node];
-      sh.ctx.invST = (float)(1.0 / sh.rowS[0][node]);
+      sh.ctx.invST = (float)(1.0 / (filtered ? sh.fK[0][node] : sh.rowS[0][node]));
       sh.ctx.cs = cs;
       sh.ctx.nrej = 0;
+      if (filtered) {
+        sh.ctx.vT = sh.fv[0][node];
+        sh.ctx.iT = sh.fi[0][node];
+      }
       if (sh.first_child[node] >= 0) {
         sh.ctx.mD = sh.rowM[1][node];
-        sh.ctx.invSD = (float)(1.0 / sh.rowS[1][node]);
+        sh.ctx.invSD = (float)(1.0 / (filtered ? sh.fK[1][node] : sh.rowS[1][node]));
+        if (filtered) {
+          sh.ctx.vD = sh.fv[1][node];
+          sh.ctx.iD = sh.fi[1][node];
+        }
       } else {
         sh.ctx.mD = 0.f;
         sh.ctx.invSD = 0.f;
@@ -1082,9 +1470,11 @@ __device__ void decide_request(
         moved = true;
         break;
       }
-      if (sh.next_sib[child] >= 0) {
+      if (sh.next_sib[child] >= 0 || filtered) {
         // mass of the next residual, needed by the next sibling's test
-        // (trees only: a chain node has a single child)
+        // (trees only: a chain node has a single child); for a filtered law
+        // after the last child too, so that a residual of zero mass falls
+        // back to the node's law before the draw is posted
         const int nrej_next = sh.ctx.nrej + 1;
         double acc = 0.0;
         for (int64_t e = (int64_t)tid * EPV; e < V; e += kSweep) {
@@ -1122,7 +1512,9 @@ __device__ void decide_request(
     // ---- the draw at `node` ----------------------------------------------
     const double u = sh.usmp[node];
     if (tid == 0) accepted_len[b] = sh.s_a;
-    if (sh.ctx.nrej > 0) {
+    // a filtered law's chunk masses are not in the statistics: every draw of
+    // a filtered request (residual or not) goes to the residual kernels
+    if (sh.ctx.nrej > 0 || filtered) {
       // residual: its chunk masses need a pass over two rows, spread over
       // the whole GPU by the next kernel
       DrawState& st = draws[b];
@@ -1170,16 +1562,17 @@ __global__ void __launch_bounds__(kDecThreads) rs_decide_kernel(
     const int32_t* __restrict__ parent, const float* __restrict__ temperature, uint64_t seed,
     uint64_t offset, uint64_t b_base, int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* stats, DrawState* __restrict__ draws, uint32_t* status) {
+    int chunk, const RowStat* stats, DrawState* __restrict__ draws, uint32_t* status,
+    const int32_t* top_k, const float* top_p, const FilterInfo* finfo) {
   __shared__ DecideSmem sh;
   pdl_trigger();
-  pdl_wait();  // the statistics come from the previous kernel
+  pdl_wait();  // the statistics (and the filters) come from the previous kernels
   // A wait of the statistics kernel that gave up left some statistics
   // unwritten: then no request of the call is decided on them.
   const bool stats_lost = (ld_volatile_u32(status) >> SPEC_ERR_TIMEOUT) & 1u;
   decide_request<T, kAligned>(target, draft, tokens, parent, temperature, seed, offset, b_base,
                               out_tokens, path, accepted_len, probe, d, n_chunks, chunk, stats,
-                              draws, status, blockIdx.x, stats_lost, sh);
+                              draws, status, blockIdx.x, stats_lost, top_k, top_p, finfo, sh);
 }
 
 // Passes 3 and 4: the residual draws.
@@ -1285,7 +1678,8 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
         if (lane == 0) {
           out_tokens[(int64_t)b * M + a_acc] = tk;
           if (probe != nullptr) {
-            probe[((int64_t)b * M + node) * 4 + 2] = (float)Z;
+            // a draw from the node's own (filtered) law reports Z = 1
+            probe[((int64_t)b * M + node) * 4 + 2] = ctx.nrej > 0 ? (float)Z : 1.0f;
             probe[((int64_t)b * M + node) * 4 + 3] = (float)((double)w / Z);
           }
         }
@@ -1309,7 +1703,7 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
   } else {
     chunk_draw<T, kAligned>(trow, drow, (int64_t)s_chunk * chunk, chunk, d.V, ctx, ctx.nrej,
                             s_trel, &ds);
-    Zrep = s_z;
+    Zrep = ctx.nrej > 0 ? s_z : 1.0;
   }
   if (tid == 0) {
     out_tokens[(int64_t)b * M + a_acc] = ds.token;
@@ -1631,6 +2025,7 @@ __device__ __noinline__ void fused_decide(
   const double u = (double)u24(r.w[1]);
   const RowNorm ta = ld_norm(nb + a);
   DecideCtx c;
+  ctx_no_filter(c);
   c.mT = ta.m;
   c.invST = (float)(1.0 / ta.S);
   c.cs = cs;
@@ -1717,6 +2112,7 @@ __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
   const uint4 r2 = __ldcg(reinterpret_cast<const uint4*>(ent) + 2);
   const int b = (int)r0.x, node = (int)r0.y, a_acc = (int)r0.z;
   DecideCtx ctx;
+  ctx_no_filter(ctx);
   ctx.mT = __uint_as_float(r1.x);
   ctx.mD = __uint_as_float(r1.y);
   ctx.invST = __uint_as_float(r1.z);
@@ -2159,11 +2555,26 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3((unsigned)d.B);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, rs_decide_kernel<T, kAligned>, tgt, dft, a.tokens,
-                                     a.parent, a.temperature, a.seed, a.offset, a.b_base,
-                                     a.out_tokens, a.path, a.accepted_len, a.probe, d,
-                                     lay.rs_chunks, lay.rs_chunk, (const RowStat*)stats, draws,
-                                     status);
+  // filtered laws (top-k / top-p): each row's kept prefix, after the
+  // statistics and before the decisions
+  const bool filters = a.top_k != nullptr || a.top_p != nullptr;
+  FilterInfo* finfo = filters ? reinterpret_cast<FilterInfo*>(ws + lay.rs_filt_off) : nullptr;
+  cudaError_t e;
+  if (filters) {
+    cfg.blockDim = dim3(kFiltThreads);
+    cfg.gridDim = dim3((unsigned)(2 * d.M), (unsigned)d.B);
+    e = cudaLaunchKernelEx(&cfg, rs_filter_kernel<T, kAligned>, tgt, dft, a.parent, a.temperature,
+                           a.top_k, a.top_p, d, lay.rs_chunks, (const RowStat*)stats, finfo);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.gridDim = dim3((unsigned)d.B);
+  }
+  e = cudaLaunchKernelEx(&cfg, rs_decide_kernel<T, kAligned>, tgt, dft, a.tokens, a.parent,
+                         a.temperature, a.seed, a.offset, a.b_base, a.out_tokens, a.path,
+                         a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk,
+                         (const RowStat*)stats, draws, status, a.top_k, a.top_p,
+                         (const FilterInfo*)finfo);
   if (e != cudaSuccess) return e;
   cfg.blockDim = dim3(kResThreads);
   cfg.gridDim = dim3((unsigned)((int64_t)rs_res_spans(lay.rs_chunks) * d.B));
@@ -2236,7 +2647,9 @@ cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int
   const bool aligned = ((size_t)a.d.V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0;
-  const bool fused_ok = rso_supported(a.d, aligned, a.parent == nullptr);
+  // the one-kernel path takes neither trees nor filters
+  const bool fused_ok = rso_supported(a.d, aligned, a.parent == nullptr) &&
+                        a.top_k == nullptr && a.top_p == nullptr;
   if (a.d.reject_impl == SPEC_REJECT_FUSED || (a.d.reject_impl == SPEC_REJECT_AUTO && fused_ok)) {
     if (!fused_ok) return cudaErrorNotSupported;
     return a.d.logits_dtype == SPEC_BF16 ? launch_fused_t<__nv_bfloat16>(a, lay, st, launches)

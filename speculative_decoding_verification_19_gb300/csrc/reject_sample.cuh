@@ -19,9 +19,14 @@ constexpr int kRsMaxM = kMaxNodes;
 // node's target / draft rows, and the masses of the residuals taken so far.
 struct DecideCtx {
   float mT, mD;          // row maxima of the node's target / draft rows
-  float invST, invSD;    // 1 / row sums (fp32)
+  float invST, invSD;    // 1 / row sums (fp32); 1 / kept mass for a filtered row
   float cs;              // log2(e) / T
   int nrej;              // rejections so far at this node (working P = P_nrej)
+  // filtered laws (top-k / top-p): a token of the target (draft) row is kept
+  // iff its logit is above vT (vD), or equal with an index at most iT (iD);
+  // -inf and INT_MAX keep every token
+  float vT, vD;
+  int iT, iD;
   float invZ[kRsMaxM];   // 1 / Z_j of the residuals taken so far (element path)
   double Z[kRsMaxM];     // Z_j in fp64 (accept-test path)
 };
@@ -34,12 +39,23 @@ struct DrawState {
   int node, a, pending, pad;
 };
 
+// The kept prefix of a filtered row (see DecideCtx) and its mass
+// K = sum over kept tokens of exp2((z - m) cs); K = 0: the row is not
+// filtered.
+struct FilterInfo {
+  float v;
+  int idx;
+  double K;
+};
+
 struct RsArgs {
   const void* target;
   const void* draft;
   const int32_t* tokens;
   const int32_t* parent;
   const float* temperature;
+  const int32_t* top_k;  // [B] or NULL
+  const float* top_p;    // [B] or NULL
   uint64_t seed, offset, b_base;
   int32_t* out_tokens;
   int32_t* path;

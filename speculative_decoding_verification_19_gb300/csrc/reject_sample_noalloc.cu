@@ -164,6 +164,8 @@ extern "C" spec_status spec_reject_sample_noalloc(
   a.tokens = tokens;
   a.parent = parent;
   a.temperature = temperature;
+  a.top_k = nullptr;
+  a.top_p = nullptr;
   a.seed = seed;
   a.offset = offset;
   a.b_base = b_base;

@@ -123,14 +123,30 @@ __device__ __forceinline__ void load_vec(const T* row, int64_t e, int V, float (
   }
 }
 
-// Weight of an element of the node's sampling / residual law:
+// Whether element e (logit z) is in a filtered row's kept prefix (v, idx).
+__device__ __forceinline__ bool kept_at(float z, int64_t e, float v, int idx) {
+  return z > v || (z == v && e <= (int64_t)idx);
+}
+// No filter on either row of the law.
+__device__ __forceinline__ void ctx_no_filter(DecideCtx& c) {
+  c.vT = -INFINITY;
+  c.vD = -INFINITY;
+  c.iT = 0x7fffffff;
+  c.iD = 0x7fffffff;
+}
+
+// Weight of element e of the node's sampling / residual law:
 //   nrej == 0:  exp2((z - mT) * cs)                     (unnormalised p)
 //   nrej >= 1:  max(0, P_{nrej-1} - q)                  (unnormalised residual)
-// with P_0 = p and P_j = max(0, P_{j-1} - q) / Z_j.
-__device__ __forceinline__ float weight_of(float zt, float zd, const DecideCtx& c, int nrej) {
-  const float et = fast_exp2((zt - c.mT) * c.cs);
+// with P_0 = p and P_j = max(0, P_{j-1} - q) / Z_j; p and q are zero outside
+// their rows' kept prefixes (filtered laws).
+__device__ __forceinline__ float weight_of(float zt, float zd, int64_t e, const DecideCtx& c,
+                                           int nrej) {
+  float et = fast_exp2((zt - c.mT) * c.cs);
+  if (!kept_at(zt, e, c.vT, c.iT)) et = 0.f;
   if (nrej == 0) return et;
-  const float qv = fast_exp2((zd - c.mD) * c.cs) * c.invSD;
+  float qv = fast_exp2((zd - c.mD) * c.cs) * c.invSD;
+  if (!kept_at(zd, e, c.vD, c.iD)) qv = 0.f;
   float P = et * c.invST;
   for (int j = 1; j < nrej; ++j) P = fmaxf(P - qv, 0.f) * c.invZ[j];
   return fmaxf(P - qv, 0.f);

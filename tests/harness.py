@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 import speculative_decoding_verification_19_gb300 as sv
-from oracle import (oracle_kv_append, oracle_kv_commit, oracle_reject_sample,
+from oracle import (FILTER_NEAR, oracle_kv_append, oracle_kv_commit, oracle_reject_sample,
                     oracle_verify_attn)
 
 ATT_ABS, ATT_REL = 2e-2, 1e-2      # attention outputs (bf16 in, fp32 accumulate)
@@ -34,7 +34,7 @@ def impls_for(wl):
     """Attention kernels that support this shape (CUDA cores, tensor cores)."""
     R = (wl.Hq // wl.Hkv) * wl.M
     out = []
-    if R <= 64:
+    if R <= 128:
         out.append(sv.ATTN_CUDA_CORES)
     if wl.dtype == "bf16" and wl.D == 128 and R <= 128:
         out.append(sv.ATTN_TENSOR_CORES)
@@ -45,7 +45,8 @@ def impls_for(wl):
 # reject sample
 # ---------------------------------------------------------------------------
 
-def gpu_reject(wl, lg, seed, offset, b_base=0, dims=None, ws=None, probe=True):
+def gpu_reject(wl, lg, seed, offset, b_base=0, dims=None, ws=None, probe=True, top_k=None,
+               top_p=None):
     B, M, V = lg["target"].shape
     dt = tdtype(wl)
     dims = dims or dims_for(wl, B, V=V)
@@ -60,8 +61,10 @@ def gpu_reject(wl, lg, seed, offset, b_base=0, dims=None, ws=None, probe=True):
     path = torch.full((B, M), -7, dtype=torch.int32, device="cuda")
     acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     pr = torch.full((B, M, 4), float("nan"), dtype=torch.float32, device="cuda") if probe else None
+    tk = None if top_k is None else to_dev(top_k, torch.int32)
+    tp = None if top_p is None else to_dev(top_p, torch.float32)
     sv.spec_reject_sample(t, d, tok, par, temp, seed, offset, out_tokens, path,
-                          acc, pr, dims, ws, b_base=b_base)
+                          acc, pr, dims, ws, b_base=b_base, top_k=tk, top_p=tp)
     torch.cuda.synchronize()
     res = dict(out_tokens=out_tokens.cpu().numpy(), path=path.cpu().numpy(),
                accepted_len=acc.cpu().numpy(),
@@ -80,10 +83,14 @@ def compare_reject(g, o):
     otherwise the GPU's token must lie in the oracle's band (the tokens a
     draw within 1e-6 of u could select) and carry positive mass.  Returns
     the number of requests with a near-threshold accept test (excluded).
+    A request whose top-p cut lies within FILTER_NEAR (relative) of its
+    target mass is excluded the same way (its kept set is ambiguous).
     """
     bad = o["status"] != 0
     assert np.array_equal(g["accepted_len"][bad], o["accepted_len"][bad])
     acc_clear = (o["acc_margin"] >= NEAR) & ~bad
+    if "flt_margin" in o:
+        acc_clear &= o["flt_margin"] >= FILTER_NEAR
     for key in ("accepted_len", "path"):
         assert np.array_equal(g[key][acc_clear], o[key][acc_clear]), key
     B, M = o["path"].shape

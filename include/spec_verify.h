@@ -77,14 +77,19 @@ typedef enum spec_attn_impl {
 
 /* Reject-sample kernel selection (spec_dims.reject_impl). */
 typedef enum spec_reject_impl {
-  SPEC_REJECT_AUTO = 0,        /* the fused kernel for 16-byte aligned rows, else the
-                                  staged kernels */
-  SPEC_REJECT_STAGED = 1,      /* four kernels: logit statistics, decisions, residual
-                                  masses, residual draws; any alignment, V up to 2^20 */
-  SPEC_REJECT_FUSED = 2        /* one kernel: most SMs stream the logit statistics while
-                                  a few decide each request as soon as its rows are
-                                  done; 16-byte aligned rows (V * element size a
-                                  multiple of 16, aligned row pointers), V up to 2^20;
+  SPEC_REJECT_AUTO = 0,        /* the staged kernels (the faster choice measured on
+                                  GB300 at every shape tried) */
+  SPEC_REJECT_STAGED = 1,      /* logit statistics, then for a chain with 16-byte
+                                  aligned rows and no filter one tail kernel
+                                  (decisions, residual masses and draw, several CTAs
+                                  per request), else three kernels (decisions,
+                                  residual masses, residual draws); any alignment,
+                                  V up to 2^20 */
+  SPEC_REJECT_FUSED = 2        /* one kernel for a chain: every warp streams logit
+                                  statistics and decides each request as soon as its
+                                  rows are done; chains with 16-byte aligned rows
+                                  (V * element size a multiple of 16, aligned row
+                                  pointers), V up to 2^20, no filter;
                                   SPEC_ERR_UNSUPPORTED otherwise */
 } spec_reject_impl;
 

@@ -60,6 +60,7 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
   L.rs_filt_off = take(sizeof(FilterInfo) * (size_t)d.B * 2 * d.M);
+  L.rs_tail_off = take(sizeof(uint32_t) * (size_t)d.B);
   off = rsf_layout(d, off, &L);
   L.total = off;
   return L;

@@ -157,6 +157,7 @@ struct WsLayout {
   size_t rs_draw_off;     // [B] DrawState: residual draws left for pass 3
   size_t rs_zsum_off;     // [B, n_chunks] f64: residual mass of each statistics chunk
   size_t rs_filt_off;     // [B, 2, M] 16-byte kept prefix of each filtered row
+  size_t rs_tail_off;     // [B] u32 slices of the chain tail kernel finished per request
   int rs_chunk;           // logits per statistics chunk
   int rs_chunks;          // statistics chunks per row
   // the one-kernel reject path (laid out by rsf_layout)

@@ -1715,6 +1715,305 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// The tail of a chain in one kernel: decisions, residual masses and the draw
+// ---------------------------------------------------------------------------
+// For a chain with 16-byte aligned rows and unfiltered laws, the three
+// latency-bound kernels after the statistics pass (decide, residual sums,
+// residual draw) are one launch: S CTAs per request ("slices").  Every slice
+// forms the request's row normalisers from the chunk statistics and makes
+// the same accept decisions (a few loads of data still in L2; no slice waits
+// for another).  Slice 0 writes the outputs.  After a rejection at node a,
+// slice s computes the residual's mass over its share of the statistics
+// chunks of a's two rows (one warp per chunk, every load of a chunk in flight
+// at once); the slice that finishes last (a fence and a counter) picks the
+// chunk from the masses and the token inside it.  A bonus draw from p needs
+// no pass over the row: slice 0 picks the chunk from the statistics.
+constexpr int kTailThreads = 256;
+constexpr int kTailWarps = kTailThreads / kWarp;
+constexpr int kTailItems = 4;  // chunk statistics per lane per row in one round of loads
+
+struct TailSmem {
+  float rowM[2][kMaxM];
+  double rowS[2][kMaxM];
+  int rowA[2][kMaxM];
+  int tok[kMaxM];
+  float gzt[kMaxM], gzd[kMaxM];
+  int rej[kMaxM];
+  float pp[kMaxM], qq[kMaxM];
+  int first_rej;
+  int last;
+};
+
+// Row normaliser (m, S, first argmax) of one row by one warp from its chunk
+// statistics: fp32 maximum, fp64 sum of the rescaled chunk sums, as
+// rs_decide_kernel forms them; kTailItems statistics per lane in flight.
+__device__ __forceinline__ void tail_row_norm(const RowStat* st, int n_chunks, int chunk, float cs,
+                                              float* m_out, double* s_out, int* a_out) {
+  const int lane = threadIdx.x % kWarp;
+  float m = -INFINITY;
+  int cfirst = 0x7fffffff, afirst = 0;
+  // pass 1: the maximum and its first chunk
+  for (int c0 = 0; c0 < n_chunks; c0 += kWarp * kTailItems) {
+    RowStat x[kTailItems];
+#pragma unroll
+    for (int j = 0; j < kTailItems; ++j) {
+      const int c = c0 + lane + j * kWarp;
+      x[j] = c < n_chunks ? st[c] : RowStat{-INFINITY, 0.f, 0.0};
+    }
+#pragma unroll
+    for (int j = 0; j < kTailItems; ++j) {
+      const int c = c0 + lane + j * kWarp;
+      if (c < n_chunks && (x[j].m > m || (x[j].m == m && c < cfirst))) {
+        if (x[j].m > m) m = x[j].m;
+        cfirst = c;
+        afirst = unpack_index(x[j].pad);
+      }
+    }
+  }
+  const float mw = warp_max(m);
+  const int cw = __reduce_min_sync(0xffffffffu, m == mw ? cfirst : 0x7fffffff);
+  const unsigned own = __ballot_sync(0xffffffffu, m == mw && cfirst == cw);
+  const int aw = __shfl_sync(0xffffffffu, afirst, own ? __ffs(own) - 1 : 0);
+  // pass 2: the sum (the statistics are in L1 / L2 now)
+  double s = 0.0;
+  for (int c = lane; c < n_chunks; c += kWarp) {
+    const RowStat x = st[c];
+    if (x.m != -INFINITY) s += x.s * (double)fast_exp2((x.m - mw) * cs);
+  }
+  s = warp_sum(s);
+  *m_out = mw;
+  *s_out = s;
+  *a_out = cw < n_chunks ? cw * chunk + aw : 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft, const int32_t* __restrict__ tokens,
+    const float* __restrict__ temperature, uint64_t seed, uint64_t offset, uint64_t b_base,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
+    int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
+    int chunk, const RowStat* __restrict__ stats, double* __restrict__ zsum,
+    uint32_t* __restrict__ done_cnt, uint32_t* __restrict__ status, int S) {
+  __shared__ TailSmem sh;
+  const int b = blockIdx.x / S, s = blockIdx.x % S;
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  const int M = d.M, V = d.V;
+  // the drafted tokens and the temperature do not depend on the statistics
+  int32_t x = 0;
+  if (tid < M) x = tokens[(int64_t)b * M + tid];
+  const float temp = temperature[b];
+  pdl_trigger();
+  pdl_wait();  // the statistics come from the previous kernel
+  int32_t* ot = out_tokens + (int64_t)b * M;
+  int32_t* pt = path + (int64_t)b * M;
+  float* pr = probe != nullptr ? probe + (int64_t)b * M * 4 : nullptr;
+  auto fail = [&](int code) {  // slice 0: the request's outputs say it failed
+    if (s != 0) return;
+    for (int i = tid; i < M; i += kTailThreads) {
+      ot[i] = -1;
+      pt[i] = -1;
+    }
+    if (pr != nullptr)
+      for (int i = tid; i < 4 * M; i += kTailThreads) pr[i] = -1.f;
+    if (tid == 0) {
+      accepted_len[b] = -1;
+      if (code >= 0) raise_status(status, code);
+    }
+  };
+  // a statistics wait that gave up: no decision on what it left unwritten
+  if ((ld_volatile_u32(status) >> SPEC_ERR_TIMEOUT) & 1u) {
+    fail(-1);
+    return;
+  }
+  const bool greedy = temp == 0.f;
+  const float cs = stat_scale(temp);
+  int bad_arg = !temperature_valid(temp);
+  int bad_tok = tid >= 1 && tid < M && (x < 0 || x >= V);
+  if (tid < M) sh.tok[tid] = x;
+  // the accept tests' logits: draft n's token in the rows of node n - 1
+  if (tid >= 1 && tid < M && !bad_tok) {
+    const int64_t o = ((int64_t)b * M + tid - 1) * V + x;
+    sh.gzt[tid] = to_f32(target[o]);
+    sh.gzd[tid] = to_f32(draft[o]);
+  }
+  // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row
+  int bad_row = 0;
+  for (int r = warp; r < 2 * M - 1; r += kTailWarps) {
+    const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
+    float m;
+    double sm;
+    int am;
+    tail_row_norm(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks, n_chunks, chunk, cs, &m,
+                  &sm, &am);
+    if (lane == 0) {
+      sh.rowM[which][n] = m;
+      sh.rowS[which][n] = sm;
+      sh.rowA[which][n] = am;
+    }
+    bad_row |= !(m > -INFINITY && m < INFINITY && sm > 0.0 && sm < INFINITY);
+  }
+  bad_arg = __syncthreads_or(bad_arg);
+  bad_tok = __syncthreads_or(bad_tok);
+  bad_row = __syncthreads_or(bad_row);
+  if (bad_arg || bad_tok || bad_row) {
+    fail(bad_arg ? SPEC_ERR_INVALID_ARG : bad_tok ? SPEC_ERR_DEVICE_BOUNDS : SPEC_ERR_NONFINITE);
+    return;
+  }
+
+  // ---- the accept tests of every draft at once (rs_decide_kernel's chain
+  // arithmetic) and the first rejection
+  const uint64_t bglob = b_base + (uint64_t)b;
+  if (tid == 0) sh.first_rej = M;
+  __syncthreads();
+  if (tid >= 1 && tid < M) {
+    const int p = tid - 1;
+    bool rej;
+    float pp, qq;
+    if (greedy) {
+      rej = x != sh.rowA[0][p];
+      pp = rej ? 0.f : 1.f;
+      qq = x == sh.rowA[1][p] ? 1.f : 0.f;
+    } else {
+      const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
+      const float uacc = (float)u24(r.w[0]);
+      const double cs64 = (double)cs;
+      const double et = ((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64;
+      const double ed = ((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64;
+      const float st_f = (float)sh.rowS[0][p], sd_f = (float)sh.rowS[1][p];
+      bool acc;
+      if (ed == -INFINITY) {
+        acc = et != -INFINITY;
+      } else if (et == -INFINITY) {
+        acc = false;
+      } else {
+        const double e = et - ed;
+        const double ei = rint(e);
+        const float ratio =
+            ldexpf(fast_exp2((float)(e - ei)), (int)fmax(fmin(ei, 300.0), -300.0)) * (sd_f / st_f);
+        acc = uacc < ratio;
+      }
+      rej = !acc;
+      pp = exp2f((float)et) / st_f;
+      qq = exp2f((float)ed) / sd_f;
+    }
+    sh.pp[tid] = pp;
+    sh.qq[tid] = qq;
+    if (rej) atomicMin(&sh.first_rej, tid);
+  }
+  __syncthreads();
+  const int fr = sh.first_rej;            // first rejected draft, M if none
+  const int a = fr < M ? fr - 1 : M - 1;  // accepted drafts = the node that draws
+  if (s == 0) {
+    for (int n = tid; n < M; n += kTailThreads) {
+      pt[n] = n <= a ? n : -1;
+      if (n < a) ot[n] = sh.tok[n + 1];
+      else if (n > a) ot[n] = -1;
+      if (pr != nullptr) {
+        const bool tested = n >= 1 && n <= fr && n < M;
+        pr[n * 4 + 0] = tested ? sh.pp[n] : -1.f;
+        pr[n * 4 + 1] = tested ? sh.qq[n] : -1.f;
+        pr[n * 4 + 2] = -1.f;
+        pr[n * 4 + 3] = -1.f;
+      }
+    }
+    if (tid == 0) accepted_len[b] = a;
+  }
+  if (greedy) {
+    if (s == 0 && tid == 0) {
+      ot[a] = sh.rowA[0][a];
+      if (pr != nullptr) {
+        pr[a * 4 + 2] = 1.f;
+        pr[a * 4 + 3] = 1.f;
+      }
+    }
+    return;
+  }
+  const Philox4 r = philox4x64_10((uint64_t)a + 1, bglob, offset, 0, seed, 0);
+  const double u = (double)u24(r.w[1]);
+  DecideCtx c;
+  ctx_no_filter(c);
+  c.mT = sh.rowM[0][a];
+  c.invST = (float)(1.0 / sh.rowS[0][a]);
+  c.cs = cs;
+  const T* trow = target + ((int64_t)b * M + a) * V;
+  if (fr == M) {
+    // every draft accepted: the bonus token from p of node a
+    if (s != 0 || warp != 0) return;
+    c.mD = 0.f;
+    c.invSD = 0.f;
+    c.nrej = 0;
+    float w;
+    double z;
+    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
+    const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &w, &z);
+    if (lane == 0) {
+      ot[a] = tk;
+      if (pr != nullptr) {
+        pr[a * 4 + 2] = 1.0f;
+        pr[a * 4 + 3] = (float)((double)w / z);
+      }
+    }
+    return;
+  }
+  // a rejection: the residual max(0, p_a - q_a), this slice's chunks
+  c.mD = sh.rowM[1][a];
+  c.invSD = (float)(1.0 / sh.rowS[1][a]);
+  c.nrej = 1;
+  const T* drow = draft + ((int64_t)b * M + a) * V;
+  double* zs = zsum + (int64_t)b * n_chunks;
+  const int c0 = (int)((int64_t)n_chunks * s / S), c1 = (int)((int64_t)n_chunks * (s + 1) / S);
+  for (int cc = c0 + warp; cc < c1; cc += kTailWarps) {
+    uint4 raw_t[kStatVecs], raw_d[kStatVecs];
+    const float ls = lane_weights<T>(trow, drow, (int64_t)cc * chunk, V, c, 1, raw_t, raw_d);
+    const dfloat tot = df_warp_sum(df_make(ls));
+    if (lane == 0) {
+      zs[cc] = df_to_d(tot);
+      __threadfence();  // the mass before this slice's count
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    sh.last = atomicAdd(done_cnt + b, 1u) == (uint32_t)(S - 1);
+  }
+  __syncthreads();
+  if (!sh.last || warp != 0) return;
+  // the last slice: the chunk from the masses, then the token
+  __threadfence();
+  double Z = 0.0;
+  for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
+  Z = warp_sum(Z);
+  float w;
+  int tk;
+  double zrep;
+  if (Z > 0.0) {
+    double pre;
+    const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
+    const double trel = u * Z - pre;
+    const float th = (float)trel;
+    tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, c, 1,
+                            dfloat{th, (float)(trel - (double)th)}, &w);
+    zrep = Z;
+  } else {
+    // a residual of zero mass: the draw from p of the node
+    c.nrej = 0;
+    double z;
+    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
+    tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &w, &z);
+    zrep = z;
+    Z = 1.0;
+  }
+  if (lane == 0) {
+    ot[a] = tk;
+    if (pr != nullptr) {
+      pr[a * 4 + 2] = (float)Z;
+      pr[a * 4 + 3] = (float)((double)w / zrep);
+    }
+    done_cnt[b] = 0u;  // ready for the next call
+  }
+}
+
+// ---------------------------------------------------------------------------
 // One kernel for a chain: statistics, decisions and draws, all warps alike.
 //
 // Every warp streams statistics chunks through a private ring of 4 KB
@@ -2543,6 +2842,22 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
                                              a.parent, a.temperature, d, lay.rs_chunks, stats);
     if (e != cudaSuccess) return e;
   }
+  // a chain of aligned, unfiltered rows: the whole tail in one launch
+  if (kAligned && a.parent == nullptr && a.top_k == nullptr && a.top_p == nullptr) {
+    const int want_s = (lay.rs_chunks + 7) / 8;  // about eight chunks of the residual per slice
+    const int cap_s = (4 * sms + d.B - 1) / d.B;
+    int S = want_s < cap_s ? want_s : cap_s;
+    if (S > 16) S = 16;
+    if (S < 1) S = 1;
+    PdlLaunch L(dim3((unsigned)((int64_t)d.B * S)), dim3(kTailThreads), 0, st);
+    const cudaError_t e = cudaLaunchKernelEx(
+        &L.cfg, rs_chain_tail_kernel<T>, tgt, dft, a.tokens, a.temperature, a.seed, a.offset,
+        a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk,
+        (const RowStat*)stats, zsum, reinterpret_cast<uint32_t*>(ws + lay.rs_tail_off), status, S);
+    if (e != cudaSuccess) return e;
+    *launches += 2;
+    return cudaGetLastError();
+  }
   // passes 2 and 3 start while their predecessor drains (programmatic
   // dependent launch); each waits for its predecessor's results in-kernel
   cudaLaunchAttribute attr;
@@ -2650,7 +2965,7 @@ cudaError_t rs_launch(const RsArgs& a, const WsLayout& lay, cudaStream_t st, int
   // the one-kernel path takes neither trees nor filters
   const bool fused_ok = rso_supported(a.d, aligned, a.parent == nullptr) &&
                         a.top_k == nullptr && a.top_p == nullptr;
-  if (a.d.reject_impl == SPEC_REJECT_FUSED || (a.d.reject_impl == SPEC_REJECT_AUTO && fused_ok)) {
+  if (a.d.reject_impl == SPEC_REJECT_FUSED) {
     if (!fused_ok) return cudaErrorNotSupported;
     return a.d.logits_dtype == SPEC_BF16 ? launch_fused_t<__nv_bfloat16>(a, lay, st, launches)
                                          : launch_fused_t<float>(a, lay, st, launches);

@@ -118,20 +118,21 @@ extern "C" spec_status spec_reject_sample_noalloc(
   if (!target_logits || !draft_logits || !tokens || !temperature || !out_tokens || !path ||
       !accepted_len)
     return SPEC_ERR_INVALID_ARG;
-  // The call runs the kernels spec_reject_sample would run on these inputs:
-  // the fused kernel when the shape allows it, else the staged ones.  Each
-  // has its own scratch layout, which must fit the fixed array.
+  // The call runs the kernels spec_reject_sample would run on these inputs
+  // and dims->reject_impl: the one-kernel path when asked for (and the
+  // shape allows it), else the staged ones.  Each has its own scratch
+  // layout, which must fit the fixed array.
   const int esz = dims->logits_dtype == SPEC_BF16 ? 2 : 4;
   const bool aligned = ((size_t)dims->V * esz) % 16 == 0 &&
                        (reinterpret_cast<uintptr_t>(target_logits) % 16) == 0 &&
                        (reinterpret_cast<uintptr_t>(draft_logits) % 16) == 0;
-  const bool fused = dims->reject_impl != SPEC_REJECT_STAGED &&
+  const bool fused = dims->reject_impl == SPEC_REJECT_FUSED &&
                      rso_supported(*dims, aligned, parent == nullptr);
   if (dims->reject_impl == SPEC_REJECT_FUSED && !fused) return SPEC_ERR_UNSUPPORTED;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   // status, the chunk statistics, the draw states, the residual chunk
-  // masses; for the one-kernel path also its control words, row
-  // normalisers and counters
+  // masses, the chain tail's counters; for the one-kernel path also its
+  // control words, row normalisers and counters
   WsLayout lay;
   memset(&lay, 0, sizeof(lay));
   lay.status_off = 0;
@@ -141,7 +142,8 @@ extern "C" spec_status spec_reject_sample_noalloc(
   lay.rs_bytes = sizeof(RowStat) * (size_t)dims->B * 2 * dims->M * lay.rs_chunks;
   lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
   lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
-  lay.total = lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks;
+  lay.rs_tail_off = up(lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks);
+  lay.total = lay.rs_tail_off + sizeof(uint32_t) * (size_t)dims->B;
   if (fused) lay.total = rsf_layout(*dims, up(lay.total), &lay);
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
@@ -154,6 +156,9 @@ extern "C" spec_status spec_reject_sample_noalloc(
   // read is written earlier in the same call.
   char* sb = static_cast<char*>(scratch);
   if (cudaMemsetAsync(sb, 0, kNoAllocStatusBytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(sb + lay.rs_tail_off, 0, sizeof(uint32_t) * (size_t)dims->B, st) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
   if (fused && cudaMemsetAsync(sb + lay.rsf_ctl_off, 0, lay.total - lay.rsf_ctl_off, st) !=
                    cudaSuccess)
     return SPEC_ERR_CUDA;

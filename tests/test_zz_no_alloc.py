@@ -70,8 +70,8 @@ def test_same_inputs_twice():
 
 def test_refuses_sizes_beyond_its_scratch():
     # 16384 requests x 5 rows of a 16-logit vocabulary: the kernels these
-    # sizes run on (the staged ones: the rows are too short for the fused
-    # kernel) need 16 MB of scratch, far beyond the 1 MiB array.  The
+    # sizes run on (the staged ones) need 16 MB of scratch, far beyond the
+    # 1 MiB array.  The
     # buffers have the full sizes, so nothing could be read out of bounds
     # even if the call went ahead.
     B, M, V = 16384, 5, 16

@@ -1792,18 +1792,16 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     const float* __restrict__ temperature, uint64_t seed, uint64_t offset, uint64_t b_base,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* __restrict__ stats, double* __restrict__ zsum,
-    uint32_t* __restrict__ done_cnt, uint32_t* __restrict__ status, int S) {
+    int chunk, const RowStat* stats, double* zsum, uint32_t* done_cnt, uint32_t* status, int S) {
   __shared__ TailSmem sh;
   const int b = blockIdx.x / S, s = blockIdx.x % S;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int M = d.M, V = d.V;
-  // the drafted tokens and the temperature do not depend on the statistics
+  pdl_trigger();
+  pdl_wait();  // the statistics (and any input) come from earlier kernels
   int32_t x = 0;
   if (tid < M) x = tokens[(int64_t)b * M + tid];
   const float temp = temperature[b];
-  pdl_trigger();
-  pdl_wait();  // the statistics come from the previous kernel
   int32_t* ot = out_tokens + (int64_t)b * M;
   int32_t* pt = path + (int64_t)b * M;
   float* pr = probe != nullptr ? probe + (int64_t)b * M * 4 : nullptr;

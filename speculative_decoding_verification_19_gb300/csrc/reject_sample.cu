@@ -843,7 +843,7 @@ __device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int 
   if (threadIdx.x < kWarp) {
     const int lane = threadIdx.x;
     double Z = 0.0;
-    for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(st[k], c.mT, c.cs);
+    for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(ld_stat_cg(st + k), c.mT, c.cs);
     Z = warp_sum(Z);
     const double t = u * Z;
     double base = 0.0;
@@ -851,7 +851,7 @@ __device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int 
     double sel_pre = 0.0;
     for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
       const int k = k0 + lane;
-      const double wk = k < n_chunks ? chunk_mass(st[k], c.mT, c.cs) : 0.0;
+      const double wk = k < n_chunks ? chunk_mass(ld_stat_cg(st + k), c.mT, c.cs) : 0.0;
       double incl = wk;
 #pragma unroll
       for (int o = 1; o < kWarp; o <<= 1) {
@@ -872,7 +872,7 @@ __device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int 
     if (sel < 0) {  // rounding at the very top: the last chunk with mass
       sel = lastpos < 0 ? 0 : lastpos;
       double pre = 0.0;
-      for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(st[k], c.mT, c.cs);
+      for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(ld_stat_cg(st + k), c.mT, c.cs);
       sel_pre = warp_sum(pre);
     }
     if (lane == 0) {
@@ -1037,7 +1037,7 @@ __device__ int warp_draw_from_p(const T* trow, const RowStat* st, int n_chunks, 
                                 const DecideCtx& c, double u, float* w, double* zsum) {
   const int lane = threadIdx.x % kWarp;
   double Z = 0.0;
-  for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(st[k], c.mT, c.cs);
+  for (int k = lane; k < n_chunks; k += kWarp) Z += chunk_mass(ld_stat_cg(st + k), c.mT, c.cs);
   Z = warp_sum(Z);
   const double t = u * Z;
   double base = 0.0;
@@ -1045,7 +1045,7 @@ __device__ int warp_draw_from_p(const T* trow, const RowStat* st, int n_chunks, 
   double sel_pre = 0.0;
   for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
     const int k = k0 + lane;
-    const double wk = k < n_chunks ? chunk_mass(st[k], c.mT, c.cs) : 0.0;
+    const double wk = k < n_chunks ? chunk_mass(ld_stat_cg(st + k), c.mT, c.cs) : 0.0;
     double incl = wk;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
@@ -1066,7 +1066,7 @@ __device__ int warp_draw_from_p(const T* trow, const RowStat* st, int n_chunks, 
   if (sel < 0) {  // rounding at the very top: the last chunk with mass
     sel = lastpos < 0 ? 0 : lastpos;
     double pre = 0.0;
-    for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(st[k], c.mT, c.cs);
+    for (int k = lane; k < sel; k += kWarp) pre += chunk_mass(ld_stat_cg(st + k), c.mT, c.cs);
     sel_pre = warp_sum(pre);
   }
   *zsum = Z;
@@ -1758,7 +1758,7 @@ __device__ __forceinline__ void tail_row_norm(const RowStat* st, int n_chunks, i
 #pragma unroll
     for (int j = 0; j < kTailItems; ++j) {
       const int c = c0 + lane + j * kWarp;
-      x[j] = c < n_chunks ? st[c] : RowStat{-INFINITY, 0.f, 0.0};
+      x[j] = c < n_chunks ? ld_stat_cg(st + c) : RowStat{-INFINITY, 0.f, 0.0};
     }
 #pragma unroll
     for (int j = 0; j < kTailItems; ++j) {
@@ -1777,7 +1777,7 @@ __device__ __forceinline__ void tail_row_norm(const RowStat* st, int n_chunks, i
   // pass 2: the sum (the statistics are in L1 / L2 now)
   double s = 0.0;
   for (int c = lane; c < n_chunks; c += kWarp) {
-    const RowStat x = st[c];
+    const RowStat x = ld_stat_cg(st + c);
     if (x.m != -INFINITY) s += x.s * (double)fast_exp2((x.m - mw) * cs);
   }
   s = warp_sum(s);

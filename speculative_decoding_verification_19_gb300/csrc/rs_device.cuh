@@ -106,6 +106,19 @@ __device__ __forceinline__ int chunk_argmax(const uint4 (&raw)[kStatVecs], int n
   }
   return __reduce_min_sync(0xffffffffu, best);
 }
+// A chunk statistic written by an earlier kernel of the chain (or another
+// SM), read through L2 by a load the compiler keeps after the dependency
+// wait (volatile asm, memory clobber).
+__device__ __forceinline__ RowStat ld_stat_cg(const RowStat* p) {
+  unsigned long long lo, hi;
+  asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "l"(p) : "memory");
+  RowStat r;
+  r.m = __uint_as_float((uint32_t)lo);
+  r.pad = __uint_as_float((uint32_t)(lo >> 32));
+  r.s = __longlong_as_double((long long)hi);
+  return r;
+}
+
 // The chunk statistics keep the argmax index in RowStat's spare word.
 __device__ __forceinline__ float pack_index(int i) { return __int_as_float(i); }
 __device__ __forceinline__ int unpack_index(float f) { return __float_as_int(f); }

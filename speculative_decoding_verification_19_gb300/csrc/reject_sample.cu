@@ -1730,7 +1730,6 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 // no pass over the row: slice 0 picks the chunk from the statistics.
 constexpr int kTailThreads = 256;
 constexpr int kTailWarps = kTailThreads / kWarp;
-constexpr int kTailItems = 4;  // chunk statistics per lane per row in one round of loads
 
 struct TailSmem {
   float rowM[2][kMaxM];
@@ -1745,45 +1744,46 @@ struct TailSmem {
 };
 
 // Row normaliser (m, S, first argmax) of one row by one warp from its chunk
-// statistics: fp32 maximum, fp64 sum of the rescaled chunk sums, as
-// rs_decide_kernel forms them; kTailItems statistics per lane in flight.
+// statistics, formed as rs_decide_kernel forms it: fp32 maximum, fp64 sum of
+// the rescaled chunk sums, the first chunk holding the maximum; every load
+// of the row in flight at once (n_chunks <= 512).
 __device__ __forceinline__ void tail_row_norm(const RowStat* st, int n_chunks, int chunk, float cs,
                                               float* m_out, double* s_out, int* a_out) {
   const int lane = threadIdx.x % kWarp;
+  constexpr int kItems = 16;
+  float im[kItems];
+  double is[kItems];
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    const int c = lane + j * kWarp;
+    if (c < n_chunks) {
+      const RowStat x = ld_stat_cg(st + c);
+      im[j] = x.m;
+      is[j] = x.s;
+    } else {
+      im[j] = -INFINITY;
+      is[j] = 0.0;
+    }
+  }
   float m = -INFINITY;
-  int cfirst = 0x7fffffff, afirst = 0;
-  // pass 1: the maximum and its first chunk
-  for (int c0 = 0; c0 < n_chunks; c0 += kWarp * kTailItems) {
-    RowStat x[kTailItems];
 #pragma unroll
-    for (int j = 0; j < kTailItems; ++j) {
-      const int c = c0 + lane + j * kWarp;
-      x[j] = c < n_chunks ? ld_stat_cg(st + c) : RowStat{-INFINITY, 0.f, 0.0};
-    }
-#pragma unroll
-    for (int j = 0; j < kTailItems; ++j) {
-      const int c = c0 + lane + j * kWarp;
-      if (c < n_chunks && (x[j].m > m || (x[j].m == m && c < cfirst))) {
-        if (x[j].m > m) m = x[j].m;
-        cfirst = c;
-        afirst = unpack_index(x[j].pad);
-      }
-    }
-  }
-  const float mw = warp_max(m);
-  const int cw = __reduce_min_sync(0xffffffffu, m == mw ? cfirst : 0x7fffffff);
-  const unsigned own = __ballot_sync(0xffffffffu, m == mw && cfirst == cw);
-  const int aw = __shfl_sync(0xffffffffu, afirst, own ? __ffs(own) - 1 : 0);
-  // pass 2: the sum (the statistics are in L1 / L2 now)
+  for (int j = 0; j < kItems; ++j) m = fmaxf(m, im[j]);
+  m = warp_max(m);
   double s = 0.0;
-  for (int c = lane; c < n_chunks; c += kWarp) {
-    const RowStat x = ld_stat_cg(st + c);
-    if (x.m != -INFINITY) s += x.s * (double)fast_exp2((x.m - mw) * cs);
-  }
+#pragma unroll
+  for (int j = 0; j < kItems; ++j)
+    if (im[j] != -INFINITY) s += is[j] * (double)fast_exp2((im[j] - m) * cs);
   s = warp_sum(s);
-  *m_out = mw;
+  int c_first = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    const int c = lane + j * kWarp;
+    if (c < n_chunks && im[j] == m && c < c_first) c_first = c;
+  }
+  c_first = __reduce_min_sync(0xffffffffu, c_first);
+  *m_out = m;
   *s_out = s;
-  *a_out = cw < n_chunks ? cw * chunk + aw : 0;
+  *a_out = c_first < n_chunks ? c_first * chunk + unpack_index(ld_stat_cg(st + c_first).pad) : 0;
 }
 
 template <typename T>

@@ -1737,10 +1737,10 @@ struct TailSmem {
   int rowA[2][kMaxM];
   int tok[kMaxM];
   float gzt[kMaxM], gzd[kMaxM];
-  int rej[kMaxM];
   float pp[kMaxM], qq[kMaxM];
   int first_rej;
   int last;
+  int bad;  // bit 0: argument, bit 1: token, bit 2: row without a distribution
 };
 
 // Row normaliser (m, S, first argmax) of one row by one warp from its chunk
@@ -1825,17 +1825,18 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   }
   const bool greedy = temp == 0.f;
   const float cs = stat_scale(temp);
-  int bad_arg = !temperature_valid(temp);
-  int bad_tok = tid >= 1 && tid < M && (x < 0 || x >= V);
+  if (tid == 0) sh.bad = temperature_valid(temp) ? 0 : 1;
+  const bool tok_bad = tid >= 1 && tid < M && (x < 0 || x >= V);
   if (tid < M) sh.tok[tid] = x;
+  __syncthreads();
+  if (tok_bad) atomicOr(&sh.bad, 2);
   // the accept tests' logits: draft n's token in the rows of node n - 1
-  if (tid >= 1 && tid < M && !bad_tok) {
+  if (tid >= 1 && tid < M && !tok_bad) {
     const int64_t o = ((int64_t)b * M + tid - 1) * V + x;
     sh.gzt[tid] = to_f32(target[o]);
     sh.gzd[tid] = to_f32(draft[o]);
   }
   // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row
-  int bad_row = 0;
   for (int r = warp; r < 2 * M - 1; r += kTailWarps) {
     const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
     float m;
@@ -1847,14 +1848,13 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       sh.rowM[which][n] = m;
       sh.rowS[which][n] = sm;
       sh.rowA[which][n] = am;
+      if (!(isfinite(m) && sm > 0.0 && isfinite(sm))) atomicOr(&sh.bad, 4);
     }
-    bad_row |= !(m > -INFINITY && m < INFINITY && sm > 0.0 && sm < INFINITY);
   }
-  bad_arg = __syncthreads_or(bad_arg);
-  bad_tok = __syncthreads_or(bad_tok);
-  bad_row = __syncthreads_or(bad_row);
-  if (bad_arg || bad_tok || bad_row) {
-    fail(bad_arg ? SPEC_ERR_INVALID_ARG : bad_tok ? SPEC_ERR_DEVICE_BOUNDS : SPEC_ERR_NONFINITE);
+  __syncthreads();
+  const int bad = sh.bad;
+  if (bad != 0) {
+    fail((bad & 1) ? SPEC_ERR_INVALID_ARG : (bad & 2) ? SPEC_ERR_DEVICE_BOUNDS : SPEC_ERR_NONFINITE);
     return;
   }
 

@@ -989,9 +989,10 @@ __device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
 }
 
 // Picks the chunk holding t from per-chunk masses zs[0..n) (fp64, read
-// through L2), by one warp: the smallest k with a positive mass and an
-// inclusive prefix above t, else the last chunk of positive mass.  Returns
-// the chunk; *pre = the masses before it.
+// through L2, or from shared memory with kShared), by one warp: the smallest
+// k with a positive mass and an inclusive prefix above t, else the last
+// chunk of positive mass.  Returns the chunk; *pre = the masses before it.
+template <bool kShared = false>
 __device__ __forceinline__ int warp_select_chunk(const double* zs, int n, double t, double* pre) {
   const int lane = threadIdx.x % kWarp;
   double base = 0.0;
@@ -999,7 +1000,7 @@ __device__ __forceinline__ int warp_select_chunk(const double* zs, int n, double
   double sel_pre = 0.0, last_pre = 0.0;
   for (int k0 = 0; k0 < n && sel < 0; k0 += kWarp) {
     const int k = k0 + lane;
-    const double wk = k < n ? __ldcg(zs + k) : 0.0;
+    const double wk = k < n ? (kShared ? zs[k] : __ldcg(zs + k)) : 0.0;
     double incl = wk;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
@@ -1731,7 +1732,15 @@ __global__ void __launch_bounds__(kResThreads) rs_residual_draw_kernel(
 constexpr int kTailThreads = 256;
 constexpr int kTailWarps = kTailThreads / kWarp;
 
+constexpr int kTailStage = 2048;  // chunk statistics of one request held in shared memory
+
 struct TailSmem {
+  // the request's chunk statistics (row-major), when they fit: maximum,
+  // sum, argmax word
+  float st_m[kTailStage];
+  float st_s[kTailStage];
+  int st_a[kTailStage];
+  double zs[kTailStage / 4];  // the last slice: the residual's chunk masses
   float rowM[2][kMaxM];
   double rowS[2][kMaxM];
   int rowA[2][kMaxM];
@@ -1836,14 +1845,46 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     sh.gzt[tid] = to_f32(target[o]);
     sh.gzd[tid] = to_f32(draft[o]);
   }
-  // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row
-  for (int r = warp; r < 2 * M - 1; r += kTailWarps) {
+  // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row;
+  // the statistics come in one round of loads through shared memory when
+  // they fit
+  const int rows = 2 * M - 1;
+  const bool staged = rows * n_chunks <= kTailStage;
+  if (staged) {
+    for (int i = tid; i < rows * n_chunks; i += kTailThreads) {
+      const int r = i / n_chunks, c = i - r * n_chunks;
+      const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
+      const RowStat x = ld_stat_cg(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks + c);
+      sh.st_m[i] = x.m;
+      sh.st_s[i] = (float)x.s;  // a chunk sum is an fp32 value
+      sh.st_a[i] = unpack_index(x.pad);
+    }
+    __syncthreads();
+  }
+  for (int r = warp; r < rows; r += kTailWarps) {
     const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
     float m;
     double sm;
     int am;
-    tail_row_norm(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks, n_chunks, chunk, cs, &m,
-                  &sm, &am);
+    if (staged) {
+      const float* rm = sh.st_m + r * n_chunks;
+      float mx = -INFINITY;
+      for (int c = lane; c < n_chunks; c += kWarp) mx = fmaxf(mx, rm[c]);
+      m = warp_max(mx);
+      double acc = 0.0;
+      int cf = 0x7fffffff;
+      for (int c = lane; c < n_chunks; c += kWarp) {
+        if (rm[c] != -INFINITY)
+          acc += (double)sh.st_s[r * n_chunks + c] * (double)fast_exp2((rm[c] - m) * cs);
+        if (rm[c] == m && c < cf) cf = c;
+      }
+      sm = warp_sum(acc);
+      cf = __reduce_min_sync(0xffffffffu, cf);
+      am = cf < n_chunks ? cf * chunk + sh.st_a[r * n_chunks + cf] : 0;
+    } else {
+      tail_row_norm(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks, n_chunks, chunk, cs,
+                    &m, &sm, &am);
+    }
     if (lane == 0) {
       sh.rowM[which][n] = m;
       sh.rowS[which][n] = sm;
@@ -1975,18 +2016,26 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     sh.last = atomicAdd(done_cnt + b, 1u) == (uint32_t)(S - 1);
   }
   __syncthreads();
-  if (!sh.last || warp != 0) return;
-  // the last slice: the chunk from the masses, then the token
+  if (!sh.last) return;
+  // the last slice: the chunk from the masses (all loaded at once into
+  // shared memory when they fit), then the token
   __threadfence();
+  const bool zsh = n_chunks <= kTailStage / 4;
+  if (zsh) {
+    for (int k = tid; k < n_chunks; k += kTailThreads) sh.zs[k] = __ldcg(zs + k);
+    __syncthreads();
+  }
+  if (warp != 0) return;
   double Z = 0.0;
-  for (int k = lane; k < n_chunks; k += kWarp) Z += __ldcg(zs + k);
+  for (int k = lane; k < n_chunks; k += kWarp) Z += zsh ? sh.zs[k] : __ldcg(zs + k);
   Z = warp_sum(Z);
   float w;
   int tk;
   double zrep;
   if (Z > 0.0) {
     double pre;
-    const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
+    const int sel = zsh ? warp_select_chunk<true>(sh.zs, n_chunks, u * Z, &pre)
+                        : warp_select_chunk(zs, n_chunks, u * Z, &pre);
     const double trel = u * Z - pre;
     const float th = (float)trel;
     tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, c, 1,
@@ -2842,8 +2891,10 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
   }
   // a chain of aligned, unfiltered rows: the whole tail in one launch
   if (kAligned && a.parent == nullptr && a.top_k == nullptr && a.top_p == nullptr) {
-    const int want_s = (lay.rs_chunks + 7) / 8;  // about eight chunks of the residual per slice
-    const int cap_s = (4 * sms + d.B - 1) / d.B;
+    // about eight chunks of the residual per slice (one per warp), and no
+    // more CTAs than fit on the GPU at once (two per SM)
+    const int want_s = (lay.rs_chunks + 7) / 8;
+    const int cap_s = (2 * sms) / d.B > 1 ? (2 * sms) / d.B : 1;
     int S = want_s < cap_s ? want_s : cap_s;
     if (S > 16) S = 16;
     if (S < 1) S = 1;

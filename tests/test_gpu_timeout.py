@@ -32,6 +32,14 @@ TIMEOUT_BIT = 1 << 7
 TINY = 1  # thousand SM clocks
 
 
+def _flush_l2():
+    """Evict the inputs from L2 (a write larger than it), so that the first
+    bulk copies come from HBM and outlast the thousand-clock limit."""
+    buf = torch.empty(96 << 20, dtype=torch.float32, device="cuda")
+    buf.fill_(1.0)
+    torch.cuda.synchronize()
+
+
 def test_attention_wait_gives_up_then_recovers():
     # one 40k-token request: each (request, KV head) pair is split over
     # about twenty CTAs, so the CTA holding a pair's first tile waits for the
@@ -62,6 +70,7 @@ def test_reject_wait_gives_up_then_recovers(impl):
     dims.reject_impl = impl
     dims.wait_limit_kcycles = TINY
     ws = sv.workspace(dims)
+    _flush_l2()
     g = gpu_reject(wl, lg, seed=5, offset=0, dims=dims, ws=ws)
     assert g["status"] & TIMEOUT_BIT
     # no request is decided on lost statistics: both paths fail every
@@ -91,6 +100,7 @@ def test_noalloc_wait_gives_up_then_recovers():
     out = torch.full((B, M), -7, dtype=torch.int32, device="cuda")
     path = torch.full((B, M), -7, dtype=torch.int32, device="cuda")
     acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    _flush_l2()
     sv.spec_reject_sample_noalloc(*args, out, path, acc, None, dims)
     torch.cuda.synchronize()
     a = acc.cpu().numpy()

@@ -1478,7 +1478,21 @@ __device__ void decide_request(
         // back to the node's law before the draw is posted
         const int nrej_next = sh.ctx.nrej + 1;
         double acc = 0.0;
-        for (int64_t e = (int64_t)tid * EPV; e < V; e += kSweep) {
+        // eight sweeps' loads in flight at a time (a row of 32k bf16 logits
+        // is eight sweeps: one round trip instead of eight)
+        int64_t e = (int64_t)tid * EPV;
+        for (; e + 7 * (int64_t)kSweep < V; e += 8 * (int64_t)kSweep) {
+          float part[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float w[EPV];
+            part[k] = vec_weights<T, kAligned>(trow, drow, e + k * (int64_t)kSweep, V, sh.ctx,
+                                               nrej_next, w);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc += (double)part[k];  // as the loop below sums
+        }
+        for (; e < V; e += kSweep) {
           float w[EPV];
           acc += (double)vec_weights<T, kAligned>(trow, drow, e, V, sh.ctx, nrej_next, w);  // lim = V
         }

@@ -1865,13 +1865,27 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   const int rows = 2 * M - 1;
   const bool staged = rows * n_chunks <= kTailStage;
   if (staged) {
-    for (int i = tid; i < rows * n_chunks; i += kTailThreads) {
-      const int r = i / n_chunks, c = i - r * n_chunks;
-      const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
-      const RowStat x = ld_stat_cg(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks + c);
-      sh.st_m[i] = x.m;
-      sh.st_s[i] = (float)x.s;  // a chunk sum is an fp32 value
-      sh.st_a[i] = unpack_index(x.pad);
+    // the statistics of rows 0..M-1 (target) and M..2M-2 (draft rows
+    // 0..M-2) are contiguous per row kind: two runs of items, all loads of a
+    // thread issued before any is stored
+    const RowStat* tgt_st = stats + ((int64_t)b * 2 + 0) * M * n_chunks;
+    const RowStat* dft_st = stats + ((int64_t)b * 2 + 1) * M * n_chunks;
+    const int nt = M * n_chunks, items = rows * n_chunks;
+    constexpr int kPer = kTailStage / kTailThreads;  // 8
+    RowStat x[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = k * kTailThreads + tid;
+      if (i < items) x[k] = ld_stat_cg(i < nt ? tgt_st + i : dft_st + (i - nt));
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = k * kTailThreads + tid;
+      if (i < items) {
+        sh.st_m[i] = x[k].m;
+        sh.st_s[i] = (float)x[k].s;  // a chunk sum is an fp32 value
+        sh.st_a[i] = unpack_index(x[k].pad);
+      }
     }
     __syncthreads();
   }

@@ -333,7 +333,7 @@ def verify_statistics(wl, acc, st, parent):
     path = st.path.cpu().numpy()  # the last step's path (for the tree figure)
     for k in range(K):
         sst = step_stats(acc[k], path=path if k == K - 1 else None,
-                         parent=parent if k == K - 1 else None)
+                         parent=parent if k == K - 1 else None, M=wl.M)
         pos += np.asarray(sst["rejection_pos"][:wl.M + 1])
         if k == K - 1 and parent is not None:
             twe.append(sst["tree_width_effective"])

@@ -121,11 +121,12 @@ class Controller:
                 for f, _ in CtrlMetrics._fields_}
 
 
-def step_stats(accepted_len, path=None, parent=None) -> dict:
+def step_stats(accepted_len, path=None, parent=None, M=None) -> dict:
+    """spec_step_stats over host copies of one step's outputs; M (the rows
+    per request) comes from path or parent when given."""
     L = _setup()
     a, ap = _i32(accepted_len)
     B = a.shape[0]
-    M = None
     pp = qp = None
     if path is not None:
         p, pp = _i32(path)

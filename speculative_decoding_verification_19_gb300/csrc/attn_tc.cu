@@ -168,10 +168,28 @@ __device__ __forceinline__ unsigned long long mask_window(unsigned long long lo,
 // Keys of a tile visible to a row, bit j for tile column j: below the
 // tile's valid keys and the request's length L, and either in the cached
 // prefix (position < ctx) or a new position that is an ancestor-or-self of
-// the row's node (bit pos - ctx of the 128-bit mask anc_lo, anc_hi).
+// the row's node (bit pos - ctx of anc: up to 64 new rows).
 __device__ __forceinline__ unsigned long long tile_visibility(int kpos0, int nkeys, int ctx, int L,
-                                                              unsigned long long anc_lo,
-                                                              unsigned long long anc_hi, bool real) {
+                                                              unsigned long long anc, bool real) {
+  if (!real) return 0ull;
+  const int lim = min(L - kpos0, nkeys);  // nkeys is 16..64
+  unsigned long long v = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1));
+  const int c0 = ctx - kpos0;  // tile columns in the cached prefix
+  unsigned long long vm;
+  if (c0 >= 64)
+    vm = ~0ull;
+  else if (c0 > 0)
+    vm = ((1ull << c0) - 1) | (anc << c0);
+  else
+    vm = -c0 >= 64 ? 0ull : (anc >> -c0);
+  return v & vm;
+}
+
+// The same for up to 128 new rows: the 128-bit mask (anc_lo, anc_hi).
+__device__ __forceinline__ unsigned long long tile_visibility_wide(int kpos0, int nkeys, int ctx,
+                                                                   int L, unsigned long long anc_lo,
+                                                                   unsigned long long anc_hi,
+                                                                   bool real) {
   if (!real) return 0ull;
   const int lim = min(L - kpos0, nkeys);  // nkeys is 16..64
   unsigned long long v = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1));
@@ -205,6 +223,9 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
   }
 }
 
+// kWide: more than 64 new rows per request (128-bit ancestor masks); the
+// narrow kernel keeps one 64-bit word per row.
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ k_cache,
@@ -589,7 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
       cu.start(st0, st1, rq, B);
       int64_t t = 0;
       float m_used = -INFINITY, l = 0.f;
-      ulonglong2 anc = make_ulonglong2(0ull, 0ull), anc_n = anc;
+      unsigned long long anc = 0, anc_n = 0;        // mask bits 0..63
+      unsigned long long anc_hi = 0, anc_hi_n = 0;  // bits 64..127 (kWide)
       int anc_b = -1, anc_nb = -1;  // requests whose masks anc and anc_n hold
       int ctx = 0, L = 0, tile0 = 0;
       int n_whole = 0;  // pair ends with output so far (barrier phase)
@@ -605,14 +627,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           m_used = -INFINITY;
           l = 0.f;
           if (anc_ws == nullptr) {
-            chain_mask(i, &anc.x, &anc.y);
+            if (kWide) chain_mask(i, &anc, &anc_hi);
+            else anc = (i >= 63) ? ~0ull : ((1ull << (i + 1)) - 1);
           } else if (real && cu.b != anc_b) {
             // tree masks come from the prep kernel; the next request's mask
             // is loaded one request ahead
-            anc = cu.b == anc_nb ? anc_n : __ldcg(anc_ws + (int64_t)cu.b * M + i);
+            const unsigned long long* aw = reinterpret_cast<const unsigned long long*>(anc_ws);
+            if (cu.b == anc_nb) {
+              anc = anc_n;
+              if (kWide) anc_hi = anc_hi_n;
+            } else {
+              anc = __ldcg(aw + 2 * ((int64_t)cu.b * M + i));
+              if (kWide) anc_hi = __ldcg(aw + 2 * ((int64_t)cu.b * M + i) + 1);
+            }
             anc_b = cu.b;
             if (cu.next_b < B) {
-              anc_n = __ldcg(anc_ws + (int64_t)cu.next_b * M + i);
+              anc_n = __ldcg(aw + 2 * ((int64_t)cu.next_b * M + i));
+              if (kWide) anc_hi_n = __ldcg(aw + 2 * ((int64_t)cu.next_b * M + i) + 1);
               anc_nb = cu.next_b;
             }
           }
@@ -657,7 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         } else {
           // visibility of the tile's keys as a bitmask, then the same maximum
           // as the plain path over the visible ones
-          const unsigned long long vis = tile_visibility(kpos0, nkeys, ctx, L, anc.x, anc.y, real);
+          const unsigned long long vis =
+              kWide ? tile_visibility_wide(kpos0, nkeys, ctx, L, anc, anc_hi, real)
+                    : tile_visibility(kpos0, nkeys, ctx, L, anc, real);
           vh = (uint32_t)(vis >> jbase);
           const uint32_t vo = (uint32_t)(vis >> (jbase ^ 32));
           float a0 = -INFINITY, a1 = -INFINITY;
@@ -1182,13 +1215,14 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   ++*launches;
-  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes);
+  const bool wide = d.M > 64;
+  auto kern = wide ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const float qscale2 = a.scale * 1.4426950408889634f;
   {
     PdlLaunch L(dim3(G), dim3(kThreads), kSmemBytes, st);
-    e = cudaLaunchKernelEx(&L.cfg, attn_tc_kernel, tm_q,
+    e = cudaLaunchKernelEx(&L.cfg, kern, tm_q,
                            static_cast<const __nv_bfloat16*>(a.k_new),
                            static_cast<const __nv_bfloat16*>(a.v_new),
                            static_cast<__nv_bfloat16*>(a.k_cache),

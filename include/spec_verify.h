@@ -264,6 +264,48 @@ spec_status spec_reject_sample_filtered(const void* target_logits,
                                         size_t ws_bytes, void* stream);
 
 /*
+ * spec_lm_head -- logits of an LM head: logits[r, v] = sum_k hidden[r, k] *
+ * weight[v, k] (bf16 inputs, fp32 accumulation on the tensor cores, bf16
+ * output rounded to nearest even).
+ *
+ * Page 2 §1.2: decoding is bound by weight and logit reads; this is the
+ * product the verify step's logits come from.
+ *   hidden  [rows, H] bf16   row-major, 16-byte aligned
+ *   weight  [V, H]    bf16   row-major (one vocabulary row of H weights)
+ *   logits  [rows, V] bf16   output
+ *   ws, ws_bytes             at least 16 bytes (its first word is the status
+ *                            word of spec_get_device_status)
+ * H must be a multiple of 64 and V of 256 (else SPEC_ERR_UNSUPPORTED).
+ */
+spec_status spec_lm_head(const void* hidden, const void* weight, int32_t rows, int32_t H,
+                         int32_t V, void* logits, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * spec_reject_sample_lm_head -- the LM heads and the verify decisions in one
+ * call, without a second pass over the logit rows.
+ *
+ * The target and draft logits of the B*M new rows are computed as in
+ * spec_lm_head (target: hidden_target [B, M, Ht] x weight_target [V, Ht];
+ * draft: hidden_draft [B, M, Hd] x weight_draft [V, Hd]) into target_logits
+ * and draft_logits ([B, M, V] bf16, written); their epilogue also forms the
+ * per-chunk statistics the decisions need (page 2 §1.2: the logit rows are
+ * read once less), and spec_reject_sample's decisions and draws follow on
+ * them.  Arguments after draft_logits and the outputs are those of
+ * spec_reject_sample; dims->logits_dtype must be bf16, Ht and Hd multiples
+ * of 64, dims->V a multiple of 256; SPEC_REJECT_FUSED is refused.
+ */
+spec_status spec_reject_sample_lm_head(const void* hidden_target, const void* weight_target,
+                                       int32_t Ht, const void* hidden_draft,
+                                       const void* weight_draft, int32_t Hd,
+                                       void* target_logits, void* draft_logits,
+                                       const int32_t* tokens, const int32_t* parent,
+                                       const float* temperature, uint64_t seed, uint64_t offset,
+                                       uint64_t b_base, int32_t* out_tokens, int32_t* path,
+                                       int32_t* accepted_len, float* probe,
+                                       const spec_dims* dims, void* ws, size_t ws_bytes,
+                                       void* stream);
+
+/*
  * kv_commit -- roll back / compact the cache to the accepted path.
  *
  * Page 2 §3.3: after a partial acceptance the cache past the accepted

@@ -53,3 +53,4 @@ from .attention import (  # noqa: F401
     ancestors_or_self,
 )
 from .kv import oracle_kv_commit  # noqa: F401
+from .lm_head import oracle_lm_head  # noqa: F401

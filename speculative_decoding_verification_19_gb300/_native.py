@@ -29,7 +29,7 @@ REJECT_AUTO, REJECT_STAGED, REJECT_FUSED = 0, 1, 2
 EXPORTS = (
     "spec_workspace_size", "spec_workspace_init", "spec_get_device_status",
     "spec_verify_attn", "spec_reject_sample", "spec_reject_sample_filtered", "kv_commit",
-    "spec_philox_block",
+    "spec_philox_block", "spec_lm_head", "spec_reject_sample_lm_head",
     "spec_status_string", "spec_last_launch_count", "spec_reject_sample_noalloc",
     "spec_ctrl_default_config", "spec_ctrl_init", "spec_ctrl_update", "spec_ctrl_metrics",
     "spec_step_stats",
@@ -83,6 +83,11 @@ def lib() -> ctypes.CDLL:
     L.spec_reject_sample_filtered.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u64, u64, vp,
                                               vp, vp, vp, pd, vp, sz, vp]
     L.spec_reject_sample_filtered.restype = i32
+    L.spec_lm_head.argtypes = [vp, vp, i32, i32, i32, vp, vp, sz, vp]
+    L.spec_lm_head.restype = i32
+    L.spec_reject_sample_lm_head.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, u64,
+                                             u64, u64, vp, vp, vp, vp, pd, vp, sz, vp]
+    L.spec_reject_sample_lm_head.restype = i32
     L.spec_reject_sample_noalloc.argtypes = [vp, vp, vp, vp, vp, u64, u64, u64, vp, vp,
                                              vp, vp, pd, vp]
     L.spec_reject_sample_noalloc.restype = i32
@@ -191,6 +196,33 @@ def spec_reject_sample(target_logits, draft_logits, tokens, parent, temperature,
             _ptr(accepted_len), _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(),
             _stream(stream))
         _check("spec_reject_sample_filtered", code)
+    return lib().spec_last_launch_count()
+
+
+def spec_lm_head(hidden, weight, logits, ws, stream=None) -> int:
+    """logits [rows, V] = hidden [rows, H] @ weight [V, H]^T (bf16)."""
+    rows, H = hidden.shape
+    V = weight.shape[0]
+    code = lib().spec_lm_head(_ptr(hidden), _ptr(weight), rows, H, V, _ptr(logits), _ptr(ws),
+                              ws.numel(), _stream(stream))
+    _check("spec_lm_head", code)
+    return lib().spec_last_launch_count()
+
+
+def spec_reject_sample_lm_head(hidden_target, weight_target, hidden_draft, weight_draft,
+                               target_logits, draft_logits, tokens, parent, temperature, seed,
+                               offset, out_tokens, path, accepted_len, probe, dims: SpecDims, ws,
+                               b_base=0, stream=None) -> int:
+    """The target and draft LM heads with the verify decisions (the
+    statistics formed in the LM heads' epilogue)."""
+    code = lib().spec_reject_sample_lm_head(
+        _ptr(hidden_target), _ptr(weight_target), hidden_target.shape[-1], _ptr(hidden_draft),
+        _ptr(weight_draft), hidden_draft.shape[-1], _ptr(target_logits), _ptr(draft_logits),
+        _ptr(tokens), _ptr(parent), _ptr(temperature), int(seed) % (1 << 64),
+        int(offset) % (1 << 64), int(b_base) % (1 << 64), _ptr(out_tokens), _ptr(path),
+        _ptr(accepted_len), _ptr(probe), ctypes.byref(dims), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("spec_reject_sample_lm_head", code)
     return lib().spec_last_launch_count()
 
 

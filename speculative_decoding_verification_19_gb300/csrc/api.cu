@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "kv_commit.cuh"
 #include "philox.cuh"
+#include "lm_head.cuh"
 #include "reject_sample.cuh"
 
 namespace specv {
@@ -257,6 +258,90 @@ spec_status spec_reject_sample_filtered(const void* target_logits, const void* d
   return reject_common(target_logits, draft_logits, tokens, parent, temperature, top_k, top_p,
                        seed, offset, b_base, out_tokens, path, accepted_len, probe, dims, ws,
                        ws_bytes, stream);
+}
+
+spec_status spec_lm_head(const void* hidden, const void* weight, int32_t rows, int32_t H,
+                         int32_t V, void* logits, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!hidden || !weight || !logits || ws == nullptr || ws_bytes < 16 || !aligned16(ws))
+    return SPEC_ERR_INVALID_ARG;
+  if (rows < 1 || H < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!lm_head_supported(rows, H, V)) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits)) return SPEC_ERR_INVALID_ARG;
+  spec_dims d;
+  memset(&d, 0, sizeof(d));  // the default wait limit
+  int launches = 0;
+  const cudaError_t e =
+      lm_head_launch(hidden, weight, rows, H, V, logits, nullptr, 0, 1, 0, nullptr, d,
+                     static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream), &launches);
+  g_launches = launches;
+  return e == cudaErrorInvalidValue ? SPEC_ERR_UNSUPPORTED : from_cuda(e);
+}
+
+spec_status spec_reject_sample_lm_head(const void* hidden_target, const void* weight_target,
+                                       int32_t Ht, const void* hidden_draft,
+                                       const void* weight_draft, int32_t Hd, void* target_logits,
+                                       void* draft_logits, const int32_t* tokens,
+                                       const int32_t* parent, const float* temperature,
+                                       uint64_t seed, uint64_t offset, uint64_t b_base,
+                                       int32_t* out_tokens, int32_t* path, int32_t* accepted_len,
+                                       float* probe, const spec_dims* dims, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  spec_status s = check_common(dims);
+  if (s != SPEC_OK) return s;
+  if ((s = check_ws(dims, ws, ws_bytes)) != SPEC_OK) return s;
+  if (!hidden_target || !weight_target || !hidden_draft || !weight_draft || !target_logits ||
+      !draft_logits || !tokens || !temperature || !out_tokens || !path || !accepted_len)
+    return SPEC_ERR_INVALID_ARG;
+  if (dims->logits_dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (dims->reject_impl == SPEC_REJECT_FUSED) return SPEC_ERR_UNSUPPORTED;
+  const int R = dims->B * dims->M;
+  if ((int64_t)dims->B * dims->M >= ((int64_t)1 << 31) / 2) return SPEC_ERR_UNSUPPORTED;
+  if (!lm_head_supported(R, Ht, dims->V) || !lm_head_supported(R, Hd, dims->V))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(hidden_target) || !aligned16(weight_target) || !aligned16(hidden_draft) ||
+      !aligned16(weight_draft) || !aligned16(target_logits) || !aligned16(draft_logits))
+    return SPEC_ERR_INVALID_ARG;
+  const WsLayout lay = workspace_layout(*dims);
+  if ((int64_t)lay.rs_chunks * 2 * dims->M * dims->B >= (int64_t)1 << 31) return SPEC_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  RowStat* stats = reinterpret_cast<RowStat*>(w + lay.rs_off);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + lay.status_off);
+  int launches = 0;
+  cudaError_t e = lm_head_launch(hidden_target, weight_target, R, Ht, dims->V, target_logits,
+                                 stats, 0, dims->M, lay.rs_chunks, temperature, *dims, status, st,
+                                 &launches);
+  if (e == cudaSuccess)
+    e = lm_head_launch(hidden_draft, weight_draft, R, Hd, dims->V, draft_logits, stats, 1,
+                       dims->M, lay.rs_chunks, temperature, *dims, status, st, &launches);
+  if (e != cudaSuccess) {
+    g_launches = launches;
+    return e == cudaErrorInvalidValue ? SPEC_ERR_UNSUPPORTED : SPEC_ERR_CUDA;
+  }
+  RsArgs a;
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.tokens = tokens;
+  a.parent = parent;
+  a.temperature = temperature;
+  a.top_k = nullptr;
+  a.top_p = nullptr;
+  a.seed = seed;
+  a.offset = offset;
+  a.b_base = b_base;
+  a.out_tokens = out_tokens;
+  a.path = path;
+  a.accepted_len = accepted_len;
+  a.probe = probe;
+  a.d = *dims;
+  a.d.reject_impl = SPEC_REJECT_STAGED;
+  a.ws = ws;
+  a.stats_ready = true;
+  e = rs_launch(a, lay, st, &launches);
+  g_launches = launches;
+  return from_cuda(e);
 }
 
 spec_status kv_commit(void* k_cache, void* v_cache, const int32_t* block_table,

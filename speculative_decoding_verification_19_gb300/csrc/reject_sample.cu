@@ -2899,7 +2899,9 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t ntask = (int64_t)lay.rs_chunks * 2 * d.M * d.B;
   const int64_t want = (ntask + kRsThreads / kWarp - 1) / (kRsThreads / kWarp);
-  if (kAligned) {
+  if (a.stats_ready) {
+    // the LM head wrote the statistics
+  } else if (kAligned) {
     const int64_t wantb = (ntask + kBulkWarps - 1) / kBulkWarps;
     const unsigned gb = (unsigned)(wantb < sms ? wantb : sms);
     cudaError_t e = cudaFuncSetAttribute(rs_rowstats_bulk_kernel<T>,
@@ -2932,7 +2934,7 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
         a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk,
         (const RowStat*)stats, zsum, reinterpret_cast<uint32_t*>(ws + lay.rs_tail_off), status, S);
     if (e != cudaSuccess) return e;
-    *launches += 2;
+    *launches += a.stats_ready ? 1 : 2;
     return cudaGetLastError();
   }
   // passes 2 and 3 start while their predecessor drains (programmatic
@@ -2978,7 +2980,7 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
                          lay.rs_chunk, (const RowStat*)stats, (const DrawState*)draws,
                          (const double*)zsum, a.out_tokens, a.probe);
   if (e != cudaSuccess) return e;
-  *launches += 4;
+  *launches += a.stats_ready ? 3 : 4;
   return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ struct RsArgs {
   float* probe;
   spec_dims d;
   void* ws;
+  bool stats_ready = false;  // the chunk statistics are already in the workspace
 };
 
 int rs_chunk_elems(int logits_dtype);       // statistics chunk (one warp task)

@@ -160,8 +160,11 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -385,6 +388,75 @@ def greedy_reject(st, K, peak, rej_b):
             "emitted_tokens_per_step": int((a + 1).sum())}
 
 
+# The LM heads of the stress workload's rows: a 70B-class target (hidden size
+# 64 heads x 128) and a small draft head, on random bf16 weights.
+LM_HEAD_HT, LM_HEAD_HD = 8192, 1024
+
+
+def lm_head_step(wl, lg, st, K, peaks):
+    """spec_reject_sample_lm_head on the default workload's shape (the
+    statistics formed in the LM heads' epilogue) against the same LM heads
+    followed by spec_reject_sample (a second pass over the logit rows),
+    each timed over K calls with CUDA events; the target head alone gives the
+    tensor-core rate."""
+    sv = st.sv
+    dev = st.target.device
+    B, M, V = wl.B, wl.M, wl.V
+    g = torch.Generator(device=dev)
+    g.manual_seed(20261202)
+    ht = torch.randn(B, M, LM_HEAD_HT, device=dev, generator=g).to(torch.bfloat16)
+    wt = (torch.randn(V, LM_HEAD_HT, device=dev, generator=g) * (3.0 / LM_HEAD_HT ** 0.5)).to(torch.bfloat16)
+    hd = torch.randn(B, M, LM_HEAD_HD, device=dev, generator=g).to(torch.bfloat16)
+    wd = (torch.randn(V, LM_HEAD_HD, device=dev, generator=g) * (3.0 / LM_HEAD_HD ** 0.5)).to(torch.bfloat16)
+    tl = torch.empty(B, M, V, dtype=torch.bfloat16, device=dev)
+    dl = torch.empty_like(tl)
+    ws = st.ws
+
+    def fused(i):
+        return sv.spec_reject_sample_lm_head(ht, wt, hd, wd, tl, dl, st.tokens, st.parent,
+                                             st.temperature, 3, i, st.out_tokens, st.path,
+                                             st.acc[0], None, st.dims, ws)
+
+    def unfused(i):
+        n = sv.spec_lm_head(ht.view(B * M, -1), wt, tl.view(B * M, -1), ws)
+        n += sv.spec_lm_head(hd.view(B * M, -1), wd, dl.view(B * M, -1), ws)
+        n += sv.spec_reject_sample(tl, dl, st.tokens, st.parent, st.temperature, 3, i,
+                                   st.out_tokens, st.path, st.acc[0], None, st.dims, ws)
+        return n
+
+    def target_head(i):
+        return sv.spec_lm_head(ht.view(B * M, -1), wt, tl.view(B * M, -1), ws)
+
+    res = {}
+    for name, f in (("fused", fused), ("unfused", unfused), ("target_head", target_head)):
+        for i in range(3):
+            f(i)
+        torch.cuda.synchronize()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        for i in range(K):
+            launches = f(i)
+        b_.record()
+        torch.cuda.synchronize()
+        res[name] = (a_.elapsed_time(b_) / K, launches)
+    assert sv.device_status(ws) == 0
+    a = st.acc[0].cpu().numpy()
+    assert np.all(a >= 0)
+    flops = 2.0 * B * M * LM_HEAD_HT * V
+    t_ms = res["target_head"][0]
+    achieved = flops / (t_ms / 1e3) / 1e12
+    return {"workload": f"{wl.name} rows (B {B} x M {M}), V {V}, target hidden {LM_HEAD_HT}, "
+                        f"draft hidden {LM_HEAD_HD}, random bf16 weights",
+            "fused_ms": round(res["fused"][0], 4), "fused_launches": res["fused"][1],
+            "unfused_ms": round(res["unfused"][0], 4), "unfused_launches": res["unfused"][1],
+            "target_head_ms": round(t_ms, 4),
+            "roofline": {"bound": "tensor", "kernel": "lm_head_kernel (target head)",
+                         "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "peak_source": peaks["source"] + " bf16 burst", "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "flops_per_call": flops}}
+
+
 def second_workload(name, seed, device, K, W, peak):
     """The other workload the HBM bar is set on, timed the same way in the
     same process after the main timed region (its own inputs, K steps)."""
@@ -531,6 +603,7 @@ def run_native(args, wl, world, rank, local):
     workloads = {wl.name: {"attn_frac": round(attn_b / (attn_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                            "reject_frac": round(rej_b / (rej_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}}
     workloads[wl.name + " (temperature 0)"] = greedy_reject(st, K, peaks["hbm_gbs"], rej_b)
+    lm_head = lm_head_step(wl, lg, st, K, peaks) if not args.no_second else None
     if not args.no_second and wl.name in BAR_WORKLOADS:
         for other in BAR_WORKLOADS:
             if other != wl.name:
@@ -566,6 +639,7 @@ def run_native(args, wl, world, rank, local):
                     "reject_frac": round(rej_b / (rej_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                     "reject_bytes": rej_b},
         "workloads": workloads,
+        "lm_head": lm_head,
         "verify_stats": verify_stats,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * K / e2e_s, 3), "unit": UNIT,

@@ -224,8 +224,9 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
 }
 
 // kWide: more than 64 new rows per request (128-bit ancestor masks); the
-// narrow kernel keeps one 64-bit word per row.
-template <bool kWide>
+// narrow kernel keeps one 64-bit word per row.  kShort: the wait limit is
+// short (ptx::mbar_wait_t).
+template <bool kWide, bool kShort>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ k_cache,
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
   // so that the fence before the count stalls no softmax warp.
   const int helper = n_sm_warps <= 2 ? kCopyWarpLargeR : (n_sm_warps == 3 ? 3 : -1);
   if (warp == helper && lane == 0 && st0.w > 0) {
-    if (ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
+    if (ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
       __threadfence();
       atomicAdd(pairs + (int64_t)st0.y * Hkv + st0.z, (int)min((int64_t)(st1.y - st0.w), g1 - g0));
     }
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         if (warp == kProducerWarp) {
           if (lane == 0) {
             const int qb = seg % kQBufs;
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
+            ok = ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->q_empty[qb]), ((seg / kQBufs) & 1) ^ 1, abort,
                                 wait);
             if (ok) {
               const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
 #pragma unroll
       for (int p = 0; p < kPages; ++p) blk[p] = __shfl_sync(0xffffffffu, ids[p], src);
       const int stage = (int)(t % kStages);
-      ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
+      ok = ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->empty[stage]), (uint32_t)((t / kStages) & 1) ^ 1u,
                           abort, wait);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -528,15 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           L = cu.ctx + M;
         }
         const int qb = seg % kQBufs;
-        if (first && !ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]),
+        if (first && !ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->q_full[qb]),
                                      (uint32_t)((seg / kQBufs) & 1), abort, wait))
           break;
         const int stage = (int)(t % kStages);
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
+        if (!ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->full[stage]), (uint32_t)((t / kStages) & 1),
                             abort, wait))
           break;
         // PV(t - kSBufs) read P out of the S buffer this tile's QK writes
-        if (t >= kSBufs && !ptx::mbar_wait(ptx::smem_u32(&bars->o_done[t % kSBufs]),
+        if (t >= kSBufs && !ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->o_done[t % kSBufs]),
                                            (uint32_t)(((t - kSBufs) / kSBufs) & 1), abort,
                                            wait))
           break;
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         const int np = tile_pages(L, cu.tile);
         const int sbuf = (int)(u % kSBufs);
         const int stage = (int)(u % kStages);
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u / kSBufs) & 1), abort,
+        if (!ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->p_full[sbuf]), (uint32_t)((u / kSBufs) & 1), abort,
                             wait))
           break;
         ptx::tc_fence_after();
@@ -649,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
           }
         }
         const int sbuf = (int)(t % kSBufs);  // S / P buffer in TMEM
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sbuf]),
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->s_full[sbuf]),
                                                      (uint32_t)((t / kSBufs) & 1), abort, wait)))
           break;
         ptx::tc_fence_after();
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         if (__any_sync(0xffffffffu, need)) {
           // O is rescaled in place (this half's 64 columns): PV(t-1) must have landed
           if (!__all_sync(0xffffffffu,
-                          ptx::mbar_wait(ptx::smem_u32(&bars->o_done[(t - 1) % kSBufs]),
+                          ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->o_done[(t - 1) % kSBufs]),
                                          (uint32_t)(((t - 1) / kSBufs) & 1), abort, wait)))
             break;
           ptx::tc_fence_after();
@@ -772,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sbuf]));
         if (last) {
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->o_done[sbuf]),
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->o_done[sbuf]),
                                                        (uint32_t)((t / kSBufs) & 1), abort, wait)))
             break;
           ptx::tc_fence_after();
@@ -810,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ebar));
             if (helper < 0 && warp == 0 && lane == 0 &&
-                ptx::mbar_wait(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
+                ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->ebar), 0, abort, wait)) {
               // every row of the partial is written (the barrier above); the
               // fence makes them visible GPU-wide before the tiles are counted
               __threadfence();
@@ -823,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(
             bars->xl[half][row] = l;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->lbar[sp]));
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->lbar[sp]),
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_t<kShort>(ptx::smem_u32(&bars->lbar[sp]),
                                                          (uint32_t)(n_whole & 1), abort, wait)))
               break;
             ++n_whole;
@@ -1215,8 +1216,9 @@ cudaError_t attn_launch_tc(const AttnArgs& a, const WsLayout& lay, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   ++*launches;
-  const bool wide = d.M > 64;
-  auto kern = wide ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  const bool wide = d.M > 64, short_wait = wait_limit_cycles(d) < ptx::kShortWait;
+  auto kern = wide ? (short_wait ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
+                   : (short_wait ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const float qscale2 = a.scale * 1.4426950408889634f;

@@ -106,6 +106,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait with the choice of path made at compile time: kernels that run
+// their hot loops on mbarrier waits are instantiated twice, for short
+// limits (kShort: test_wait polling, the limit honoured closely) and for
+// the usual ones (try_wait), so that the loop carries no runtime branch.
+template <bool kShort>
+__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile int* abort,
+                                            uint64_t timeout_cycles) {
+  if (kShort) return mbar_wait_short(bar, parity, abort, timeout_cycles);
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 1023u) {
+      if (*abort) return false;
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if ((uint64_t)(now - t0) > timeout_cycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Wait for work this CTA already issued (bulk copies, MMAs) to complete
 // before it exits or frees what that work writes: the same polling as
 // mbar_wait, but the CTA's abort flag does not cut it short -- the work lands

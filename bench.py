@@ -343,13 +343,14 @@ def verify_statistics(wl, acc, st, parent):
     # a controller fed the steps at the workload's fixed draft length (its
     # proposals are reported, not applied: the workload's shape is fixed)
     from speculative_decoding_verification_19_gb300.controller import default_config
-    ctl = Controller(B, gamma0=wl.gamma if not wl.is_tree else wl.M - 1,
+    # (a tree's draft length is its depth: the longest path it can accept)
+    ctl = Controller(B, gamma0=min(wl.gamma, 63),
                      cfg=default_config(window=min(16, K), max_gamma=63, min_efficiency=0.0))
     proposed = None
     for k in range(K):
         # the draft length stays the workload's: feed each step as drafted at it
         for r in ctl.reqs:
-            r.gamma = wl.gamma if not wl.is_tree else wl.M - 1
+            r.gamma = min(wl.gamma, 63)
         proposed = ctl.update(acc[k])
     m = ctl.metrics()
     out = {"rejection_position_hist": pos.tolist(),
@@ -455,6 +456,62 @@ def lm_head_step(wl, lg, st, K, peaks):
                          "peak_source": peaks["source"] + " bf16 burst", "unit": "TFLOP/s",
                          "frac": round(achieved / peaks["bf16_tflops"], 4),
                          "flops_per_call": flops}}
+
+
+def run_only(args, wl):
+    """One entry point alone on the workload's shapes: W untimed calls, then
+    K calls between CUDA events (no flush: for profiler captures and per-call
+    comparisons, not a bench line).  reject: spec_reject_sample on the
+    workload's logits; lm_head: spec_lm_head on rows B x M of random hidden
+    states against a random V x LM_HEAD_HT weight."""
+    import speculative_decoding_verification_19_gb300 as sv
+    from synth import logits_inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, M, V = wl.B, wl.M, wl.V
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    T = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to(dev, t)  # noqa: E731
+    if args.only == "reject":
+        lg = logits_inputs(wl, args.seed)
+        dims = sv.make_dims(B=B, M=M, V=V, logits_dtype=dt)
+        ws = sv.workspace(dims, device=dev)
+        tgt, dft = T(lg["target"], dt), T(lg["draft"], dt)
+        tok, temp = T(lg["tokens"], torch.int32), T(lg["temperature"], torch.float32)
+        par = None if lg["parent"] is None else T(lg["parent"], torch.int32)
+        out = torch.empty(B, M, dtype=torch.int32, device=dev)
+        path = torch.empty_like(out)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def call(i):
+            return sv.spec_reject_sample(tgt, dft, tok, par, temp, 20261202, i, out, path, acc,
+                                         None, dims, ws)
+    else:
+        g = torch.Generator(device=dev)
+        g.manual_seed(20261202)
+        h = torch.randn(B * M, LM_HEAD_HT, device=dev, generator=g).to(torch.bfloat16)
+        w = (torch.randn(V, LM_HEAD_HT, device=dev, generator=g)
+             * (3.0 / LM_HEAD_HT ** 0.5)).to(torch.bfloat16)
+        logits = torch.empty(B * M, V, dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(64, dtype=torch.uint8, device=dev)
+
+        def call(i):
+            return sv.spec_lm_head(h, w, logits, ws)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_.record()
+    for i in range(args.steps):
+        launches = call(args.warmup + i)
+    b_.record()
+    torch.cuda.synchronize()
+    assert sv.device_status(ws) == 0
+    ms = a_.elapsed_time(b_) / args.steps
+    line = {"only": args.only, "workload": wl.name, "B": B, "M": M, "V": V,
+            "ms_per_call": round(ms, 4), "launches_per_call": launches, "calls": args.steps}
+    if args.only == "lm_head":
+        line["tflops"] = round(2.0 * B * M * LM_HEAD_HT * V / (ms / 1e3) / 1e12, 1)
+    print(json.dumps(line), flush=True)
 
 
 def second_workload(name, seed, device, K, W, peak):
@@ -711,12 +768,17 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-second", action="store_true",
                     help="time only the selected workload")
+    ap.add_argument("--only", choices=("reject", "lm_head"), default=None,
+                    help="run one entry point alone (for profiler captures); no bench line")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed steps
     from synth import workload
     wl = workload(args.workload)
     if args.batch is not None:
         wl = wl.scaled(B=args.batch)
+    if args.only is not None:
+        run_only(args, wl)
+        return
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, world, rank)

@@ -62,6 +62,13 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
   L.rs_filt_off = take(sizeof(FilterInfo) * (size_t)d.B * 2 * d.M);
   L.rs_tail_off = take(sizeof(uint32_t) * (size_t)d.B);
+  // the LM heads' split statistics (rows B * M, bf16 logits)
+  const int64_t lm_units = (int64_t)ceil_div64((int64_t)d.B * d.M, 128) * L.rs_chunks;
+  if (d.logits_dtype == SPEC_BF16 && lm_units <= kLmSplitMaxUnits) {
+    L.lm_units = lm_units;
+    L.lm_part_off = take(sizeof(RowStat) * 2 * (size_t)lm_units * kLmMaxPieces * 128);
+    L.lm_cnt_off = take(sizeof(uint32_t) * 2 * (size_t)lm_units * 4);
+  }
   off = rsf_layout(d, off, &L);
   L.total = off;
   return L;
@@ -273,7 +280,8 @@ spec_status spec_lm_head(const void* hidden, const void* weight, int32_t rows, i
   int launches = 0;
   const cudaError_t e =
       lm_head_launch(hidden, weight, rows, H, V, logits, nullptr, 0, 1, 0, nullptr, d,
-                     static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream), &launches);
+                     static_cast<uint32_t*>(ws), nullptr, nullptr,
+                     static_cast<cudaStream_t>(stream), &launches);
   g_launches = launches;
   return e == cudaErrorInvalidValue ? SPEC_ERR_UNSUPPORTED : from_cuda(e);
 }
@@ -310,12 +318,17 @@ spec_status spec_reject_sample_lm_head(const void* hidden_target, const void* we
   RowStat* stats = reinterpret_cast<RowStat*>(w + lay.rs_off);
   uint32_t* status = reinterpret_cast<uint32_t*>(w + lay.status_off);
   int launches = 0;
+  // the split statistics' workspace, when laid out for these rows
+  const bool split = lay.lm_units > 0 && lay.lm_units == lm_head_units(R, dims->V);
+  RowStat* part = split ? reinterpret_cast<RowStat*>(w + lay.lm_part_off) : nullptr;
+  uint32_t* cnt = split ? reinterpret_cast<uint32_t*>(w + lay.lm_cnt_off) : nullptr;
   cudaError_t e = lm_head_launch(hidden_target, weight_target, R, Ht, dims->V, target_logits,
-                                 stats, 0, dims->M, lay.rs_chunks, temperature, *dims, status, st,
-                                 &launches);
+                                 stats, 0, dims->M, lay.rs_chunks, temperature, *dims, status,
+                                 part, cnt, st, &launches);
   if (e == cudaSuccess)
     e = lm_head_launch(hidden_draft, weight_draft, R, Hd, dims->V, draft_logits, stats, 1,
-                       dims->M, lay.rs_chunks, temperature, *dims, status, st, &launches);
+                       dims->M, lay.rs_chunks, temperature, *dims, status, part, cnt, st,
+                       &launches);
   if (e != cudaSuccess) {
     g_launches = launches;
     return e == cudaErrorInvalidValue ? SPEC_ERR_UNSUPPORTED : SPEC_ERR_CUDA;

@@ -158,6 +158,9 @@ struct WsLayout {
   size_t rs_zsum_off;     // [B, n_chunks] f64: residual mass of each statistics chunk
   size_t rs_filt_off;     // [B, 2, M] 16-byte kept prefix of each filtered row
   size_t rs_tail_off;     // [B] u32 slices of the chain tail kernel finished per request
+  size_t lm_part_off;     // LM heads' split statistics: [2][units][4][128] RowStat
+  size_t lm_cnt_off;      // [2][units][4] u32 pieces finished per (unit, 32-row warp)
+  int64_t lm_units;       // units laid out (0: LM-head units are not split)
   int rs_chunk;           // logits per statistics chunk
   int rs_chunks;          // statistics chunks per row
   // the one-kernel reject path (laid out by rsf_layout)

@@ -20,10 +20,15 @@
 //   warps 4-7   epilogue, one TMEM sub-partition (32 rows) each: the
 //               accumulator read 32 columns at a time, rounded to bf16,
 //               stored, and folded into the row's running chunk statistics.
-// A CTA's work unit is one 128-row tile by one 2048-column chunk (eight
-// 256-column sub-tiles), so a chunk's statistics are complete inside one
-// thread; units are taken chunk-major, so the CTAs working at one time read
-// the same W tiles (from L2 after the first).
+// A unit is one 128-row tile by one 2048-column chunk (eight 256-column
+// sub-tiles).  A CTA's work item is one of P equal pieces of a unit (P = 1,
+// 2, 4 or 8, chosen at launch so that the items fill the last wave of CTAs):
+// with P = 1 a chunk's statistics are complete inside one thread; with
+// P > 1 every piece leaves its partial statistics in the workspace and the
+// piece that finishes last (per 32-row warp, a fence and a counter) merges
+// them in piece order.  Items are taken chunk-major with the row tile
+// fastest, so the CTAs working at one time read the same W tiles (from L2
+// after the first).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -67,13 +72,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Work item w: piece p of unit (row tile mt, chunk nu), sub-tiles [j0, j1)
+// of the row (empty for a piece past the end of a short last chunk).
+struct Piece {
+  int mt, nu, p, j0, j1;
+  int64_t u;  // the unit, chunk-major
+};
+
+__device__ __forceinline__ Piece piece_of(int64_t w, int m_tiles, int P, int n_subs) {
+  Piece q;
+  q.mt = (int)(w % m_tiles);
+  const int64_t rest = w / m_tiles;
+  q.p = (int)(rest % P);
+  q.nu = (int)(rest / P);
+  q.u = (int64_t)q.nu * m_tiles + q.mt;
+  const int per = kSubs / P;
+  q.j0 = q.nu * kSubs + q.p * per;
+  q.j1 = min(n_subs, q.j0 + per);
+  if (q.j1 < q.j0) q.j1 = q.j0;
+  return q;
+}
+
 // Row r of the logits / hidden states is node n = r % M of request r / M;
 // its chunk statistics go where the reject-sample kernels read them (target
 // rows: which = 0, draft rows: which = 1).
 __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
     const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int R,
     int H, int V, __nv_bfloat16* __restrict__ logits, RowStat* stats, int which, int M,
-    int n_chunks, const float* temperature, spec_dims d, uint32_t* status) {
+    int n_chunks, const float* temperature, spec_dims d, uint32_t* status, int P,
+    RowStat* part, uint32_t* cnt) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -114,16 +141,17 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
   const int n_subs = V / kBN;                        // V is a multiple of 256
   const int n_units_n = (n_subs + kSubs - 1) / kSubs;
   const int64_t units = (int64_t)m_tiles * n_units_n;
+  const int64_t items = units * P;
   const int kblocks = H / kBK;                       // H is a multiple of 64
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       int64_t it = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int nu = (int)(u / m_tiles), mt = (int)(u - (int64_t)nu * m_tiles);
-        const int j1 = min(n_subs, (nu + 1) * kSubs);
-        for (int j = nu * kSubs; j < j1 && ok; ++j)
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+        const Piece q = piece_of(w, m_tiles, P, n_subs);
+        const int mt = q.mt;
+        for (int j = q.j0; j < q.j1 && ok; ++j)
           for (int kb = 0; kb < kblocks; ++kb, ++it) {
             const int s = (int)(it % kStages);
             if (it >= kStages &&
@@ -151,10 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
       const uint64_t db0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kABytes), 16, 1024);
       int64_t it = 0, t = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int nu = (int)(u / m_tiles);
-        const int j1 = min(n_subs, (nu + 1) * kSubs);
-        for (int j = nu * kSubs; j < j1 && ok; ++j, ++t) {
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+        const Piece q = piece_of(w, m_tiles, P, n_subs);
+        for (int j = q.j0; j < q.j1 && ok; ++j, ++t) {
           const int acc = (int)(t & 1);
           if (t >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[acc]),
                                         (uint32_t)(((t >> 1) & 1) ^ 1), abort, wait)) {
@@ -191,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
     const int sub = warp - kEpiWarp0;  // TMEM sub-partition: lanes 32 sub .. 32 sub + 31
     const uint32_t lane_base = tmem + ((uint32_t)(sub * 32) << 16);
     int64_t t = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-      const int nu = (int)(u / m_tiles), mt = (int)(u - (int64_t)nu * m_tiles);
+    for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+      const Piece q = piece_of(w, m_tiles, P, n_subs);
+      const int nu = q.nu, mt = q.mt;
       const int row = mt * kBM + sub * 32 + lane;
       const bool valid = row < R;
       float cs = 1.f;
@@ -205,9 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
       float m_run = -INFINITY;
       dfloat s_run = df_make(0.f);
       int am_run = 0;  // column of the chunk's first maximum, inside the chunk
-      const int j1 = min(n_subs, (nu + 1) * kSubs);
       bool ok = true;
-      for (int j = nu * kSubs; j < j1; ++j, ++t) {
+      for (int j = q.j0; j < q.j1; ++j, ++t) {
         const int acc = (int)(t & 1);
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[acc]),
                                                     (uint32_t)((t >> 1) & 1), abort, wait))) {
@@ -275,12 +302,56 @@ __global__ void __launch_bounds__(kThreads, 1) lm_head_kernel(
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[acc]));
       }
       if (!ok) break;
-      if (stats != nullptr && valid) {
+      if (stats == nullptr) continue;
+      RowStat rs;
+      rs.m = m_run;
+      rs.pad = pack_index(am_run);
+      rs.s = df_to_d(s_run);
+      if (P > 1) {
+        // this piece's partial statistics, then the count of the unit's
+        // pieces finished (per warp: the warp's 32 rows); the last merges
+        // the pieces in order -- the maximum, the first piece holding it
+        // for the argmax, the sums rescaled to it
+        RowStat* slot = part + ((((int64_t)which * units + q.u) * P) * kBM) + sub * 32 + lane;
+        if (valid) slot[(int64_t)q.p * kBM] = rs;
+        __threadfence();
+        __syncwarp();
+        uint32_t prev = 0;
+        uint32_t* c = cnt + ((int64_t)which * units + q.u) * 4 + sub;
+        if (lane == 0) prev = atomicAdd(c, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != (uint32_t)(P - 1)) continue;
+        __threadfence();
+        if (lane == 0) *c = 0u;  // ready for the next call
+        if (!valid) continue;
+        RowStat pc[kSubs];
+#pragma unroll
+        for (int k = 0; k < kSubs; ++k)
+          if (k < P && k != q.p) pc[k] = ld_stat_cg(slot + (int64_t)k * kBM);
+        float mm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kSubs; ++k)
+          if (k < P) mm = fmaxf(mm, k == q.p ? rs.m : pc[k].m);
+        double sm = 0.0;
+        float pad = pack_index(0);
+        bool found = false;
+#pragma unroll
+        for (int k = 0; k < kSubs; ++k) {
+          if (k >= P) continue;
+          const RowStat x = k == q.p ? rs : pc[k];
+          if (x.m != -INFINITY) sm += x.s * (double)fast_exp2((x.m - mm) * cs);
+          if (!found && x.m == mm) {
+            pad = x.pad;
+            found = true;
+          }
+        }
+        rs.m = mm;
+        rs.pad = pad;
+        rs.s = sm;
+      }
+      if (valid) {
         const int b = row / M, n = row - b * M;
-        RowStat rs;
-        rs.m = m_run;
-        rs.pad = pack_index(greedy ? am_run : 0);
-        rs.s = df_to_d(s_run);
+        if (!greedy) rs.pad = pack_index(0);
         stats[(((int64_t)b * 2 + which) * M + n) * n_chunks + nu] = rs;
       }
     }
@@ -325,10 +396,32 @@ bool lm_head_supported(int R, int H, int V) {
   return R >= 1 && H >= lm::kBK && H % lm::kBK == 0 && V >= lm::kBN && V % lm::kBN == 0;
 }
 
+// Pieces per unit: the P in {1, 2, 4, 8} (at most max_pieces) whose items
+// take the fewest sub-tile rounds, ceil(units P / CTAs) * 8 / P; the smallest
+// among equals (fewer merges).
+static int lm_pieces(int64_t units, int sms, int max_pieces) {
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int P = 1; P <= max_pieces && P <= lm::kSubs; P *= 2) {
+    const int64_t items = units * P;
+    const int64_t ctas = items < sms ? items : sms;
+    const int64_t cost = (items + ctas - 1) / ctas * (lm::kSubs / P);
+    if (best_cost < 0 || cost < best_cost) {
+      best = P;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+int64_t lm_head_units(int R, int V) {
+  return (int64_t)((R + lm::kBM - 1) / lm::kBM) * ((V / lm::kBN + lm::kSubs - 1) / lm::kSubs);
+}
+
 cudaError_t lm_head_launch(const void* hidden, const void* weight, int R, int H, int V,
                            void* logits, RowStat* stats, int which, int M, int n_chunks,
                            const float* temperature, const spec_dims& d, uint32_t* status,
-                           cudaStream_t st, int* launches) {
+                           RowStat* part, uint32_t* cnt, cudaStream_t st, int* launches) {
   CUtensorMap ta, tb;
   if (!lm_make_map(&ta, hidden, R, H, lm::kBM) || !lm_make_map(&tb, weight, V, H, lm::kBN))
     return cudaErrorInvalidValue;
@@ -339,13 +432,17 @@ cudaError_t lm_head_launch(const void* hidden, const void* weight, int R, int H,
   e = cudaFuncSetAttribute(lm::lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)lm::kSmem);
   if (e != cudaSuccess) return e;
-  const int m_tiles = (R + lm::kBM - 1) / lm::kBM;
-  const int64_t units = (int64_t)m_tiles * ((V / lm::kBN + lm::kSubs - 1) / lm::kSubs);
-  const unsigned grid = (unsigned)(units < sms ? units : sms);
+  const int64_t units = lm_head_units(R, V);
+  // without statistics the pieces need no merge; with them, only as many
+  // as the workspace holds partials for
+  const int max_pieces = stats == nullptr ? lm::kSubs : (part != nullptr ? kLmMaxPieces : 1);
+  const int P = lm_pieces(units, sms, max_pieces);
+  const int64_t items = units * P;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
   PdlLaunch L(dim3(grid), dim3(lm::kThreads), lm::kSmem, st);
   e = cudaLaunchKernelEx(&L.cfg, lm::lm_head_kernel, ta, tb, R, H, V,
                          static_cast<__nv_bfloat16*>(logits), stats, which, M, n_chunks,
-                         temperature, d, status);
+                         temperature, d, status, P, part, cnt);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaGetLastError();

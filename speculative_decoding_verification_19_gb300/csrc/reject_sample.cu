@@ -263,8 +263,10 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
     uint32_t* __restrict__ status) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr int kChunk = kWarp * kStatVecs * EPV;
-  pdl_trigger();
   pdl_wait();  // the logits may come from the previous kernel
+  // the dependent launches only now, when everything before this kernel has
+  // completed: the tree walk reads its inputs without waiting for this one
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -2933,6 +2935,15 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
         &L.cfg, rs_chain_tail_kernel<T>, tgt, dft, a.tokens, a.temperature, a.seed, a.offset,
         a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk,
         (const RowStat*)stats, zsum, reinterpret_cast<uint32_t*>(ws + lay.rs_tail_off), status, S);
+    if (e != cudaSuccess) return e;
+    *launches += a.stats_ready ? 1 : 2;
+    return cudaGetLastError();
+  }
+  // a tree of aligned, unfiltered rows: the walk by clusters, beside the
+  // statistics pass (after the LM heads it waits for them first)
+  if (rs_tree_walk_supported(d, kAligned, a.parent != nullptr,
+                             a.top_k != nullptr || a.top_p != nullptr)) {
+    const cudaError_t e = rs_tree_walk_launch(a, lay, !a.stats_ready, st);
     if (e != cudaSuccess) return e;
     *launches += a.stats_ready ? 1 : 2;
     return cudaGetLastError();

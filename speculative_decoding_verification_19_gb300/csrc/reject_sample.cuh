@@ -79,5 +79,12 @@ bool rso_supported(const spec_dims& d, bool aligned, bool chain);
 // Lays out the one-kernel path's scratch from byte offset `off` (256-byte
 // aligned) and returns the end.
 size_t rsf_layout(const spec_dims& d, size_t off, WsLayout* L);
+// The tree walk by clusters (rs_tree_walk.cu): trees of 16-byte aligned
+// rows without filters.  inputs_ready: launched right after the statistics
+// kernel (which lets it start once everything before that kernel has
+// completed); false after the LM heads (it waits for its predecessor).
+bool rs_tree_walk_supported(const spec_dims& d, bool aligned, bool tree, bool filters);
+cudaError_t rs_tree_walk_launch(const RsArgs& a, const WsLayout& lay, bool inputs_ready,
+                                cudaStream_t st);
 
 }  // namespace specv

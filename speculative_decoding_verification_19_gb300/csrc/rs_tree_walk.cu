@@ -39,7 +39,7 @@
 namespace specv {
 
 constexpr int kTwCtas = 8;  // CTAs per request (one cluster)
-constexpr int kTwThreads = 128;
+constexpr int kTwThreads = 256;
 constexpr int kTwWarps = kTwThreads / kWarp;
 constexpr int kTwBatch = 4;  // 16-byte vectors of a row loaded together per thread
 
@@ -104,7 +104,7 @@ __device__ __forceinline__ Run run_merge(Run x, Run y, float cs) {
   o.m = fmaxf(x.m, y.m);
   o.s = (x.m == -INFINITY ? 0.f : x.s * fast_exp2((x.m - o.m) * cs)) +
         (y.m == -INFINITY ? 0.f : y.s * fast_exp2((y.m - o.m) * cs));
-  o.a = x.m == y.m ? min(x.a, y.a) : (x.m > y.m ? x.a : y.a);
+  o.a = x.m == y.m ? min(x.a, y.a) : (x.m > y.m ? x.a : y.a);  // first index on ties
   if (o.m != o.m) o.a = 0;  // NaN: the row fails later
   return o;
 }
@@ -139,12 +139,13 @@ struct Smem {
   int kids[kMaxNodes];
   double px[kMaxNodes], qx[kMaxNodes];  // per child of the node (position in kids)
   float gzt[kMaxNodes], gzd[kMaxNodes];
-  double uacc[kMaxNodes], usmp[kMaxNodes];
+  double uk[kMaxNodes];  // accept uniform of each child of the node (position in kids)
+  double ST, invST64, invSD64;
   DecideCtx ctx;
   double invZ64[kMaxNodes + 1];
   double wp[kTwCtas];                   // mass of p of the node per slice
   double wr[kTwCtas];                   // mass of the last residual per slice
-  double ST, SD;                        // the node's row sums
+  double SD;                            // the node's row sums: ST above
   Run rt[kTwWarps], rd[kTwWarps];
   float rz[kTwWarps];
   dfloat scan[kTwWarps];
@@ -218,20 +219,44 @@ __device__ void tw_slice_runs(const T* trow, const T* drow, int64_t v0, int64_t 
       xd[k] = (drow != nullptr && v < v1) ? __ldg(reinterpret_cast<const uint4*>(drow) + v)
                                           : make_uint4(0, 0, 0, 0);
     }
+    // the batch: its maximum and first argmax, then its sum against that
+    // maximum (independent terms), merged into the running values
+    float ft[kTwBatch][EPV], fd[kTwBatch][EPV];
+    tw::Run bt{-INFINITY, 0.f, 0x7fffffff}, bd{-INFINITY, 0.f, 0x7fffffff};
 #pragma unroll
     for (int k = 0; k < kTwBatch; ++k) {
       const int64_t v = base + (int64_t)k * kTwThreads;
-      if (v >= v1) continue;
-      float ft[EPV], fd[EPV];
-      unpack16(xt[k], ft);
-      unpack16(xd[k], fd);
+      unpack16(xt[k], ft[k]);
+      unpack16(xd[k], fd[k]);
 #pragma unroll
       for (int i = 0; i < EPV; ++i) {
+        if (v >= v1) {
+          ft[k][i] = -INFINITY;
+          fd[k][i] = -INFINITY;
+        }
         const int e = (int)(v * EPV + i);
-        tw::run_add(rt, ft[i], e, cs);
-        if (drow != nullptr) tw::run_add(rd, fd[i], e, cs);
+        if (ft[k][i] > bt.m) {
+          bt.m = ft[k][i];
+          bt.a = e;
+        }
+        if (fd[k][i] > bd.m) {
+          bd.m = fd[k][i];
+          bd.a = e;
+        }
       }
     }
+    float st[2] = {0.f, 0.f}, sd[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < kTwBatch; ++k)
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) {
+        if (ft[k][i] != -INFINITY) st[i & 1] += fast_exp2((ft[k][i] - bt.m) * cs);
+        if (fd[k][i] != -INFINITY) sd[i & 1] += fast_exp2((fd[k][i] - bd.m) * cs);
+      }
+    bt.s = st[0] + st[1];
+    bd.s = sd[0] + sd[1];
+    rt = tw::run_merge(rt, bt, cs);
+    if (drow != nullptr) rd = tw::run_merge(rd, bd, cs);
   }
   rt = tw::run_warp(rt, cs);
   rd = tw::run_warp(rd, cs);
@@ -265,8 +290,10 @@ __device__ float tw_slice_mass(const T* trow, const T* drow, int64_t v0, int64_t
       float ft[EPV], fd[EPV];
       unpack16(xt[k], ft);
       unpack16(xd[k], fd);
+      float s2[2] = {0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) s += weight_of(ft[i], fd[i], v * EPV + i, c, nrej);
+      for (int i = 0; i < EPV; ++i) s2[i & 1] += weight_of(ft[i], fd[i], v * EPV + i, c, nrej);
+      s += s2[0] + s2[1];
     }
   }
   s = warp_sum(s);
@@ -460,11 +487,6 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
     sh.path[0] = 0;
   }
   const uint64_t bglob = b_base + (uint64_t)b;
-  for (int n = tid; n < M; n += kTwThreads) {
-    const Philox4 r = philox4x64_10((uint64_t)n + 1, bglob, offset, 0, seed, 0);
-    sh.uacc[n] = (double)u24(r.w[0]);
-    sh.usmp[n] = (double)u24(r.w[1]);
-  }
   tw::cluster_sync();  // the mbarriers of every CTA are ready
 
   const int64_t NV = V / EPV;  // rows are whole 16-byte vectors
@@ -484,13 +506,18 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
     }
     __syncthreads();
     const int nk = sh.nkids;
-    // the children's logits (every CTA alike) while the slice streams in
+    // the children's logits (every CTA alike), loaded with the slice
+    T g_t = T(0.f), g_d = T(0.f);
     if (tid < nk) {
       const int64_t o = ((int64_t)b * M + node) * V + sh.tok[sh.kids[tid]];
-      sh.gzt[tid] = to_f32(target[o]);
-      sh.gzd[tid] = to_f32(draft[o]);
+      g_t = target[o];
+      g_d = draft[o];
     }
     tw_slice_runs<T>(trow, has_kids ? drow : nullptr, v0, v1, cs, sh);
+    if (tid < nk) {
+      sh.gzt[tid] = to_f32(g_t);
+      sh.gzd[tid] = to_f32(g_d);
+    }
     if (tid == 0) {
       tw::Run rt = sh.rt[0], rd = sh.rd[0];
       for (int w = 1; w < kTwWarps; ++w) {
@@ -509,42 +536,47 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
     __syncthreads();
     if (!tw_exchange(sh, rank, limit, round)) break;
     const int par = (round - 1) & 1;
-    if (tid == 0) {
-      // the node's normalisers from the slices, in rank order
-      float mT = -INFINITY, mD = -INFINITY;
-      for (int r = 0; r < kTwCtas; ++r) {
-        mT = fmaxf(mT, __uint_as_float(sh.xbuf[par][r][0]));
-        mD = fmaxf(mD, __uint_as_float(sh.xbuf[par][r][3]));
+    if (warp == 0) {
+      // the node's normalisers from the slices: lane r < kTwCtas holds
+      // slice r; the same shuffles in every CTA give the same values
+      const bool live = lane < kTwCtas;
+      const uint32_t* x = sh.xbuf[par][live ? lane : 0];
+      const float mr = live ? __uint_as_float(x[0]) : -INFINITY;
+      const float sr = live ? __uint_as_float(x[1]) : 0.f;
+      const float mdr = live ? __uint_as_float(x[3]) : -INFINITY;
+      const float sdr = live ? __uint_as_float(x[4]) : 0.f;
+      const float mT = warp_max(mr), mD = warp_max(mdr);
+      const dfloat wt = mr == -INFINITY ? df_make(0.f)
+                                        : df_mul_f(df_make(sr), fast_exp2((mr - mT) * cs));
+      const dfloat wd = mdr == -INFINITY ? df_make(0.f)
+                                         : df_mul_f(df_make(sdr), fast_exp2((mdr - mD) * cs));
+      const dfloat sT = df_warp_sum(wt), sD = df_warp_sum(wd);
+      // the first slice (lowest indices) holding the maximum gives the argmax
+      const unsigned ht = __ballot_sync(0xffffffffu, live && mr == mT);
+      const unsigned hd = __ballot_sync(0xffffffffu, live && mdr == mD);
+      const int aT = __shfl_sync(0xffffffffu, live ? (int)x[2] : 0, ht ? __ffs(ht) - 1 : 0);
+      const int aD = __shfl_sync(0xffffffffu, live ? (int)x[5] : 0, hd ? __ffs(hd) - 1 : 0);
+      if (live) {
+        sh.wp[lane] = df_to_d(wt);
+        sh.wr[lane] = 0.0;
       }
-      dfloat sT = df_make(0.f), sD = df_make(0.f);
-      int aT = -1, aD = -1;
-      for (int r = 0; r < kTwCtas; ++r) {
-        const float mr = __uint_as_float(sh.xbuf[par][r][0]);
-        const float sr = __uint_as_float(sh.xbuf[par][r][1]);
-        const dfloat wt = mr == -INFINITY ? df_make(0.f)
-                                          : df_mul_f(df_make(sr), fast_exp2((mr - mT) * cs));
-        sT = df_add(sT, wt);
-        sh.wp[r] = df_to_d(wt);
-        if (aT < 0 && mr == mT) aT = (int)sh.xbuf[par][r][2];
-        const float mdr = __uint_as_float(sh.xbuf[par][r][3]);
-        const float sdr = __uint_as_float(sh.xbuf[par][r][4]);
-        if (mdr != -INFINITY) sD = df_add(sD, df_mul_f(df_make(sdr), fast_exp2((mdr - mD) * cs)));
-        if (aD < 0 && mdr == mD) aD = (int)sh.xbuf[par][r][5];
+      if (lane == 0) {
+        const double ST = df_to_d(sT), SD = df_to_d(sD);
+        sh.aT = ht == 0 || aT < 0 || aT >= V ? 0 : aT;
+        sh.aD = hd == 0 || aD < 0 || aD >= V ? 0 : aD;
+        ctx_no_filter(sh.ctx);
+        sh.ctx.mT = mT;
+        sh.ctx.invST = (float)(1.0 / ST);
+        sh.ctx.cs = cs;
+        sh.ctx.nrej = 0;
+        sh.ctx.mD = has_kids ? mD : 0.f;
+        sh.ctx.invSD = has_kids ? (float)(1.0 / SD) : 0.f;
+        sh.invZ64[0] = 1.0;
+        sh.ST = ST;
+        sh.SD = SD;
+        sh.invST64 = 1.0 / ST;
+        sh.invSD64 = 1.0 / SD;
       }
-      const double ST = df_to_d(sT), SD = df_to_d(sD);
-      for (int r = 0; r < kTwCtas; ++r) sh.wr[r] = 0.0;
-      sh.aT = aT < 0 || aT >= V ? 0 : aT;
-      sh.aD = aD < 0 || aD >= V ? 0 : aD;
-      ctx_no_filter(sh.ctx);
-      sh.ctx.mT = mT;
-      sh.ctx.invST = (float)(1.0 / ST);
-      sh.ctx.cs = cs;
-      sh.ctx.nrej = 0;
-      sh.ctx.mD = has_kids ? mD : 0.f;
-      sh.ctx.invSD = has_kids ? (float)(1.0 / SD) : 0.f;
-      sh.invZ64[0] = 1.0;
-      sh.ST = ST;
-      sh.SD = SD;
     }
     __syncthreads();
     if (tid < nk) {
@@ -555,11 +587,14 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
       }
     }
     if (!greedy && tid < nk) {
-      const double ST = sh.ST, SD = sh.SD;
+      // P(x), Q(x) of each child, and its accept uniform (counter word 0:
+      // the child's node index + 1)
       const double et = ((double)sh.gzt[tid] - (double)sh.ctx.mT) * cs64;
       const double ed = ((double)sh.gzd[tid] - (double)sh.ctx.mD) * cs64;
-      sh.qx[tid] = tw::exp2_split(ed) / SD;
-      sh.px[tid] = tw::exp2_split(et) / ST;
+      sh.qx[tid] = tw::exp2_split(ed) * sh.invSD64;
+      sh.px[tid] = tw::exp2_split(et) * sh.invST64;
+      const Philox4 r = philox4x64_10((uint64_t)sh.kids[tid] + 1, bglob, offset, 0, seed, 0);
+      sh.uk[tid] = (double)u24(r.w[0]);
     }
     __syncthreads();
     // ---- the children in order ---------------------------------------------
@@ -581,7 +616,7 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
           const double Q = sh.qx[i];
           double P = sh.px[i];
           for (int j = 1; j <= sh.ctx.nrej; ++j) P = fmax(P - Q, 0.0) * sh.invZ64[j];
-          acc = sh.uacc[c] * Q < P;
+          acc = sh.uk[i] * Q < P;
           sh.probe[c][0] = (float)P;
           sh.probe[c][1] = (float)Q;
         }
@@ -595,25 +630,26 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
         const int nrej_next = sh.ctx.nrej + 1;
         tw_slice_mass<T>(trow, drow, v0, v1, sh.ctx, nrej_next, sh);
         if (!tw_exchange(sh, rank, limit, round)) break;
-        if (tid == 0) {
+        if (warp == 0) {
           const int p2 = (round - 1) & 1;
-          dfloat Zd = df_make(0.f);
-          for (int r = 0; r < kTwCtas; ++r) {
-            const dfloat zr{__uint_as_float(sh.xbuf[p2][r][0]), __uint_as_float(sh.xbuf[p2][r][1])};
-            Zd = df_add(Zd, zr);
-            sh.wr[r] = df_to_d(zr);
-          }
-          const double Z = df_to_d(Zd);
-          if (Z > 0.0) {
-            const int j = nrej_next;
-            sh.ctx.nrej = j;
-            sh.ctx.invZ[j] = (float)(1.0 / Z);
-            sh.ctx.Z[j] = Z;
-            sh.invZ64[j] = 1.0 / Z;
-            sh.Zdraw = Z;
-          } else {
-            // a residual of zero mass: back to p of the node
-            sh.ctx.nrej = 0;
+          const bool live = lane < kTwCtas;
+          const dfloat zr = live ? dfloat{__uint_as_float(sh.xbuf[p2][lane][0]),
+                                          __uint_as_float(sh.xbuf[p2][lane][1])}
+                                 : df_make(0.f);
+          const dfloat Zd = df_warp_sum(zr);
+          if (live) sh.wr[lane] = df_to_d(zr);
+          if (lane == 0) {
+            const double Z = df_to_d(Zd);
+            if (Z > 0.0) {
+              const int j = nrej_next;
+              sh.ctx.nrej = j;
+              sh.ctx.Z[j] = Z;
+              sh.invZ64[j] = 1.0 / Z;
+              sh.ctx.invZ[j] = (float)sh.invZ64[j];
+            } else {
+              // a residual of zero mass: back to p of the node
+              sh.ctx.nrej = 0;
+            }
           }
         }
       }
@@ -652,7 +688,8 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
       const double* wm = nrej > 0 ? sh.wr : sh.wp;
       double Z = 0.0;
       for (int r = 0; r < kTwCtas; ++r) Z += wm[r];
-      const double t = sh.usmp[node] * Z;
+      const Philox4 r = philox4x64_10((uint64_t)node + 1, bglob, offset, 0, seed, 0);
+      const double t = (double)u24(r.w[1]) * Z;
       int owner = -1, lastpos = -1;
       double pre = 0.0, pre_owner = 0.0, pre_last = 0.0;
       for (int r = 0; r < kTwCtas; ++r) {

@@ -140,12 +140,10 @@ struct Smem {
   double px[kMaxNodes], qx[kMaxNodes];  // per child of the node (position in kids)
   float gzt[kMaxNodes], gzd[kMaxNodes];
   double uk[kMaxNodes];  // accept uniform of each child of the node (position in kids)
-  double ST, invST64, invSD64;
   DecideCtx ctx;
   double invZ64[kMaxNodes + 1];
-  double wp[kTwCtas];                   // mass of p of the node per slice
-  double wr[kTwCtas];                   // mass of the last residual per slice
-  double SD;                            // the node's row sums: ST above
+  dfloat wp[kTwCtas];                   // mass of p of the node per slice
+  dfloat wr[kTwCtas];                   // mass of the last residual per slice
   Run rt[kTwWarps], rd[kTwWarps];
   float rz[kTwWarps];
   dfloat scan[kTwWarps];
@@ -154,7 +152,7 @@ struct Smem {
   int aT, aD;
   int owner, tok_out;
   float w_out;
-  double trel, Zdraw;
+  dfloat trel, Zdraw;
   int tile_hit, last_pos;
 };
 
@@ -318,7 +316,7 @@ __device__ void tw_slice_draw(const T* trow, const T* drow, int64_t v0, int64_t 
                               const DecideCtx& c, int nrej, tw::Smem& sh) {
   constexpr int EPV = 16 / sizeof(T);
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-  double rem_d = sh.trel;
+  dfloat rem = sh.trel;
   if (tid == 0) {
     sh.last_pos = -1;
     sh.tok_out = -1;
@@ -356,8 +354,6 @@ __device__ void tw_slice_draw(const T* trow, const T* drow, int64_t v0, int64_t 
     }
     incl = df_add(incl, wbase);
     const dfloat excl = df_sub(incl, df_make(ts));
-    const float rh = (float)rem_d;
-    const dfloat rem{rh, (float)(rem_d - (double)rh)};
     const bool hit = ts > 0.f && !df_gt(excl, rem) && df_gt(incl, rem);
     const unsigned hb = __ballot_sync(0xffffffffu, hit);
     const unsigned pb = __ballot_sync(0xffffffffu, ts > 0.f);
@@ -386,7 +382,7 @@ __device__ void tw_slice_draw(const T* trow, const T* drow, int64_t v0, int64_t 
       __syncthreads();
       return;
     }
-    rem_d -= df_to_d(total);
+    rem = df_sub(rem, total);
     __syncthreads();
   }
   // rounding at the very top: the last element of positive weight in the
@@ -442,7 +438,7 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
     sh.owner = -3;
     sh.tok_out = -1;
     sh.w_out = 0.f;
-    sh.Zdraw = 1.0;
+    sh.Zdraw = df_make(1.f);
     sh.moved = 0;
   }
   __syncthreads();
@@ -557,52 +553,49 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
       const int aT = __shfl_sync(0xffffffffu, live ? (int)x[2] : 0, ht ? __ffs(ht) - 1 : 0);
       const int aD = __shfl_sync(0xffffffffu, live ? (int)x[5] : 0, hd ? __ffs(hd) - 1 : 0);
       if (live) {
-        sh.wp[lane] = df_to_d(wt);
-        sh.wr[lane] = 0.0;
+        sh.wp[lane] = wt;
+        sh.wr[lane] = df_make(0.f);
+      }
+      // the children's P(x), Q(x) and accept uniforms (counter word 0: the
+      // child's node index + 1), one child a lane; the row sums' reciprocals
+      // meanwhile on the last two lanes (fp64 is slow here: its dependent
+      // chains are kept short and side by side)
+      double inv = 0.0;
+      if (lane == kWarp - 1) inv = 1.0 / df_to_d(sT);
+      if (lane == kWarp - 2) inv = has_kids ? 1.0 / df_to_d(sD) : 0.0;
+      const double invST = __shfl_sync(0xffffffffu, inv, kWarp - 1);
+      const double invSD = __shfl_sync(0xffffffffu, inv, kWarp - 2);
+      for (int i = lane; i < nk; i += kWarp) {
+        const int x = sh.tok[sh.kids[i]];
+        if (greedy) {
+          sh.px[i] = x == aT ? 1.0 : 0.0;
+          sh.qx[i] = x == aD ? 1.0 : 0.0;
+        } else {
+          const double et = ((double)sh.gzt[i] - (double)mT) * cs64;
+          const double ed = ((double)sh.gzd[i] - (double)mD) * cs64;
+          sh.px[i] = tw::exp2_split(et) * invST;
+          sh.qx[i] = tw::exp2_split(ed) * invSD;
+          const Philox4 r = philox4x64_10((uint64_t)sh.kids[i] + 1, bglob, offset, 0, seed, 0);
+          sh.uk[i] = (double)u24(r.w[0]);
+        }
       }
       if (lane == 0) {
-        const double ST = df_to_d(sT), SD = df_to_d(sD);
         sh.aT = ht == 0 || aT < 0 || aT >= V ? 0 : aT;
         sh.aD = hd == 0 || aD < 0 || aD >= V ? 0 : aD;
         ctx_no_filter(sh.ctx);
         sh.ctx.mT = mT;
-        sh.ctx.invST = (float)(1.0 / ST);
+        sh.ctx.invST = (float)invST;
         sh.ctx.cs = cs;
         sh.ctx.nrej = 0;
         sh.ctx.mD = has_kids ? mD : 0.f;
-        sh.ctx.invSD = has_kids ? (float)(1.0 / SD) : 0.f;
+        sh.ctx.invSD = has_kids ? (float)invSD : 0.f;
         sh.invZ64[0] = 1.0;
-        sh.ST = ST;
-        sh.SD = SD;
-        sh.invST64 = 1.0 / ST;
-        sh.invSD64 = 1.0 / SD;
+        sh.child_i = 0;
+        sh.moved = 0;
       }
-    }
-    __syncthreads();
-    if (tid < nk) {
-      if (greedy) {
-        const int x = sh.tok[sh.kids[tid]];
-        sh.px[tid] = x == sh.aT ? 1.0 : 0.0;
-        sh.qx[tid] = x == sh.aD ? 1.0 : 0.0;
-      }
-    }
-    if (!greedy && tid < nk) {
-      // P(x), Q(x) of each child, and its accept uniform (counter word 0:
-      // the child's node index + 1)
-      const double et = ((double)sh.gzt[tid] - (double)sh.ctx.mT) * cs64;
-      const double ed = ((double)sh.gzd[tid] - (double)sh.ctx.mD) * cs64;
-      sh.qx[tid] = tw::exp2_split(ed) * sh.invSD64;
-      sh.px[tid] = tw::exp2_split(et) * sh.invST64;
-      const Philox4 r = philox4x64_10((uint64_t)sh.kids[tid] + 1, bglob, offset, 0, seed, 0);
-      sh.uk[tid] = (double)u24(r.w[0]);
     }
     __syncthreads();
     // ---- the children in order ---------------------------------------------
-    if (tid == 0) {
-      sh.child_i = 0;
-      sh.moved = 0;
-    }
-    __syncthreads();
     while (sh.child_i < nk) {
       const int i = sh.child_i;
       const int c = sh.kids[i];
@@ -637,7 +630,7 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
                                           __uint_as_float(sh.xbuf[p2][lane][1])}
                                  : df_make(0.f);
           const dfloat Zd = df_warp_sum(zr);
-          if (live) sh.wr[lane] = df_to_d(zr);
+          if (live) sh.wr[lane] = zr;
           if (lane == 0) {
             const double Z = df_to_d(Zd);
             if (Z > 0.0) {
@@ -675,43 +668,34 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
         sh.owner = -1;
         sh.tok_out = sh.aT;
         sh.w_out = 1.f;
-        sh.Zdraw = 1.0;
+        sh.Zdraw = df_make(1.f);
         sh.probe[node][2] = 1.f;
         sh.probe[node][3] = 1.f;
       }
       __syncthreads();
       break;
     }
-    if (tid == 0) {
+    if (warp == 0) {
+      // the slice holding u * Z: the first of positive mass whose running
+      // mass (in rank order) exceeds it, else the last of positive mass
       const int nrej = sh.ctx.nrej;
-      // the slices' masses: of the last residual, or of p of the node
-      const double* wm = nrej > 0 ? sh.wr : sh.wp;
-      double Z = 0.0;
-      for (int r = 0; r < kTwCtas; ++r) Z += wm[r];
+      const bool live = lane < kTwCtas;
+      const dfloat w = live ? (nrej > 0 ? sh.wr[lane] : sh.wp[lane]) : df_make(0.f);
+      const dfloat incl = df_warp_scan(w);
+      const dfloat Z = df_shfl(incl, kWarp - 1);
       const Philox4 r = philox4x64_10((uint64_t)node + 1, bglob, offset, 0, seed, 0);
-      const double t = (double)u24(r.w[1]) * Z;
-      int owner = -1, lastpos = -1;
-      double pre = 0.0, pre_owner = 0.0, pre_last = 0.0;
-      for (int r = 0; r < kTwCtas; ++r) {
-        const double w = wm[r];
-        if (w > 0.0) {
-          if (owner < 0 && pre + w > t) {
-            owner = r;
-            pre_owner = pre;
-          }
-          lastpos = r;
-          pre_last = pre;
-        }
-        pre += w;
+      const dfloat t = df_mul_f(Z, u24(r.w[1]));
+      const bool pos = live && w.hi > 0.f;
+      const unsigned hit = __ballot_sync(0xffffffffu, pos && df_gt(incl, t));
+      const unsigned pb = __ballot_sync(0xffffffffu, pos);
+      const int owner = hit ? __ffs(hit) - 1 : (pb ? 31 - __clz(pb) : 0);
+      const dfloat excl = df_shfl(df_sub(incl, w), owner);
+      if (lane == 0) {
+        sh.owner = owner;
+        sh.trel = df_sub(t, excl);
+        sh.Zdraw = Z;
+        sh.probe[node][2] = nrej > 0 ? (float)sh.ctx.Z[nrej] : 1.f;
       }
-      if (owner < 0) {
-        owner = lastpos < 0 ? 0 : lastpos;
-        pre_owner = lastpos < 0 ? 0.0 : pre_last;
-      }
-      sh.owner = owner;
-      sh.trel = t - pre_owner;
-      sh.Zdraw = Z;
-      sh.probe[node][2] = nrej > 0 ? (float)sh.ctx.Z[nrej] : 1.f;
     }
     __syncthreads();
     if (sh.owner == rank) tw_slice_draw<T>(trow, drow, v0, v1, sh.ctx, sh.ctx.nrej, sh);
@@ -770,7 +754,7 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
       path[(int64_t)b * M + n] = fail ? -1 : sh.path[n];
       if (probe != nullptr) {
         float pv[4] = {sh.probe[n][0], sh.probe[n][1], sh.probe[n][2], sh.probe[n][3]};
-        if (!fail && n == sh.node && !greedy) pv[3] = (float)((double)wtok / sh.Zdraw);
+        if (!fail && n == sh.node && !greedy) pv[3] = wtok / df_to_f(sh.Zdraw);
         for (int k = 0; k < 4; ++k) probe[((int64_t)b * M + n) * 4 + k] = fail ? -1.f : pv[k];
       }
     }

@@ -48,7 +48,7 @@ BAR_WORKLOADS = ("stress_gqa_152k", "chain_gqa_128k")
 # the 128 requests of the default workload and scaled to 128 by the
 # algorithmic bytes (traffic grows with the KV bytes read).  Valid only for
 # the attention kernel sources whose digest is recorded with it.
-TRAFFIC = {"digest": "7690e82e2badf8c4", "bytes_per_call": 10104562368}
+TRAFFIC = {"digest": "fe3f2ab1fed2d51f", "bytes_per_call": 10104592002}
 TRAFFIC_ALG_BYTES = 10051956736  # algorithmic bytes per call of that workload (seed 0)
 
 

@@ -86,6 +86,30 @@ def test_reject_wait_gives_up_then_recovers(impl):
     compare_reject(g, o)
 
 
+def test_tree_walk_wait_gives_up_then_recovers():
+    # trees of aligned rows: the statistics stream and the cluster walk,
+    # whose exchanges wait (bounded) on mbarriers that the other CTAs of the
+    # cluster arrive on; after a wait gives up the walk still meets the
+    # cluster barrier at its end, and every request of the call fails
+    wl = workload("tree_64")
+    lg = logits_inputs(wl, seed=34)
+    B, M, V = lg["target"].shape
+    dims = dims_for(wl, B, V=V)
+    dims.wait_limit_kcycles = TINY
+    ws = sv.workspace(dims)
+    _flush_l2()
+    g = gpu_reject(wl, lg, seed=6, offset=0, dims=dims, ws=ws)
+    assert g["status"] & TIMEOUT_BIT
+    assert np.all(g["accepted_len"] == -1)
+    dims.wait_limit_kcycles = 0
+    ws = sv.workspace(dims)
+    g = gpu_reject(wl, lg, seed=6, offset=1, dims=dims, ws=ws)
+    assert g["status"] == 0
+    o = oracle_reject_sample(lg["target"], lg["draft"], lg["tokens"], lg["parent"],
+                             lg["temperature"], 6, 1)
+    compare_reject(g, o)
+
+
 def test_noalloc_wait_gives_up_then_recovers():
     # the no-allocation entry point cannot report its status word: a wait
     # that gave up shows as accepted_len = -1 for the requests it touched

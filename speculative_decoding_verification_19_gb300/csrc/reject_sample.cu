@@ -893,7 +893,7 @@ __device__ void draw_from_p(const T* trow, const RowStat* st, int n_chunks, int 
 // double-floats, and the owning lane's elements are spread over the warp
 // (one 32-bit word per lane) and scanned again.  Same law and rounding-gap
 // rule as chunk_draw.
-template <typename T>
+template <typename T, bool kFilt = true>
 __device__ __forceinline__ float lane_weights(const T* trow, const T* drow, int64_t e0, int V,
                                               const DecideCtx& c, int nrej,
                                               uint4 (&raw_t)[kStatVecs], uint4 (&raw_d)[kStatVecs]) {
@@ -916,7 +916,7 @@ __device__ __forceinline__ float lane_weights(const T* trow, const T* drow, int6
     unpack16(raw_t[v], zt);
     unpack16(raw_d[v], zd);
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) s += weight_of(zt[i], zd[i], e + v * EPV + i, c, nrej);
+    for (int i = 0; i < EPV; ++i) s += weight_sel<kFilt>(zt[i], zd[i], e + v * EPV + i, c, nrej);
   }
   return s;
 }
@@ -925,7 +925,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <typename T>
+template <typename T, bool kFilt = true>
 __device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
                                const DecideCtx& c, int nrej, dfloat trel, float* w_out) {
   constexpr int EPV = 16 / sizeof(T);
@@ -933,7 +933,7 @@ __device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
   constexpr int EW = 4 / sizeof(T);   // elements per 32-bit word
   const int lane = threadIdx.x % kWarp;
   uint4 raw_t[kStatVecs], raw_d[kStatVecs];
-  const float vs = lane_weights<T>(trow, drow, e0, V, c, nrej, raw_t, raw_d);
+  const float vs = lane_weights<T, kFilt>(trow, drow, e0, V, c, nrej, raw_t, raw_d);
   const dfloat incl = df_warp_scan(df_make(vs));
   const dfloat excl = df_sub(incl, df_make(vs));
   const unsigned hit =
@@ -967,7 +967,7 @@ __device__ int warp_chunk_draw(const T* trow, const T* drow, int64_t e0, int V,
       zd = __uint_as_float(wd);
     }
     const bool in = seg + lane * EW + i < V;
-    w[i] = in ? weight_of(zt, zd, seg + lane * EW + i, c, nrej) : 0.f;
+    w[i] = in ? weight_sel<kFilt>(zt, zd, seg + lane * EW + i, c, nrej) : 0.f;
     ls += w[i];
   }
   const dfloat cum = df_warp_scan(df_make(ls));
@@ -1756,9 +1756,9 @@ struct TailSmem {
   float st_m[kTailStage];
   float st_s[kTailStage];
   int st_a[kTailStage];
-  double zs[kTailStage / 4];  // the last slice: the residual's chunk masses
   float rowM[2][kMaxM];
   double rowS[2][kMaxM];
+  float rowInv[2][kMaxM];  // (float)(1 / rowS), formed once per row
   int rowA[2][kMaxM];
   int tok[kMaxM];
   float gzt[kMaxM], gzd[kMaxM];
@@ -1901,14 +1901,17 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       float mx = -INFINITY;
       for (int c = lane; c < n_chunks; c += kWarp) mx = fmaxf(mx, rm[c]);
       m = warp_max(mx);
-      double acc = 0.0;
+      // the rescaled chunk sums in double-float (products exact by FMA):
+      // fp64 arithmetic is slow on this part
+      dfloat acc = df_make(0.f);
       int cf = 0x7fffffff;
       for (int c = lane; c < n_chunks; c += kWarp) {
         if (rm[c] != -INFINITY)
-          acc += (double)sh.st_s[r * n_chunks + c] * (double)fast_exp2((rm[c] - m) * cs);
+          acc = df_add(acc, df_prod(sh.st_s[r * n_chunks + c], fast_exp2((rm[c] - m) * cs)));
         if (rm[c] == m && c < cf) cf = c;
       }
-      sm = warp_sum(acc);
+      acc = df_warp_sum(acc);
+      sm = lane == 0 ? df_to_d(acc) : 0.0;
       cf = __reduce_min_sync(0xffffffffu, cf);
       am = cf < n_chunks ? cf * chunk + sh.st_a[r * n_chunks + cf] : 0;
     } else {
@@ -1918,6 +1921,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     if (lane == 0) {
       sh.rowM[which][n] = m;
       sh.rowS[which][n] = sm;
+      sh.rowInv[which][n] = (float)(1.0 / sm);
       sh.rowA[which][n] = am;
       if (!(isfinite(m) && sm > 0.0 && isfinite(sm))) atomicOr(&sh.bad, 4);
     }
@@ -2002,7 +2006,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   DecideCtx c;
   ctx_no_filter(c);
   c.mT = sh.rowM[0][a];
-  c.invST = (float)(1.0 / sh.rowS[0][a]);
+  c.invST = sh.rowInv[0][a];
   c.cs = cs;
   const T* trow = target + ((int64_t)b * M + a) * V;
   if (fr == M) {
@@ -2026,17 +2030,17 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   }
   // a rejection: the residual max(0, p_a - q_a), this slice's chunks
   c.mD = sh.rowM[1][a];
-  c.invSD = (float)(1.0 / sh.rowS[1][a]);
+  c.invSD = sh.rowInv[1][a];
   c.nrej = 1;
   const T* drow = draft + ((int64_t)b * M + a) * V;
   double* zs = zsum + (int64_t)b * n_chunks;
   const int c0 = (int)((int64_t)n_chunks * s / S), c1 = (int)((int64_t)n_chunks * (s + 1) / S);
   for (int cc = c0 + warp; cc < c1; cc += kTailWarps) {
     uint4 raw_t[kStatVecs], raw_d[kStatVecs];
-    const float ls = lane_weights<T>(trow, drow, (int64_t)cc * chunk, V, c, 1, raw_t, raw_d);
+    const float ls = lane_weights<T, false>(trow, drow, (int64_t)cc * chunk, V, c, 1, raw_t, raw_d);
     const dfloat tot = df_warp_sum(df_make(ls));
     if (lane == 0) {
-      zs[cc] = df_to_d(tot);
+      reinterpret_cast<float2*>(zs)[cc] = make_float2(tot.hi, tot.lo);
       __threadfence();  // the mass before this slice's count
     }
   }
@@ -2050,41 +2054,67 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   // the last slice: the chunk from the masses (all loaded at once into
   // shared memory when they fit), then the token
   __threadfence();
-  const bool zsh = n_chunks <= kTailStage / 4;
-  if (zsh) {
-    for (int k = tid; k < n_chunks; k += kTailThreads) sh.zs[k] = __ldcg(zs + k);
-    __syncthreads();
-  }
+  // the masses (double-floats) one chunk a lane, scanned in order: the
+  // first chunk of positive mass whose running mass exceeds u * Z, else the
+  // last of positive mass
   if (warp != 0) return;
-  double Z = 0.0;
-  for (int k = lane; k < n_chunks; k += kWarp) Z += zsh ? sh.zs[k] : __ldcg(zs + k);
-  Z = warp_sum(Z);
+  const float2* zf = reinterpret_cast<const float2*>(zs);
+  dfloat Zd = df_make(0.f);
+  for (int k = lane; k < n_chunks; k += kWarp) {
+    const float2 v = __ldcg(zf + k);
+    Zd = df_add(Zd, dfloat{v.x, v.y});
+  }
+  Zd = df_warp_sum(Zd);
   float w;
   int tk;
-  double zrep;
-  if (Z > 0.0) {
-    double pre;
-    const int sel = zsh ? warp_select_chunk<true>(sh.zs, n_chunks, u * Z, &pre)
-                        : warp_select_chunk(zs, n_chunks, u * Z, &pre);
-    const double trel = u * Z - pre;
-    const float th = (float)trel;
-    tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, c, 1,
-                            dfloat{th, (float)(trel - (double)th)}, &w);
-    zrep = Z;
+  float Zrep, zden;
+  if (Zd.hi > 0.f) {
+    const dfloat t = df_mul_f(Zd, (float)u);  // u is a 24-bit fraction: exact in fp32
+    dfloat base = df_make(0.f), sel_pre = df_make(0.f), last_pre = df_make(0.f);
+    int sel = -1, lastpos = -1;
+    for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
+      const int k = k0 + lane;
+      const float2 v = k < n_chunks ? __ldcg(zf + k) : make_float2(0.f, 0.f);
+      const dfloat wk{v.x, v.y};
+      const dfloat incl = df_add(base, df_warp_scan(wk));
+      const dfloat excl = df_sub(incl, wk);
+      const bool pos = wk.hi > 0.f;
+      const unsigned hit = __ballot_sync(0xffffffffu, pos && df_gt(incl, t));
+      const unsigned pb = __ballot_sync(0xffffffffu, pos);
+      if (pb) {
+        const int l = 31 - __clz(pb);
+        lastpos = k0 + l;
+        last_pre = df_shfl(excl, l);
+      }
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        sel = k0 + l;
+        sel_pre = df_shfl(excl, l);
+      }
+      base = df_shfl(incl, kWarp - 1);
+    }
+    if (sel < 0) {  // rounding at the very top: the last chunk with mass
+      sel = lastpos < 0 ? 0 : lastpos;
+      sel_pre = lastpos < 0 ? df_make(0.f) : last_pre;
+    }
+    tk = warp_chunk_draw<T, false>(trow, drow, (int64_t)sel * chunk, V, c, 1, df_sub(t, sel_pre),
+                                   &w);
+    Zrep = df_to_f(Zd);
+    zden = Zrep;
   } else {
     // a residual of zero mass: the draw from p of the node
     c.nrej = 0;
     double z;
     const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
     tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &w, &z);
-    zrep = z;
-    Z = 1.0;
+    zden = (float)z;
+    Zrep = 1.f;
   }
   if (lane == 0) {
     ot[a] = tk;
     if (pr != nullptr) {
-      pr[a * 4 + 2] = (float)Z;
-      pr[a * 4 + 3] = (float)((double)w / zrep);
+      pr[a * 4 + 2] = Zrep;
+      pr[a * 4 + 3] = w / zden;
     }
     done_cnt[b] = 0u;  // ready for the next call
   }
@@ -2502,7 +2532,7 @@ __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
   const int c1 = min(n_chunks, (g + 1) * kFUnit);
   for (int c = g * kFUnit; c < c1; ++c) {
     uint4 raw_t[kStatVecs], raw_d[kStatVecs];
-    const float ls = lane_weights<T>(trow, drow, (int64_t)c * chunk, V, ctx, 1, raw_t, raw_d);
+    const float ls = lane_weights<T, false>(trow, drow, (int64_t)c * chunk, V, ctx, 1, raw_t, raw_d);
     const dfloat tot = df_warp_sum(df_make(ls));
     if (lane == 0) zs[c] = df_to_d(tot);
   }
@@ -2527,7 +2557,7 @@ __device__ __noinline__ bool fused_residual_unit(const T* __restrict__ target,
     const int sel = warp_select_chunk(zs, n_chunks, u * Z, &pre);
     const double trel = u * Z - pre;
     const float th = (float)trel;
-    tk = warp_chunk_draw<T>(trow, drow, (int64_t)sel * chunk, V, ctx, 1,
+    tk = warp_chunk_draw<T, false>(trow, drow, (int64_t)sel * chunk, V, ctx, 1,
                             dfloat{th, (float)(trel - (double)th)}, &wt);
     zrep = Z;
   } else {

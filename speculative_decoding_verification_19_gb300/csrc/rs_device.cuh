@@ -50,6 +50,11 @@ __device__ __forceinline__ bool df_gt(dfloat a, dfloat b) {
   return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
 }
 __device__ __forceinline__ float df_to_f(dfloat x) { return __fadd_rn(x.hi, x.lo); }
+// a * b exactly, as a double-float (the rounding error by one FMA)
+__device__ __forceinline__ dfloat df_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return dfloat{p, fmaf(a, b, -p)};
+}
 __device__ __forceinline__ double df_to_d(dfloat x) { return (double)x.hi + (double)x.lo; }
 __device__ __forceinline__ dfloat df_shfl_xor(dfloat x, int o) {
   return dfloat{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
@@ -163,6 +168,23 @@ __device__ __forceinline__ float weight_of(float zt, float zd, int64_t e, const 
   float P = et * c.invST;
   for (int j = 1; j < nrej; ++j) P = fmaxf(P - qv, 0.f) * c.invZ[j];
   return fmaxf(P - qv, 0.f);
+}
+
+// weight_of for laws without filters: the same operations in the same order
+// (every token is kept), without the per-element index compares.
+__device__ __forceinline__ float weight_plain(float zt, float zd, const DecideCtx& c, int nrej) {
+  const float et = fast_exp2((zt - c.mT) * c.cs);
+  if (nrej == 0) return et;
+  const float qv = fast_exp2((zd - c.mD) * c.cs) * c.invSD;
+  float P = et * c.invST;
+  for (int j = 1; j < nrej; ++j) P = fmaxf(P - qv, 0.f) * c.invZ[j];
+  return fmaxf(P - qv, 0.f);
+}
+// weight_of, or weight_plain when the law is known to have no filter.
+template <bool kFilt>
+__device__ __forceinline__ float weight_sel(float zt, float zd, int64_t e, const DecideCtx& c,
+                                            int nrej) {
+  return kFilt ? weight_of(zt, zd, e, c, nrej) : weight_plain(zt, zd, c, nrej);
 }
 
 // Mass of a chunk of the node's target row under exp2((z - mT) * cs), from

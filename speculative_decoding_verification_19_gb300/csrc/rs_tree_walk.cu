@@ -290,7 +290,7 @@ __device__ float tw_slice_mass(const T* trow, const T* drow, int64_t v0, int64_t
       unpack16(xd[k], fd);
       float s2[2] = {0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) s2[i & 1] += weight_of(ft[i], fd[i], v * EPV + i, c, nrej);
+      for (int i = 0; i < EPV; ++i) s2[i & 1] += weight_plain(ft[i], fd[i], c, nrej);
       s += s2[0] + s2[1];
     }
   }
@@ -335,7 +335,7 @@ __device__ void tw_slice_draw(const T* trow, const T* drow, int64_t v0, int64_t 
       unpack16(xd, fd);
 #pragma unroll
       for (int i = 0; i < EPV; ++i) {
-        w[i] = weight_of(ft[i], fd[i], v * EPV + i, c, nrej);
+        w[i] = weight_plain(ft[i], fd[i], c, nrej);
         ts += w[i];
       }
     } else {
@@ -396,7 +396,7 @@ __device__ void tw_slice_draw(const T* trow, const T* drow, int64_t v0, int64_t 
     unpack16(xt, ft);
     unpack16(xd, fd);
     for (int i = EPV - 1; i >= 0; --i) {
-      const float wi = weight_of(ft[i], fd[i], v * EPV + i, c, nrej);
+      const float wi = weight_plain(ft[i], fd[i], c, nrej);
       if (wi > 0.f) {
         sh.tok_out = (int)(v * EPV + i);
         sh.w_out = wi;

@@ -91,8 +91,10 @@ def test_maximum_sizes(B, gamma, V, dtype):
 
 
 @pytest.mark.parametrize("impl", TREE_IMPLS)
-@pytest.mark.parametrize("V", [64, 32000])
+@pytest.mark.parametrize("V", [64, 1001, 32000])
 def test_trees(V, impl):
+    # V = 1001: bf16 rows of 2002 bytes are not 16-byte vectors, so the tree
+    # takes the staged kernels; the others take the cluster walk
     wl = workload("tree_64").scaled(B=6, V=V)
     lg = logits_inputs(wl, seed=3)
     for offset in range(4):

@@ -1766,7 +1766,78 @@ struct TailSmem {
   int first_rej;
   int last;
   int bad;  // bit 0: argument, bit 1: token, bit 2: row without a distribution
+  // the last slice's draw
+  dfloat dscan[kTailWarps];
+  dfloat trel;
+  int sel, zero, hit, lastp, tok_out;
+  float w_out, Zf;
 };
+
+// Inverse CDF inside statistics chunk [e0, e0 + chunk) of the residual of
+// node a, by the whole CTA (the last slice): thread t takes the chunk's
+// 16-byte vector t of both rows (every chunk of an aligned row is whole
+// vectors, the last one maybe shorter), the threads' sums are scanned in
+// double-float, and the thread whose interval holds trel walks its
+// elements to the first whose running sum exceeds it; a rounding gap falls
+// back to the last element of positive weight.  sh.tok_out / sh.w_out get
+// the token and its weight.
+template <typename T>
+__device__ void tail_block_draw(const T* trow, const T* drow, int64_t e0, int V,
+                                const DecideCtx& c, dfloat trel, TailSmem& sh) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  const int64_t e = e0 + (int64_t)tid * EPV;
+  float w[EPV];
+  float ts = 0.f;
+  if (e < V) {
+    const uint4 xt = __ldg(reinterpret_cast<const uint4*>(trow + e));
+    const uint4 xd = __ldg(reinterpret_cast<const uint4*>(drow + e));
+    float ft[EPV], fd[EPV];
+    unpack16(xt, ft);
+    unpack16(xd, fd);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      w[i] = weight_plain(ft[i], fd[i], c, 1);
+      ts += w[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) w[i] = 0.f;
+  }
+  dfloat incl = df_warp_scan(df_make(ts));
+  if (lane == kWarp - 1) sh.dscan[warp] = incl;
+  if (tid == 0) {
+    sh.hit = 0x7fffffff;
+    sh.lastp = -1;
+  }
+  __syncthreads();
+  dfloat base = df_make(0.f);
+  for (int k = 0; k < warp; ++k) base = df_add(base, sh.dscan[k]);
+  incl = df_add(incl, base);
+  const dfloat excl = df_sub(incl, df_make(ts));
+  if (ts > 0.f && !df_gt(excl, trel) && df_gt(incl, trel)) atomicMin(&sh.hit, tid);
+  if (ts > 0.f) atomicMax(&sh.lastp, tid);
+  __syncthreads();
+  const bool gap = sh.hit == 0x7fffffff;
+  const int owner = gap ? (sh.lastp < 0 ? 0 : sh.lastp) : sh.hit;
+  if (tid == owner) {
+    dfloat cum = excl;
+    int k = -1, klast = -1;
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      if (w[i] > 0.f) {
+        klast = i;
+        cum = df_add(cum, df_make(w[i]));
+        if (k < 0 && df_gt(cum, trel)) k = i;
+      }
+    }
+    if (k < 0 || gap) k = klast;
+    if (k < 0) k = 0;
+    sh.tok_out = (int)(e + k);
+    sh.w_out = w[k];
+  }
+  __syncthreads();
+}
 
 // Row normaliser (m, S, first argmax) of one row by one warp from its chunk
 // statistics, formed as rs_decide_kernel forms it: fp32 maximum, fp64 sum of
@@ -1949,25 +2020,31 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     } else {
       const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
       const float uacc = (float)u24(r.w[0]);
-      const double cs64 = (double)cs;
-      const double et = ((double)sh.gzt[tid] - (double)sh.rowM[0][p]) * cs64;
-      const double ed = ((double)sh.gzd[tid] - (double)sh.rowM[1][p]) * cs64;
+      const float zt = sh.gzt[tid], zd = sh.gzd[tid];
       const float st_f = (float)sh.rowS[0][p], sd_f = (float)sh.rowS[1][p];
+      const bool t_inf = zt == -INFINITY, d_inf = zd == -INFINITY;
+      // the exponents of p(x), q(x) (log2 of the unnormalised terms) and of
+      // their ratio in double-float (the differences exact, the products by
+      // FMA), split into integer and fraction, so that one fp32 exp2 gives
+      // the ratio to about 3e-7 relative
+      const dfloat et = df_mul_f(df_two_sum(zt, -sh.rowM[0][p]), cs);
+      const dfloat ed = df_mul_f(df_two_sum(zd, -sh.rowM[1][p]), cs);
       bool acc;
-      if (ed == -INFINITY) {
-        acc = et != -INFINITY;
-      } else if (et == -INFINITY) {
-        acc = false;
+      if (d_inf) {
+        acc = !t_inf;  // q(x) = 0: accepted iff p(x) > 0
+      } else if (t_inf) {
+        acc = false;   // p(x) = 0 < u q(x)
       } else {
-        const double e = et - ed;
-        const double ei = rint(e);
+        const dfloat e = df_sub(et, ed);
+        const float ei = rintf(e.hi);
+        const float f = (e.hi - ei) + e.lo;
         const float ratio =
-            ldexpf(fast_exp2((float)(e - ei)), (int)fmax(fmin(ei, 300.0), -300.0)) * (sd_f / st_f);
+            ldexpf(fast_exp2(f), (int)fmaxf(fminf(ei, 300.f), -300.f)) * (sd_f / st_f);
         acc = uacc < ratio;
       }
       rej = !acc;
-      pp = exp2f((float)et) / st_f;
-      qq = exp2f((float)ed) / sd_f;
+      pp = t_inf ? 0.f : exp2f(df_to_f(et)) / st_f;
+      qq = d_inf ? 0.f : exp2f(df_to_f(ed)) / sd_f;
     }
     sh.pp[tid] = pp;
     sh.qq[tid] = qq;
@@ -2001,17 +2078,20 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     }
     return;
   }
-  const Philox4 r = philox4x64_10((uint64_t)a + 1, bglob, offset, 0, seed, 0);
-  const double u = (double)u24(r.w[1]);
   DecideCtx c;
   ctx_no_filter(c);
   c.mT = sh.rowM[0][a];
   c.invST = sh.rowInv[0][a];
   c.cs = cs;
   const T* trow = target + ((int64_t)b * M + a) * V;
+  // the draw's uniform (counter word 0: node a + 1), by the warp that draws
+  auto draw_u = [&]() {
+    return (double)u24(philox4x64_10((uint64_t)a + 1, bglob, offset, 0, seed, 0).w[1]);
+  };
   if (fr == M) {
     // every draft accepted: the bonus token from p of node a
     if (s != 0 || warp != 0) return;
+    const double u = draw_u();
     c.mD = 0.f;
     c.invSD = 0.f;
     c.nrej = 0;
@@ -2054,67 +2134,82 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   // the last slice: the chunk from the masses (all loaded at once into
   // shared memory when they fit), then the token
   __threadfence();
-  // the masses (double-floats) one chunk a lane, scanned in order: the
-  // first chunk of positive mass whose running mass exceeds u * Z, else the
-  // last of positive mass
+  // the masses (double-floats) one chunk a lane, scanned in order by warp
+  // 0: the first chunk of positive mass whose running mass exceeds u * Z,
+  // else the last of positive mass; then the whole CTA searches that chunk
+  const double u = warp == 0 ? draw_u() : 0.0;
+  if (warp == 0) {
+    const float2* zf = reinterpret_cast<const float2*>(zs);
+    dfloat Zd = df_make(0.f);
+    for (int k = lane; k < n_chunks; k += kWarp) {
+      const float2 v = __ldcg(zf + k);
+      Zd = df_add(Zd, dfloat{v.x, v.y});
+    }
+    Zd = df_warp_sum(Zd);
+    if (Zd.hi > 0.f) {
+      const dfloat t = df_mul_f(Zd, (float)u);  // u is a 24-bit fraction: exact in fp32
+      dfloat base = df_make(0.f), sel_pre = df_make(0.f), last_pre = df_make(0.f);
+      int sel = -1, lastpos = -1;
+      for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
+        const int k = k0 + lane;
+        const float2 v = k < n_chunks ? __ldcg(zf + k) : make_float2(0.f, 0.f);
+        const dfloat wk{v.x, v.y};
+        const dfloat incl = df_add(base, df_warp_scan(wk));
+        const dfloat excl = df_sub(incl, wk);
+        const bool pos = wk.hi > 0.f;
+        const unsigned hit = __ballot_sync(0xffffffffu, pos && df_gt(incl, t));
+        const unsigned pb = __ballot_sync(0xffffffffu, pos);
+        if (pb) {
+          const int l = 31 - __clz(pb);
+          lastpos = k0 + l;
+          last_pre = df_shfl(excl, l);
+        }
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          sel = k0 + l;
+          sel_pre = df_shfl(excl, l);
+        }
+        base = df_shfl(incl, kWarp - 1);
+      }
+      if (sel < 0) {  // rounding at the very top: the last chunk with mass
+        sel = lastpos < 0 ? 0 : lastpos;
+        sel_pre = lastpos < 0 ? df_make(0.f) : last_pre;
+      }
+      if (lane == 0) {
+        sh.zero = 0;
+        sh.sel = sel;
+        sh.trel = df_sub(t, sel_pre);
+        sh.Zf = df_to_f(Zd);
+      }
+    } else if (lane == 0) {
+      sh.zero = 1;
+    }
+  }
+  __syncthreads();
+  if (!sh.zero) {
+    tail_block_draw<T>(trow, drow, (int64_t)sh.sel * chunk, V, c, sh.trel, sh);
+    if (tid == 0) {
+      ot[a] = sh.tok_out;
+      if (pr != nullptr) {
+        pr[a * 4 + 2] = sh.Zf;
+        pr[a * 4 + 3] = sh.w_out / sh.Zf;
+      }
+      done_cnt[b] = 0u;  // ready for the next call
+    }
+    return;
+  }
+  // a residual of zero mass: the draw from p of the node
   if (warp != 0) return;
-  const float2* zf = reinterpret_cast<const float2*>(zs);
-  dfloat Zd = df_make(0.f);
-  for (int k = lane; k < n_chunks; k += kWarp) {
-    const float2 v = __ldcg(zf + k);
-    Zd = df_add(Zd, dfloat{v.x, v.y});
-  }
-  Zd = df_warp_sum(Zd);
+  c.nrej = 0;
   float w;
-  int tk;
-  float Zrep, zden;
-  if (Zd.hi > 0.f) {
-    const dfloat t = df_mul_f(Zd, (float)u);  // u is a 24-bit fraction: exact in fp32
-    dfloat base = df_make(0.f), sel_pre = df_make(0.f), last_pre = df_make(0.f);
-    int sel = -1, lastpos = -1;
-    for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
-      const int k = k0 + lane;
-      const float2 v = k < n_chunks ? __ldcg(zf + k) : make_float2(0.f, 0.f);
-      const dfloat wk{v.x, v.y};
-      const dfloat incl = df_add(base, df_warp_scan(wk));
-      const dfloat excl = df_sub(incl, wk);
-      const bool pos = wk.hi > 0.f;
-      const unsigned hit = __ballot_sync(0xffffffffu, pos && df_gt(incl, t));
-      const unsigned pb = __ballot_sync(0xffffffffu, pos);
-      if (pb) {
-        const int l = 31 - __clz(pb);
-        lastpos = k0 + l;
-        last_pre = df_shfl(excl, l);
-      }
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        sel = k0 + l;
-        sel_pre = df_shfl(excl, l);
-      }
-      base = df_shfl(incl, kWarp - 1);
-    }
-    if (sel < 0) {  // rounding at the very top: the last chunk with mass
-      sel = lastpos < 0 ? 0 : lastpos;
-      sel_pre = lastpos < 0 ? df_make(0.f) : last_pre;
-    }
-    tk = warp_chunk_draw<T, false>(trow, drow, (int64_t)sel * chunk, V, c, 1, df_sub(t, sel_pre),
-                                   &w);
-    Zrep = df_to_f(Zd);
-    zden = Zrep;
-  } else {
-    // a residual of zero mass: the draw from p of the node
-    c.nrej = 0;
-    double z;
-    const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
-    tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &w, &z);
-    zden = (float)z;
-    Zrep = 1.f;
-  }
+  double z;
+  const RowStat* tst = stats + (((int64_t)b * 2 + 0) * M + a) * n_chunks;
+  const int tk = warp_draw_from_p<T>(trow, tst, n_chunks, chunk, V, c, u, &w, &z);
   if (lane == 0) {
     ot[a] = tk;
     if (pr != nullptr) {
-      pr[a * 4 + 2] = Zrep;
-      pr[a * 4 + 3] = w / zden;
+      pr[a * 4 + 2] = 1.f;
+      pr[a * 4 + 3] = (float)((double)w / z);
     }
     done_cnt[b] = 0u;  // ready for the next call
   }

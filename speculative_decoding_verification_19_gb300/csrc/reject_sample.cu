@@ -1757,8 +1757,8 @@ struct TailSmem {
   float st_s[kTailStage];
   int st_a[kTailStage];
   float rowM[2][kMaxM];
-  double rowS[2][kMaxM];
-  float rowInv[2][kMaxM];  // (float)(1 / rowS), formed once per row
+  float rowS[2][kMaxM];     // row sums (the double-float sum rounded to fp32)
+  float rowInv[2][kMaxM];  // 1 / rowS, formed once per row
   int rowA[2][kMaxM];
   int tok[kMaxM];
   float gzt[kMaxM], gzd[kMaxM];
@@ -1888,16 +1888,34 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     const float* __restrict__ temperature, uint64_t seed, uint64_t offset, uint64_t b_base,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ path,
     int32_t* __restrict__ accepted_len, float* __restrict__ probe, spec_dims d, int n_chunks,
-    int chunk, const RowStat* stats, double* zsum, uint32_t* done_cnt, uint32_t* status, int S) {
+    int chunk, const RowStat* stats, double* zsum, uint32_t* done_cnt, uint32_t* status, int S,
+    int inputs_ready) {
   __shared__ TailSmem sh;
   const int b = blockIdx.x / S, s = blockIdx.x % S;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int M = d.M, V = d.V;
   pdl_trigger();
-  pdl_wait();  // the statistics (and any input) come from earlier kernels
+  // Launched once everything before the statistics kernel has completed
+  // (inputs_ready), the kernel reads its inputs before the statistics are
+  // done: the tokens, the accept tests' logits and their uniforms; after
+  // the LM heads it waits for its predecessor first.
+  if (!inputs_ready) pdl_wait();
   int32_t x = 0;
   if (tid < M) x = tokens[(int64_t)b * M + tid];
   const float temp = temperature[b];
+  const bool greedy = temp == 0.f;
+  const bool tok_bad = tid >= 1 && tid < M && (x < 0 || x >= V);
+  // the accept tests' logits: draft n's token in the rows of node n - 1
+  float g_t = 0.f, g_d = 0.f, uacc = 0.f;
+  if (tid >= 1 && tid < M && !tok_bad) {
+    const int64_t o = ((int64_t)b * M + tid - 1) * V + x;
+    g_t = to_f32(target[o]);
+    g_d = to_f32(draft[o]);
+  }
+  const uint64_t bglob = b_base + (uint64_t)b;
+  if (!greedy && tid >= 1 && tid < M)
+    uacc = u24(philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0).w[0]);
+  pdl_wait();  // the statistics come from the previous kernel
   int32_t* ot = out_tokens + (int64_t)b * M;
   int32_t* pt = path + (int64_t)b * M;
   float* pr = probe != nullptr ? probe + (int64_t)b * M * 4 : nullptr;
@@ -1919,18 +1937,14 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
     fail(-1);
     return;
   }
-  const bool greedy = temp == 0.f;
   const float cs = stat_scale(temp);
   if (tid == 0) sh.bad = temperature_valid(temp) ? 0 : 1;
-  const bool tok_bad = tid >= 1 && tid < M && (x < 0 || x >= V);
   if (tid < M) sh.tok[tid] = x;
   __syncthreads();
   if (tok_bad) atomicOr(&sh.bad, 2);
-  // the accept tests' logits: draft n's token in the rows of node n - 1
-  if (tid >= 1 && tid < M && !tok_bad) {
-    const int64_t o = ((int64_t)b * M + tid - 1) * V + x;
-    sh.gzt[tid] = to_f32(target[o]);
-    sh.gzd[tid] = to_f32(draft[o]);
+  if (tid >= 1 && tid < M) {
+    sh.gzt[tid] = g_t;
+    sh.gzd[tid] = g_d;
   }
   // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row;
   // the statistics come in one round of loads through shared memory when
@@ -1964,8 +1978,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   }
   for (int r = warp; r < rows; r += kTailWarps) {
     const int which = r < M ? 0 : 1, n = r < M ? r : r - M;
-    float m;
-    double sm;
+    float m, sm;
     int am;
     if (staged) {
       const float* rm = sh.st_m + r * n_chunks;
@@ -1982,19 +1995,21 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
         if (rm[c] == m && c < cf) cf = c;
       }
       acc = df_warp_sum(acc);
-      sm = lane == 0 ? df_to_d(acc) : 0.0;
+      sm = df_to_f(acc);
       cf = __reduce_min_sync(0xffffffffu, cf);
       am = cf < n_chunks ? cf * chunk + sh.st_a[r * n_chunks + cf] : 0;
     } else {
+      double sd;
       tail_row_norm(stats + (((int64_t)b * 2 + which) * M + n) * n_chunks, n_chunks, chunk, cs,
-                    &m, &sm, &am);
+                    &m, &sd, &am);
+      sm = (float)sd;
     }
     if (lane == 0) {
       sh.rowM[which][n] = m;
       sh.rowS[which][n] = sm;
-      sh.rowInv[which][n] = (float)(1.0 / sm);
+      sh.rowInv[which][n] = 1.0f / sm;
       sh.rowA[which][n] = am;
-      if (!(isfinite(m) && sm > 0.0 && isfinite(sm))) atomicOr(&sh.bad, 4);
+      if (!(isfinite(m) && sm > 0.f && isfinite(sm))) atomicOr(&sh.bad, 4);
     }
   }
   __syncthreads();
@@ -2006,7 +2021,6 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
 
   // ---- the accept tests of every draft at once (rs_decide_kernel's chain
   // arithmetic) and the first rejection
-  const uint64_t bglob = b_base + (uint64_t)b;
   if (tid == 0) sh.first_rej = M;
   __syncthreads();
   if (tid >= 1 && tid < M) {
@@ -2018,10 +2032,8 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       pp = rej ? 0.f : 1.f;
       qq = x == sh.rowA[1][p] ? 1.f : 0.f;
     } else {
-      const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
-      const float uacc = (float)u24(r.w[0]);
       const float zt = sh.gzt[tid], zd = sh.gzd[tid];
-      const float st_f = (float)sh.rowS[0][p], sd_f = (float)sh.rowS[1][p];
+      const float st_f = sh.rowS[0][p], sd_f = sh.rowS[1][p];
       const bool t_inf = zt == -INFINITY, d_inf = zd == -INFINITY;
       // the exponents of p(x), q(x) (log2 of the unnormalised terms) and of
       // their ratio in double-float (the differences exact, the products by
@@ -3059,7 +3071,8 @@ static cudaError_t launch_rs_t(const RsArgs& a, const WsLayout& lay, cudaStream_
     const cudaError_t e = cudaLaunchKernelEx(
         &L.cfg, rs_chain_tail_kernel<T>, tgt, dft, a.tokens, a.temperature, a.seed, a.offset,
         a.b_base, a.out_tokens, a.path, a.accepted_len, a.probe, d, lay.rs_chunks, lay.rs_chunk,
-        (const RowStat*)stats, zsum, reinterpret_cast<uint32_t*>(ws + lay.rs_tail_off), status, S);
+        (const RowStat*)stats, zsum, reinterpret_cast<uint32_t*>(ws + lay.rs_tail_off), status, S,
+        a.stats_ready ? 0 : 1);
     if (e != cudaSuccess) return e;
     *launches += a.stats_ready ? 1 : 2;
     return cudaGetLastError();

@@ -1753,7 +1753,7 @@ constexpr int kTailStage = 2048;  // chunk statistics of one request held in sha
 struct TailSmem {
   // the request's chunk statistics (row-major), when they fit: maximum,
   // sum, argmax word
-  float st_m[kTailStage];
+  alignas(16) float st_m[kTailStage];  // (also the residual masses as float2 in the last slice)
   float st_s[kTailStage];
   int st_a[kTailStage];
   float rowM[2][kMaxM];
@@ -1763,6 +1763,7 @@ struct TailSmem {
   int tok[kMaxM];
   float gzt[kMaxM], gzd[kMaxM];
   float pp[kMaxM], qq[kMaxM];
+  float usmp[kMaxM];  // the draw's uniform at each node
   int first_rej;
   int last;
   int bad;  // bit 0: argument, bit 1: token, bit 2: row without a distribution
@@ -1906,15 +1907,20 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   const bool greedy = temp == 0.f;
   const bool tok_bad = tid >= 1 && tid < M && (x < 0 || x >= V);
   // the accept tests' logits: draft n's token in the rows of node n - 1
-  float g_t = 0.f, g_d = 0.f, uacc = 0.f;
+  float g_t = 0.f, g_d = 0.f, uacc = 0.f, usmp = 0.f;
   if (tid >= 1 && tid < M && !tok_bad) {
     const int64_t o = ((int64_t)b * M + tid - 1) * V + x;
     g_t = to_f32(target[o]);
     g_d = to_f32(draft[o]);
   }
+  // node tid's uniforms (counter word 0: tid + 1): the accept test of draft
+  // tid and the draw at node tid
   const uint64_t bglob = b_base + (uint64_t)b;
-  if (!greedy && tid >= 1 && tid < M)
-    uacc = u24(philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0).w[0]);
+  if (!greedy && tid < M) {
+    const Philox4 r = philox4x64_10((uint64_t)tid + 1, bglob, offset, 0, seed, 0);
+    uacc = u24(r.w[0]);
+    usmp = u24(r.w[1]);
+  }
   pdl_wait();  // the statistics come from the previous kernel
   int32_t* ot = out_tokens + (int64_t)b * M;
   int32_t* pt = path + (int64_t)b * M;
@@ -1942,9 +1948,10 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   if (tid < M) sh.tok[tid] = x;
   __syncthreads();
   if (tok_bad) atomicOr(&sh.bad, 2);
-  if (tid >= 1 && tid < M) {
+  if (tid < M) {
     sh.gzt[tid] = g_t;
     sh.gzd[tid] = g_d;
+    sh.usmp[tid] = usmp;
   }
   // row normalisers: target rows 0..M-1, draft rows 0..M-2, one warp a row;
   // the statistics come in one round of loads through shared memory when
@@ -2096,10 +2103,8 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   c.invST = sh.rowInv[0][a];
   c.cs = cs;
   const T* trow = target + ((int64_t)b * M + a) * V;
-  // the draw's uniform (counter word 0: node a + 1), by the warp that draws
-  auto draw_u = [&]() {
-    return (double)u24(philox4x64_10((uint64_t)a + 1, bglob, offset, 0, seed, 0).w[1]);
-  };
+  // the draw's uniform (counter word 0: node a + 1)
+  auto draw_u = [&]() { return (double)sh.usmp[a]; };
   if (fr == M) {
     // every draft accepted: the bonus token from p of node a
     if (s != 0 || warp != 0) return;
@@ -2151,10 +2156,14 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   // else the last of positive mass; then the whole CTA searches that chunk
   const double u = warp == 0 ? draw_u() : 0.0;
   if (warp == 0) {
+    // the masses in one round of loads, kept in shared memory (the
+    // statistics staging area, free by now) for the scan
     const float2* zf = reinterpret_cast<const float2*>(zs);
+    float2* zm = reinterpret_cast<float2*>(sh.st_m);  // 1024 entries >= n_chunks
     dfloat Zd = df_make(0.f);
     for (int k = lane; k < n_chunks; k += kWarp) {
       const float2 v = __ldcg(zf + k);
+      zm[k] = v;
       Zd = df_add(Zd, dfloat{v.x, v.y});
     }
     Zd = df_warp_sum(Zd);
@@ -2164,7 +2173,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       int sel = -1, lastpos = -1;
       for (int k0 = 0; k0 < n_chunks && sel < 0; k0 += kWarp) {
         const int k = k0 + lane;
-        const float2 v = k < n_chunks ? __ldcg(zf + k) : make_float2(0.f, 0.f);
+        const float2 v = k < n_chunks ? zm[k] : make_float2(0.f, 0.f);
         const dfloat wk{v.x, v.y};
         const dfloat incl = df_add(base, df_warp_scan(wk));
         const dfloat excl = df_sub(incl, wk);

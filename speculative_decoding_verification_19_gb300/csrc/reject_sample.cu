@@ -2131,8 +2131,16 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
   c.nrej = 1;
   const T* drow = draft + ((int64_t)b * M + a) * V;
   double* zs = zsum + (int64_t)b * n_chunks;
-  const int c0 = (int)((int64_t)n_chunks * s / S), c1 = (int)((int64_t)n_chunks * (s + 1) / S);
-  for (int cc = c0 + warp; cc < c1; cc += kTailWarps) {
+  // Each warp's first chunk is fixed (warp w of slice s: chunk s * 8 + w);
+  // the rest are claimed one at a time from the request's counter, each
+  // warp holding its next claim in flight while it works on the current
+  // chunk, so that a slice on a less busy SM takes more of them.
+  uint32_t* claim = done_cnt + d.B;
+  const int nfixed = S * kTailWarps;
+  int cc = s * kTailWarps + warp;
+  while (cc < n_chunks) {
+    uint32_t nxt = 0;
+    if (lane == 0) nxt = atomicAdd(claim + b, 1u);
     uint4 raw_t[kStatVecs], raw_d[kStatVecs];
     const float ls = lane_weights<T, false>(trow, drow, (int64_t)cc * chunk, V, c, 1, raw_t, raw_d);
     const dfloat tot = df_warp_sum(df_make(ls));
@@ -2140,6 +2148,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       reinterpret_cast<float2*>(zs)[cc] = make_float2(tot.hi, tot.lo);
       __threadfence();  // the mass before this slice's count
     }
+    cc = nfixed + __shfl_sync(0xffffffffu, (int)nxt, 0);
   }
   __syncthreads();
   if (tid == 0) {
@@ -2216,6 +2225,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
         pr[a * 4 + 3] = sh.w_out / sh.Zf;
       }
       done_cnt[b] = 0u;  // ready for the next call
+      claim[b] = 0u;
     }
     return;
   }
@@ -2233,6 +2243,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) rs_chain_tail_kernel(
       pr[a * 4 + 3] = (float)((double)w / z);
     }
     done_cnt[b] = 0u;  // ready for the next call
+    claim[b] = 0u;
   }
 }
 

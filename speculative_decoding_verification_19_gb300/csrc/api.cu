@@ -61,8 +61,9 @@ WsLayout workspace_layout(const spec_dims& d) {
   L.rs_draw_off = take(sizeof(DrawState) * (size_t)d.B);
   L.rs_zsum_off = take(sizeof(double) * (size_t)d.B * L.rs_chunks);
   L.rs_filt_off = take(sizeof(FilterInfo) * (size_t)d.B * 2 * d.M);
-  // the chain tail: per request, slices finished, then residual chunks claimed
-  L.rs_tail_off = take(sizeof(uint32_t) * 2 * (size_t)d.B);
+  // the chain tail: per request, slices finished, then residual chunks
+  // claimed; then the statistics stream's pool counters (claimed, warps done)
+  L.rs_tail_off = take(sizeof(uint32_t) * (2 * (size_t)d.B + 2));
   // the LM heads' split statistics (rows B * M, bf16 logits)
   const int64_t lm_units = (int64_t)ceil_div64((int64_t)d.B * d.M, 128) * L.rs_chunks;
   if (d.logits_dtype == SPEC_BF16 && lm_units <= kLmSplitMaxUnits) {

@@ -143,7 +143,7 @@ extern "C" spec_status spec_reject_sample_noalloc(
   lay.rs_draw_off = up(lay.rs_off + lay.rs_bytes);
   lay.rs_zsum_off = up(lay.rs_draw_off + sizeof(DrawState) * (size_t)dims->B);
   lay.rs_tail_off = up(lay.rs_zsum_off + sizeof(double) * (size_t)dims->B * lay.rs_chunks);
-  lay.total = lay.rs_tail_off + sizeof(uint32_t) * 2 * (size_t)dims->B;
+  lay.total = lay.rs_tail_off + sizeof(uint32_t) * (2 * (size_t)dims->B + 2);
   if (fused) lay.total = rsf_layout(*dims, up(lay.total), &lay);
   if (lay.total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
 
@@ -156,7 +156,7 @@ extern "C" spec_status spec_reject_sample_noalloc(
   // read is written earlier in the same call.
   char* sb = static_cast<char*>(scratch);
   if (cudaMemsetAsync(sb, 0, kNoAllocStatusBytes, st) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (cudaMemsetAsync(sb + lay.rs_tail_off, 0, sizeof(uint32_t) * 2 * (size_t)dims->B, st) !=
+  if (cudaMemsetAsync(sb + lay.rs_tail_off, 0, sizeof(uint32_t) * (2 * (size_t)dims->B + 2), st) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
   if (fused && cudaMemsetAsync(sb + lay.rsf_ctl_off, 0, lay.total - lay.rsf_ctl_off, st) !=

@@ -63,7 +63,9 @@ def test_attention_wait_gives_up_then_recovers():
 
 @pytest.mark.parametrize("impl", [sv.REJECT_STAGED, sv.REJECT_FUSED])
 def test_reject_wait_gives_up_then_recovers(impl):
-    wl = workload("stress_gqa_152k").scaled(B=48)
+    # the full stress batch: 350 MB of logits, so that the statistics'
+    # copies queue at HBM and some wait outlasts the thousand-clock limit
+    wl = workload("stress_gqa_152k")
     lg = logits_inputs(wl, seed=32)
     B, M, V = lg["target"].shape
     dims = dims_for(wl, B, V=V)
@@ -91,7 +93,9 @@ def test_tree_walk_wait_gives_up_then_recovers():
     # whose exchanges wait (bounded) on mbarriers that the other CTAs of the
     # cluster arrive on; after a wait gives up the walk still meets the
     # cluster barrier at its end, and every request of the call fails
-    wl = workload("tree_64")
+    # rows of the stress vocabulary: 623 MB of logits, more than L2 holds even
+    # right after they are written, so the statistics' copies come from HBM
+    wl = workload("tree_64").scaled(B=16, V=152064)
     lg = logits_inputs(wl, seed=34)
     B, M, V = lg["target"].shape
     dims = dims_for(wl, B, V=V)

@@ -14,8 +14,9 @@
 // nodes -- so a cluster of kTwCtas CTAs walks each request: CTA r owns slice
 // r of every row (1/kTwCtas of the vocabulary, whole 16-byte vectors).  Per
 // visited node, one exchange through distributed shared memory gives every
-// CTA the node's normalisers (slice maxima and sums, combined in rank
-// order), each rejected child one more exchange for the residual's mass,
+// CTA the node's normalisers (the slices' maxima and sums, combined the same
+// way in every CTA), each rejected child one more exchange for the
+// residual's mass,
 // and the draw's slice is searched by the CTA that owns it.  Every CTA makes
 // the same decisions from the same exchanged values.  An exchange is eight
 // remote stores and eight remote mbarrier arrivals per CTA, and a bounded
@@ -201,7 +202,8 @@ __device__ __forceinline__ bool tw_exchange(tw::Smem& sh, int rank, uint64_t lim
 }
 
 // Block-wide: rows `trow` (and `drow` when non-null) of this CTA's slice
-// [v0, v1) of 16-byte vectors -> the CTA's runs in sh.rt[0] / sh.rd[0].
+// [v0, v1) of 16-byte vectors -> each warp's runs in sh.rt[warp] /
+// sh.rd[warp] (the caller merges the warps).
 template <typename T>
 __device__ void tw_slice_runs(const T* trow, const T* drow, int64_t v0, int64_t v1, float cs,
                               tw::Smem& sh) {
@@ -265,10 +267,11 @@ __device__ void tw_slice_runs(const T* trow, const T* drow, int64_t v0, int64_t 
   __syncthreads();
 }
 
-// Block-wide: this CTA's mass of weight_of(., nrej) over its slice (fp32
-// per thread, fp32 per warp; the warps combined by thread 0).
+// Block-wide: this CTA's mass of the residual weights (nrej rejections so
+// far) over its slice -- fp32 per thread and per warp, the warps combined by
+// thread 0 in double-float -- left as this CTA's words in sh.mine.
 template <typename T>
-__device__ float tw_slice_mass(const T* trow, const T* drow, int64_t v0, int64_t v1,
+__device__ void tw_slice_mass(const T* trow, const T* drow, int64_t v0, int64_t v1,
                                const DecideCtx& c, int nrej, tw::Smem& sh) {
   constexpr int EPV = 16 / sizeof(T);
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -304,7 +307,6 @@ __device__ float tw_slice_mass(const T* trow, const T* drow, int64_t v0, int64_t
     sh.mine[1] = __float_as_uint(t.lo);
   }
   __syncthreads();
-  return 0.f;
 }
 
 // Block-wide inverse CDF inside this CTA's slice: the smallest element whose
@@ -418,7 +420,6 @@ __global__ void __launch_bounds__(kTwThreads) rs_tree_walk_kernel(
   __shared__ tw::Smem sh;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   const int rank = (int)tw::cluster_rank();
-  (void)lane;
   const int b = blockIdx.x / kTwCtas;
   const int M = d.M, V = d.V;
   const uint64_t limit = wait_limit_cycles(d);

@@ -114,6 +114,36 @@ def test_wide_tree_128_nodes(impl):
 
 
 @pytest.mark.parametrize("impl", TREE_IMPLS)
+def test_tree_walk_fp32_greedy_mix_and_shards(impl):
+    # fp32 rows (the walk's float instance), every other request greedy, and
+    # request shards with b_base reproducing the whole batch draw for draw
+    wl = workload("tree_64").scaled(B=6, V=4096, dtype="f32")
+    lg = logits_inputs(wl, seed=23)
+    lg["temperature"][::2] = 0.0
+    whole, _, _ = _run(wl, lg, seed=21, offset=1, impl=impl)
+    assert whole["status"] == 0
+    for lo, hi in [(0, 2), (2, 6)]:
+        part = {k: (v[lo:hi] if isinstance(v, np.ndarray) else v) for k, v in lg.items()}
+        g, _, _ = _run(wl.scaled(B=hi - lo), part, seed=21, offset=1, b_base=lo, impl=impl)
+        for key in ("out_tokens", "path", "accepted_len"):
+            assert np.array_equal(g[key], whole[key][lo:hi]), (key, lo)
+
+
+@pytest.mark.parametrize("impl", TREE_IMPLS)
+def test_single_node_and_two_level_trees(impl):
+    # a tree of the root alone (the bonus draw from p of node 0, nothing
+    # tested) and a three-node tree
+    for nodes, depth in [(1, 0), (3, 2)]:
+        wl = workload("tree_64").scaled(B=5, V=2048, gamma=depth, tree_nodes=nodes)
+        lg = logits_inputs(wl, seed=24 + nodes)
+        assert lg["parent"].shape[1] == nodes
+        g, o, _ = _run(wl, lg, seed=22, offset=0, impl=impl)
+        assert g["status"] == 0
+        if nodes == 1:
+            assert np.all(g["accepted_len"] == 0)
+
+
+@pytest.mark.parametrize("impl", TREE_IMPLS)
 def test_small_trees_many_rejections(impl):
     # wide fan-out, noisy draft: several rejections per node
     wl = workload("tree_64").scaled(B=8, V=48, gamma=2, tree_width=8,

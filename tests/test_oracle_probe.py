@@ -166,3 +166,62 @@ def test_tree_rejection_then_uncertain_child_uses_updated_mass():
     else:
         assert res["accepted_len"][0] == 0 and res["out_tokens"][0, 0] == 0
         np.testing.assert_allclose(pr[0, 2:], [11 / 15, 1.0], atol=1e-12)
+
+
+def _closed_form_walk(p, q, xs, u_acc):
+    """The root's children tested in order, from a closed form of the
+    sequential residual updates (derived here, not the oracle's loop): after
+    j rejections the working target is max(0, p - c_j q) / D_j with
+    c_0 = 0, D_0 = 1, c_{j+1} = c_j + D_j and D_{j+1} = sum max(0, p -
+    c_{j+1} q) -- by induction, max(0, max(0, p - c q) / D - q) equals
+    max(0, p - (c + D) q) / D, so the normaliser of that residual is
+    sum max(0, p - (c + D) q) / D.  Returns the (P(x), Q(x)) of each tested
+    child, the accepted child (or None), and the residual mass of the last
+    rejection (Z, the probe's column 2 at the root)."""
+    c, D = 0.0, 1.0
+    tested, Z = [], 1.0
+    for k, x in enumerate(xs):
+        P = max(0.0, p[x] - c * q[x]) / D
+        tested.append((P, q[x]))
+        if u_acc[k + 1] * q[x] < P:
+            return tested, k + 1, Z
+        c = c + D
+        D_next = float(np.maximum(p - c * q, 0.0).sum())
+        Z = D_next / D
+        D = D_next
+    return tested, None, Z
+
+
+@pytest.mark.parametrize("mode", ["favoured", "mixed"])
+@pytest.mark.parametrize("seed", range(6))
+def test_tree_many_sibling_rejections_closed_form(seed, mode):
+    # a root with seven leaf children; random p and q over 9 tokens with
+    # every entry positive, so no residual has zero mass.  "favoured": the
+    # drafted tokens are the ones the draft favours most over the target
+    # (most often rejected: up to seven residual updates in a row);
+    # "mixed": those alternate with tokens from the middle of that order,
+    # whose residual probabilities stay positive along the walk
+    rng = np.random.default_rng((100 if mode == "favoured" else 200) + seed)
+    V, W = 9, 7
+    p = rng.dirichlet(np.ones(V))
+    q = rng.dirichlet(np.ones(V) * 0.5)
+    q = 0.9 * q + 0.1 / V
+    order = np.argsort(-q / p)
+    picks = range(W) if mode == "favoured" else (0, 4, 1, 5, 2, 6, 3)
+    xs = [int(order[i]) for i in picks]
+    leaf = np.full(V, 1.0 / V)
+    M = 1 + W
+    res = _run([p] + [leaf] * W, [q] + [leaf] * W, [0] + xs, [-1] + [0] * W, 1.0)
+    pr = res["probe"][0]
+    u_acc = uniforms_for(SEED, OFFSET, 0, M)[0]
+    tested, accepted, Z = _closed_form_walk(p, q, xs, u_acc)
+    for k, (P, Q) in enumerate(tested):
+        np.testing.assert_allclose(pr[k + 1, :2], [P, Q], rtol=1e-10, atol=1e-12)
+    if accepted is None:
+        assert res["accepted_len"][0] == 0
+        np.testing.assert_allclose(pr[0, 2], Z, rtol=1e-10)
+    else:
+        assert res["accepted_len"][0] == 1 and res["path"][0, 1] == accepted
+    # children after the accepted one are not tested
+    for k in range(len(tested) + 1, M):
+        assert np.all(pr[k, :2] == -1.0)

@@ -82,7 +82,10 @@ typedef enum spec_reject_impl {
   SPEC_REJECT_STAGED = 1,      /* logit statistics, then for a chain with 16-byte
                                   aligned rows and no filter one tail kernel
                                   (decisions, residual masses and draw, several CTAs
-                                  per request), else three kernels (decisions,
+                                  per request); for a tree with such rows and no
+                                  filter the walk by a cluster of 8 CTAs per request
+                                  beside the statistics (which still decide which
+                                  requests fail); else three kernels (decisions,
                                   residual masses, residual draws); any alignment,
                                   V up to 2^20 */
   SPEC_REJECT_FUSED = 2        /* one kernel for a chain: every warp streams logit

@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_bulk_kernel
   constexpr int kChunk = kWarp * kStatVecs * EPV;
   pdl_wait();  // the logits may come from the previous kernel
   // the dependent launches only now, when everything before this kernel has
-  // completed: the tree walk reads its inputs without waiting for this one
+  // completed: the kernel after it (the chain tail, the tree walk) reads
+  // its inputs without waiting for this one
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -384,7 +385,8 @@ __global__ void __launch_bounds__(kBulkWarps * kWarp, 1) rs_rowstats_pool_kernel
   constexpr int kChunk = kWarp * kStatVecs * EPV;
   pdl_wait();  // the logits may come from the previous kernel
   // the dependent launches only now, when everything before this kernel has
-  // completed: the tree walk reads its inputs without waiting for this one
+  // completed: the kernel after it (the chain tail, the tree walk) reads
+  // its inputs without waiting for this one
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
